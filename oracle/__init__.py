@@ -1,0 +1,135 @@
+"""fp64 CPU oracle for the fused attention forward -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg may load
+this package.  It shares no code with the CUDA library and imports nothing
+from the product package.
+
+What it computes (attention formula of "flash-attn 实现 prefill 阶段",
+problem analysis; scale after the dot product and natural-exp softmax of
+flash-attention-minimal ``forward_kernel``) is documented in
+``attn_oracle.c``.  ``build()`` compiles that file with the host C compiler
+into ``liboracle.so`` next to it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle (plain C, -O2, OpenMP) if missing or stale."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    cc = os.environ.get("CC", "gcc")
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = [cc, "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _bind(lib):
+    dp = ctypes.POINTER(ctypes.c_double)
+    i64 = ctypes.c_int64
+    lib.oracle_num_threads.restype = ctypes.c_int
+    lib.oracle_attn_fwd_f64.restype = ctypes.c_int
+    lib.oracle_attn_fwd_f64.argtypes = [dp, dp, dp, dp, dp, i64, i64, i64, i64, i64,
+                                        ctypes.c_int, ctypes.c_double]
+    lib.oracle_attn_online_f64.restype = ctypes.c_int
+    lib.oracle_attn_online_f64.argtypes = [dp, dp, dp, dp, dp, i64, i64, i64, i64, i64,
+                                           ctypes.c_int, ctypes.c_double, i64]
+    lib.oracle_attn_head_rows_f64.restype = ctypes.c_int
+    lib.oracle_attn_head_rows_f64.argtypes = [dp, dp, dp, i64, i64, i64, ctypes.c_int,
+                                              ctypes.c_double,
+                                              ctypes.POINTER(ctypes.c_int64), i64, dp, dp]
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = _bind(ctypes.CDLL(_LIB))
+    return _lib
+
+
+def load_library(path: str):
+    """Bind the oracle API of another build of attn_oracle.c (the tests use
+    this to check that the pins reject deliberately broken copies)."""
+    return _bind(ctypes.CDLL(path))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def num_threads(lib=None) -> int:
+    return int((lib or _load()).oracle_num_threads())
+
+
+def attn_fwd(q, k, v, causal: bool, scale: float, lib=None):
+    """Definition: O = softmax(scale * Q K^T [+ causal mask]) V and LSE.
+
+    q: [b, h, sq, d], k/v: [b, h, sk, d] (any float dtype; used as fp64).
+    Returns (o [b, h, sq, d] fp64, lse [b, h, sq] fp64).
+    """
+    lib = lib or _load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    b, h, sq, d = q.shape
+    sk = k.shape[2]
+    assert k.shape == (b, h, sk, d) and v.shape == (b, h, sk, d)
+    o = np.zeros((b, h, sq, d), np.float64)
+    lse = np.zeros((b, h, sq), np.float64)
+    rc = lib.oracle_attn_fwd_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                 b, h, sq, sk, d, int(bool(causal)), float(scale))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_fwd_f64 failed: {rc}")
+    return o, lse
+
+
+def attn_fwd_online(q, k, v, causal: bool, scale: float, bc: int, lib=None):
+    """The flash-attention-minimal tile recurrence (tile of ``bc`` keys)."""
+    lib = lib or _load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    b, h, sq, d = q.shape
+    sk = k.shape[2]
+    o = np.zeros((b, h, sq, d), np.float64)
+    lse = np.zeros((b, h, sq), np.float64)
+    rc = lib.oracle_attn_online_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                    b, h, sq, sk, d, int(bool(causal)), float(scale),
+                                    int(bc))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_online_f64 failed: {rc}")
+    return o, lse
+
+
+def attn_head_rows(q_head, k_head, v_head, rows, causal: bool, scale: float, lib=None):
+    """Selected query rows of one head: q_head [sq, d], k/v_head [sk, d]."""
+    lib = lib or _load()
+    q_head, k_head, v_head = _f64(q_head), _f64(k_head), _f64(v_head)
+    sq, d = q_head.shape
+    sk = k_head.shape[0]
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    o = np.zeros((rows.size, d), np.float64)
+    lse = np.zeros((rows.size,), np.float64)
+    rc = lib.oracle_attn_head_rows_f64(
+        _ptr(q_head), _ptr(k_head), _ptr(v_head), sq, sk, d, int(bool(causal)),
+        float(scale), rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), rows.size,
+        _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_head_rows_f64 failed: {rc}")
+    return o, lse

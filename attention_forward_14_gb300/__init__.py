@@ -1,0 +1,15 @@
+"""GB300-native fused attention forward (sm_103a).
+
+The compute path is the C-ABI library ``libattn_fwd.so`` built from ``csrc/``;
+``attn_fwd`` and friends (in ``binding``) only marshal arguments to it.  The
+library is loaded on first use, and any failure to load it is an error: there
+is no fallback path.
+"""
+from .binding import (  # noqa: F401
+    AttnError,
+    attn_fwd,
+    attn_fwd_host,
+    lib_path,
+    load,
+    status,
+)

@@ -1,0 +1,183 @@
+"""ctypes binding of libattn_fwd.so (the C ABI in include/attn_fwd.h).
+
+Argument marshalling only: every step of the forward runs in the library's
+CUDA kernels.  PyTorch provides device memory and streams.  If the library is
+missing or cannot be loaded, every call raises -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(HERE, "libattn_fwd.so")
+_lib = None
+_lock = threading.Lock()
+
+FP16, BF16 = 0, 1
+ERRORS = {
+    0: "ATTN_OK", -1: "ATTN_ERR_NULL", -2: "ATTN_ERR_SHAPE", -3: "ATTN_ERR_HEADDIM", -4: "ATTN_ERR_DTYPE",
+    -5: "ATTN_ERR_SCALE", -6: "ATTN_ERR_ALIGN", -7: "ATTN_ERR_ARCH", -8: "ATTN_ERR_CUDA", -9: "ATTN_ERR_WATCHDOG",
+}
+# Every function include/attn_fwd.h declares.
+EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_last_error", "attn_fwd_status", "attn_fwd_status_clear",
+           "attn_fwd_watchdog_selftest", "attn_version"]
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{ERRORS.get(code, code)}: {message}")
+        self.code = code
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def _bind(lib):
+    i64, vp, c_int, c_float = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.attn_fwd.restype = c_int
+    lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_float, c_int, vp]
+    lib.attn_fwd_host.restype = c_int
+    lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                  i64, i64, i64, i64, i64, c_int, c_float, c_int, vp]
+    lib.attn_last_error.restype = ctypes.c_char_p
+    lib.attn_last_error.argtypes = []
+    lib.attn_fwd_status.restype = c_int
+    lib.attn_fwd_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    lib.attn_fwd_status_clear.restype = c_int
+    lib.attn_fwd_status_clear.argtypes = []
+    lib.attn_fwd_watchdog_selftest.restype = c_int
+    lib.attn_fwd_watchdog_selftest.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_float,
+                                               c_int, c_int, c_int, vp]
+    lib.attn_version.restype = ctypes.c_char_p
+    lib.attn_version.argtypes = []
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (once) and bind the C ABI.  Raises if the library is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _LIB_PATH
+        if not os.path.exists(p):
+            raise AttnError(-8, f"{p} not built; run python -m attention_forward_14_gb300.build")
+        lib = _bind(ctypes.CDLL(p))
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(rc: int, lib) -> int:
+    if rc < 0:
+        raise AttnError(rc, lib.attn_last_error().decode(errors="replace"))
+    return rc
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return FP16
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise AttnError(-4, f"unsupported dtype {t.dtype}")
+
+
+def _stream_handle(stream, device):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None,
+             return_lse: bool = True, stream=None):
+    """O = softmax(scale * Q K^T [+ causal]) V on the GPU.
+
+    q: [b, h, sq, d], k/v: [b, h, sk, d] contiguous CUDA tensors (fp16 or
+    bf16, same dtype and device).  ``scale`` defaults to 1/sqrt(d).  ``o``
+    and ``lse`` may be given (preallocated outputs); otherwise they are
+    allocated with torch.  Returns (o, lse) -- lse is None when
+    ``return_lse`` is False and no ``lse`` was given.
+    """
+    import torch
+    lib = load()
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise AttnError(-2, "q, k, v must be 4-D [b, h, s, d]")
+    b, h, sq, d = q.shape
+    sk = k.shape[2]
+    if tuple(k.shape) != (b, h, sk, d) or tuple(v.shape) != (b, h, sk, d):
+        raise AttnError(-2, f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise AttnError(-4, "q, k, v dtypes differ")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise AttnError(-2, f"{name} must be a contiguous CUDA tensor")
+    if scale is None:
+        scale = 1.0 / float(d) ** 0.5
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((b, h, sq), dtype=torch.float32, device=q.device)
+    if o.shape != q.shape or o.dtype != q.dtype or not o.is_contiguous():
+        raise AttnError(-2, "o must be a contiguous tensor shaped and typed like q")
+    if lse is not None and (tuple(lse.shape) != (b, h, sq) or lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise AttnError(-2, "lse must be contiguous fp32 [b, h, sq]")
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                          lse.data_ptr() if lse is not None else None,
+                          b, h, sq, sk, d, int(bool(causal)), float(scale), _dtype_code(q),
+                          _stream_handle(stream, q.device))
+    _check(rc, lib)
+    return o, lse
+
+
+def attn_fwd_host(q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev, o_dev, lse_dev,
+                  causal: bool = False, scale: float | None = None, stream=None):
+    """End-to-end call on host (ideally pinned) tensors through the C ABI:
+    host->device copies, the forward, device->host copies, all enqueued on
+    ``stream``.  The caller synchronises the stream before reading o_host."""
+    import torch
+    lib = load()
+    b, h, sq, d = q_host.shape
+    sk = k_host.shape[2]
+    if scale is None:
+        scale = 1.0 / float(d) ** 0.5
+    with torch.cuda.device(q_dev.device):
+        rc = lib.attn_fwd_host(q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(), o_host.data_ptr(),
+                               lse_host.data_ptr() if lse_host is not None else None,
+                               q_dev.data_ptr(), k_dev.data_ptr(), v_dev.data_ptr(), o_dev.data_ptr(),
+                               lse_dev.data_ptr() if lse_dev is not None else None,
+                               b, h, sq, sk, d, int(bool(causal)), float(scale), _dtype_code(q_host),
+                               _stream_handle(stream, q_dev.device))
+    _check(rc, lib)
+
+
+def status():
+    """(code, block, warp, site) of the device watchdog (synchronises)."""
+    lib = load()
+    out = (ctypes.c_uint32 * 4)()
+    _check(lib.attn_fwd_status(out), lib)
+    return tuple(int(x) for x in out)
+
+
+def status_clear():
+    lib = load()
+    _check(lib.attn_fwd_status_clear(), lib)
+
+
+def watchdog_selftest(q, k, v, o, lse, causal, scale, withheld_load: int, timeout_ms: int):
+    """Run the forward with one K/V load withheld; returns the recorded code."""
+    import torch
+    lib = load()
+    b, h, sq, d = q.shape
+    sk = k.shape[2]
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd_watchdog_selftest(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                            lse.data_ptr() if lse is not None else None,
+                                            b, h, sq, sk, d, int(bool(causal)), float(scale), _dtype_code(q),
+                                            int(withheld_load), int(timeout_ms),
+                                            _stream_handle(None, q.device))
+    return _check(rc, lib)

@@ -1,0 +1,287 @@
+// C ABI of the fused attention forward (declared in include/attn_fwd.h):
+// argument validation, TMA tensor maps, persistent grid sizing, dispatch to
+// the <head_dim, dtype, causal> instances, device watchdog status.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/attn_fwd.h"
+#include "launch.h"
+
+namespace {
+
+using namespace attn;
+
+thread_local std::string g_err;
+
+int fail(int code, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(ATTN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Watchdog status word, one per device that loads this library.
+__device__ uint32_t g_watchdog[4];
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    uint32_t *status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+// Queried once per device, with that device current.
+int device_info(DeviceInfo **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_CUDA, "device ordinal %d out of range", dev);
+    DeviceInfo &di = g_dev[dev];
+    std::call_once(di.once, [&] {
+        cudaError_t r = cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (r == cudaSuccess) r = cudaDeviceGetAttribute(&di.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (r == cudaSuccess) r = cudaDeviceGetAttribute(&di.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (r == cudaSuccess && di.cc_major == 10 && di.cc_minor == 3)
+            r = cudaGetSymbolAddress(reinterpret_cast<void **>(&di.status), g_watchdog);
+        di.err = r;
+    });
+    if (di.err != cudaSuccess) return cuda_fail(di.err, "device query");
+    if (di.cc_major != 10 || di.cc_minor != 3)
+        return fail(ATTN_ERR_ARCH, "device %d is compute capability %d.%d; this library is built for sm_103a only", dev,
+                    di.cc_major, di.cc_minor);
+    *out = &di;
+    return ATTN_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int get_encode(PFN_cuTensorMapEncodeTiled_v12000 *fn)
+{
+    std::call_once(g_encode_once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    if (!g_encode) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled not available from the driver");
+    *fn = g_encode;
+    return ATTN_OK;
+}
+
+// 3-D view [bh, s, d] of a contiguous [b, h, s, d] tensor; box = 128 rows x
+// 64 elements (one 128-byte swizzle panel), so rows past s of each head are
+// zero-filled by the copy engine rather than read from the next head.
+int make_map(CUtensorMap *map, const void *ptr, int dtype, int64_t bh, int64_t s, int64_t d)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    int rc = get_encode(&enc);
+    if (rc != ATTN_OK) return rc;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(s), static_cast<cuuint64_t>(bh)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2), static_cast<cuuint64_t>(s * d * 2)};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                     const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    return ATTN_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr int64_t kMaxSeq = int64_t(1) << 30;
+
+int validate(const void *q, const void *k, const void *v, const void *o, const float *lse, int64_t b, int64_t h,
+             int64_t sq, int64_t sk, int64_t d, float scale, int dtype, bool *nothing)
+{
+    if (b < 0 || h < 0 || sq < 0 || sk < 0)
+        return fail(ATTN_ERR_SHAPE, "negative size: b=%lld h=%lld sq=%lld sk=%lld", (long long)b, (long long)h,
+                    (long long)sq, (long long)sk);
+    if (sq > kMaxSeq || sk > kMaxSeq)
+        return fail(ATTN_ERR_SHAPE, "sequence length above 2^30: sq=%lld sk=%lld", (long long)sq, (long long)sk);
+    if (b > 0 && h >= (int64_t(1) << 31) / b)
+        return fail(ATTN_ERR_SHAPE, "b*h not below 2^31: b=%lld h=%lld", (long long)b, (long long)h);
+    if (d != 64 && d != 128) return fail(ATTN_ERR_HEADDIM, "head dim %lld not supported (64 or 128)", (long long)d);
+    if (dtype != ATTN_FP16 && dtype != ATTN_BF16) return fail(ATTN_ERR_DTYPE, "dtype %d is not fp16 (0) or bf16 (1)", dtype);
+    if (!std::isfinite(scale)) return fail(ATTN_ERR_SCALE, "scale is not finite");
+    *nothing = (b * h * sq == 0);
+    if (*nothing) return ATTN_OK;
+    if (!o) return fail(ATTN_ERR_NULL, "o is NULL");
+    if (sk > 0 && (!q || !k || !v)) return fail(ATTN_ERR_NULL, "q, k or v is NULL");
+    if (!aligned(o, 16) || (sk > 0 && (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16))))
+        return fail(ATTN_ERR_ALIGN, "q, k, v and o must be 16-byte aligned");
+    if (lse && !aligned(lse, 4)) return fail(ATTN_ERR_ALIGN, "lse must be 4-byte aligned");
+    return ATTN_OK;
+}
+
+template <int D, typename T>
+cudaError_t dispatch_causal(const LaunchArgs &a, bool causal)
+{
+    return causal ? launch_fwd<D, T, true>(a) : launch_fwd<D, T, false>(a);
+}
+
+int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_t b, int64_t h, int64_t sq, int64_t sk,
+        int64_t d, int causal, float scale, int dtype, cudaStream_t stream, int withheld_load, uint64_t timeout_ns)
+{
+    bool nothing = false;
+    int rc = validate(q, k, v, o, lse, b, h, sq, sk, d, scale, dtype, &nothing);
+    if (rc != ATTN_OK || nothing) return rc;
+    DeviceInfo *di = nullptr;
+    rc = device_info(&di);
+    if (rc != ATTN_OK) return rc;
+    const int64_t bh = b * h;
+    cudaError_t e;
+    if (sk == 0) {
+        e = (dtype == ATTN_BF16) ? launch_fill_empty<__nv_bfloat16>(o, lse, bh * sq, static_cast<int>(d), stream)
+                                 : launch_fill_empty<__half>(o, lse, bh * sq, static_cast<int>(d), stream);
+        return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "launch (empty keys)");
+    }
+    LaunchArgs a;
+    if ((rc = make_map(&a.q, q, dtype, bh, sq, d)) != ATTN_OK) return rc;
+    if ((rc = make_map(&a.k, k, dtype, bh, sk, d)) != ATTN_OK) return rc;
+    if ((rc = make_map(&a.v, v, dtype, bh, sk, d)) != ATTN_OK) return rc;
+    FwdParams &p = a.p;
+    p.o = o;
+    p.lse = lse;
+    p.status = di->status;
+    p.bh = static_cast<int32_t>(bh);
+    p.sq = static_cast<int32_t>(sq);
+    p.sk = static_cast<int32_t>(sk);
+    p.num_mblk = static_cast<int32_t>((sq + 255) / 256);
+    const int64_t units = bh * p.num_mblk;
+    if (units > INT32_MAX) return fail(ATTN_ERR_SHAPE, "too many work units (%lld)", (long long)units);
+    p.num_units = static_cast<int32_t>(units);
+    p.sl2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    p.timeout_ns = timeout_ns;
+    p.withheld_load = withheld_load;
+    a.grid = static_cast<int>(units < di->sm_count ? units : di->sm_count);
+    a.stream = stream;
+    const bool c = causal != 0;
+    if (d == 64)
+        e = (dtype == ATTN_BF16) ? dispatch_causal<64, __nv_bfloat16>(a, c) : dispatch_causal<64, __half>(a, c);
+    else
+        e = (dtype == ATTN_BF16) ? dispatch_causal<128, __nv_bfloat16>(a, c) : dispatch_causal<128, __half>(a, c);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return ATTN_OK;
+}
+
+constexpr uint64_t kDefaultTimeoutNs = 2000ull * 1000ull * 1000ull;  // 2 s per wait
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t b, int64_t h, int64_t sq,
+             int64_t sk, int64_t d, int causal, float scale, int dtype, void *stream)
+{
+    g_err.clear();
+    return run(q, k, v, o, lse, b, h, sq, sk, d, causal, scale, dtype, static_cast<cudaStream_t>(stream), -1,
+               kDefaultTimeoutNs);
+}
+
+int attn_fwd_host(const void *q_host, const void *k_host, const void *v_host, void *o_host, float *lse_host,
+                  void *q_dev, void *k_dev, void *v_dev, void *o_dev, float *lse_dev, int64_t b, int64_t h, int64_t sq,
+                  int64_t sk, int64_t d, int causal, float scale, int dtype, void *stream)
+{
+    g_err.clear();
+    bool nothing = false;
+    int rc = validate(q_dev, k_dev, v_dev, o_dev, lse_dev, b, h, sq, sk, d, scale, dtype, &nothing);
+    if (rc != ATTN_OK || nothing) return rc;
+    if (!o_host || (sk > 0 && (!q_host || !k_host || !v_host)))
+        return fail(ATTN_ERR_NULL, "a host buffer is NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t qbytes = static_cast<size_t>(b * h * sq * d) * 2;
+    const size_t kvbytes = static_cast<size_t>(b * h * sk * d) * 2;
+    cudaError_t e;
+    if (sk > 0) {
+        if ((e = cudaMemcpyAsync(q_dev, q_host, qbytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+            return cuda_fail(e, "copy q to device");
+        if ((e = cudaMemcpyAsync(k_dev, k_host, kvbytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+            return cuda_fail(e, "copy k to device");
+        if ((e = cudaMemcpyAsync(v_dev, v_host, kvbytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+            return cuda_fail(e, "copy v to device");
+    }
+    rc = run(q_dev, k_dev, v_dev, o_dev, lse_dev, b, h, sq, sk, d, causal, scale, dtype, st, -1, kDefaultTimeoutNs);
+    if (rc != ATTN_OK) return rc;
+    if ((e = cudaMemcpyAsync(o_host, o_dev, qbytes, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+        return cuda_fail(e, "copy o to host");
+    if (lse_host && lse_dev &&
+        (e = cudaMemcpyAsync(lse_host, lse_dev, static_cast<size_t>(b * h * sq) * 4, cudaMemcpyDeviceToHost, st)) !=
+            cudaSuccess)
+        return cuda_fail(e, "copy lse to host");
+    return ATTN_OK;
+}
+
+const char *attn_last_error(void) { return g_err.c_str(); }
+
+int attn_fwd_status(uint32_t *out)
+{
+    g_err.clear();
+    DeviceInfo *di = nullptr;
+    int rc = device_info(&di);
+    if (rc != ATTN_OK) return rc;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    uint32_t w[4];
+    e = cudaMemcpy(w, di->status, sizeof(w), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read watchdog status");
+    if (out) memcpy(out, w, sizeof(w));
+    return static_cast<int>(w[0]);
+}
+
+int attn_fwd_status_clear(void)
+{
+    g_err.clear();
+    DeviceInfo *di = nullptr;
+    int rc = device_info(&di);
+    if (rc != ATTN_OK) return rc;
+    cudaError_t e = cudaMemset(di->status, 0, 4 * sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "clear watchdog status");
+}
+
+int attn_fwd_watchdog_selftest(const void *q, const void *k, const void *v, void *o, float *lse, int64_t b, int64_t h,
+                               int64_t sq, int64_t sk, int64_t d, int causal, float scale, int dtype, int withheld_load,
+                               int timeout_ms, void *stream)
+{
+    g_err.clear();
+    if (timeout_ms <= 0 || timeout_ms > 10000) return fail(ATTN_ERR_SHAPE, "timeout_ms must be in 1..10000");
+    if (withheld_load < 0) return fail(ATTN_ERR_SHAPE, "withheld_load must be >= 0");
+    if (b < 0 || h < 0 || sq < 0 || b * h * sq > 4096 || sk > 1024)
+        return fail(ATTN_ERR_SHAPE, "self-test wants a tiny problem");
+    int rc = attn_fwd_status_clear();
+    if (rc != ATTN_OK) return rc;
+    rc = run(q, k, v, o, lse, b, h, sq, sk, d, causal, scale, dtype, static_cast<cudaStream_t>(stream), withheld_load,
+             static_cast<uint64_t>(timeout_ms) * 1000000ull);
+    if (rc != ATTN_OK) return rc;
+    return attn_fwd_status(nullptr);
+}
+
+const char *attn_version(void) { return "attn_fwd sm_103a 0.1"; }
+
+}  // extern "C"

@@ -1,0 +1,516 @@
+// Fused attention forward for sm_103a (GB300): TMA + mbarrier ring +
+// tcgen05.mma into tensor memory, online exp2 softmax with lazy rescaling.
+//
+// What is computed: O = softmax(scale * Q K^T [+ causal mask]) V and the
+// natural log-sum-exp per row ("flash-attn 实现 prefill 阶段", 问题分析:
+// attention formula over [b, h, s, d]; flash-attention-minimal
+// forward_kernel: scale after the dot product, online recurrence with a
+// running row max m and row sum l, O rescaled when m changes).
+//
+// How (one persistent CTA per SM, 10 warps):
+//   warps 0-3  softmax group 0  -- Q tile 0 (rows 0..127 of the unit)
+//   warps 4-7  softmax group 1  -- Q tile 1 (rows 128..255 of the unit)
+//   warp  8    MMA issuer (one thread) + tensor-memory owner
+//   warp  9    TMA producer (one thread)
+// A work unit is (batch*head, 256-row block).  Per unit the producer loads
+// the two Q tiles once and streams K_j, V_j tiles (128 keys each) through an
+// NSLOT-deep shared-memory ring.  The MMA thread computes S_t = Q_t K_j^T
+// into tensor memory (128 lanes x 128 fp32 columns per tile), waits for the
+// softmax group to overwrite S_t in place with P_t (rounded to the input
+// type, two per 32-bit column), then issues O_t += P_t V_j with P read from
+// tensor memory.  The two Q tiles alternate so that one group's softmax runs
+// while the tensor core works on the other tile.  Each softmax thread owns
+// one row (one tensor-memory lane): no cross-thread reductions.
+//
+// Softmax (per row, log2 domain): x = s * scale * log2(e); m_new =
+// max(m, rowmax x).  O and l are rescaled by 2^(m - m_new) only when
+// m_new - m > 8 for some row of the warp (lazy rescale; the stale max cancels
+// exactly between O and l, and p = 2^(x - m) stays <= 256).  Epilogue:
+// O / l rounded to the input type; LSE = (m + log2 l) * ln 2.
+//
+// Every wait is bounded: when a wait runs out the kernel records where in a
+// status word, tells the other warps, waits for its own copies and MMAs,
+// frees tensor memory and returns.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <type_traits>
+
+#include "ptx.cuh"
+
+namespace attn {
+
+struct FwdParams {
+    void *o;               // [bh, sq, D] of T
+    float *lse;            // [bh, sq] or nullptr
+    uint32_t *status;      // 4 words: code, block, warp, site
+    int32_t bh;            // b * h
+    int32_t sq, sk;
+    int32_t num_mblk;      // ceil(sq / 256)
+    int32_t num_units;     // bh * num_mblk
+    float sl2e;            // scale * log2(e)
+    uint64_t timeout_ns;   // bound of every wait
+    int32_t withheld_load; // K/V load index never issued (watchdog self-test), -1 = none
+};
+
+// Watchdog sites (recorded in status[3]).
+enum : uint32_t {
+    SITE_LOAD_Q_EMPTY = 1,
+    SITE_LOAD_KV_EMPTY = 2,
+    SITE_MMA_Q_FULL = 3,
+    SITE_MMA_KV_FULL = 4,
+    SITE_MMA_P_FULL = 5,
+    SITE_SOFTMAX_S_FULL = 6,
+    SITE_SOFTMAX_O_FULL = 7,
+    SITE_DRAIN = 8,
+};
+
+template <int D_>
+struct Cfg {
+    static constexpr int D = D_;
+    static constexpr int BM = 128;                 // rows per Q tile = TMEM lanes
+    static constexpr int QT = 2;                   // Q tiles per unit
+    static constexpr int UNIT_ROWS = BM * QT;      // 256
+    static constexpr int BN = 128;                 // keys per K/V tile
+    static constexpr int PANEL_ELEMS = 64;         // 128-byte swizzle panel (16-bit elems)
+    static constexpr int NPANEL = D / PANEL_ELEMS;
+    static constexpr int PANEL_BYTES = 128 * 128;  // 128 rows x 128 B
+    static constexpr int TILE_BYTES = NPANEL * PANEL_BYTES;  // one Q, K or V tile
+    static constexpr int NSLOT = (D == 128) ? 5 : 8;
+    static constexpr int CTL_BYTES = 1024;
+    static constexpr int Q_OFF = CTL_BYTES;
+    static constexpr int KV_OFF = Q_OFF + QT * TILE_BYTES;
+    static constexpr int SMEM_BYTES = KV_OFF + NSLOT * TILE_BYTES + 1024;  // +1 KiB for alignment
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int TMEM_S = 0;               // S_t at column t*BN (P_t aliases it)
+    static constexpr int TMEM_O = QT * BN;         // O_t at TMEM_O + t*D
+    static constexpr int THREADS = 320;
+    static constexpr float TAU = 8.0f;             // lazy-rescale threshold (log2 units)
+    static_assert(TMEM_O + QT * D <= TMEM_COLS, "tensor memory budget");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+struct Ctl {
+    uint64_t q_full[2], q_empty[2];
+    uint64_t kv_full[8], kv_empty[8];
+    uint64_t s_full[2], p_full[2], o_full[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    uint32_t abort;
+};
+static_assert(sizeof(Ctl) <= 1024, "control block");
+
+struct Unit {
+    int bh, row0, n;
+};
+
+template <int D, bool CAUSAL>
+__device__ __forceinline__ Unit decode_unit(int u, const FwdParams &p)
+{
+    using C = Cfg<D>;
+    Unit un;
+    int mblk;
+    if (CAUSAL) {  // heaviest row blocks first
+        mblk = p.num_mblk - 1 - u / p.bh;
+        un.bh = u % p.bh;
+    } else {       // consecutive units share a head (K/V reuse in L2)
+        un.bh = u / p.num_mblk;
+        mblk = u % p.num_mblk;
+    }
+    un.row0 = mblk * C::UNIT_ROWS;
+    int last = min(un.row0 + C::UNIT_ROWS - 1, p.sq - 1);
+    int kend = CAUSAL ? min(p.sk, last + 1 + (p.sk - p.sq)) : p.sk;
+    un.n = kend > 0 ? (kend + C::BN - 1) / C::BN : 0;
+    return un;
+}
+
+static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl *ctl, const FwdParams &p,
+                                              uint32_t site, bool honour_abort)
+{
+    volatile uint32_t *abort_flag = &ctl->abort;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (honour_abort && *abort_flag) return false;
+        if (global_timer_ns() - t0 > p.timeout_ns) {
+            *abort_flag = 1u;
+            if (atomicCAS(&p.status[0], 0u, 1u) == 0u) {
+                p.status[1] = blockIdx.x;
+                p.status[2] = threadIdx.x >> 5;
+                p.status[3] = site;
+                __threadfence();
+            }
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, Ctl *ctl, const FwdParams &p,
+                                         uint32_t site)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, ctl, p, site, true);
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi)
+{
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+template <typename T>
+__device__ __forceinline__ void store_row_zero(const FwdParams &p, int bh, int row, int D)
+{
+    if (row >= p.sq) return;
+    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.o) + (static_cast<size_t>(bh) * p.sq + row) * D);
+    for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+    if (p.lse) p.lse[static_cast<size_t>(bh) * p.sq + row] = -INFINITY;
+}
+
+template <int D, typename T, bool CAUSAL>
+__global__ void __launch_bounds__(320, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const FwdParams p)
+{
+    using C = Cfg<D>;
+    constexpr bool BF16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t IDESC_QK = idesc_f16(128, C::BN, BF16, false);
+    constexpr uint32_t IDESC_PV = idesc_f16(128, D, BF16, true);
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base_addr - raw_addr);
+    Ctl *ctl = reinterpret_cast<Ctl *>(smem);
+    const uint32_t sQ = base_addr + C::Q_OFF;    // Q tile t at sQ + t*TILE_BYTES
+    const uint32_t sKV = base_addr + C::KV_OFF;  // slot s at sKV + s*TILE_BYTES
+
+    auto B = [&](const uint64_t &bar) { return smem_addr(&bar); };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(B(ctl->q_full[t]), 1);
+            mbar_init(B(ctl->q_empty[t]), 1);
+            mbar_init(B(ctl->s_full[t]), 1);
+            mbar_init(B(ctl->p_full[t]), 128);
+            mbar_init(B(ctl->o_full[t]), 1);
+        }
+        for (int s = 0; s < C::NSLOT; ++s) {
+            mbar_init(B(ctl->kv_full[s]), 1);
+            mbar_init(B(ctl->kv_empty[s]), 1);
+        }
+        mbar_init(B(ctl->mma_done), 1);
+        ctl->abort = 0u;
+        fence_barrier_init();
+    }
+    if (warp == 8) {
+        tmem_alloc(smem_addr(&ctl->tmem_base), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 9 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+
+    if (warp == 9) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t kv_it = 0, q_it = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+                const Unit un = decode_unit<D, CAUSAL>(u, p);
+                if (un.n == 0) continue;
+                for (int t = 0; t < C::QT && ok; ++t) {
+                    ok = bar_wait(B(ctl->q_empty[t]), (q_it & 1u) ^ 1u, ctl, p, SITE_LOAD_Q_EMPTY);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(B(ctl->q_full[t]), C::TILE_BYTES);
+                    for (int pn = 0; pn < C::NPANEL; ++pn)
+                        tma_load_3d(sQ + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tmQ, B(ctl->q_full[t]),
+                                    pn * C::PANEL_ELEMS, un.row0 + t * C::BM, un.bh);
+                }
+                if (!ok) break;
+                ++q_it;
+                for (int j = 0; j < un.n && ok; ++j) {
+                    for (int which = 0; which < 2; ++which) {
+                        const uint32_t slot = kv_it % C::NSLOT;
+                        ok = bar_wait(B(ctl->kv_empty[slot]), ((kv_it / C::NSLOT) & 1u) ^ 1u, ctl, p,
+                                      SITE_LOAD_KV_EMPTY);
+                        if (!ok) break;
+                        if (static_cast<int32_t>(kv_it) != p.withheld_load) {
+                            mbar_arrive_expect_tx(B(ctl->kv_full[slot]), C::TILE_BYTES);
+                            const CUtensorMap *m = which ? &tmV : &tmK;
+                            for (int pn = 0; pn < C::NPANEL; ++pn)
+                                tma_load_3d(sKV + slot * C::TILE_BYTES + pn * C::PANEL_BYTES, m,
+                                            B(ctl->kv_full[slot]), pn * C::PANEL_ELEMS, j * C::BN, un.bh);
+                        }
+                        ++kv_it;
+                    }
+                }
+            }
+            if (!ok || *reinterpret_cast<volatile uint32_t *>(&ctl->abort)) {
+                // Wind-down: wait (bounded) for every copy this thread issued
+                // and nobody consumed, so no copy lands after the CTA exits.
+                const uint32_t first = kv_it > C::NSLOT ? kv_it - C::NSLOT : 0u;
+                for (uint32_t i = first; i < kv_it; ++i) {
+                    if (static_cast<int32_t>(i) == p.withheld_load) continue;
+                    wait_slow(B(ctl->kv_full[i % C::NSLOT]), (i / C::NSLOT) & 1u, ctl, p, SITE_DRAIN, false);
+                }
+                if (q_it > 0)
+                    for (int t = 0; t < C::QT; ++t)
+                        wait_slow(B(ctl->q_full[t]), (q_it - 1) & 1u, ctl, p, SITE_DRAIN, false);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 8) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t kv_it = 0, q_it = 0;
+            uint32_t p_ph[2] = {0u, 0u};
+            bool ok = true;
+            auto kv_wait = [&](uint32_t &slot) -> bool {
+                slot = kv_it % C::NSLOT;
+                bool r = bar_wait(B(ctl->kv_full[slot]), (kv_it / C::NSLOT) & 1u, ctl, p, SITE_MMA_KV_FULL);
+                ++kv_it;
+                return r;
+            };
+            auto issue_qk = [&](int t, uint32_t kslot) {
+                const uint32_t a0 = sQ + t * C::TILE_BYTES;
+                const uint32_t b0 = sKV + kslot * C::TILE_BYTES;
+                const uint32_t d = tmem + C::TMEM_S + t * C::BN;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
+                    mma_ss(d, smem_desc_sw128(a0 + off, 16, 1024), smem_desc_sw128(b0 + off, 16, 1024), IDESC_QK,
+                           kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int t, uint32_t vslot, bool accumulate) {
+                const uint32_t b0 = sKV + vslot * C::TILE_BYTES;
+                const uint32_t a = tmem + C::TMEM_S + t * C::BN;  // P_t, 2 elements per column
+                const uint32_t d = tmem + C::TMEM_O + t * D;
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk)
+                    mma_ts(d, a + kk * 8, smem_desc_sw128(b0 + kk * 16 * 128, C::PANEL_BYTES, 1024), IDESC_PV,
+                           (accumulate || kk > 0) ? 1u : 0u);
+            };
+            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+                const Unit un = decode_unit<D, CAUSAL>(u, p);
+                if (un.n == 0) continue;
+                for (int t = 0; t < C::QT && ok; ++t)
+                    ok = bar_wait(B(ctl->q_full[t]), q_it & 1u, ctl, p, SITE_MMA_Q_FULL);
+                if (!ok) break;
+                ++q_it;
+                uint32_t kslot;
+                if (!(ok = kv_wait(kslot))) break;
+                tc_fence_after();
+                issue_qk(0, kslot);
+                tc_commit(B(ctl->s_full[0]));
+                issue_qk(1, kslot);
+                tc_commit(B(ctl->s_full[1]));
+                tc_commit(B(ctl->kv_empty[kslot]));
+                if (un.n == 1) {
+                    tc_commit(B(ctl->q_empty[0]));
+                    tc_commit(B(ctl->q_empty[1]));
+                }
+                for (int j = 0; j < un.n && ok; ++j) {
+                    const bool more = j + 1 < un.n;
+                    uint32_t vslot, nslot = 0;
+                    if (!(ok = kv_wait(vslot))) break;
+                    if (more && !(ok = kv_wait(nslot))) break;
+                    // tile 0
+                    if (!(ok = bar_wait(B(ctl->p_full[0]), p_ph[0], ctl, p, SITE_MMA_P_FULL))) break;
+                    p_ph[0] ^= 1u;
+                    tc_fence_after();
+                    issue_pv(0, vslot, j > 0);
+                    if (!more) tc_commit(B(ctl->o_full[0]));
+                    if (more) {
+                        issue_qk(0, nslot);
+                        tc_commit(B(ctl->s_full[0]));
+                        if (j + 2 == un.n) tc_commit(B(ctl->q_empty[0]));
+                    }
+                    // tile 1
+                    if (!(ok = bar_wait(B(ctl->p_full[1]), p_ph[1], ctl, p, SITE_MMA_P_FULL))) break;
+                    p_ph[1] ^= 1u;
+                    tc_fence_after();
+                    issue_pv(1, vslot, j > 0);
+                    tc_commit(B(ctl->kv_empty[vslot]));
+                    if (!more) tc_commit(B(ctl->o_full[1]));
+                    if (more) {
+                        issue_qk(1, nslot);
+                        tc_commit(B(ctl->s_full[1]));
+                        tc_commit(B(ctl->kv_empty[nslot]));
+                        if (j + 2 == un.n) tc_commit(B(ctl->q_empty[1]));
+                    }
+                }
+            }
+            // Every MMA issued must complete before tensor memory is freed.
+            tc_commit(B(ctl->mma_done));
+            wait_slow(B(ctl->mma_done), 0u, ctl, p, SITE_DRAIN, false);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax groups
+        const int t = warp >> 2;      // Q tile of this group
+        const int quad = warp & 3;    // TMEM lane quadrant this warp may access
+        const int r_in_tile = quad * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tS = tmem + lane_off + C::TMEM_S + t * C::BN;
+        const uint32_t tO = tmem + lane_off + C::TMEM_O + t * D;
+        const float sl2e = p.sl2e;
+        uint32_t s_ph = 0u, o_ph = 0u;
+        bool ok = true;
+        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+            const Unit un = decode_unit<D, CAUSAL>(u, p);
+            const int row = un.row0 + t * C::BM + r_in_tile;
+            if (un.n == 0) {
+                store_row_zero<T>(p, un.bh, row, D);
+                continue;
+            }
+            // keys visible to this row: [0, kend)
+            const int kend = CAUSAL ? min(p.sk, row + 1 + (p.sk - p.sq)) : p.sk;
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < un.n; ++j) {
+                bool w = bar_wait(B(ctl->s_full[t]), s_ph, ctl, p, SITE_SOFTMAX_S_FULL);
+                ok = __all_sync(0xffffffffu, w);
+                if (!ok) break;
+                s_ph ^= 1u;
+                tc_fence_after();
+                uint32_t sr[128];
+                tmem_ld128_wait(tS, sr);
+                float x[128];
+#pragma unroll
+                for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]) * sl2e;
+                const int lim = kend - j * C::BN;  // columns >= lim are masked
+                if (lim < C::BN) {
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) x[c] = (c < lim) ? x[c] : -INFINITY;
+                }
+                float mx8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = x[i];
+#pragma unroll
+                for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                const float m_new = fmaxf(m, mx);
+                if (j > 0) {
+                    const bool need = (m_new - m) > C::TAU;
+                    if (__any_sync(0xffffffffu, need)) {
+                        const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m - m_new);
+#pragma unroll
+                        for (int ch = 0; ch < D / 32; ++ch) {
+                            uint32_t orr[32];
+                            tmem_ld32_wait(tO + ch * 32, orr);
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
+                            tmem_st32(tO + ch * 32, orr);
+                        }
+                        l *= alpha;
+                        m = m_new;
+                    }
+                } else {
+                    m = m_new;
+                }
+                const float m_use = (m == -INFINITY) ? 0.f : m;
+                float sum8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) sum8[i] = 0.f;
+                uint32_t pa[32], pb[32];
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const float p0 = ex2_approx(x[2 * c] - m_use);
+                    const float p1 = ex2_approx(x[2 * c + 1] - m_use);
+                    sum8[(2 * c) & 7] += p0;
+                    sum8[(2 * c + 1) & 7] += p1;
+                    if (c < 32)
+                        pa[c] = pack2<T>(p0, p1);
+                    else
+                        pb[c - 32] = pack2<T>(p0, p1);
+                }
+                l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+                tmem_st32(tS, pa);
+                tmem_st32(tS + 32, pb);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(B(ctl->p_full[t]));
+            }
+            if (!ok) break;
+            // ---- epilogue: O / l -> T, LSE
+            {
+                bool w = bar_wait(B(ctl->o_full[t]), o_ph, ctl, p, SITE_SOFTMAX_O_FULL);
+                ok = __all_sync(0xffffffffu, w);
+                if (!ok) break;
+                o_ph ^= 1u;
+                tc_fence_after();
+                const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+                const bool valid = row < p.sq;
+                uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.o) +
+                                                       (static_cast<size_t>(un.bh) * p.sq + (valid ? row : 0)) * D);
+#pragma unroll
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t orr[32];
+                    tmem_ld32_wait(tO + ch * 32, orr);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        pk[c] = pack2<T>(__uint_as_float(orr[2 * c]) * inv_l, __uint_as_float(orr[2 * c + 1]) * inv_l);
+                    if (valid) {
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            dst[ch * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                    }
+                }
+                if (valid && p.lse)
+                    p.lse[static_cast<size_t>(un.bh) * p.sq + row] =
+                        (l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                tc_fence_before();
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// sk == 0: every row sees no key.  O = 0, LSE = -inf.
+template <typename T>
+__global__ void attn_fill_empty_kernel(T *o, float *lse, int64_t rows, int d)
+{
+    const int64_t n = rows * d;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        o[i] = T(0.f);
+    if (lse)
+        for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < rows;
+             i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+            lse[i] = -INFINITY;
+}
+
+}  // namespace attn

@@ -1,0 +1,54 @@
+// Internal launch interface between the C-ABI layer and the kernel
+// instantiations (one translation unit per group of instances so that the
+// build compiles them in parallel).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "attn_fwd_kernel.cuh"
+
+namespace attn {
+
+struct LaunchArgs {
+    CUtensorMap q, k, v;
+    FwdParams p;
+    int grid;
+    cudaStream_t stream;
+};
+
+template <int D, typename T, bool CAUSAL>
+cudaError_t launch_fwd(const LaunchArgs &a)
+{
+    constexpr int smem = Cfg<D>::SMEM_BYTES;
+    auto kern = attn_fwd_kernel<D, T, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<a.grid, Cfg<D>::THREADS, smem, a.stream>>>(a.q, a.k, a.v, a.p);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_fill_empty(void *o, float *lse, int64_t rows, int d, cudaStream_t stream)
+{
+    int64_t n = rows * d;
+    int blocks = static_cast<int>((n + 255) / 256);
+    if (blocks > 4096) blocks = 4096;
+    if (blocks < 1) blocks = 1;
+    attn_fill_empty_kernel<T><<<blocks, 256, 0, stream>>>(static_cast<T *>(o), lse, rows, d);
+    return cudaGetLastError();
+}
+
+#define ATTN_DECLARE_INSTANCE(D, T, C) extern template cudaError_t launch_fwd<D, T, C>(const LaunchArgs &);
+#define ATTN_DEFINE_INSTANCE(D, T, C) template cudaError_t launch_fwd<D, T, C>(const LaunchArgs &);
+
+ATTN_DECLARE_INSTANCE(64, __half, false)
+ATTN_DECLARE_INSTANCE(64, __half, true)
+ATTN_DECLARE_INSTANCE(64, __nv_bfloat16, false)
+ATTN_DECLARE_INSTANCE(64, __nv_bfloat16, true)
+ATTN_DECLARE_INSTANCE(128, __half, false)
+ATTN_DECLARE_INSTANCE(128, __half, true)
+ATTN_DECLARE_INSTANCE(128, __nv_bfloat16, false)
+ATTN_DECLARE_INSTANCE(128, __nv_bfloat16, true)
+
+}  // namespace attn

@@ -1,0 +1,106 @@
+"""Seeded synthetic inputs for the attention forward.
+
+This module is shared by the tests, the benchmark and the smoke check; it
+holds no attention arithmetic, only shapes, seeds and random draws, so that the
+CUDA path and the fp64 oracle always see the same inputs.  It imports nothing
+from the rest of the package.
+
+Recipe: a CPU ``torch.Generator`` seeded per workload draws Q, K, V in that
+order with ``randn`` in fp32 (Q and K multiplied by ``qk_std``), then each is
+rounded to the workload dtype.  The oracle consumes the rounded values, so
+input quantisation is not counted as kernel error.  The shapes follow the
+[b, h, s, d] layout of "flash-attn 实现 prefill 阶段" (问题分析); the scale is
+1/sqrt(d) as in flash-attention-minimal ``forward()``.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16}
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    b: int
+    h: int
+    sq: int
+    sk: int
+    d: int
+    dtype: str
+    causal: bool
+    qk_std: float
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return DTYPES[self.dtype]
+
+    def flops(self) -> float:
+        """Counted work: 4*b*h*sq*sk*d, half of it when causal."""
+        f = 4.0 * self.b * self.h * self.sq * self.sk * self.d
+        return f * 0.5 if self.causal else f
+
+    def bytes(self) -> int:
+        """Algorithmic HBM bytes: Q, K, V read once, O written once, fp32 LSE."""
+        e = 2
+        return (e * self.b * self.h * (2 * self.sq * self.d + 2 * self.sk * self.d)
+                + 4 * self.b * self.h * self.sq)
+
+
+# The five workloads the project is measured on, named by what they are.
+WORKLOADS = {
+    w.name: w for w in [
+        Workload("noncausal_b1_h2_s256_d128_fp16", 1, 2, 256, 256, 128, "fp16", False, 1.0, 20260000),
+        Workload("noncausal_b4_h16_s1024_d128_fp16", 4, 16, 1024, 1024, 128, "fp16", False, 1.0, 20260001),
+        Workload("noncausal_b8_h16_s1000_d64_bf16", 8, 16, 1000, 1000, 64, "bf16", False, 1.0, 20260002),
+        Workload("causal_b2_h32_s4096_d128_bf16", 2, 32, 4096, 4096, 128, "bf16", True, 1.0, 20260003),
+        Workload("causal_b1_h32_s16384_d128_bf16_qk3", 1, 32, 16384, 16384, 128, "bf16", True, 3.0, 20260004),
+    ]
+}
+ORDER = list(WORKLOADS)
+HEADLINE = "causal_b1_h32_s16384_d128_bf16_qk3"
+
+
+def draw(b, h, sq, sk, d, dtype, seed, qk_std=1.0, v_std=1.0):
+    """Seeded Q [b,h,sq,d], K/V [b,h,sk,d] as CPU tensors of ``dtype``."""
+    tdt = DTYPES[dtype] if isinstance(dtype, str) else dtype
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    q = torch.randn((b, h, sq, d), generator=g, dtype=torch.float32)
+    k = torch.randn((b, h, sk, d), generator=g, dtype=torch.float32)
+    v = torch.randn((b, h, sk, d), generator=g, dtype=torch.float32)
+    if qk_std != 1.0:
+        q.mul_(qk_std)
+        k.mul_(qk_std)
+    if v_std != 1.0:
+        v.mul_(v_std)
+    return q.to(tdt), k.to(tdt), v.to(tdt)
+
+
+def inputs(w: Workload):
+    """CPU tensors (q, k, v) of the workload."""
+    return draw(w.b, w.h, w.sq, w.sk, w.d, w.dtype, w.seed, w.qk_std)
+
+
+def sample_heads(w: Workload, n: int = 4, seed: int = 7):
+    """Seeded sample of (batch, head) pairs, always including the first and
+    the last pair."""
+    pairs = [(0, 0)]
+    if (w.b - 1, w.h - 1) != (0, 0):
+        pairs.append((w.b - 1, w.h - 1))
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    while len(pairs) < min(n, w.b * w.h):
+        bi = int(torch.randint(0, w.b, (1,), generator=g))
+        hi = int(torch.randint(0, w.h, (1,), generator=g))
+        if (bi, hi) not in pairs:
+            pairs.append((bi, hi))
+    return pairs

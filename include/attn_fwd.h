@@ -1,0 +1,136 @@
+/*
+ * attn_fwd.h -- C ABI of the GB300 (sm_103a) fused attention forward.
+ *
+ * Operation (all entry points):
+ *   O[b, h, i, :] = sum_j P[i, j] V[b, h, j, :],
+ *   P[i, :] = softmax_j(scale * Q[b, h, i, :] . K[b, h, j, :]  [+ causal mask])
+ *   LSE[b, h, i] = ln sum_j exp(scale * Q[b, h, i, :] . K[b, h, j, :])   (visible j)
+ * This is the attention formula of "flash-attn 实现 prefill 阶段" (问题分析),
+ * over [b, h, s, d] tensors as laid out there, with the scale applied after
+ * the dot product and a natural-exponent softmax as in flash-attention-minimal
+ * forward_kernel; it is computed with the online-softmax recurrence of that
+ * kernel (running row max m and row sum l, O rescaled as K/V tiles arrive),
+ * so S and P never reach memory.
+ *
+ * Causal mask ("05 · kernel 工程与四代演化", 2.1 names `causal` without
+ * defining it): bottom-right aligned -- key j is visible to query i iff
+ * j <= i + (sk - sq); for sq == sk this is j <= i.  A query row that sees no
+ * key gets O = 0 and LSE = -inf.
+ *
+ * Layout: Q and O are contiguous [b, h, sq, d]; K and V are contiguous
+ * [b, h, sk, d]; all four have the element type `dtype` (fp16 or bf16).
+ * LSE is contiguous fp32 [b, h, sq].  d must be 64 or 128.
+ *
+ * Ownership: every pointer is owned by the caller.  attn_fwd allocates
+ * nothing and keeps no reference after it returns.
+ *
+ * Execution: attn_fwd enqueues its work on `stream` (a cudaStream_t, NULL =
+ * legacy default stream) of the current device and returns without
+ * synchronising; results are ready when the stream reaches that point.  It
+ * may be called from several host threads on different streams.
+ *
+ * Errors: a negative return code, never an exception or abort.  The message
+ * of the last failing call on the calling thread is given by
+ * attn_last_error().  Argument errors are detected before anything is
+ * enqueued.  Precision: fp32 accumulation and statistics; P is rounded to
+ * `dtype` before the P.V product; O is rounded to nearest-even into `dtype`.
+ */
+#ifndef ATTN_FWD_H
+#define ATTN_FWD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { ATTN_FP16 = 0, ATTN_BF16 = 1 } attn_dtype_t;
+
+enum {
+    ATTN_OK = 0,
+    ATTN_ERR_NULL = -1,    /* a required pointer is NULL                       */
+    ATTN_ERR_SHAPE = -2,   /* negative or too large b, h, sq, sk               */
+    ATTN_ERR_HEADDIM = -3, /* d is not 64 or 128                               */
+    ATTN_ERR_DTYPE = -4,   /* dtype is not ATTN_FP16 / ATTN_BF16               */
+    ATTN_ERR_SCALE = -5,   /* scale is NaN or infinite                         */
+    ATTN_ERR_ALIGN = -6,   /* q/k/v/o not 16-byte aligned, lse not 4-byte     */
+    ATTN_ERR_ARCH = -7,    /* current device is not compute capability 10.3   */
+    ATTN_ERR_CUDA = -8,    /* a CUDA runtime/driver call failed                */
+    ATTN_ERR_WATCHDOG = -9 /* a device-side wait gave up (see attn_fwd_status) */
+};
+
+/*
+ * attn_fwd: the fused forward.
+ *   q, k, v : device pointers, layout above, 16-byte aligned.
+ *   o       : device pointer, [b, h, sq, d] of dtype, 16-byte aligned.
+ *   lse     : device pointer to fp32 [b, h, sq], 4-byte aligned, or NULL to
+ *             skip writing it.
+ *   b, h    : batch and heads (>= 0, b*h < 2^31).  sq, sk : query / key
+ *             lengths (0 .. 2^30).  d : head dimension, 64 or 128.
+ *   causal  : 0 = no mask, nonzero = bottom-right causal mask.
+ *   scale   : finite multiplier of Q.K (1/sqrt(d) in the pages' formula).
+ *   dtype   : attn_dtype_t of q, k, v, o.
+ *   stream  : cudaStream_t to enqueue on.
+ * b*h*sq == 0 returns ATTN_OK with nothing enqueued; sk == 0 writes O = 0 and
+ * LSE = -inf.  Returns ATTN_OK or a negative ATTN_ERR_* code.
+ */
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+             int64_t b, int64_t h, int64_t sq, int64_t sk, int64_t d,
+             int causal, float scale, int dtype, void *stream);
+
+/*
+ * attn_fwd_host: attn_fwd for inputs and outputs in HOST memory, with the
+ * host<->device copies on `stream`: copies q_host/k_host/v_host into the
+ * caller's device buffers q_dev/k_dev/v_dev, runs attn_fwd into o_dev/lse_dev,
+ * then copies O (and LSE when both lse pointers are non-NULL) back into
+ * o_host/lse_host.  All buffers are caller-owned with the layouts of
+ * attn_fwd; host buffers should be page-locked for the copies to be
+ * asynchronous.  The call returns once everything is enqueued; the host
+ * outputs are valid after the stream is synchronised.  Same error codes as
+ * attn_fwd (copy failures give ATTN_ERR_CUDA).
+ */
+int attn_fwd_host(const void *q_host, const void *k_host, const void *v_host,
+                  void *o_host, float *lse_host,
+                  void *q_dev, void *k_dev, void *v_dev, void *o_dev,
+                  float *lse_dev,
+                  int64_t b, int64_t h, int64_t sq, int64_t sk, int64_t d,
+                  int causal, float scale, int dtype, void *stream);
+
+/* Thread-local message describing the last non-OK return on this thread
+ * ("" if none).  The pointer stays valid until the next call on the thread. */
+const char *attn_last_error(void);
+
+/*
+ * Device watchdog.  Every wait inside the kernels is bounded; a wait that
+ * runs out records a nonzero code in a per-device status word and the kernel
+ * winds down (waits for its own copies and MMAs, frees tensor memory) and
+ * returns instead of hanging.  attn_fwd_status synchronises the current
+ * device, copies the status into out[0..3] = {code, block, warp, site} (out
+ * may be NULL) and returns code (0 = no timeout, <0 = CUDA error while
+ * reading).  attn_fwd_status_clear zeroes it.
+ */
+int attn_fwd_status(uint32_t *out);
+int attn_fwd_status_clear(void);
+
+/*
+ * attn_fwd_watchdog_selftest: launches the forward on tiny caller-provided
+ * buffers (same contract as attn_fwd) with the key/value load number
+ * `withheld_load` deliberately never issued and the wait limit set to
+ * `timeout_ms`, so that the waits run out.  It synchronises and returns the
+ * status code the kernel recorded (expected nonzero), or a negative error.
+ * Exists only to test the watchdog without faulting or hanging the GPU.
+ */
+int attn_fwd_watchdog_selftest(const void *q, const void *k, const void *v,
+                               void *o, float *lse, int64_t b, int64_t h,
+                               int64_t sq, int64_t sk, int64_t d, int causal,
+                               float scale, int dtype, int withheld_load,
+                               int timeout_ms, void *stream);
+
+/* Library version string. */
+const char *attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_FWD_H */

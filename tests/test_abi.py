@@ -1,0 +1,85 @@
+"""The C-ABI library loads, exports every declared symbol and rejects bad
+arguments before touching the GPU (CPU only: no compute calls)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import attention_forward_14_gb300 as af
+from attention_forward_14_gb300 import binding
+from attention_forward_14_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn_fwd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return binding.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_expected_entry_points():
+    assert set(declared_functions()) == set(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.attn_version().decode().startswith("attn_fwd sm_103a")
+
+
+def test_library_is_sm103a_only():
+    from attention_forward_14_gb300 import build as b
+    assert b.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+BUF = ctypes.create_string_buffer(4096 + 512)
+P = ctypes.addressof(BUF) + (-ctypes.addressof(BUF)) % 256  # 256-aligned host address
+
+
+def call(lib, q=P, k=P, v=P, o=P, lse=None, b=1, h=1, sq=4, sk=4, d=64, causal=0, scale=0.125, dtype=1):
+    rc = lib.attn_fwd(q, k, v, o, lse, b, h, sq, sk, d, causal, scale, dtype, None)
+    return rc, lib.attn_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), -3), (dict(d=0), -3), (dict(d=256), -3),
+    (dict(dtype=2), -4), (dict(dtype=-1), -4),
+    (dict(b=-1), -2), (dict(sq=-3), -2), (dict(sk=-1), -2), (dict(sq=1 << 31), -2),
+    (dict(b=1 << 16, h=1 << 16), -2),
+    (dict(scale=math.nan), -5), (dict(scale=math.inf), -5),
+    (dict(o=None), -1), (dict(q=None), -1), (dict(k=None), -1), (dict(v=None), -1),
+    (dict(q=P + 8), -6), (dict(o=P + 2), -6), (dict(lse=P + 2), -6),
+])
+def test_argument_errors(lib, kw, code):
+    rc, msg = call(lib, **kw)
+    assert rc == code, (rc, msg)
+    assert msg
+
+
+@pytest.mark.parametrize("kw", [dict(b=0), dict(h=0), dict(sq=0), dict(b=0, q=None, k=None, v=None, o=None)])
+def test_empty_problem_is_ok_without_launch(lib, kw):
+    rc, msg = call(lib, **kw)
+    assert rc == 0 and msg == ""
+
+
+def test_no_device_gives_error_not_crash(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc, msg = call(lib)
+    assert rc in (-7, -8) and msg
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(af.AttnError):
+        binding.load(str(tmp_path / "missing.so"))

@@ -270,9 +270,10 @@ __global__ void __launch_bounds__(320, 1)
                     }
                 }
             }
-            if (!ok || *reinterpret_cast<volatile uint32_t *>(&ctl->abort)) {
-                // Wind-down: wait (bounded) for every copy this thread issued
-                // and nobody consumed, so no copy lands after the CTA exits.
+            {
+                // Wind-down: wait (bounded) for the last copies this thread
+                // issued, so that no copy lands after the CTA exits even when
+                // a consumer gave up (normally these have long completed).
                 const uint32_t first = kv_it > C::NSLOT ? kv_it - C::NSLOT : 0u;
                 for (uint32_t i = first; i < kv_it; ++i) {
                     if (static_cast<int32_t>(i) == p.withheld_load) continue;

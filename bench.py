@@ -1,0 +1,315 @@
+"""Benchmark of the fused attention forward on GB300.
+
+One step = one attn_fwd call over the whole workload (default: the causal
+b=1, h=32, s=16384, d=128 bf16 problem with Q, K ~ N(0, 9)).  Prints one JSON
+line (rank 0).  Work is counted as 4*b*h*sq*sk*d FLOPs, half of it when
+causal; `value` is whole-job TFLOPS over all ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, same metric
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own independent
+problem of the same shape (the forward has no exchange step), so scaling is
+weak; the only collectives are the timing barrier and the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOPS on 1 GB300 (d=128, bf16, causal) and % of dense tensor peak"
+L2_BYTES = 129e6
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(bf16=float(d["bf16_tflops"]), bf16_sustained=float(d["bf16_tflops_sustained"]),
+                    hbm=float(d["hbm_gbs"]), source="measured")
+    return dict(bf16=1900.0, bf16_sustained=1700.0, hbm=6800.0, source="fallback")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_forward_14_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    or None when no summary exists or the kernel sources changed since."""
+    p = os.path.join(ROOT, "profiles", f"attn_fwd_kernel_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(w, q, k, v, target_s: float = 12.0):
+    """The fp64 oracle, as it stands, on the host cores: a bounded sample of
+    query rows of the first head, sized to ~target_s seconds.  Returns
+    (TFLOPS, description, cores, seconds)."""
+    import numpy as np
+    import oracle
+
+    qh, kh, vh = (t[0, 0].double().numpy() for t in (q, k, v))
+    cores = oracle.num_threads()
+
+    def visible(rows):
+        if not w.causal:
+            return np.full(len(rows), w.sk, dtype=np.float64)
+        return np.clip(np.asarray(rows) + 1 + (w.sk - w.sq), 0, w.sk).astype(np.float64)
+
+    def run(rows):
+        t0 = time.perf_counter()
+        oracle.attn_head_rows(qh, kh, vh, rows, w.causal, w.scale)
+        return time.perf_counter() - t0
+
+    rng = np.random.default_rng(w.seed)
+    probe = np.sort(rng.choice(w.sq, size=min(w.sq, 4 * cores), replace=False))
+    dt = run(probe)
+    rate = 4.0 * w.d * visible(probe).sum() / max(dt, 1e-6)  # flop/s of the oracle
+    per_row = 4.0 * w.d * visible(np.arange(w.sq)).mean()
+    n = int(min(w.sq, max(len(probe), target_s * rate / per_row)))
+    rows = np.sort(rng.choice(w.sq, size=n, replace=False))
+    dt = run(rows)
+    flops = 4.0 * w.d * visible(rows).sum()
+    desc = (f"{n} seeded query rows of head (0,0) of {w.name}, each against all its visible keys "
+            f"({flops / 1e9:.1f} GFLOP counted as 4*d per visible key)")
+    return flops / dt / 1e12, desc, cores, dt
+
+
+def bench_reference(args, w):
+    """The oracle arm: each step is one bounded sample (fp64, host cores)."""
+    from attention_forward_14_gb300 import workloads as W
+    q, k, v = W.inputs(w)
+    per = max(1.0, 120.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_baseline(w, q, k, v, target_s=per / 4)
+    vals, descs, times = [], [], []
+    cores = None
+    for _ in range(args.steps):
+        tf, desc, cores, dt = cpu_baseline(w, q, k, v, target_s=per)
+        vals.append(tf)
+        descs.append(desc)
+        times.append(dt)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "b": w.b, "h": w.h, "sq": w.sq, "sk": w.sk, "d": w.d,
+                   "causal": w.causal, "input_dtype": w.dtype},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": descs[-1]},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    from attention_forward_14_gb300 import workloads as W
+    w = W.WORKLOADS[args.workload or W.HEADLINE]
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            bench_reference(args, w)
+        return
+
+    import torch
+    import attention_forward_14_gb300 as af
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    q, k, v = W.inputs(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    in_bytes = 3 * q.numel() * q.element_size() if w.sq == w.sk else (q.numel() + 2 * k.numel()) * q.element_size()
+
+    def step():
+        af.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, o=o, lse=lse, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    t_all0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    sampler.stop()
+    total_ms = t_all0.elapsed_time(t_all1)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+    value = world * w.flops() / (ms * 1e-3) / 1e12
+
+    # end to end through the host-buffer entry point: H2D of Q, K, V from
+    # pinned memory, the forward, D2H of O and LSE, every step.
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    oh = torch.empty_like(qh).pin_memory()
+    lh = torch.empty(q.shape[:3], dtype=torch.float32).pin_memory()
+    for _ in range(2):
+        af.attn_fwd_host(qh, kh, vh, oh, lh, qd, kd, vd, o, lse, causal=w.causal, scale=w.scale, stream=stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        af.attn_fwd_host(qh, kh, vh, oh, lh, qd, kd, vd, o, lse, causal=w.causal, scale=w.scale, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * w.flops() / (e2e_ms * 1e-3) / 1e12
+
+    if rank == 0:
+        peaks = load_peaks()
+        kern_ms = statistics.mean(launch_ms)
+        achieved = w.flops() / (kern_ms * 1e-3) / 1e12
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "fp16", "data": "synthetic",
+            "config": {"workload": w.name, "b": w.b, "h": w.h, "sq": w.sq, "sk": w.sk, "d": w.d,
+                       "causal": w.causal, "qk_std": w.qk_std, "flops_per_step": w.flops(),
+                       "l2": f"inputs {in_bytes / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB, no flush"
+                       if in_bytes > L2_BYTES else "inputs fit in L2 (no flush)"},
+            "pct_of_peak": 100.0 * value / world / peaks["bf16"],
+            "pct_of_sustained_peak": 100.0 * value / world / peaks["bf16_sustained"],
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                         "frac": achieved / peaks["bf16"], "traffic": profiled_traffic(w.name),
+                         "peak_kind": f"{peaks['source']} bf16 dense burst (cuBLAS)",
+                         "kernel": "attn_fwd_kernel", "algorithmic_bytes": w.bytes()},
+            "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": in_bytes,
+                    "d2h_bytes_per_step": q.numel() * q.element_size() + lse.numel() * 4,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps,
+            "clocks": sampler.summary(),
+        }
+        if not args.no_cpu_baseline and world == 1:
+            tf, desc, cores, dt = cpu_baseline(w, q, k, v)
+            line["cpu_baseline"] = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                                    "sample": desc, "seconds": dt}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

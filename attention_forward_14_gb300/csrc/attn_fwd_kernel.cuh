@@ -23,10 +23,13 @@
 // one row (one tensor-memory lane): no cross-thread reductions.
 //
 // Softmax (per row, log2 domain): x = s * scale * log2(e); m_new =
-// max(m, rowmax x).  O and l are rescaled by 2^(m - m_new) only when
-// m_new - m > 8 for some row of the warp (lazy rescale; the stale max cancels
-// exactly between O and l, and p = 2^(x - m) stays <= 256).  Epilogue:
-// O / l rounded to the input type; LSE = (m + log2 l) * ln 2.
+// max(m, rowmax x).  O and the row sums are rescaled by 2^(m - m_new) only
+// when m_new - m > 8 for some row of the warp (lazy rescale; the stale max
+// cancels exactly between O and the sums, and p = 2^(x - m) stays <= 256).
+// Two row sums are kept: l of the fp32 p (LSE = (m + log2 l) * ln 2) and lr
+// of p as rounded to the input type for the P.V product; O is divided by lr
+// so that the weights applied to V sum to one (the rounding of a dominant p
+// then cancels instead of showing up in O).
 //
 // Every wait is bounded: when a wait runs out the kernel records where in a
 // status word, tells the other warps, waits for its own copies and MMAs,
@@ -171,6 +174,23 @@ __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi)
 {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// The two values a packed pair holds after rounding (low half first).
+template <typename T>
+__device__ __forceinline__ float2 unpack2(uint32_t u);
+
+template <>
+__device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t u)
+{
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+}
+
+template <>
+__device__ __forceinline__ float2 unpack2<__half>(uint32_t u)
+{
+    __half2 h = *reinterpret_cast<__half2 *>(&u);
+    return __half22float2(h);
 }
 
 template <typename T>
@@ -392,7 +412,9 @@ __global__ void __launch_bounds__(320, 1)
             }
             // keys visible to this row: [0, kend)
             const int kend = CAUSAL ? min(p.sk, row + 1 + (p.sk - p.sq)) : p.sk;
-            float m = -INFINITY, l = 0.f;
+            // l: sum of p in fp32 (gives LSE); lr: sum of p as rounded for
+            // the P.V product (normalises O, so its weights sum to one).
+            float m = -INFINITY, l = 0.f, lr = 0.f;
             for (int j = 0; j < un.n; ++j) {
                 bool w = bar_wait(B(ctl->s_full[t]), s_ph, ctl, p, SITE_SOFTMAX_S_FULL);
                 ok = __all_sync(0xffffffffu, w);
@@ -430,28 +452,32 @@ __global__ void __launch_bounds__(320, 1)
                             tmem_st32(tO + ch * 32, orr);
                         }
                         l *= alpha;
+                        lr *= alpha;
                         m = m_new;
                     }
                 } else {
                     m = m_new;
                 }
                 const float m_use = (m == -INFINITY) ? 0.f : m;
-                float sum8[8];
+                float sum4[4], sumr4[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) sum8[i] = 0.f;
+                for (int i = 0; i < 4; ++i) sum4[i] = sumr4[i] = 0.f;
                 uint32_t pa[32], pb[32];
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
                     const float p0 = ex2_approx(x[2 * c] - m_use);
                     const float p1 = ex2_approx(x[2 * c + 1] - m_use);
-                    sum8[(2 * c) & 7] += p0;
-                    sum8[(2 * c + 1) & 7] += p1;
+                    const uint32_t pk = pack2<T>(p0, p1);
+                    const float2 r = unpack2<T>(pk);
+                    sum4[c & 3] += p0 + p1;
+                    sumr4[c & 3] += r.x + r.y;
                     if (c < 32)
-                        pa[c] = pack2<T>(p0, p1);
+                        pa[c] = pk;
                     else
-                        pb[c - 32] = pack2<T>(p0, p1);
+                        pb[c - 32] = pk;
                 }
-                l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+                l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+                lr += (sumr4[0] + sumr4[1]) + (sumr4[2] + sumr4[3]);
                 tmem_st32(tS, pa);
                 tmem_st32(tS + 32, pb);
                 tmem_wait_st();
@@ -466,7 +492,7 @@ __global__ void __launch_bounds__(320, 1)
                 if (!ok) break;
                 o_ph ^= 1u;
                 tc_fence_after();
-                const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+                const float inv_l = (lr > 0.f) ? 1.f / lr : 0.f;
                 const bool valid = row < p.sq;
                 uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.o) +
                                                        (static_cast<size_t>(un.bh) * p.sq + (valid ? row : 0)) * D);

@@ -7,11 +7,15 @@
 // forward_kernel: scale after the dot product, online recurrence with a
 // running row max m and row sum l, O rescaled when m changes).
 //
-// How (one persistent CTA per SM, 10 warps):
-//   warps 0-3  softmax group 0  -- Q tile 0 (rows 0..127 of the unit)
-//   warps 4-7  softmax group 1  -- Q tile 1 (rows 128..255 of the unit)
-//   warp  8    MMA issuer (one thread) + tensor-memory owner
-//   warp  9    TMA producer (one thread)
+// How (one persistent CTA per SM, 12 warps):
+//   warps 0-3   softmax group 0  -- Q tile 0 (rows 0..127 of the unit)
+//   warps 4-7   softmax group 1  -- Q tile 1 (rows 128..255 of the unit)
+//   warp  8     MMA issuer (one thread) + tensor-memory owner
+//   warp  9     TMA producer (one thread)
+//   warps 10-11 no work (they complete warpgroup 2, whose registers are
+//               handed to the softmax groups: 216 per softmax thread, 72
+//               for the others; 256*216 + 128*72 = 384*168 at launch,
+//               and 216 + 216 + 72 = 3*168 on each SM sub-partition)
 // A work unit is (batch*head, 256-row block).  Per unit the producer loads
 // the two Q tiles once and streams K_j, V_j tiles (128 keys each) through an
 // NSLOT-deep shared-memory ring.  The MMA thread computes S_t = Q_t K_j^T
@@ -90,7 +94,9 @@ struct Cfg {
     static constexpr int TMEM_COLS = 512;
     static constexpr int TMEM_S = 0;               // S_t at column t*BN (P_t aliases it)
     static constexpr int TMEM_O = QT * BN;         // O_t at TMEM_O + t*D
-    static constexpr int THREADS = 320;
+    static constexpr int THREADS = 384;
+    static constexpr int REGS_SOFTMAX = 208;
+    static constexpr int REGS_OTHER = 88;
     static constexpr float TAU = 8.0f;             // lazy-rescale threshold (log2 units)
     static_assert(TMEM_O + QT * D <= TMEM_COLS, "tensor memory budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -130,15 +136,15 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams &p)
     return un;
 }
 
-static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl *ctl, const FwdParams &p,
-                                              uint32_t site, bool honour_abort)
+static __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl *ctl, const FwdParams &p,
+                                              uint32_t site)
 {
     volatile uint32_t *abort_flag = &ctl->abort;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (honour_abort && *abort_flag) return false;
+        if (*abort_flag) return false;
         if (global_timer_ns() - t0 > p.timeout_ns) {
             *abort_flag = 1u;
             if (atomicCAS(&p.status[0], 0u, 1u) == 0u) {
@@ -152,11 +158,20 @@ static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl
     }
 }
 
+// Bounded wait that ignores the abort flag (used to let this thread's own
+// copies and MMAs land before the CTA frees its resources).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
+{
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - t0 > timeout_ns) break;
+}
+
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, Ctl *ctl, const FwdParams &p,
                                          uint32_t site)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    return wait_slow(bar, parity, ctl, p, site, true);
+    return wait_slow(bar, parity, ctl, p, site);
 }
 
 template <typename T>
@@ -176,21 +191,19 @@ __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// The two values a packed pair holds after rounding (low half first).
 template <typename T>
-__device__ __forceinline__ float2 unpack2(uint32_t u);
+__device__ __forceinline__ float add_halves(uint32_t u, float acc);
 
 template <>
-__device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t u)
+__device__ __forceinline__ float add_halves<__nv_bfloat16>(uint32_t u, float acc)
 {
-    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+    return add_halves_bf16(u, acc);
 }
 
 template <>
-__device__ __forceinline__ float2 unpack2<__half>(uint32_t u)
+__device__ __forceinline__ float add_halves<__half>(uint32_t u, float acc)
 {
-    __half2 h = *reinterpret_cast<__half2 *>(&u);
-    return __half22float2(h);
+    return add_halves_f16(u, acc);
 }
 
 template <typename T>
@@ -203,7 +216,7 @@ __device__ __forceinline__ void store_row_zero(const FwdParams &p, int bh, int r
 }
 
 template <int D, typename T, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p)
 {
@@ -255,7 +268,11 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
 
-    if (warp == 9) {
+    if (warp >= 8) {
+      // Warpgroup 2: the setmaxnreg and all of this warpgroup's work sit in
+      // one warpgroup-uniform branch, so the compiler knows the budget.
+      regs_dec<C::REGS_OTHER>();
+      if (warp == 9) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t kv_it = 0, q_it = 0;
@@ -297,11 +314,11 @@ __global__ void __launch_bounds__(320, 1)
                 const uint32_t first = kv_it > C::NSLOT ? kv_it - C::NSLOT : 0u;
                 for (uint32_t i = first; i < kv_it; ++i) {
                     if (static_cast<int32_t>(i) == p.withheld_load) continue;
-                    wait_slow(B(ctl->kv_full[i % C::NSLOT]), (i / C::NSLOT) & 1u, ctl, p, SITE_DRAIN, false);
+                    drain_wait(B(ctl->kv_full[i % C::NSLOT]), (i / C::NSLOT) & 1u, p.timeout_ns);
                 }
                 if (q_it > 0)
                     for (int t = 0; t < C::QT; ++t)
-                        wait_slow(B(ctl->q_full[t]), (q_it - 1) & 1u, ctl, p, SITE_DRAIN, false);
+                        drain_wait(B(ctl->q_full[t]), (q_it - 1) & 1u, p.timeout_ns);
             }
         }
         __syncwarp();
@@ -317,25 +334,29 @@ __global__ void __launch_bounds__(320, 1)
                 ++kv_it;
                 return r;
             };
+            // Low descriptor words of the first k-step; later k-steps add
+            // their byte offset >> 4 to the start-address field, which cannot
+            // carry (shared addresses stay below 2^18).
+            const uint32_t dq0 = desc_lo(sQ, 16);
+            const uint32_t dk0 = desc_lo(sKV, 16);
+            const uint32_t dv0 = desc_lo(sKV, C::PANEL_BYTES);
             auto issue_qk = [&](int t, uint32_t kslot) {
-                const uint32_t a0 = sQ + t * C::TILE_BYTES;
-                const uint32_t b0 = sKV + kslot * C::TILE_BYTES;
+                const uint32_t a0 = dq0 + ((t * C::TILE_BYTES) >> 4);
+                const uint32_t b0 = dk0 + ((kslot * C::TILE_BYTES) >> 4);
                 const uint32_t d = tmem + C::TMEM_S + t * C::BN;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
-                    mma_ss(d, smem_desc_sw128(a0 + off, 16, 1024), smem_desc_sw128(b0 + off, 16, 1024), IDESC_QK,
-                           kk > 0 ? 1u : 0u);
+                    const uint32_t off = ((kk / 4) * C::PANEL_BYTES + (kk % 4) * 32) >> 4;
+                    mma_ss(d, a0 + off, b0 + off, IDESC_QK, kk > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int t, uint32_t vslot, bool accumulate) {
-                const uint32_t b0 = sKV + vslot * C::TILE_BYTES;
+                const uint32_t b0 = dv0 + ((vslot * C::TILE_BYTES) >> 4);
                 const uint32_t a = tmem + C::TMEM_S + t * C::BN;  // P_t, 2 elements per column
                 const uint32_t d = tmem + C::TMEM_O + t * D;
 #pragma unroll
                 for (int kk = 0; kk < C::BN / 16; ++kk)
-                    mma_ts(d, a + kk * 8, smem_desc_sw128(b0 + kk * 16 * 128, C::PANEL_BYTES, 1024), IDESC_PV,
-                           (accumulate || kk > 0) ? 1u : 0u);
+                    mma_ts(d, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
             };
             for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
                 const Unit un = decode_unit<D, CAUSAL>(u, p);
@@ -389,10 +410,12 @@ __global__ void __launch_bounds__(320, 1)
             }
             // Every MMA issued must complete before tensor memory is freed.
             tc_commit(B(ctl->mma_done));
-            wait_slow(B(ctl->mma_done), 0u, ctl, p, SITE_DRAIN, false);
+            drain_wait(B(ctl->mma_done), 0u, p.timeout_ns);
         }
         __syncwarp();
+      }
     } else {
+        regs_inc<C::REGS_SOFTMAX>();
         // ------------------------------------------------------------ softmax groups
         const int t = warp >> 2;      // Q tile of this group
         const int quad = warp & 3;    // TMEM lane quadrant this warp may access
@@ -401,6 +424,7 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t tS = tmem + lane_off + C::TMEM_S + t * C::BN;
         const uint32_t tO = tmem + lane_off + C::TMEM_O + t * D;
         const float sl2e = p.sl2e;
+        const bool neg = sl2e < 0.f;  // the row maximum of scale*s is scale*min(s)
         uint32_t s_ph = 0u, o_ph = 0u;
         bool ok = true;
         for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
@@ -423,32 +447,58 @@ __global__ void __launch_bounds__(320, 1)
                 tc_fence_after();
                 uint32_t sr[128];
                 tmem_ld128_wait(tS, sr);
-                float x[128];
-#pragma unroll
-                for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]) * sl2e;
                 const int lim = kend - j * C::BN;  // columns >= lim are masked
-                if (lim < C::BN) {
+                const bool masked = lim < C::BN;
+                // row max of the raw logits (min when the scale is negative),
+                // masked columns excluded
+                const float ident = neg ? INFINITY : -INFINITY;
+                if (masked) {
 #pragma unroll
-                    for (int c = 0; c < 128; ++c) x[c] = (c < lim) ? x[c] : -INFINITY;
+                    for (int c = 0; c < 128; ++c)
+                        sr[c] = (c < lim) ? sr[c] : __float_as_uint(ident);
                 }
-                float mx8[8];
+                float r4[4];
+                if (!neg) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = x[i];
+                    for (int i = 0; i < 4; ++i) r4[i] = __uint_as_float(sr[i]);
 #pragma unroll
-                for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                    for (int c = 4; c < 128; c += 8)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            r4[i] = (c + 2 * i + 1 < 128)
+                                        ? max3f(r4[i], __uint_as_float(sr[c + 2 * i]), __uint_as_float(sr[c + 2 * i + 1]))
+                                        : r4[i];
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) r4[i] = __uint_as_float(sr[i]);
+#pragma unroll
+                    for (int c = 4; c < 128; c += 8)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            r4[i] = (c + 2 * i + 1 < 128)
+                                        ? min3f(r4[i], __uint_as_float(sr[c + 2 * i]), __uint_as_float(sr[c + 2 * i + 1]))
+                                        : r4[i];
+                }
+                const float mraw = neg ? fminf(fminf(r4[0], r4[1]), fminf(r4[2], r4[3]))
+                                       : fmaxf(fmaxf(r4[0], r4[1]), fmaxf(r4[2], r4[3]));
+                const float mx = (mraw == ident) ? -INFINITY : mraw * sl2e;
                 const float m_new = fmaxf(m, mx);
                 if (j > 0) {
                     const bool need = (m_new - m) > C::TAU;
                     if (__any_sync(0xffffffffu, need)) {
                         const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m - m_new);
+                        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
                         for (int ch = 0; ch < D / 32; ++ch) {
                             uint32_t orr[32];
                             tmem_ld32_wait(tO + ch * 32, orr);
 #pragma unroll
-                            for (int c = 0; c < 32; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
+                            for (int c = 0; c < 16; ++c) {
+                                float2 v = __fmul2_rn(make_float2(__uint_as_float(orr[2 * c]),
+                                                                  __uint_as_float(orr[2 * c + 1])), a2);
+                                orr[2 * c] = __float_as_uint(v.x);
+                                orr[2 * c + 1] = __float_as_uint(v.y);
+                            }
                             tmem_st32(tO + ch * 32, orr);
                         }
                         l *= alpha;
@@ -459,25 +509,40 @@ __global__ void __launch_bounds__(320, 1)
                     m = m_new;
                 }
                 const float m_use = (m == -INFINITY) ? 0.f : m;
-                float sum4[4], sumr4[4];
+                const float2 sc2 = make_float2(sl2e, sl2e);
+                const float2 nm2 = make_float2(-m_use, -m_use);
+                float2 l4[4];
+                float lr4[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) sum4[i] = sumr4[i] = 0.f;
+                for (int i = 0; i < 4; ++i) {
+                    l4[i] = make_float2(0.f, 0.f);
+                    lr4[i] = 0.f;
+                }
                 uint32_t pa[32], pb[32];
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
-                    const float p0 = ex2_approx(x[2 * c] - m_use);
-                    const float p1 = ex2_approx(x[2 * c + 1] - m_use);
+                    float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])),
+                                          sc2, nm2);
+                    if (masked) {
+                        x.x = (2 * c < lim) ? x.x : -INFINITY;
+                        x.y = (2 * c + 1 < lim) ? x.y : -INFINITY;
+                    }
+                    const float p0 = ex2_approx(x.x);
+                    const float p1 = ex2_approx(x.y);
+                    l4[c & 3] = __fadd2_rn(l4[c & 3], make_float2(p0, p1));
                     const uint32_t pk = pack2<T>(p0, p1);
-                    const float2 r = unpack2<T>(pk);
-                    sum4[c & 3] += p0 + p1;
-                    sumr4[c & 3] += r.x + r.y;
+                    lr4[c & 3] = add_halves<T>(pk, lr4[c & 3]);
                     if (c < 32)
                         pa[c] = pk;
                     else
                         pb[c - 32] = pk;
                 }
-                l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-                lr += (sumr4[0] + sumr4[1]) + (sumr4[2] + sumr4[3]);
+                {
+                    const float2 a = __fadd2_rn(l4[0], l4[1]);
+                    const float2 b = __fadd2_rn(l4[2], l4[3]);
+                    l += (a.x + a.y) + (b.x + b.y);
+                    lr += (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]);
+                }
                 tmem_st32(tS, pa);
                 tmem_st32(tS + 32, pb);
                 tmem_wait_st();
@@ -502,8 +567,11 @@ __global__ void __launch_bounds__(320, 1)
                     tmem_ld32_wait(tO + ch * 32, orr);
                     uint32_t pk[16];
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        pk[c] = pack2<T>(__uint_as_float(orr[2 * c]) * inv_l, __uint_as_float(orr[2 * c + 1]) * inv_l);
+                    for (int c = 0; c < 16; ++c) {
+                        const float2 v = __fmul2_rn(make_float2(__uint_as_float(orr[2 * c]), __uint_as_float(orr[2 * c + 1])),
+                                                    make_float2(inv_l, inv_l));
+                        pk[c] = pack2<T>(v.x, v.y);
+                    }
                     if (valid) {
 #pragma unroll
                         for (int v4 = 0; v4 < 4; ++v4)

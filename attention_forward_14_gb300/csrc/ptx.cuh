@@ -112,27 +112,42 @@ __device__ __forceinline__ void tc_commit(uint32_t bar)
                  : "memory");
 }
 
+// Shared-memory matrix descriptors (tcgen05 format, 64-bit) are passed as
+// their low word only: start address >> 4 (bits 0-13) and leading byte
+// offset >> 4 (bits 16-29).  The high word -- stride byte offset 1024 B >> 4
+// (bits 32-45), descriptor version 1 (bit 46), 128-byte swizzle = 2 (bits
+// 61-63) -- is the same for every operand here.
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+
+__host__ __device__ constexpr uint32_t desc_lo(uint32_t saddr, uint32_t lbo_bytes)
+{
+    return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+
 // D(tmem) (+)= A(smem desc) * B(smem desc), kind::f16, fp32 accumulate.
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
                                        uint32_t accumulate)
 {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "mov.b64 da, {%1, %5};\n\t"
+        "mov.b64 db, {%2, %5};\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi)
         : "memory");
 }
 
 // D(tmem) (+)= A(tmem) * B(smem desc), kind::f16, fp32 accumulate.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
                                        uint32_t accumulate)
 {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "mov.b64 db, {%2, %5};\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi)
         : "memory");
 }
 
@@ -199,6 +214,53 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 #undef ATTN_W8
 
+// Three-input max / min (sm_100+).
+__device__ __forceinline__ float max3f(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ float min3f(float a, float b, float c)
+{
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// acc + (both 16-bit halves of a packed bf16x2 / f16x2 word), in fp32.
+__device__ __forceinline__ float add_halves_bf16(uint32_t u, float acc)
+{
+    float d;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+        "add.rn.f32.bf16 %0, lo, %2;\n\tadd.rn.f32.bf16 %0, hi, %0;\n\t}"
+        : "=f"(d) : "r"(u), "f"(acc));
+    return d;
+}
+
+__device__ __forceinline__ float add_halves_f16(uint32_t u, float acc)
+{
+    float d;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+        "add.rn.f32.f16 %0, lo, %2;\n\tadd.rn.f32.f16 %0, hi, %0;\n\t}"
+        : "=f"(d) : "r"(u), "f"(acc));
+    return d;
+}
+
+// Register budget changes for a whole warpgroup.
+template <int N>
+__device__ __forceinline__ void regs_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int N>
+__device__ __forceinline__ void regs_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ float ex2_approx(float x)
 {
     float y;
@@ -207,19 +269,6 @@ __device__ __forceinline__ float ex2_approx(float x)
 }
 
 // ---------------------------------------------------------------- descriptors
-
-// Shared-memory matrix descriptor (tcgen05 format): start address, leading
-// and stride byte offsets (16-byte units), version 1, 128-byte swizzle.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes)
-{
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-    d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
-    d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
-    d |= static_cast<uint64_t>(1) << 46;   // descriptor version for tcgen05
-    d |= static_cast<uint64_t>(2) << 61;   // SWIZZLE_128B
-    return d;
-}
 
 // Instruction descriptor, kind::f16, fp32 accumulator, dense, A K-major.
 //   bf16: element type of A and B (0 = f16, 1 = bf16); b_mn: B is MN-major.

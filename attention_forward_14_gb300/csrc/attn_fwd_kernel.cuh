@@ -95,8 +95,8 @@ struct Cfg {
     static constexpr int TMEM_S = 0;               // S_t at column t*BN (P_t aliases it)
     static constexpr int TMEM_O = QT * BN;         // O_t at TMEM_O + t*D
     static constexpr int THREADS = 384;
-    static constexpr int REGS_SOFTMAX = 208;
-    static constexpr int REGS_OTHER = 88;
+    static constexpr int REGS_SOFTMAX = 216;
+    static constexpr int REGS_OTHER = 72;
     static constexpr float TAU = 8.0f;             // lazy-rescale threshold (log2 units)
     static_assert(TMEM_O + QT * D <= TMEM_COLS, "tensor memory budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -134,6 +134,19 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams &p)
     int kend = CAUSAL ? min(p.sk, last + 1 + (p.sk - p.sq)) : p.sk;
     un.n = kend > 0 ? (kend + C::BN - 1) / C::BN : 0;
     return un;
+}
+
+// The i-th work unit of this CTA.  Rounds of gridDim.x units are dealt out
+// in alternating directions (boustrophedon): with the causal heaviest-first
+// order this evens out the per-CTA work to within a fraction of a percent
+// (a plain stride leaves the CTAs that draw the heaviest unit of every round
+// several percent behind).  The last round may be partial: callers skip
+// indices >= num_units and keep going until i * gridDim.x >= num_units.
+__device__ __forceinline__ int unit_at(int i)
+{
+    const int g = static_cast<int>(gridDim.x);
+    const int c = (i & 1) ? (g - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+    return i * g + c;
 }
 
 static __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl *ctl, const FwdParams &p,
@@ -277,7 +290,9 @@ __global__ void __launch_bounds__(384, 1)
         if (lane == 0) {
             uint32_t kv_it = 0, q_it = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+            for (int i = 0; i * static_cast<int>(gridDim.x) < p.num_units && ok; ++i) {
+                const int u = unit_at(i);
+                if (u >= p.num_units) continue;
                 const Unit un = decode_unit<D, CAUSAL>(u, p);
                 if (un.n == 0) continue;
                 for (int t = 0; t < C::QT && ok; ++t) {
@@ -358,7 +373,9 @@ __global__ void __launch_bounds__(384, 1)
                 for (int kk = 0; kk < C::BN / 16; ++kk)
                     mma_ts(d, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
             };
-            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+            for (int i = 0; i * static_cast<int>(gridDim.x) < p.num_units && ok; ++i) {
+                const int u = unit_at(i);
+                if (u >= p.num_units) continue;
                 const Unit un = decode_unit<D, CAUSAL>(u, p);
                 if (un.n == 0) continue;
                 for (int t = 0; t < C::QT && ok; ++t)
@@ -427,7 +444,9 @@ __global__ void __launch_bounds__(384, 1)
         const bool neg = sl2e < 0.f;  // the row maximum of scale*s is scale*min(s)
         uint32_t s_ph = 0u, o_ph = 0u;
         bool ok = true;
-        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        for (int i = 0; i * static_cast<int>(gridDim.x) < p.num_units && ok; ++i) {
+                const int u = unit_at(i);
+                if (u >= p.num_units) continue;
             const Unit un = decode_unit<D, CAUSAL>(u, p);
             const int row = un.row0 + t * C::BM + r_in_tile;
             if (un.n == 0) {
@@ -536,6 +555,7 @@ __global__ void __launch_bounds__(384, 1)
                         pa[c] = pk;
                     else
                         pb[c - 32] = pk;
+                    if (c == 31) tmem_st32(tS, pa);  // overlaps the second half
                 }
                 {
                     const float2 a = __fadd2_rn(l4[0], l4[1]);
@@ -543,7 +563,6 @@ __global__ void __launch_bounds__(384, 1)
                     l += (a.x + a.y) + (b.x + b.y);
                     lr += (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]);
                 }
-                tmem_st32(tS, pa);
                 tmem_st32(tS + 32, pb);
                 tmem_wait_st();
                 tc_fence_before();

@@ -42,16 +42,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
-// True once the phase with the given parity has completed.
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+// True once the phase with the given parity has completed.  While it has
+// not, the hardware may suspend the thread for up to `suspend_ns` (it wakes
+// early when the phase completes), so a waiting warp does not spin through
+// issue slots that the warps sharing its SM sub-partition need.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t suspend_ns = 0x100000u)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(suspend_ns)
         : "memory");
     return ok != 0;
 }

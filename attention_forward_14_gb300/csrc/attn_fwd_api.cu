@@ -112,6 +112,10 @@ int make_map(CUtensorMap *map, const void *ptr, int dtype, int64_t bh, int64_t s
     return ATTN_OK;
 }
 
+#ifdef ATTN_TRACE_ENABLE
+unsigned long long *g_trace_buf = nullptr;  // timeline builds only
+#endif
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 constexpr int64_t kMaxSeq = int64_t(1) << 30;
@@ -179,6 +183,9 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_
     p.sl2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     p.timeout_ns = timeout_ns;
     p.withheld_load = withheld_load;
+#ifdef ATTN_TRACE_ENABLE
+    p.trace = g_trace_buf;
+#endif
     a.grid = static_cast<int>(units < di->sm_count ? units : di->sm_count);
     a.stream = stream;
     const bool c = causal != 0;
@@ -283,5 +290,10 @@ int attn_fwd_watchdog_selftest(const void *q, const void *k, const void *v, void
 }
 
 const char *attn_version(void) { return "attn_fwd sm_103a 0.1"; }
+
+#ifdef ATTN_TRACE_ENABLE
+// Timeline builds only: device buffer that later launches record into.
+void attn_trace_set(unsigned long long *device_buffer) { g_trace_buf = device_buffer; }
+#endif
 
 }  // extern "C"

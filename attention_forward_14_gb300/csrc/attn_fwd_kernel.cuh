@@ -61,6 +61,36 @@ struct FwdParams {
     float sl2e;            // scale * log2(e)
     uint64_t timeout_ns;   // bound of every wait
     int32_t withheld_load; // K/V load index never issued (watchdog self-test), -1 = none
+#ifdef ATTN_TRACE_ENABLE
+    unsigned long long *trace;  // per-warp event records (timeline builds only)
+#endif
+};
+
+// Pipeline timeline hooks.  Compiled out unless ATTN_TRACE_ENABLE is defined
+// (a separate diagnostic build that records {clock, event, arg} per warp).
+#ifdef ATTN_TRACE_ENABLE
+#define ATTN_TRACE_DECL uint32_t attn_trace_n = 0;
+#define ATTN_TRACE(ev, arg) attn_trace_record(p, attn_trace_n, (ev), (arg))
+__device__ __forceinline__ void attn_trace_record(const FwdParams &p, uint32_t &n, uint32_t ev, uint32_t arg)
+{
+    constexpr uint32_t kCtas = 4, kWarps = 12, kEvents = 16384;
+    if (p.trace == nullptr || blockIdx.x >= kCtas || (threadIdx.x & 31) != 0 || n >= kEvents) return;
+    const uint32_t w = threadIdx.x >> 5;
+    unsigned long long *rec = p.trace + 2ull * ((blockIdx.x * kWarps + w) * kEvents + n);
+    rec[0] = clock64();
+    rec[1] = (static_cast<unsigned long long>(ev) << 32) | arg;
+    ++n;
+}
+#else
+#define ATTN_TRACE_DECL
+#define ATTN_TRACE(ev, arg) ((void)0)
+#endif
+
+enum : uint32_t {
+    EV_SM_WAIT_S = 1, EV_SM_GOT_S, EV_SM_LD, EV_SM_MAX, EV_SM_RESCALE, EV_SM_EXP, EV_SM_ARRIVE,
+    EV_SM_EPI_WAIT, EV_SM_EPI_GOT, EV_SM_EPI_DONE,
+    EV_MMA_WAIT_Q = 20, EV_MMA_GOT_Q, EV_MMA_WAIT_KV, EV_MMA_GOT_KV, EV_MMA_WAIT_P, EV_MMA_GOT_P, EV_MMA_ISSUED,
+    EV_LD_WAIT = 40, EV_LD_GOT,
 };
 
 // Watchdog sites (recorded in status[3]).
@@ -250,6 +280,7 @@ __global__ void __launch_bounds__(384, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    ATTN_TRACE_DECL
 
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
@@ -308,8 +339,10 @@ __global__ void __launch_bounds__(384, 1)
                 for (int j = 0; j < un.n && ok; ++j) {
                     for (int which = 0; which < 2; ++which) {
                         const uint32_t slot = kv_it % C::NSLOT;
+                        ATTN_TRACE(EV_LD_WAIT, kv_it);
                         ok = bar_wait(B(ctl->kv_empty[slot]), ((kv_it / C::NSLOT) & 1u) ^ 1u, ctl, p,
                                       SITE_LOAD_KV_EMPTY);
+                        ATTN_TRACE(EV_LD_GOT, kv_it);
                         if (!ok) break;
                         if (static_cast<int32_t>(kv_it) != p.withheld_load) {
                             mbar_arrive_expect_tx(B(ctl->kv_full[slot]), C::TILE_BYTES);
@@ -345,7 +378,9 @@ __global__ void __launch_bounds__(384, 1)
             bool ok = true;
             auto kv_wait = [&](uint32_t &slot) -> bool {
                 slot = kv_it % C::NSLOT;
+                ATTN_TRACE(EV_MMA_WAIT_KV, kv_it);
                 bool r = bar_wait(B(ctl->kv_full[slot]), (kv_it / C::NSLOT) & 1u, ctl, p, SITE_MMA_KV_FULL);
+                ATTN_TRACE(EV_MMA_GOT_KV, kv_it);
                 ++kv_it;
                 return r;
             };
@@ -378,8 +413,10 @@ __global__ void __launch_bounds__(384, 1)
                 if (u >= p.num_units) continue;
                 const Unit un = decode_unit<D, CAUSAL>(u, p);
                 if (un.n == 0) continue;
+                ATTN_TRACE(EV_MMA_WAIT_Q, u);
                 for (int t = 0; t < C::QT && ok; ++t)
                     ok = bar_wait(B(ctl->q_full[t]), q_it & 1u, ctl, p, SITE_MMA_Q_FULL);
+                ATTN_TRACE(EV_MMA_GOT_Q, u);
                 if (!ok) break;
                 ++q_it;
                 uint32_t kslot;
@@ -400,7 +437,9 @@ __global__ void __launch_bounds__(384, 1)
                     if (!(ok = kv_wait(vslot))) break;
                     if (more && !(ok = kv_wait(nslot))) break;
                     // tile 0
+                    ATTN_TRACE(EV_MMA_WAIT_P, 0);
                     if (!(ok = bar_wait(B(ctl->p_full[0]), p_ph[0], ctl, p, SITE_MMA_P_FULL))) break;
+                    ATTN_TRACE(EV_MMA_GOT_P, 0);
                     p_ph[0] ^= 1u;
                     tc_fence_after();
                     issue_pv(0, vslot, j > 0);
@@ -411,7 +450,9 @@ __global__ void __launch_bounds__(384, 1)
                         if (j + 2 == un.n) tc_commit(B(ctl->q_empty[0]));
                     }
                     // tile 1
+                    ATTN_TRACE(EV_MMA_WAIT_P, 1);
                     if (!(ok = bar_wait(B(ctl->p_full[1]), p_ph[1], ctl, p, SITE_MMA_P_FULL))) break;
+                    ATTN_TRACE(EV_MMA_GOT_P, 1);
                     p_ph[1] ^= 1u;
                     tc_fence_after();
                     issue_pv(1, vslot, j > 0);
@@ -459,13 +500,16 @@ __global__ void __launch_bounds__(384, 1)
             // the P.V product (normalises O, so its weights sum to one).
             float m = -INFINITY, l = 0.f, lr = 0.f;
             for (int j = 0; j < un.n; ++j) {
+                ATTN_TRACE(EV_SM_WAIT_S, j);
                 bool w = bar_wait(B(ctl->s_full[t]), s_ph, ctl, p, SITE_SOFTMAX_S_FULL);
                 ok = __all_sync(0xffffffffu, w);
                 if (!ok) break;
+                ATTN_TRACE(EV_SM_GOT_S, j);
                 s_ph ^= 1u;
                 tc_fence_after();
                 uint32_t sr[128];
                 tmem_ld128_wait(tS, sr);
+                ATTN_TRACE(EV_SM_LD, j);
                 const int lim = kend - j * C::BN;  // columns >= lim are masked
                 const bool masked = lim < C::BN;
                 // row max of the raw logits (min when the scale is negative),
@@ -523,10 +567,12 @@ __global__ void __launch_bounds__(384, 1)
                         l *= alpha;
                         lr *= alpha;
                         m = m_new;
+                        ATTN_TRACE(EV_SM_RESCALE, j);
                     }
                 } else {
                     m = m_new;
                 }
+                ATTN_TRACE(EV_SM_MAX, j);
                 const float m_use = (m == -INFINITY) ? 0.f : m;
                 const float2 sc2 = make_float2(sl2e, sl2e);
                 const float2 nm2 = make_float2(-m_use, -m_use);
@@ -563,17 +609,21 @@ __global__ void __launch_bounds__(384, 1)
                     l += (a.x + a.y) + (b.x + b.y);
                     lr += (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]);
                 }
+                ATTN_TRACE(EV_SM_EXP, j);
                 tmem_st32(tS + 32, pb);
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(B(ctl->p_full[t]));
+                ATTN_TRACE(EV_SM_ARRIVE, j);
             }
             if (!ok) break;
             // ---- epilogue: O / l -> T, LSE
             {
+                ATTN_TRACE(EV_SM_EPI_WAIT, u);
                 bool w = bar_wait(B(ctl->o_full[t]), o_ph, ctl, p, SITE_SOFTMAX_O_FULL);
                 ok = __all_sync(0xffffffffu, w);
                 if (!ok) break;
+                ATTN_TRACE(EV_SM_EPI_GOT, u);
                 o_ph ^= 1u;
                 tc_fence_after();
                 const float inv_l = (lr > 0.f) ? 1.f / lr : 0.f;
@@ -600,6 +650,7 @@ __global__ void __launch_bounds__(384, 1)
                 if (valid && p.lse)
                     p.lse[static_cast<size_t>(un.bh) * p.sq + row] =
                         (l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                ATTN_TRACE(EV_SM_EPI_DONE, u);
                 tc_fence_before();
             }
         }

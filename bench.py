@@ -31,6 +31,24 @@ METRIC = "attention fwd TFLOPS on 1 GB300 (d=128, bf16, causal) and % of dense t
 L2_BYTES = 129e6
 
 
+def shard_heads(bh: int, world: int, rank: int):
+    """Contiguous [start, end) range of the b*h heads owned by `rank` when one
+    problem is split across ranks (heads are independent: no exchange)."""
+    base, rem = divmod(bh, world)
+    start = rank * base + min(rank, rem)
+    return start, start + base + (1 if rank < rem else 0)
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """The slowest rank's time (the job finishes when the last rank does)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -244,12 +262,8 @@ def main():
     if dist:
         dist.barrier()
     sampler.stop()
-    total_ms = t_all0.elapsed_time(t_all1)
+    total_ms = max_over_ranks(t_all0.elapsed_time(t_all1), dist, dev)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
     ms = total_ms / args.steps
     value = world * w.flops() / (ms * 1e-3) / 1e12
 
@@ -270,11 +284,7 @@ def main():
         af.attn_fwd_host(qh, kh, vh, oh, lh, qd, kd, vd, o, lse, causal=w.causal, scale=w.scale, stream=stream)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, dist, dev)
     e2e_value = world * w.flops() / (e2e_ms * 1e-3) / 1e12
 
     if rank == 0:

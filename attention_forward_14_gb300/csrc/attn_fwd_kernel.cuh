@@ -217,6 +217,13 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, Ctl *ctl
     return wait_slow(bar, parity, ctl, p, site);
 }
 
+// bar_wait by every lane of a warp, with a warp-uniform result.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Ctl *ctl, const FwdParams &p, uint32_t site)
+{
+    const bool w = bar_wait(bar, parity, ctl, p, site);
+    return __all_sync(0xffffffffu, w);
+}
+
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi);
 
@@ -318,110 +325,117 @@ __global__ void __launch_bounds__(384, 1)
       regs_dec<C::REGS_OTHER>();
       if (warp == 9) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            uint32_t kv_it = 0, q_it = 0;
-            bool ok = true;
-            for (int i = 0; i * static_cast<int>(gridDim.x) < p.num_units && ok; ++i) {
-                const int u = unit_at(i);
-                if (u >= p.num_units) continue;
-                const Unit un = decode_unit<D, CAUSAL>(u, p);
-                if (un.n == 0) continue;
-                for (int t = 0; t < C::QT && ok; ++t) {
-                    ok = bar_wait(B(ctl->q_empty[t]), (q_it & 1u) ^ 1u, ctl, p, SITE_LOAD_Q_EMPTY);
-                    if (!ok) break;
+        // The whole warp walks the schedule, so counters and addresses are
+        // warp-uniform; one elected lane issues the copies.
+        uint32_t kv_it = 0, q_it = 0;
+        bool ok = true;
+        for (int i = 0; i * static_cast<int>(gridDim.x) < p.num_units && ok; ++i) {
+            const int u = unit_at(i);
+            if (u >= p.num_units) continue;
+            const Unit un = decode_unit<D, CAUSAL>(u, p);
+            if (un.n == 0) continue;
+            for (int t = 0; t < C::QT && ok; ++t) {
+                ok = warp_wait(B(ctl->q_empty[t]), (q_it & 1u) ^ 1u, ctl, p, SITE_LOAD_Q_EMPTY);
+                if (!ok) break;
+                if (elect_one()) {
                     mbar_arrive_expect_tx(B(ctl->q_full[t]), C::TILE_BYTES);
                     for (int pn = 0; pn < C::NPANEL; ++pn)
                         tma_load_3d(sQ + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tmQ, B(ctl->q_full[t]),
                                     pn * C::PANEL_ELEMS, un.row0 + t * C::BM, un.bh);
                 }
-                if (!ok) break;
-                ++q_it;
-                for (int j = 0; j < un.n && ok; ++j) {
-                    for (int which = 0; which < 2; ++which) {
-                        const uint32_t slot = kv_it % C::NSLOT;
-                        ATTN_TRACE(EV_LD_WAIT, kv_it);
-                        ok = bar_wait(B(ctl->kv_empty[slot]), ((kv_it / C::NSLOT) & 1u) ^ 1u, ctl, p,
-                                      SITE_LOAD_KV_EMPTY);
-                        ATTN_TRACE(EV_LD_GOT, kv_it);
-                        if (!ok) break;
-                        if (static_cast<int32_t>(kv_it) != p.withheld_load) {
-                            mbar_arrive_expect_tx(B(ctl->kv_full[slot]), C::TILE_BYTES);
-                            const CUtensorMap *m = which ? &tmV : &tmK;
-                            for (int pn = 0; pn < C::NPANEL; ++pn)
-                                tma_load_3d(sKV + slot * C::TILE_BYTES + pn * C::PANEL_BYTES, m,
-                                            B(ctl->kv_full[slot]), pn * C::PANEL_ELEMS, j * C::BN, un.bh);
-                        }
-                        ++kv_it;
-                    }
-                }
+                __syncwarp();
             }
-            {
-                // Wind-down: wait (bounded) for the last copies this thread
-                // issued, so that no copy lands after the CTA exits even when
-                // a consumer gave up (normally these have long completed).
-                const uint32_t first = kv_it > C::NSLOT ? kv_it - C::NSLOT : 0u;
-                for (uint32_t i = first; i < kv_it; ++i) {
-                    if (static_cast<int32_t>(i) == p.withheld_load) continue;
-                    drain_wait(B(ctl->kv_full[i % C::NSLOT]), (i / C::NSLOT) & 1u, p.timeout_ns);
+            if (!ok) break;
+            ++q_it;
+            for (int j = 0; j < un.n && ok; ++j) {
+                for (int which = 0; which < 2; ++which) {
+                    const uint32_t slot = kv_it % C::NSLOT;
+                    ATTN_TRACE(EV_LD_WAIT, kv_it);
+                    ok = warp_wait(B(ctl->kv_empty[slot]), ((kv_it / C::NSLOT) & 1u) ^ 1u, ctl, p,
+                                   SITE_LOAD_KV_EMPTY);
+                    ATTN_TRACE(EV_LD_GOT, kv_it);
+                    if (!ok) break;
+                    if (static_cast<int32_t>(kv_it) != p.withheld_load && elect_one()) {
+                        mbar_arrive_expect_tx(B(ctl->kv_full[slot]), C::TILE_BYTES);
+                        const CUtensorMap *m = which ? &tmV : &tmK;
+                        for (int pn = 0; pn < C::NPANEL; ++pn)
+                            tma_load_3d(sKV + slot * C::TILE_BYTES + pn * C::PANEL_BYTES, m, B(ctl->kv_full[slot]),
+                                        pn * C::PANEL_ELEMS, j * C::BN, un.bh);
+                    }
+                    __syncwarp();
+                    ++kv_it;
                 }
-                if (q_it > 0)
-                    for (int t = 0; t < C::QT; ++t)
-                        drain_wait(B(ctl->q_full[t]), (q_it - 1) & 1u, p.timeout_ns);
             }
         }
+        {
+            // Wind-down: wait (bounded) for the last copies this warp issued,
+            // so that no copy lands after the CTA exits even when a consumer
+            // gave up (normally these have long completed).
+            const uint32_t first = kv_it > C::NSLOT ? kv_it - C::NSLOT : 0u;
+            for (uint32_t i = first; i < kv_it; ++i) {
+                if (static_cast<int32_t>(i) == p.withheld_load) continue;
+                drain_wait(B(ctl->kv_full[i % C::NSLOT]), (i / C::NSLOT) & 1u, p.timeout_ns);
+            }
+            if (q_it > 0)
+                for (int t = 0; t < C::QT; ++t)
+                    drain_wait(B(ctl->q_full[t]), (q_it - 1) & 1u, p.timeout_ns);
+        }
         __syncwarp();
-    } else if (warp == 8) {
+      } else if (warp == 8) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t kv_it = 0, q_it = 0;
-            uint32_t p_ph[2] = {0u, 0u};
-            bool ok = true;
-            auto kv_wait = [&](uint32_t &slot) -> bool {
-                slot = kv_it % C::NSLOT;
-                ATTN_TRACE(EV_MMA_WAIT_KV, kv_it);
-                bool r = bar_wait(B(ctl->kv_full[slot]), (kv_it / C::NSLOT) & 1u, ctl, p, SITE_MMA_KV_FULL);
-                ATTN_TRACE(EV_MMA_GOT_KV, kv_it);
-                ++kv_it;
-                return r;
-            };
-            // Low descriptor words of the first k-step; later k-steps add
-            // their byte offset >> 4 to the start-address field, which cannot
-            // carry (shared addresses stay below 2^18).
-            const uint32_t dq0 = desc_lo(sQ, 16);
-            const uint32_t dk0 = desc_lo(sKV, 16);
-            const uint32_t dv0 = desc_lo(sKV, C::PANEL_BYTES);
-            auto issue_qk = [&](int t, uint32_t kslot) {
-                const uint32_t a0 = dq0 + ((t * C::TILE_BYTES) >> 4);
-                const uint32_t b0 = dk0 + ((kslot * C::TILE_BYTES) >> 4);
-                const uint32_t d = tmem + C::TMEM_S + t * C::BN;
+        // The whole warp walks the schedule and waits; one elected lane (the
+        // same one every time: all lanes are active) issues the MMAs and the
+        // commits that track them.
+        uint32_t kv_it = 0, q_it = 0;
+        uint32_t p_ph0 = 0u, p_ph1 = 0u;
+        bool ok = true;
+        auto kv_wait = [&](uint32_t &slot) -> bool {
+            slot = kv_it % C::NSLOT;
+            ATTN_TRACE(EV_MMA_WAIT_KV, kv_it);
+            const bool r = warp_wait(B(ctl->kv_full[slot]), (kv_it / C::NSLOT) & 1u, ctl, p, SITE_MMA_KV_FULL);
+            ATTN_TRACE(EV_MMA_GOT_KV, kv_it);
+            ++kv_it;
+            return r;
+        };
+        // Low descriptor words of the first k-step; later k-steps add their
+        // byte offset >> 4 to the start-address field, which cannot carry
+        // (shared addresses stay below 2^18).
+        const uint32_t dq0 = desc_lo(sQ, 16);
+        const uint32_t dk0 = desc_lo(sKV, 16);
+        const uint32_t dv0 = desc_lo(sKV, C::PANEL_BYTES);
+        auto issue_qk = [&](int t, uint32_t kslot) {
+            const uint32_t a0 = dq0 + ((t * C::TILE_BYTES) >> 4);
+            const uint32_t b0 = dk0 + ((kslot * C::TILE_BYTES) >> 4);
+            const uint32_t d = tmem + C::TMEM_S + t * C::BN;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = ((kk / 4) * C::PANEL_BYTES + (kk % 4) * 32) >> 4;
-                    mma_ss(d, a0 + off, b0 + off, IDESC_QK, kk > 0 ? 1u : 0u);
-                }
-            };
-            auto issue_pv = [&](int t, uint32_t vslot, bool accumulate) {
-                const uint32_t b0 = dv0 + ((vslot * C::TILE_BYTES) >> 4);
-                const uint32_t a = tmem + C::TMEM_S + t * C::BN;  // P_t, 2 elements per column
-                const uint32_t d = tmem + C::TMEM_O + t * D;
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk / 4) * C::PANEL_BYTES + (kk % 4) * 32) >> 4;
+                mma_ss(d, a0 + off, b0 + off, IDESC_QK, kk > 0 ? 1u : 0u);
+            }
+        };
+        auto issue_pv = [&](int t, uint32_t vslot, bool accumulate) {
+            const uint32_t b0 = dv0 + ((vslot * C::TILE_BYTES) >> 4);
+            const uint32_t a = tmem + C::TMEM_S + t * C::BN;  // P_t, 2 elements per column
+            const uint32_t d = tmem + C::TMEM_O + t * D;
 #pragma unroll
-                for (int kk = 0; kk < C::BN / 16; ++kk)
-                    mma_ts(d, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
-            };
-            for (int i = 0; i * static_cast<int>(gridDim.x) < p.num_units && ok; ++i) {
-                const int u = unit_at(i);
-                if (u >= p.num_units) continue;
-                const Unit un = decode_unit<D, CAUSAL>(u, p);
-                if (un.n == 0) continue;
-                ATTN_TRACE(EV_MMA_WAIT_Q, u);
-                for (int t = 0; t < C::QT && ok; ++t)
-                    ok = bar_wait(B(ctl->q_full[t]), q_it & 1u, ctl, p, SITE_MMA_Q_FULL);
-                ATTN_TRACE(EV_MMA_GOT_Q, u);
-                if (!ok) break;
-                ++q_it;
-                uint32_t kslot;
-                if (!(ok = kv_wait(kslot))) break;
-                tc_fence_after();
+            for (int kk = 0; kk < C::BN / 16; ++kk)
+                mma_ts(d, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+        };
+        for (int i = 0; i * static_cast<int>(gridDim.x) < p.num_units && ok; ++i) {
+            const int u = unit_at(i);
+            if (u >= p.num_units) continue;
+            const Unit un = decode_unit<D, CAUSAL>(u, p);
+            if (un.n == 0) continue;
+            ATTN_TRACE(EV_MMA_WAIT_Q, u);
+            for (int t = 0; t < C::QT && ok; ++t)
+                ok = warp_wait(B(ctl->q_full[t]), q_it & 1u, ctl, p, SITE_MMA_Q_FULL);
+            ATTN_TRACE(EV_MMA_GOT_Q, u);
+            if (!ok) break;
+            ++q_it;
+            uint32_t kslot;
+            if (!(ok = kv_wait(kslot))) break;
+            tc_fence_after();
+            if (elect_one()) {
                 issue_qk(0, kslot);
                 tc_commit(B(ctl->s_full[0]));
                 issue_qk(1, kslot);
@@ -431,17 +445,20 @@ __global__ void __launch_bounds__(384, 1)
                     tc_commit(B(ctl->q_empty[0]));
                     tc_commit(B(ctl->q_empty[1]));
                 }
-                for (int j = 0; j < un.n && ok; ++j) {
-                    const bool more = j + 1 < un.n;
-                    uint32_t vslot, nslot = 0;
-                    if (!(ok = kv_wait(vslot))) break;
-                    if (more && !(ok = kv_wait(nslot))) break;
-                    // tile 0
-                    ATTN_TRACE(EV_MMA_WAIT_P, 0);
-                    if (!(ok = bar_wait(B(ctl->p_full[0]), p_ph[0], ctl, p, SITE_MMA_P_FULL))) break;
-                    ATTN_TRACE(EV_MMA_GOT_P, 0);
-                    p_ph[0] ^= 1u;
-                    tc_fence_after();
+            }
+            __syncwarp();
+            for (int j = 0; j < un.n && ok; ++j) {
+                const bool more = j + 1 < un.n;
+                uint32_t vslot, nslot = 0;
+                if (!(ok = kv_wait(vslot))) break;
+                if (more && !(ok = kv_wait(nslot))) break;
+                // tile 0
+                ATTN_TRACE(EV_MMA_WAIT_P, 0);
+                if (!(ok = warp_wait(B(ctl->p_full[0]), p_ph0, ctl, p, SITE_MMA_P_FULL))) break;
+                ATTN_TRACE(EV_MMA_GOT_P, 0);
+                p_ph0 ^= 1u;
+                tc_fence_after();
+                if (elect_one()) {
                     issue_pv(0, vslot, j > 0);
                     if (!more) tc_commit(B(ctl->o_full[0]));
                     if (more) {
@@ -449,12 +466,15 @@ __global__ void __launch_bounds__(384, 1)
                         tc_commit(B(ctl->s_full[0]));
                         if (j + 2 == un.n) tc_commit(B(ctl->q_empty[0]));
                     }
-                    // tile 1
-                    ATTN_TRACE(EV_MMA_WAIT_P, 1);
-                    if (!(ok = bar_wait(B(ctl->p_full[1]), p_ph[1], ctl, p, SITE_MMA_P_FULL))) break;
-                    ATTN_TRACE(EV_MMA_GOT_P, 1);
-                    p_ph[1] ^= 1u;
-                    tc_fence_after();
+                }
+                __syncwarp();
+                // tile 1
+                ATTN_TRACE(EV_MMA_WAIT_P, 1);
+                if (!(ok = warp_wait(B(ctl->p_full[1]), p_ph1, ctl, p, SITE_MMA_P_FULL))) break;
+                ATTN_TRACE(EV_MMA_GOT_P, 1);
+                p_ph1 ^= 1u;
+                tc_fence_after();
+                if (elect_one()) {
                     issue_pv(1, vslot, j > 0);
                     tc_commit(B(ctl->kv_empty[vslot]));
                     if (!more) tc_commit(B(ctl->o_full[1]));
@@ -465,11 +485,13 @@ __global__ void __launch_bounds__(384, 1)
                         if (j + 2 == un.n) tc_commit(B(ctl->q_empty[1]));
                     }
                 }
+                __syncwarp();
             }
-            // Every MMA issued must complete before tensor memory is freed.
-            tc_commit(B(ctl->mma_done));
-            drain_wait(B(ctl->mma_done), 0u, p.timeout_ns);
         }
+        // Every MMA issued must complete before tensor memory is freed.
+        if (elect_one()) tc_commit(B(ctl->mma_done));
+        __syncwarp();
+        drain_wait(B(ctl->mma_done), 0u, p.timeout_ns);
         __syncwarp();
       }
     } else {

@@ -19,6 +19,16 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
+// One lane of a fully active warp (the lowest) returns true.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
@@ -42,20 +52,33 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
-// True once the phase with the given parity has completed.  While it has
-// not, the hardware may suspend the thread for up to `suspend_ns` (it wakes
-// early when the phase completes), so a waiting warp does not spin through
-// issue slots that the warps sharing its SM sub-partition need.
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t suspend_ns = 0x100000u)
+// True once the phase with the given parity has completed.  With a nonzero
+// ATTN_MBAR_SUSPEND_NS the hardware may suspend the waiting thread for up to
+// that long (waking early when the phase completes) instead of returning
+// at once.
+#ifndef ATTN_MBAR_SUSPEND_NS
+#define ATTN_MBAR_SUSPEND_NS 0
+#endif
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
+#if ATTN_MBAR_SUSPEND_NS > 0
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(suspend_ns)
+        : "r"(bar), "r"(parity), "r"(static_cast<uint32_t>(ATTN_MBAR_SUSPEND_NS))
         : "memory");
+#else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+#endif
     return ok != 0;
 }
 

@@ -326,11 +326,7 @@ __global__ void __launch_bounds__(384, 1)
       if (warp == 9) {
         // ------------------------------------------------------------ producer
         // The whole warp walks the schedule, so counters and addresses are
-        // warp-uniform; one elected lane issues the copies.  L2 policies:
-        // Q is read by one unit only; each K/V tile is read again by the
-        // other units of its head that run at the same time.
-        const uint64_t pol_q = l2_policy_q();
-        const uint64_t pol_kv = l2_policy_kv();
+        // warp-uniform; one elected lane issues the copies.
         uint32_t kv_it = 0, q_it = 0;
         bool ok = true;
         for (int i = 0; i * static_cast<int>(gridDim.x) < p.num_units && ok; ++i) {
@@ -345,7 +341,7 @@ __global__ void __launch_bounds__(384, 1)
                     mbar_arrive_expect_tx(B(ctl->q_full[t]), C::TILE_BYTES);
                     for (int pn = 0; pn < C::NPANEL; ++pn)
                         tma_load_3d(sQ + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tmQ, B(ctl->q_full[t]),
-                                    pn * C::PANEL_ELEMS, un.row0 + t * C::BM, un.bh, pol_q);
+                                    pn * C::PANEL_ELEMS, un.row0 + t * C::BM, un.bh);
                 }
                 __syncwarp();
             }
@@ -364,7 +360,7 @@ __global__ void __launch_bounds__(384, 1)
                         const CUtensorMap *m = which ? &tmV : &tmK;
                         for (int pn = 0; pn < C::NPANEL; ++pn)
                             tma_load_3d(sKV + slot * C::TILE_BYTES + pn * C::PANEL_BYTES, m, B(ctl->kv_full[slot]),
-                                        pn * C::PANEL_ELEMS, j * C::BN, un.bh, pol_kv);
+                                        pn * C::PANEL_ELEMS, j * C::BN, un.bh);
                     }
                     __syncwarp();
                     ++kv_it;
@@ -454,8 +450,8 @@ __global__ void __launch_bounds__(384, 1)
             for (int j = 0; j < un.n && ok; ++j) {
                 const bool more = j + 1 < un.n;
                 uint32_t vslot, nslot = 0;
-                // V_j gates only the P.V products; K_{j+1} only the next S.
                 if (!(ok = kv_wait(vslot))) break;
+                if (more && !(ok = kv_wait(nslot))) break;
                 // tile 0
                 ATTN_TRACE(EV_MMA_WAIT_P, 0);
                 if (!(ok = warp_wait(B(ctl->p_full[0]), p_ph0, ctl, p, SITE_MMA_P_FULL))) break;
@@ -465,18 +461,13 @@ __global__ void __launch_bounds__(384, 1)
                 if (elect_one()) {
                     issue_pv(0, vslot, j > 0);
                     if (!more) tc_commit(B(ctl->o_full[0]));
-                }
-                __syncwarp();
-                if (more) {
-                    if (!(ok = kv_wait(nslot))) break;
-                    tc_fence_after();
-                    if (elect_one()) {
+                    if (more) {
                         issue_qk(0, nslot);
                         tc_commit(B(ctl->s_full[0]));
                         if (j + 2 == un.n) tc_commit(B(ctl->q_empty[0]));
                     }
-                    __syncwarp();
                 }
+                __syncwarp();
                 // tile 1
                 ATTN_TRACE(EV_MMA_WAIT_P, 1);
                 if (!(ok = warp_wait(B(ctl->p_full[1]), p_ph1, ctl, p, SITE_MMA_P_FULL))) break;

@@ -89,37 +89,16 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// 3-D tiled load global -> shared, completion counted on `bar` in bytes,
-// with an L2 cache policy (createpolicy) for the source lines.
+// 3-D tiled load global -> shared, completion counted on `bar` in bytes.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                            int32_t c0, int32_t c1, int32_t c2, uint64_t policy)
+                                            int32_t c0, int32_t c1, int32_t c2)
 {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
-
-// L2 policies of the Q and K/V streams.  ATTN_L2_HINTS selects them:
-// 0 = evict_normal for both, 1 = Q evict_first and K/V evict_last,
-// 2 = Q evict_first and K/V evict_normal.
-#ifndef ATTN_L2_HINTS
-#define ATTN_L2_HINTS 0
-#endif
-__device__ __forceinline__ uint64_t l2_policy(int kind)
-{
-    uint64_t pol;
-    if (kind == 1)
-        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    else if (kind == 2)
-        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-    else
-        asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-__device__ __forceinline__ uint64_t l2_policy_q() { return l2_policy(ATTN_L2_HINTS == 0 ? 0 : 1); }
-__device__ __forceinline__ uint64_t l2_policy_kv() { return l2_policy(ATTN_L2_HINTS == 1 ? 2 : 0); }
 
 // ---------------------------------------------------------------- tcgen05
 

@@ -12,7 +12,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
-#include "../../include/attn_fwd.h"
+#include "attn_fwd.h"
 #include "launch.h"
 
 namespace {

@@ -256,6 +256,99 @@ __device__ __forceinline__ float add_halves<__half>(uint32_t u, float acc)
     return add_halves_f16(u, acc);
 }
 
+// Columns >= lim of this row get the identity of the row reduction (+inf
+// for a min, -inf for a max), so they neither set the extreme nor, after
+// exp_store_tile's own mask, contribute a probability.
+__device__ __forceinline__ void mask_columns(uint32_t (&sr)[128], int lim, bool neg)
+{
+    const uint32_t ident = __float_as_uint(neg ? INFINITY : -INFINITY);
+#pragma unroll
+    for (int c = 0; c < 128; ++c) sr[c] = (c < lim) ? sr[c] : ident;
+}
+
+// Row maximum (minimum when NEG) of the 128 raw logits, 3-input max/min in
+// four independent chains.
+template <bool NEG>
+__device__ __forceinline__ float row_extreme(const uint32_t (&sr)[128])
+{
+    float r[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] = __uint_as_float(sr[i]);
+#pragma unroll
+    for (int c = 4; c < 124; c += 8)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float a = __uint_as_float(sr[c + 2 * i]), b = __uint_as_float(sr[c + 2 * i + 1]);
+            r[i] = NEG ? min3f(r[i], a, b) : max3f(r[i], a, b);
+        }
+    // columns 124..127
+    r[0] = NEG ? min3f(r[0], __uint_as_float(sr[124]), __uint_as_float(sr[125]))
+               : max3f(r[0], __uint_as_float(sr[124]), __uint_as_float(sr[125]));
+    r[1] = NEG ? min3f(r[1], __uint_as_float(sr[126]), __uint_as_float(sr[127]))
+               : max3f(r[1], __uint_as_float(sr[126]), __uint_as_float(sr[127]));
+    return NEG ? min3f(r[0], r[1], fminf(r[2], r[3])) : max3f(r[0], r[1], fmaxf(r[2], r[3]));
+}
+
+// O row *= alpha in tensor memory (D fp32 columns of this thread's lane).
+template <int D>
+__device__ __forceinline__ void rescale_rows(uint32_t tO, float alpha)
+{
+    const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t orr[32];
+        tmem_ld32_wait(tO + ch * 32, orr);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const float2 v = __fmul2_rn(make_float2(__uint_as_float(orr[2 * c]), __uint_as_float(orr[2 * c + 1])), a2);
+            orr[2 * c] = __float_as_uint(v.x);
+            orr[2 * c + 1] = __float_as_uint(v.y);
+        }
+        tmem_st32(tO + ch * 32, orr);
+    }
+}
+
+// p = 2^(s*sl2e - m_use) for the 128 columns of this row; P (rounded to T,
+// two per 32-bit column) is stored into the first 64 tensor-memory columns
+// at tS (the first half as soon as it is ready).  Returns {sum of p, sum
+// of p as rounded}.  The caller waits for the stores (tmem_wait_st).
+template <typename T, bool MASKED>
+__device__ __forceinline__ float2 exp_store_tile(const uint32_t (&sr)[128], int lim, float sl2e, float m_use, uint32_t tS)
+{
+    const float2 sc2 = make_float2(sl2e, sl2e);
+    const float2 nm2 = make_float2(-m_use, -m_use);
+    float2 l4[4];
+    float lr4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        l4[i] = make_float2(0.f, 0.f);
+        lr4[i] = 0.f;
+    }
+    uint32_t pa[32], pb[32];
+#pragma unroll
+    for (int c = 0; c < 64; ++c) {
+        float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sc2, nm2);
+        if (MASKED) {
+            x.x = (2 * c < lim) ? x.x : -INFINITY;
+            x.y = (2 * c + 1 < lim) ? x.y : -INFINITY;
+        }
+        const float p0 = ex2_approx(x.x);
+        const float p1 = ex2_approx(x.y);
+        l4[c & 3] = __fadd2_rn(l4[c & 3], make_float2(p0, p1));
+        const uint32_t pk = pack2<T>(p0, p1);
+        lr4[c & 3] = add_halves<T>(pk, lr4[c & 3]);
+        if (c < 32)
+            pa[c] = pk;
+        else
+            pb[c - 32] = pk;
+        if (c == 31) tmem_st32(tS, pa);  // overlaps the second half
+    }
+    tmem_st32(tS + 32, pb);
+    const float2 a = __fadd2_rn(l4[0], l4[1]);
+    const float2 b = __fadd2_rn(l4[2], l4[3]);
+    return make_float2((a.x + a.y) + (b.x + b.y), (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]));
+}
+
 template <typename T>
 __device__ __forceinline__ void store_row_zero(const FwdParams &p, int bh, int row, int D)
 {
@@ -533,59 +626,24 @@ __global__ void __launch_bounds__(384, 1)
                 tmem_ld128_wait(tS, sr);
                 ATTN_TRACE(EV_SM_LD, j);
                 const int lim = kend - j * C::BN;  // columns >= lim are masked
-                const bool masked = lim < C::BN;
-                // row max of the raw logits (min when the scale is negative),
-                // masked columns excluded
-                const float ident = neg ? INFINITY : -INFINITY;
-                if (masked) {
-#pragma unroll
-                    for (int c = 0; c < 128; ++c)
-                        sr[c] = (c < lim) ? sr[c] : __float_as_uint(ident);
-                }
-                float r4[4];
-                if (!neg) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) r4[i] = __uint_as_float(sr[i]);
-#pragma unroll
-                    for (int c = 4; c < 128; c += 8)
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            r4[i] = (c + 2 * i + 1 < 128)
-                                        ? max3f(r4[i], __uint_as_float(sr[c + 2 * i]), __uint_as_float(sr[c + 2 * i + 1]))
-                                        : r4[i];
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) r4[i] = __uint_as_float(sr[i]);
-#pragma unroll
-                    for (int c = 4; c < 128; c += 8)
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            r4[i] = (c + 2 * i + 1 < 128)
-                                        ? min3f(r4[i], __uint_as_float(sr[c + 2 * i]), __uint_as_float(sr[c + 2 * i + 1]))
-                                        : r4[i];
-                }
-                const float mraw = neg ? fminf(fminf(r4[0], r4[1]), fminf(r4[2], r4[3]))
-                                       : fmaxf(fmaxf(r4[0], r4[1]), fmaxf(r4[2], r4[3]));
-                const float mx = (mraw == ident) ? -INFINITY : mraw * sl2e;
+                // Only diagonal and last tiles need the mask; the warp takes
+                // one path or the other as a whole, so full tiles carry no
+                // per-element mask work.
+                const bool masked = __any_sync(0xffffffffu, lim < C::BN);
+                if (masked) mask_columns(sr, lim, neg);
+                float mraw;
+                if (neg)
+                    mraw = row_extreme<true>(sr);
+                else
+                    mraw = row_extreme<false>(sr);
+                // a row with no visible key in this tile contributes nothing
+                const float mx = (mraw == (neg ? INFINITY : -INFINITY)) ? -INFINITY : mraw * sl2e;
                 const float m_new = fmaxf(m, mx);
                 if (j > 0) {
                     const bool need = (m_new - m) > C::TAU;
                     if (__any_sync(0xffffffffu, need)) {
                         const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m - m_new);
-                        const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-                        for (int ch = 0; ch < D / 32; ++ch) {
-                            uint32_t orr[32];
-                            tmem_ld32_wait(tO + ch * 32, orr);
-#pragma unroll
-                            for (int c = 0; c < 16; ++c) {
-                                float2 v = __fmul2_rn(make_float2(__uint_as_float(orr[2 * c]),
-                                                                  __uint_as_float(orr[2 * c + 1])), a2);
-                                orr[2 * c] = __float_as_uint(v.x);
-                                orr[2 * c + 1] = __float_as_uint(v.y);
-                            }
-                            tmem_st32(tO + ch * 32, orr);
-                        }
+                        rescale_rows<D>(tO, alpha);
                         l *= alpha;
                         lr *= alpha;
                         m = m_new;
@@ -596,43 +654,14 @@ __global__ void __launch_bounds__(384, 1)
                 }
                 ATTN_TRACE(EV_SM_MAX, j);
                 const float m_use = (m == -INFINITY) ? 0.f : m;
-                const float2 sc2 = make_float2(sl2e, sl2e);
-                const float2 nm2 = make_float2(-m_use, -m_use);
-                float2 l4[4];
-                float lr4[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    l4[i] = make_float2(0.f, 0.f);
-                    lr4[i] = 0.f;
-                }
-                uint32_t pa[32], pb[32];
-#pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])),
-                                          sc2, nm2);
-                    if (masked) {
-                        x.x = (2 * c < lim) ? x.x : -INFINITY;
-                        x.y = (2 * c + 1 < lim) ? x.y : -INFINITY;
-                    }
-                    const float p0 = ex2_approx(x.x);
-                    const float p1 = ex2_approx(x.y);
-                    l4[c & 3] = __fadd2_rn(l4[c & 3], make_float2(p0, p1));
-                    const uint32_t pk = pack2<T>(p0, p1);
-                    lr4[c & 3] = add_halves<T>(pk, lr4[c & 3]);
-                    if (c < 32)
-                        pa[c] = pk;
-                    else
-                        pb[c - 32] = pk;
-                    if (c == 31) tmem_st32(tS, pa);  // overlaps the second half
-                }
-                {
-                    const float2 a = __fadd2_rn(l4[0], l4[1]);
-                    const float2 b = __fadd2_rn(l4[2], l4[3]);
-                    l += (a.x + a.y) + (b.x + b.y);
-                    lr += (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]);
-                }
+                float2 sums;  // {sum of p, sum of p as rounded}
+                if (masked)
+                    sums = exp_store_tile<T, true>(sr, lim, sl2e, m_use, tS);
+                else
+                    sums = exp_store_tile<T, false>(sr, lim, sl2e, m_use, tS);
+                l += sums.x;
+                lr += sums.y;
                 ATTN_TRACE(EV_SM_EXP, j);
-                tmem_st32(tS + 32, pb);
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(B(ctl->p_full[t]));

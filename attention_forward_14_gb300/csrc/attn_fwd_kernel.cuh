@@ -50,6 +50,14 @@
 
 namespace attn {
 
+// Build options of the producer (see the producer warp).
+#ifndef ATTN_KV_PREFETCH
+#define ATTN_KV_PREFETCH 3
+#endif
+#ifndef ATTN_Q_EVICT_FIRST
+#define ATTN_Q_EVICT_FIRST 1
+#endif
+
 struct FwdParams {
     void *o;               // [bh, sq, D] of T
     float *lse;            // [bh, sq] or nullptr
@@ -266,27 +274,24 @@ __device__ __forceinline__ void mask_columns(uint32_t (&sr)[128], int lim, bool 
     for (int c = 0; c < 128; ++c) sr[c] = (c < lim) ? sr[c] : ident;
 }
 
-// Row maximum (minimum when NEG) of the 128 raw logits, 3-input max/min in
-// four independent chains.
+// Row maximum (minimum when NEG) of the 128 raw logits: eight independent
+// chains (chain i takes columns i, i+8, ..., i+120) of 3-input max/min.
 template <bool NEG>
 __device__ __forceinline__ float row_extreme(const uint32_t (&sr)[128])
 {
-    float r[4];
+    auto f3 = [](float a, float b, float c) { return NEG ? min3f(a, b, c) : max3f(a, b, c); };
+    auto f2 = [](float a, float b) { return NEG ? fminf(a, b) : fmaxf(a, b); };
+    auto col = [&](int i, int k) { return __uint_as_float(sr[i + 8 * k]); };
+    float r[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) r[i] = __uint_as_float(sr[i]);
+    for (int i = 0; i < 8; ++i) {
+        r[i] = f3(col(i, 0), col(i, 1), col(i, 2));
 #pragma unroll
-    for (int c = 4; c < 124; c += 8)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float a = __uint_as_float(sr[c + 2 * i]), b = __uint_as_float(sr[c + 2 * i + 1]);
-            r[i] = NEG ? min3f(r[i], a, b) : max3f(r[i], a, b);
-        }
-    // columns 124..127
-    r[0] = NEG ? min3f(r[0], __uint_as_float(sr[124]), __uint_as_float(sr[125]))
-               : max3f(r[0], __uint_as_float(sr[124]), __uint_as_float(sr[125]));
-    r[1] = NEG ? min3f(r[1], __uint_as_float(sr[126]), __uint_as_float(sr[127]))
-               : max3f(r[1], __uint_as_float(sr[126]), __uint_as_float(sr[127]));
-    return NEG ? min3f(r[0], r[1], fminf(r[2], r[3])) : max3f(r[0], r[1], fmaxf(r[2], r[3]));
+        for (int k = 3; k < 15; k += 2) r[i] = f3(r[i], col(i, k), col(i, k + 1));
+        r[i] = f2(r[i], col(i, 15));
+    }
+    const float a = f3(r[0], r[1], r[2]), b = f3(r[3], r[4], r[5]);
+    return f3(a, b, f2(r[6], r[7]));
 }
 
 // O row *= alpha in tensor memory (D fp32 columns of this thread's lane).
@@ -419,7 +424,12 @@ __global__ void __launch_bounds__(384, 1)
       if (warp == 9) {
         // ------------------------------------------------------------ producer
         // The whole warp walks the schedule, so counters and addresses are
-        // warp-uniform; one elected lane issues the copies.
+        // warp-uniform; one elected lane issues the copies.  Q is read by
+        // one unit only (evict-first in L2).  Each K/V tile is requested
+        // from L2 ATTN_KV_PREFETCH tiles ahead of its load, so that the load
+        // (issued only when a ring slot frees up) finds it there.
+        const uint64_t pol_q = ATTN_Q_EVICT_FIRST ? l2_evict_first() : l2_evict_normal();
+        const uint64_t pol_kv = l2_evict_normal();
         uint32_t kv_it = 0, q_it = 0;
         bool ok = true;
         for (int i = 0; i * static_cast<int>(gridDim.x) < p.num_units && ok; ++i) {
@@ -434,13 +444,28 @@ __global__ void __launch_bounds__(384, 1)
                     mbar_arrive_expect_tx(B(ctl->q_full[t]), C::TILE_BYTES);
                     for (int pn = 0; pn < C::NPANEL; ++pn)
                         tma_load_3d(sQ + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tmQ, B(ctl->q_full[t]),
-                                    pn * C::PANEL_ELEMS, un.row0 + t * C::BM, un.bh);
+                                    pn * C::PANEL_ELEMS, un.row0 + t * C::BM, un.bh, pol_q);
                 }
                 __syncwarp();
             }
             if (!ok) break;
             ++q_it;
+            if (ATTN_KV_PREFETCH > 0 && elect_one()) {
+                for (int jj = 0; jj < ATTN_KV_PREFETCH && jj < un.n; ++jj)
+                    for (int pn = 0; pn < C::NPANEL; ++pn) {
+                        tma_prefetch_3d(&tmK, pn * C::PANEL_ELEMS, jj * C::BN, un.bh);
+                        tma_prefetch_3d(&tmV, pn * C::PANEL_ELEMS, jj * C::BN, un.bh);
+                    }
+            }
+            __syncwarp();
             for (int j = 0; j < un.n && ok; ++j) {
+                if (ATTN_KV_PREFETCH > 0 && j + ATTN_KV_PREFETCH < un.n && elect_one()) {
+                    for (int pn = 0; pn < C::NPANEL; ++pn) {
+                        tma_prefetch_3d(&tmK, pn * C::PANEL_ELEMS, (j + ATTN_KV_PREFETCH) * C::BN, un.bh);
+                        tma_prefetch_3d(&tmV, pn * C::PANEL_ELEMS, (j + ATTN_KV_PREFETCH) * C::BN, un.bh);
+                    }
+                }
+                __syncwarp();
                 for (int which = 0; which < 2; ++which) {
                     const uint32_t slot = kv_it % C::NSLOT;
                     ATTN_TRACE(EV_LD_WAIT, kv_it);
@@ -453,7 +478,7 @@ __global__ void __launch_bounds__(384, 1)
                         const CUtensorMap *m = which ? &tmV : &tmK;
                         for (int pn = 0; pn < C::NPANEL; ++pn)
                             tma_load_3d(sKV + slot * C::TILE_BYTES + pn * C::PANEL_BYTES, m, B(ctl->kv_full[slot]),
-                                        pn * C::PANEL_ELEMS, j * C::BN, un.bh);
+                                        pn * C::PANEL_ELEMS, j * C::BN, un.bh, pol_kv);
                     }
                     __syncwarp();
                     ++kv_it;

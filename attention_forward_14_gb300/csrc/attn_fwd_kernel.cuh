@@ -52,10 +52,10 @@ namespace attn {
 
 // Build options of the producer (see the producer warp).
 #ifndef ATTN_KV_PREFETCH
-#define ATTN_KV_PREFETCH 3
+#define ATTN_KV_PREFETCH 0
 #endif
 #ifndef ATTN_Q_EVICT_FIRST
-#define ATTN_Q_EVICT_FIRST 1
+#define ATTN_Q_EVICT_FIRST 0
 #endif
 
 struct FwdParams {

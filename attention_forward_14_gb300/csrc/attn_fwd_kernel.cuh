@@ -143,7 +143,7 @@ struct Cfg {
 struct Ctl {
     uint64_t q_full[2], q_empty[2];
     uint64_t kv_full[8], kv_empty[8];
-    uint64_t s_full[2], p_full[2], o_full[2];
+    uint64_t s_full[2], p_half[2], p_full[2], o_full[2];
     uint64_t mma_done;
     uint32_t tmem_base;
     uint32_t abort;
@@ -315,10 +315,13 @@ __device__ __forceinline__ void rescale_rows(uint32_t tO, float alpha)
 
 // p = 2^(s*sl2e - m_use) for the 128 columns of this row; P (rounded to T,
 // two per 32-bit column) is stored into the first 64 tensor-memory columns
-// at tS (the first half as soon as it is ready).  Returns {sum of p, sum
-// of p as rounded}.  The caller waits for the stores (tmem_wait_st).
+// at tS.  The first half (keys 0..63) is stored and announced on `half_bar`
+// as soon as it is ready, so the P.V product can start on it while the
+// second half is computed.  Returns {sum of p, sum of p as rounded}.  The
+// caller waits for the second store (tmem_wait_st) and announces it.
 template <typename T, bool MASKED>
-__device__ __forceinline__ float2 exp_store_tile(const uint32_t (&sr)[128], int lim, float sl2e, float m_use, uint32_t tS)
+__device__ __forceinline__ float2 exp_store_tile(const uint32_t (&sr)[128], int lim, float sl2e, float m_use, uint32_t tS,
+                                                 uint32_t half_bar)
 {
     const float2 sc2 = make_float2(sl2e, sl2e);
     const float2 nm2 = make_float2(-m_use, -m_use);
@@ -346,7 +349,12 @@ __device__ __forceinline__ float2 exp_store_tile(const uint32_t (&sr)[128], int 
             pa[c] = pk;
         else
             pb[c - 32] = pk;
-        if (c == 31) tmem_st32(tS, pa);  // overlaps the second half
+        if (c == 31) {
+            tmem_st32(tS, pa);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(half_bar);
+        }
     }
     tmem_st32(tS + 32, pb);
     const float2 a = __fadd2_rn(l4[0], l4[1]);
@@ -392,6 +400,7 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(B(ctl->q_full[t]), 1);
             mbar_init(B(ctl->q_empty[t]), 1);
             mbar_init(B(ctl->s_full[t]), 1);
+            mbar_init(B(ctl->p_half[t]), 128);
             mbar_init(B(ctl->p_full[t]), 128);
             mbar_init(B(ctl->o_full[t]), 1);
         }
@@ -531,13 +540,16 @@ __global__ void __launch_bounds__(384, 1)
                 mma_ss(d, a0 + off, b0 + off, IDESC_QK, kk > 0 ? 1u : 0u);
             }
         };
-        auto issue_pv = [&](int t, uint32_t vslot, bool accumulate) {
+        // O_t (+)= P_t V over keys [64*half, 64*half + 64) of the tile.
+        auto issue_pv = [&](int t, uint32_t vslot, bool accumulate, int half) {
             const uint32_t b0 = dv0 + ((vslot * C::TILE_BYTES) >> 4);
             const uint32_t a = tmem + C::TMEM_S + t * C::BN;  // P_t, 2 elements per column
             const uint32_t d = tmem + C::TMEM_O + t * D;
 #pragma unroll
-            for (int kk = 0; kk < C::BN / 16; ++kk)
+            for (int k2 = 0; k2 < C::BN / 32; ++k2) {
+                const int kk = half * (C::BN / 32) + k2;
                 mma_ts(d, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+            }
         };
         for (int i = 0; i * static_cast<int>(gridDim.x) < p.num_units && ok; ++i) {
             const int u = unit_at(i);
@@ -572,12 +584,16 @@ __global__ void __launch_bounds__(384, 1)
                 if (more && !(ok = kv_wait(nslot))) break;
                 // tile 0
                 ATTN_TRACE(EV_MMA_WAIT_P, 0);
+                if (!(ok = warp_wait(B(ctl->p_half[0]), p_ph0, ctl, p, SITE_MMA_P_FULL))) break;
+                tc_fence_after();
+                if (elect_one()) issue_pv(0, vslot, j > 0, 0);
+                __syncwarp();
                 if (!(ok = warp_wait(B(ctl->p_full[0]), p_ph0, ctl, p, SITE_MMA_P_FULL))) break;
                 ATTN_TRACE(EV_MMA_GOT_P, 0);
                 p_ph0 ^= 1u;
                 tc_fence_after();
                 if (elect_one()) {
-                    issue_pv(0, vslot, j > 0);
+                    issue_pv(0, vslot, true, 1);
                     if (!more) tc_commit(B(ctl->o_full[0]));
                     if (more) {
                         issue_qk(0, nslot);
@@ -588,12 +604,16 @@ __global__ void __launch_bounds__(384, 1)
                 __syncwarp();
                 // tile 1
                 ATTN_TRACE(EV_MMA_WAIT_P, 1);
+                if (!(ok = warp_wait(B(ctl->p_half[1]), p_ph1, ctl, p, SITE_MMA_P_FULL))) break;
+                tc_fence_after();
+                if (elect_one()) issue_pv(1, vslot, j > 0, 0);
+                __syncwarp();
                 if (!(ok = warp_wait(B(ctl->p_full[1]), p_ph1, ctl, p, SITE_MMA_P_FULL))) break;
                 ATTN_TRACE(EV_MMA_GOT_P, 1);
                 p_ph1 ^= 1u;
                 tc_fence_after();
                 if (elect_one()) {
-                    issue_pv(1, vslot, j > 0);
+                    issue_pv(1, vslot, true, 1);
                     tc_commit(B(ctl->kv_empty[vslot]));
                     if (!more) tc_commit(B(ctl->o_full[1]));
                     if (more) {
@@ -681,9 +701,9 @@ __global__ void __launch_bounds__(384, 1)
                 const float m_use = (m == -INFINITY) ? 0.f : m;
                 float2 sums;  // {sum of p, sum of p as rounded}
                 if (masked)
-                    sums = exp_store_tile<T, true>(sr, lim, sl2e, m_use, tS);
+                    sums = exp_store_tile<T, true>(sr, lim, sl2e, m_use, tS, B(ctl->p_half[t]));
                 else
-                    sums = exp_store_tile<T, false>(sr, lim, sl2e, m_use, tS);
+                    sums = exp_store_tile<T, false>(sr, lim, sl2e, m_use, tS, B(ctl->p_half[t]));
                 l += sums.x;
                 lr += sums.y;
                 ATTN_TRACE(EV_SM_EXP, j);

@@ -3,6 +3,8 @@
 // build compiles them in parallel).
 #pragma once
 
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -17,13 +19,23 @@ struct LaunchArgs {
     cudaStream_t stream;
 };
 
+// The dynamic shared-memory opt-in is a per-device attribute of each
+// instance: set it the first time an instance runs on a device.
 template <int D, typename T, bool CAUSAL>
 cudaError_t launch_fwd(const LaunchArgs &a)
 {
     constexpr int smem = Cfg<D>::SMEM_BYTES;
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> ready[kMaxDev];
     auto kern = attn_fwd_kernel<D, T, CAUSAL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev || ready[dev].load(std::memory_order_acquire) == 0) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDev) ready[dev].store(1, std::memory_order_release);
+    }
     kern<<<a.grid, Cfg<D>::THREADS, smem, a.stream>>>(a.q, a.k, a.v, a.p);
     return cudaGetLastError();
 }

@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     AttnError,
     attn_fwd,
     attn_fwd_host,
+    attn_fwd_splitkv,
     lib_path,
     load,
     status,

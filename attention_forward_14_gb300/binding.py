@@ -21,7 +21,8 @@ ERRORS = {
     -5: "ATTN_ERR_SCALE", -6: "ATTN_ERR_ALIGN", -7: "ATTN_ERR_ARCH", -8: "ATTN_ERR_CUDA", -9: "ATTN_ERR_WATCHDOG",
 }
 # Every function include/attn_fwd.h declares.
-EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_last_error", "attn_fwd_status", "attn_fwd_status_clear",
+EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
+           "attn_fwd_splitkv_default_splits", "attn_last_error", "attn_fwd_status", "attn_fwd_status_clear",
            "attn_fwd_watchdog_selftest", "attn_version"]
 
 
@@ -42,6 +43,13 @@ def _bind(lib):
     lib.attn_fwd_host.restype = c_int
     lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                   i64, i64, i64, i64, i64, c_int, c_float, c_int, vp]
+    lib.attn_fwd_splitkv.restype = c_int
+    lib.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_float, c_int, c_int,
+                                     vp, i64, vp]
+    lib.attn_fwd_splitkv_workspace_bytes.restype = i64
+    lib.attn_fwd_splitkv_workspace_bytes.argtypes = [i64, i64, i64, i64, c_int]
+    lib.attn_fwd_splitkv_default_splits.restype = c_int
+    lib.attn_fwd_splitkv_default_splits.argtypes = [i64, i64, i64, i64, i64, c_int]
     lib.attn_last_error.restype = ctypes.c_char_p
     lib.attn_last_error.argtypes = []
     lib.attn_fwd_status.restype = c_int
@@ -130,6 +138,49 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, 
                           lse.data_ptr() if lse is not None else None,
                           b, h, sq, sk, d, int(bool(causal)), float(scale), _dtype_code(q),
                           _stream_handle(stream, q.device))
+    _check(rc, lib)
+    return o, lse
+
+
+def splitkv_workspace_bytes(b, h, sq, d, num_splits) -> int:
+    lib = load()
+    return _check(int(lib.attn_fwd_splitkv_workspace_bytes(b, h, sq, d, num_splits)), lib)
+
+
+def splitkv_default_splits(b, h, sq, sk, d, causal=False) -> int:
+    lib = load()
+    return _check(int(lib.attn_fwd_splitkv_default_splits(b, h, sq, sk, d, int(bool(causal)))), lib)
+
+
+def attn_fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = None, num_splits: int | None = None,
+                     o=None, lse=None, workspace=None, stream=None):
+    """Split-KV forward (same result as attn_fwd).  ``num_splits`` defaults
+    to the library's choice for the device; ``workspace`` (a CUDA uint8
+    tensor) is allocated with torch when not given.  Returns (o, lse)."""
+    import torch
+    lib = load()
+    b, h, sq, d = q.shape
+    sk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / float(d) ** 0.5
+    if num_splits is None:
+        with torch.cuda.device(q.device):
+            num_splits = splitkv_default_splits(b, h, sq, sk, d, causal)
+    need = splitkv_workspace_bytes(b, h, sq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((b, h, sq), dtype=torch.float32, device=q.device)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("lse", lse)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise AttnError(-2, f"{name} must be a contiguous CUDA tensor")
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                  b, h, sq, sk, d, int(bool(causal)), float(scale), _dtype_code(q), int(num_splits),
+                                  workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                  _stream_handle(stream, q.device))
     _check(rc, lib)
     return o, lse
 

@@ -149,8 +149,22 @@ cudaError_t dispatch_causal(const LaunchArgs &a, bool causal)
     return causal ? launch_fwd<D, T, true>(a) : launch_fwd<D, T, false>(a);
 }
 
+struct SplitArgs {
+    int num_splits = 1;
+    float *o_part = nullptr;
+    float *lse_part = nullptr;
+};
+
+int64_t kv_tiles(int64_t sk) { return (sk + 127) / 128; }
+
+int64_t splitkv_bytes(int64_t bh, int64_t sq, int64_t d, int64_t splits)
+{
+    return splits * bh * sq * (d + 2) * 4;
+}
+
 int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_t b, int64_t h, int64_t sq, int64_t sk,
-        int64_t d, int causal, float scale, int dtype, cudaStream_t stream, int withheld_load, uint64_t timeout_ns)
+        int64_t d, int causal, float scale, int dtype, cudaStream_t stream, int withheld_load, uint64_t timeout_ns,
+        const SplitArgs &split = SplitArgs())
 {
     bool nothing = false;
     int rc = validate(q, k, v, o, lse, b, h, sq, sk, d, scale, dtype, &nothing);
@@ -177,7 +191,11 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_
     p.sq = static_cast<int32_t>(sq);
     p.sk = static_cast<int32_t>(sk);
     p.num_mblk = static_cast<int32_t>((sq + 255) / 256);
-    const int64_t units = bh * p.num_mblk;
+    p.num_splits = split.num_splits;
+    p.tiles_per_split = static_cast<int32_t>((kv_tiles(sk) + split.num_splits - 1) / split.num_splits);
+    p.o_part = split.o_part;
+    p.lse_part = split.lse_part;
+    const int64_t units = bh * p.num_mblk * split.num_splits;
     if (units > INT32_MAX) return fail(ATTN_ERR_SHAPE, "too many work units (%lld)", (long long)units);
     p.num_units = static_cast<int32_t>(units);
     p.sl2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
@@ -194,6 +212,20 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_
     else
         e = (dtype == ATTN_BF16) ? dispatch_causal<128, __nv_bfloat16>(a, c) : dispatch_causal<128, __half>(a, c);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    if (split.num_splits > 1) {
+        const int64_t rows = bh * sq;
+        if (d == 64)
+            e = (dtype == ATTN_BF16) ? launch_splitkv_combine<__nv_bfloat16, 64>(split.o_part, split.lse_part, o, lse,
+                                                                               rows, split.num_splits, di->sm_count, stream)
+                                     : launch_splitkv_combine<__half, 64>(split.o_part, split.lse_part, o, lse, rows,
+                                                                         split.num_splits, di->sm_count, stream);
+        else
+            e = (dtype == ATTN_BF16) ? launch_splitkv_combine<__nv_bfloat16, 128>(split.o_part, split.lse_part, o, lse,
+                                                                                rows, split.num_splits, di->sm_count, stream)
+                                     : launch_splitkv_combine<__half, 128>(split.o_part, split.lse_part, o, lse, rows,
+                                                                          split.num_splits, di->sm_count, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    }
     return ATTN_OK;
 }
 
@@ -242,6 +274,63 @@ int attn_fwd_host(const void *q_host, const void *k_host, const void *v_host, vo
             cudaSuccess)
         return cuda_fail(e, "copy lse to host");
     return ATTN_OK;
+}
+
+int64_t attn_fwd_splitkv_workspace_bytes(int64_t b, int64_t h, int64_t sq, int64_t d, int num_splits)
+{
+    g_err.clear();
+    if (b < 0 || h < 0 || sq < 0 || (d != 64 && d != 128) || num_splits < 1 || num_splits > 1024)
+        return fail(ATTN_ERR_SHAPE, "invalid split-KV workspace query");
+    return num_splits == 1 ? 0 : splitkv_bytes(b * h, sq, d, num_splits);
+}
+
+int attn_fwd_splitkv_default_splits(int64_t b, int64_t h, int64_t sq, int64_t sk, int64_t d, int causal)
+{
+    g_err.clear();
+    (void)causal;
+    if (b < 0 || h < 0 || sq < 0 || sk < 0 || (d != 64 && d != 128))
+        return fail(ATTN_ERR_SHAPE, "invalid split-KV size query");
+    DeviceInfo *di = nullptr;
+    int rc = device_info(&di);
+    if (rc != ATTN_OK) return rc;
+    const int64_t units = b * h * ((sq + 255) / 256);
+    const int64_t tiles = kv_tiles(sk);
+    const int64_t target = 2 * static_cast<int64_t>(di->sm_count);  // two waves: the tail evens out
+    if (units <= 0 || tiles <= 1 || units >= target) return 1;
+    int64_t s = (target + units - 1) / units;
+    const int64_t cap = tiles / 2 > 1 ? tiles / 2 : 1;  // keep >= 2 tiles per split
+    if (s > cap) s = cap;
+    if (s > 1024) s = 1024;
+    return static_cast<int>(s < 1 ? 1 : s);
+}
+
+int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int64_t b, int64_t h,
+                     int64_t sq, int64_t sk, int64_t d, int causal, float scale, int dtype, int num_splits,
+                     void *workspace, int64_t workspace_bytes, void *stream)
+{
+    g_err.clear();
+    bool nothing = false;
+    int rc = validate(q, k, v, o, lse, b, h, sq, sk, d, scale, dtype, &nothing);
+    if (rc != ATTN_OK || nothing) return rc;
+    if (num_splits < 1 || num_splits > 1024) return fail(ATTN_ERR_SHAPE, "num_splits %d not in 1..1024", num_splits);
+    if (sk == 0 || num_splits == 1)
+        return run(q, k, v, o, lse, b, h, sq, sk, d, causal, scale, dtype, static_cast<cudaStream_t>(stream), -1,
+                   kDefaultTimeoutNs);
+    if (num_splits > kv_tiles(sk))
+        return fail(ATTN_ERR_SHAPE, "num_splits %d exceeds the %lld key tiles of 128", num_splits,
+                    (long long)kv_tiles(sk));
+    const int64_t need = splitkv_bytes(b * h, sq, d, num_splits);
+    if (!workspace) return fail(ATTN_ERR_NULL, "split-KV workspace is NULL (%lld bytes needed)", (long long)need);
+    if (!aligned(workspace, 16)) return fail(ATTN_ERR_ALIGN, "split-KV workspace must be 16-byte aligned");
+    if (workspace_bytes < need)
+        return fail(ATTN_ERR_SHAPE, "split-KV workspace of %lld bytes is smaller than the %lld needed",
+                    (long long)workspace_bytes, (long long)need);
+    SplitArgs sa;
+    sa.num_splits = num_splits;
+    sa.o_part = static_cast<float *>(workspace);
+    sa.lse_part = sa.o_part + static_cast<int64_t>(num_splits) * b * h * sq * d;
+    return run(q, k, v, o, lse, b, h, sq, sk, d, causal, scale, dtype, static_cast<cudaStream_t>(stream), -1,
+               kDefaultTimeoutNs, sa);
 }
 
 const char *attn_last_error(void) { return g_err.c_str(); }

@@ -69,6 +69,16 @@ struct FwdParams {
     float sl2e;            // scale * log2(e)
     uint64_t timeout_ns;   // bound of every wait
     int32_t withheld_load; // K/V load index never issued (watchdog self-test), -1 = none
+    // Split-KV: each (bh, row block) is cut into num_splits ranges of
+    // tiles_per_split K/V tiles.  With num_splits > 1 the kernel writes, per
+    // split, O normalised by its own rounded-P sum (fp32, o_part
+    // [split][bh][sq][D]) and two natural log-sum-exps (lse_part
+    // [split][bh][sq][2]: of the fp32 p, and of p as rounded); a combine
+    // kernel merges the splits.  num_splits == 1: o / lse written directly.
+    int32_t num_splits;
+    int32_t tiles_per_split;
+    float *o_part;
+    float *lse_part;
 #ifdef ATTN_TRACE_ENABLE
     unsigned long long *trace;  // per-warp event records (timeline builds only)
 #endif
@@ -151,7 +161,10 @@ struct Ctl {
 static_assert(sizeof(Ctl) <= 1024, "control block");
 
 struct Unit {
-    int bh, row0, n;
+    int bh, row0;
+    int jb;     // first K/V tile of the unit
+    int n;      // number of K/V tiles (0: the rows see no key in this range)
+    int split;  // split index (0 without split-KV)
 };
 
 template <int D, bool CAUSAL>
@@ -159,18 +172,22 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams &p)
 {
     using C = Cfg<D>;
     Unit un;
+    un.split = u % p.num_splits;
+    const int v = u / p.num_splits;  // (bh, row block) index
     int mblk;
     if (CAUSAL) {  // heaviest row blocks first
-        mblk = p.num_mblk - 1 - u / p.bh;
-        un.bh = u % p.bh;
+        mblk = p.num_mblk - 1 - v / p.bh;
+        un.bh = v % p.bh;
     } else {       // consecutive units share a head (K/V reuse in L2)
-        un.bh = u / p.num_mblk;
-        mblk = u % p.num_mblk;
+        un.bh = v / p.num_mblk;
+        mblk = v % p.num_mblk;
     }
     un.row0 = mblk * C::UNIT_ROWS;
-    int last = min(un.row0 + C::UNIT_ROWS - 1, p.sq - 1);
-    int kend = CAUSAL ? min(p.sk, last + 1 + (p.sk - p.sq)) : p.sk;
-    un.n = kend > 0 ? (kend + C::BN - 1) / C::BN : 0;
+    const int last = min(un.row0 + C::UNIT_ROWS - 1, p.sq - 1);
+    const int kend = CAUSAL ? min(p.sk, last + 1 + (p.sk - p.sq)) : p.sk;
+    const int n_all = kend > 0 ? (kend + C::BN - 1) / C::BN : 0;
+    un.jb = un.split * p.tiles_per_split;
+    un.n = max(0, min(n_all, un.jb + p.tiles_per_split) - un.jb);
     return un;
 }
 
@@ -363,9 +380,17 @@ __device__ __forceinline__ float2 exp_store_tile(const uint32_t (&sr)[128], int 
 }
 
 template <typename T>
-__device__ __forceinline__ void store_row_zero(const FwdParams &p, int bh, int row, int D)
+__device__ __forceinline__ void store_row_zero(const FwdParams &p, int bh, int row, int D, int split)
 {
     if (row >= p.sq) return;
+    if (p.num_splits > 1) {  // an empty split range: weight 0 in the combine
+        const size_t r = (static_cast<size_t>(split) * p.bh + bh) * p.sq + row;
+        float4 *dst = reinterpret_cast<float4 *>(p.o_part + r * D);
+        for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        p.lse_part[2 * r] = -INFINITY;
+        p.lse_part[2 * r + 1] = -INFINITY;
+        return;
+    }
     uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.o) + (static_cast<size_t>(bh) * p.sq + row) * D);
     for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
     if (p.lse) p.lse[static_cast<size_t>(bh) * p.sq + row] = -INFINITY;
@@ -462,16 +487,16 @@ __global__ void __launch_bounds__(384, 1)
             if (ATTN_KV_PREFETCH > 0 && elect_one()) {
                 for (int jj = 0; jj < ATTN_KV_PREFETCH && jj < un.n; ++jj)
                     for (int pn = 0; pn < C::NPANEL; ++pn) {
-                        tma_prefetch_3d(&tmK, pn * C::PANEL_ELEMS, jj * C::BN, un.bh);
-                        tma_prefetch_3d(&tmV, pn * C::PANEL_ELEMS, jj * C::BN, un.bh);
+                        tma_prefetch_3d(&tmK, pn * C::PANEL_ELEMS, (un.jb + jj) * C::BN, un.bh);
+                        tma_prefetch_3d(&tmV, pn * C::PANEL_ELEMS, (un.jb + jj) * C::BN, un.bh);
                     }
             }
             __syncwarp();
             for (int j = 0; j < un.n && ok; ++j) {
                 if (ATTN_KV_PREFETCH > 0 && j + ATTN_KV_PREFETCH < un.n && elect_one()) {
                     for (int pn = 0; pn < C::NPANEL; ++pn) {
-                        tma_prefetch_3d(&tmK, pn * C::PANEL_ELEMS, (j + ATTN_KV_PREFETCH) * C::BN, un.bh);
-                        tma_prefetch_3d(&tmV, pn * C::PANEL_ELEMS, (j + ATTN_KV_PREFETCH) * C::BN, un.bh);
+                        tma_prefetch_3d(&tmK, pn * C::PANEL_ELEMS, (un.jb + j + ATTN_KV_PREFETCH) * C::BN, un.bh);
+                        tma_prefetch_3d(&tmV, pn * C::PANEL_ELEMS, (un.jb + j + ATTN_KV_PREFETCH) * C::BN, un.bh);
                     }
                 }
                 __syncwarp();
@@ -487,7 +512,7 @@ __global__ void __launch_bounds__(384, 1)
                         const CUtensorMap *m = which ? &tmV : &tmK;
                         for (int pn = 0; pn < C::NPANEL; ++pn)
                             tma_load_3d(sKV + slot * C::TILE_BYTES + pn * C::PANEL_BYTES, m, B(ctl->kv_full[slot]),
-                                        pn * C::PANEL_ELEMS, j * C::BN, un.bh, pol_kv);
+                                        pn * C::PANEL_ELEMS, (un.jb + j) * C::BN, un.bh, pol_kv);
                     }
                     __syncwarp();
                     ++kv_it;
@@ -651,7 +676,7 @@ __global__ void __launch_bounds__(384, 1)
             const Unit un = decode_unit<D, CAUSAL>(u, p);
             const int row = un.row0 + t * C::BM + r_in_tile;
             if (un.n == 0) {
-                store_row_zero<T>(p, un.bh, row, D);
+                store_row_zero<T>(p, un.bh, row, D, un.split);
                 continue;
             }
             // keys visible to this row: [0, kend)
@@ -670,7 +695,7 @@ __global__ void __launch_bounds__(384, 1)
                 uint32_t sr[128];
                 tmem_ld128_wait(tS, sr);
                 ATTN_TRACE(EV_SM_LD, j);
-                const int lim = kend - j * C::BN;  // columns >= lim are masked
+                const int lim = kend - (un.jb + j) * C::BN;  // columns >= lim are masked
                 // Only diagonal and last tiles need the mask; the warp takes
                 // one path or the other as a whole, so full tiles carry no
                 // per-element mask work.
@@ -724,6 +749,31 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_after();
                 const float inv_l = (lr > 0.f) ? 1.f / lr : 0.f;
                 const bool valid = row < p.sq;
+                if (p.num_splits > 1) {
+                    // split partial: O / lr in fp32, both log-sum-exps
+                    const size_t r = (static_cast<size_t>(un.split) * p.bh + un.bh) * p.sq + (valid ? row : 0);
+                    float4 *dstf = reinterpret_cast<float4 *>(p.o_part + r * D);
+#pragma unroll
+                    for (int ch = 0; ch < D / 32; ++ch) {
+                        uint32_t orr[32];
+                        tmem_ld32_wait(tO + ch * 32, orr);
+                        if (valid) {
+#pragma unroll
+                            for (int v4 = 0; v4 < 8; ++v4)
+                                dstf[ch * 8 + v4] = make_float4(__uint_as_float(orr[4 * v4]) * inv_l,
+                                                                __uint_as_float(orr[4 * v4 + 1]) * inv_l,
+                                                                __uint_as_float(orr[4 * v4 + 2]) * inv_l,
+                                                                __uint_as_float(orr[4 * v4 + 3]) * inv_l);
+                        }
+                    }
+                    if (valid) {
+                        p.lse_part[2 * r] = (l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                        p.lse_part[2 * r + 1] = (lr > 0.f) ? (m + log2f(lr)) * 0.69314718055994531f : -INFINITY;
+                    }
+                    ATTN_TRACE(EV_SM_EPI_DONE, u);
+                    tc_fence_before();
+                    continue;
+                }
                 uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.o) +
                                                        (static_cast<size_t>(un.bh) * p.sq + (valid ? row : 0)) * D);
 #pragma unroll
@@ -757,6 +807,60 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 8) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// Split-KV combine: one warp per query row.  The splits of a row are
+// partial softmaxes over disjoint key ranges; merging them is the same
+// rescale-and-add step as the online recurrence over key tiles
+// (flash-attention-minimal forward_kernel), done once over the splits:
+//   LSE = ln sum_s exp(lse_s)                      (fp32 sums)
+//   O   = sum_s w_s O_s,  w_s = exp(lser_s - ln sum_t exp(lser_t))
+// where O_s is normalised by its own rounded-P sum and lser_s is the
+// log of that sum, so the weights applied to V still sum to one.
+template <typename T, int D>
+__global__ void __launch_bounds__(256)
+    attn_splitkv_combine_kernel(const float *o_part, const float *lse_part, T *o, float *lse, int64_t rows,
+                                int num_splits)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    constexpr int PER_LANE = D / 32;  // 4 (D = 128) or 2 (D = 64)
+    for (int64_t r = warp; r < rows; r += nwarps) {
+        float mx = -INFINITY, mxr = -INFINITY;
+        for (int sp = lane; sp < num_splits; sp += 32) {
+            mx = fmaxf(mx, lse_part[2 * (sp * rows + r)]);
+            mxr = fmaxf(mxr, lse_part[2 * (sp * rows + r) + 1]);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            mxr = fmaxf(mxr, __shfl_xor_sync(0xffffffffu, mxr, off));
+        }
+        float acc[PER_LANE];
+#pragma unroll
+        for (int i = 0; i < PER_LANE; ++i) acc[i] = 0.f;
+        float sum = 0.f, sumr = 0.f;
+        if (mxr != -INFINITY) {
+            for (int sp = 0; sp < num_splits; ++sp) {
+                const float ls = lse_part[2 * (sp * rows + r)];
+                const float lr = lse_part[2 * (sp * rows + r) + 1];
+                sum += expf(ls - mx);
+                const float w = expf(lr - mxr);
+                sumr += w;
+                if (w > 0.f) {
+                    const float *src = o_part + (sp * rows + r) * D + lane * PER_LANE;
+#pragma unroll
+                    for (int i = 0; i < PER_LANE; ++i) acc[i] += w * src[i];
+                }
+            }
+        }
+        const float inv = (sumr > 0.f) ? 1.f / sumr : 0.f;
+        T *dst = o + r * D + lane * PER_LANE;
+#pragma unroll
+        for (int i = 0; i < PER_LANE; ++i) dst[i] = T(acc[i] * inv);
+        if (lse && lane == 0) lse[r] = (mx == -INFINITY) ? -INFINITY : mx + logf(sum);
     }
 }
 

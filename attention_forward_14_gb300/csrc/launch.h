@@ -51,6 +51,19 @@ cudaError_t launch_fill_empty(void *o, float *lse, int64_t rows, int d, cudaStre
     return cudaGetLastError();
 }
 
+template <typename T, int D>
+cudaError_t launch_splitkv_combine(const float *o_part, const float *lse_part, void *o, float *lse, int64_t rows,
+                                   int num_splits, int sm_count, cudaStream_t stream)
+{
+    int64_t blocks = (rows + 7) / 8;  // one warp per row, 8 warps per block
+    const int64_t cap = static_cast<int64_t>(sm_count) * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    attn_splitkv_combine_kernel<T, D><<<static_cast<int>(blocks), 256, 0, stream>>>(
+        o_part, lse_part, static_cast<T *>(o), lse, rows, num_splits);
+    return cudaGetLastError();
+}
+
 #define ATTN_DECLARE_INSTANCE(D, T, C) extern template cudaError_t launch_fwd<D, T, C>(const LaunchArgs &);
 #define ATTN_DEFINE_INSTANCE(D, T, C) template cudaError_t launch_fwd<D, T, C>(const LaunchArgs &);
 

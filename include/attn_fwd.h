@@ -96,6 +96,45 @@ int attn_fwd_host(const void *q_host, const void *k_host, const void *v_host,
                   int64_t b, int64_t h, int64_t sq, int64_t sk, int64_t d,
                   int causal, float scale, int dtype, void *stream);
 
+/*
+ * Split-KV forward.  "05 · kernel 工程与四代演化" 2.1 lists split-KV kernels
+ * beside the forward and backward ones.  The key range of every (b, h,
+ * 256-row block) is cut into `num_splits` ranges of whole 128-key tiles,
+ * processed by separate CTAs (this fills the GPU when b*h*ceil(sq/256) is
+ * small, as in decoding).  Each range yields a partial softmax: O normalised
+ * by its own row sum plus the range's log-sum-exp.  A second kernel merges
+ * the ranges with the rescale-and-add step of the online recurrence
+ * (flash-attention-minimal forward_kernel: m_new = max, l_new = sum of
+ * e^(m - m_new) l, O weighted accordingly).  Result and semantics are those
+ * of attn_fwd.
+ *
+ *   num_splits : 1..min(1024, ceil(sk / 128)); 1 runs attn_fwd directly.
+ *   workspace  : caller-owned device scratch, 16-byte aligned, at least
+ *                attn_fwd_splitkv_workspace_bytes(b, h, sq, d, num_splits)
+ *                bytes (fp32 partial O [num_splits, b, h, sq, d] followed by
+ *                2 fp32 log-sum-exps per partial row).  Its contents on
+ *                entry do not matter; calls on different streams need
+ *                different workspaces.
+ * Returns ATTN_OK or a negative ATTN_ERR_* code (ATTN_ERR_SHAPE for a bad
+ * split count or a too small workspace, ATTN_ERR_NULL for a missing one).
+ */
+int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o,
+                     float *lse, int64_t b, int64_t h, int64_t sq, int64_t sk,
+                     int64_t d, int causal, float scale, int dtype,
+                     int num_splits, void *workspace, int64_t workspace_bytes,
+                     void *stream);
+
+/* Bytes of workspace attn_fwd_splitkv needs (0 when num_splits == 1), or a
+ * negative ATTN_ERR_* code for invalid sizes. */
+int64_t attn_fwd_splitkv_workspace_bytes(int64_t b, int64_t h, int64_t sq,
+                                         int64_t d, int num_splits);
+
+/* A split count that gives the current device at least two work units per
+ * SM while keeping at least two key tiles per split (1 when the problem
+ * already has that many units), or a negative ATTN_ERR_* code. */
+int attn_fwd_splitkv_default_splits(int64_t b, int64_t h, int64_t sq,
+                                    int64_t sk, int64_t d, int causal);
+
 /* Thread-local message describing the last non-OK return on this thread
  * ("" if none).  The pointer stays valid until the next call on the thread. */
 const char *attn_last_error(void);

@@ -83,3 +83,22 @@ def test_no_device_gives_error_not_crash(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(af.AttnError):
         binding.load(str(tmp_path / "missing.so"))
+
+
+def test_splitkv_workspace_size(lib):
+    assert lib.attn_fwd_splitkv_workspace_bytes(2, 3, 5, 128, 4) == 4 * 2 * 3 * 5 * (128 + 2) * 4
+    assert lib.attn_fwd_splitkv_workspace_bytes(2, 3, 5, 64, 1) == 0
+    assert lib.attn_fwd_splitkv_workspace_bytes(2, 3, 5, 96, 4) == -2
+    assert lib.attn_fwd_splitkv_workspace_bytes(2, 3, 5, 128, 0) == -2
+
+
+@pytest.mark.parametrize("splits,ws,ws_bytes,code", [
+    (0, P, 1 << 20, -2), (2000, P, 1 << 20, -2),
+    (9, P, 1 << 20, -2),          # 1000 keys = 8 tiles of 128
+    (4, None, 1 << 20, -1),       # missing workspace
+    (4, P, 16, -2),               # too small
+    (4, P + 8, 1 << 20, -6),      # misaligned
+])
+def test_splitkv_argument_errors(lib, splits, ws, ws_bytes, code):
+    rc = lib.attn_fwd_splitkv(P, P, P, P, None, 1, 2, 3, 1000, 128, 0, 0.1, 1, splits, ws, ws_bytes, None)
+    assert rc == code, (rc, lib.attn_last_error())

@@ -34,6 +34,7 @@ class Workload:
     causal: bool
     qk_std: float
     seed: int
+    splitkv: bool = False  # run through the split-KV entry point (decode shapes)
 
     @property
     def scale(self) -> float:
@@ -63,9 +64,13 @@ WORKLOADS = {
         Workload("noncausal_b8_h16_s1000_d64_bf16", 8, 16, 1000, 1000, 64, "bf16", False, 1.0, 20260002),
         Workload("causal_b2_h32_s4096_d128_bf16", 2, 32, 4096, 4096, 128, "bf16", True, 1.0, 20260003),
         Workload("causal_b1_h32_s16384_d128_bf16_qk3", 1, 32, 16384, 16384, 128, "bf16", True, 3.0, 20260004),
+        # decode step: one query row per (batch, head) against a 16k-key cache
+        Workload("decode_b8_h32_q1_s16384_d128_bf16", 8, 32, 1, 16384, 128, "bf16", False, 1.0, 20260005,
+                 splitkv=True),
     ]
 }
-ORDER = list(WORKLOADS)
+ORDER = [n for n in WORKLOADS if not WORKLOADS[n].splitkv]
+DECODE = [n for n in WORKLOADS if WORKLOADS[n].splitkv]
 HEADLINE = "causal_b1_h32_s16384_d128_bf16_qk3"
 
 

@@ -236,8 +236,20 @@ def main():
     stream = torch.cuda.current_stream(dev)
     in_bytes = 3 * q.numel() * q.element_size() if w.sq == w.sk else (q.numel() + 2 * k.numel()) * q.element_size()
 
-    def step():
-        af.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, o=o, lse=lse, stream=stream)
+    if w.splitkv:
+        from attention_forward_14_gb300 import binding
+        splits = binding.splitkv_default_splits(w.b, w.h, w.sq, w.sk, w.d, w.causal)
+        ws = torch.empty(max(16, binding.splitkv_workspace_bytes(w.b, w.h, w.sq, w.d, splits)),
+                         dtype=torch.uint8, device=dev)
+
+        def step():
+            af.attn_fwd_splitkv(qd, kd, vd, causal=w.causal, scale=w.scale, num_splits=splits, o=o, lse=lse,
+                                workspace=ws, stream=stream)
+    else:
+        splits = 1
+
+        def step():
+            af.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, o=o, lse=lse, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -301,14 +313,20 @@ def main():
                        if in_bytes > L2_BYTES else "inputs fit in L2 (no flush)"},
             "pct_of_peak": 100.0 * value / world / peaks["bf16"],
             "pct_of_sustained_peak": 100.0 * value / world / peaks["bf16_sustained"],
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
-                         "frac": achieved / peaks["bf16"], "traffic": profiled_traffic(w.name),
-                         "peak_kind": f"{peaks['source']} bf16 dense burst (cuBLAS)",
-                         "kernel": "attn_fwd_kernel", "algorithmic_bytes": w.bytes()},
+            "roofline": ({"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                          "frac": achieved / peaks["bf16"], "traffic": profiled_traffic(w.name),
+                          "peak_kind": f"{peaks['source']} bf16 dense burst (cuBLAS)",
+                          "kernel": "attn_fwd_kernel", "algorithmic_bytes": w.bytes()}
+                         if not w.splitkv else
+                         {"bound": "hbm", "achieved": w.bytes() / (kern_ms * 1e-3) / 1e9, "peak": peaks["hbm"],
+                          "unit": "GB/s", "frac": w.bytes() / (kern_ms * 1e-3) / 1e9 / peaks["hbm"],
+                          "traffic": profiled_traffic(w.name), "peak_kind": f"{peaks['source']} HBM copy",
+                          "kernel": "attn_fwd_kernel + attn_splitkv_combine_kernel (one step)",
+                          "algorithmic_bytes": w.bytes(), "num_splits": splits}),
             "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": in_bytes,
                     "d2h_bytes_per_step": q.numel() * q.element_size() + lse.numel() * 4,
                     "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * (2 if splits > 1 else 1),
             "clocks": sampler.summary(),
         }
         if not args.no_cpu_baseline and world == 1:

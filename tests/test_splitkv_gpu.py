@@ -83,3 +83,15 @@ def test_splitkv_workspace_reuse_across_calls():
         o_ref, lse_ref = oracle.attn_fwd(q.double().numpy(), k.double().numpy(), v.double().numpy(), True,
                                          1 / math.sqrt(128))
         compare(o.float().cpu().double().numpy(), lse.cpu().double().numpy(), o_ref, lse_ref, "fp16", f"reuse {seed}")
+
+
+@pytest.mark.parametrize("name", W.DECODE)
+def test_decode_workload_full(name):
+    """The decode workload at full size, in the launch configuration the
+    benchmark times (default split count), every row against the oracle."""
+    w = W.WORKLOADS[name]
+    q, k, v = W.inputs(w)
+    splits = binding.splitkv_default_splits(w.b, w.h, w.sq, w.sk, w.d, w.causal)
+    o, lse = _run(q, k, v, w.causal, w.scale, splits)
+    o_ref, lse_ref = oracle.attn_fwd(q.double().numpy(), k.double().numpy(), v.double().numpy(), w.causal, w.scale)
+    compare(o, lse, o_ref, lse_ref, w.dtype, name)

@@ -22,7 +22,7 @@ ERRORS = {
 }
 # Every function include/attn_fwd.h declares.
 EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
-           "attn_fwd_splitkv_default_splits", "attn_last_error", "attn_fwd_status", "attn_fwd_status_clear",
+           "attn_fwd_splitkv_default_splits", "attn_fwd_splitkv_noalloc", "attn_last_error", "attn_fwd_status", "attn_fwd_status_clear",
            "attn_fwd_watchdog_selftest", "attn_version"]
 
 
@@ -50,6 +50,9 @@ def _bind(lib):
     lib.attn_fwd_splitkv_workspace_bytes.argtypes = [i64, i64, i64, i64, c_int]
     lib.attn_fwd_splitkv_default_splits.restype = c_int
     lib.attn_fwd_splitkv_default_splits.argtypes = [i64, i64, i64, i64, i64, c_int]
+    lib.attn_fwd_splitkv_noalloc.restype = c_int
+    lib.attn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_float, c_int,
+                                             c_int, vp]
     lib.attn_last_error.restype = ctypes.c_char_p
     lib.attn_last_error.argtypes = []
     lib.attn_fwd_status.restype = c_int

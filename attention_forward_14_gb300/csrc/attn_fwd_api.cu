@@ -231,6 +231,19 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_
 
 constexpr uint64_t kDefaultTimeoutNs = 2000ull * 1000ull * 1000ull;  // 2 s per wait
 
+// Scratch of attn_fwd_splitkv_noalloc: a fixed device array that every GPU
+// loading this library holds until the process exits.  In host code the name
+// only stands for the symbol; its device address comes from
+// cudaGetSymbolAddress, fetched once per device with that device current.
+static __device__ __align__(256) float g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+struct NoallocSlot {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    void *ptr = nullptr;
+};
+NoallocSlot g_noalloc[kMaxDevices];
+
 }  // namespace
 
 extern "C" {
@@ -331,6 +344,38 @@ int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float
     sa.lse_part = sa.o_part + static_cast<int64_t>(num_splits) * b * h * sq * d;
     return run(q, k, v, o, lse, b, h, sq, sk, d, causal, scale, dtype, static_cast<cudaStream_t>(stream), -1,
                kDefaultTimeoutNs, sa);
+}
+
+// Split-KV forward for callers that cannot allocate device memory (see the
+// header): the partial results go to the fixed scratch array above instead
+// of a caller workspace.  Allocates nothing.
+int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse, int64_t b, int64_t h,
+                             int64_t sq, int64_t sk, int64_t d, int causal, float scale, int dtype, int num_splits,
+                             void *stream)
+{
+    g_err.clear();
+    // Host-side size check first: the partials must fit the fixed scratch.
+    if (b < 0 || h < 0 || sq < 0 || (d != 64 && d != 128) || num_splits < 1 || num_splits > 1024)
+        return fail(ATTN_ERR_SHAPE, "attn_fwd_splitkv_noalloc: invalid sizes or split count");
+    const int64_t need = (num_splits == 1) ? 0 : splitkv_bytes(b * h, sq, d, num_splits);
+    if (need > static_cast<int64_t>(ATTN_NOALLOC_SCRATCH_BYTES))
+        return fail(ATTN_ERR_SHAPE,
+                    "attn_fwd_splitkv_noalloc: %d splits of b=%lld h=%lld sq=%lld d=%lld need %lld bytes of scratch, "
+                    "more than its fixed %lld; use fewer splits, or attn_fwd_splitkv with a workspace",
+                    num_splits, (long long)b, (long long)h, (long long)sq, (long long)d, (long long)need,
+                    (long long)ATTN_NOALLOC_SCRATCH_BYTES);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_CUDA, "device ordinal %d out of range", dev);
+    NoallocSlot &slot = g_noalloc[dev];
+    std::call_once(slot.once, [&] { slot.err = cudaGetSymbolAddress(&slot.ptr, g_noalloc_scratch); });
+    if (slot.err != cudaSuccess) return cuda_fail(slot.err, "cudaGetSymbolAddress of the no-alloc scratch");
+    if (slot.ptr == nullptr) return fail(ATTN_ERR_CUDA, "no-alloc scratch has no device address");
+    // Every element the merge reads is written earlier by the same call, so
+    // nothing in the scratch has to start at zero.
+    return attn_fwd_splitkv(q, k, v, o, lse, b, h, sq, sk, d, causal, scale, dtype, num_splits, slot.ptr,
+                            static_cast<int64_t>(ATTN_NOALLOC_SCRATCH_BYTES), stream);
 }
 
 const char *attn_last_error(void) { return g_err.c_str(); }

@@ -135,6 +135,38 @@ int64_t attn_fwd_splitkv_workspace_bytes(int64_t b, int64_t h, int64_t sq,
 int attn_fwd_splitkv_default_splits(int64_t b, int64_t h, int64_t sq,
                                     int64_t sk, int64_t d, int causal);
 
+/*
+ * attn_fwd_splitkv_noalloc: attn_fwd_splitkv for callers that cannot
+ * allocate device memory.  The pages have no counterpart to this entry
+ * point.  Some callers have no workspace to pass and may not call cudaMalloc
+ * themselves: for example a plugin whose host program's memory planner owns
+ * every device allocation, or latency-critical code that must not pay the
+ * implicit device synchronisation of an allocation.  This entry point keeps
+ * the split partials in a fixed scratch array of ATTN_NOALLOC_SCRATCH_BYTES
+ * (16 MiB) compiled into the library; every GPU that loads the library holds
+ * that array until the process exits.  The caller still passes the inputs
+ * and outputs, with the layouts and semantics of attn_fwd.  It allocates
+ * nothing.
+ *
+ *   num_splits : as for attn_fwd_splitkv.  Sizes whose partials need more
+ *                than ATTN_NOALLOC_SCRATCH_BYTES (see
+ *                attn_fwd_splitkv_workspace_bytes) are rejected with
+ *                ATTN_ERR_SHAPE and a message saying how much they need.
+ *
+ * The first call on each device looks up the array's device address on that
+ * device; make that first call before any stream capture.  All calls on a
+ * device share the one array, and it keeps the last call's contents (nothing
+ * in it needs to start at zero: each call writes what it reads).  Calls that
+ * overlap on the GPU -- on different streams, or from different host threads
+ * -- race on the array; serialise them.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v,
+                             void *o, float *lse, int64_t b, int64_t h,
+                             int64_t sq, int64_t sk, int64_t d, int causal,
+                             float scale, int dtype, int num_splits,
+                             void *stream);
+
 /* Thread-local message describing the last non-OK return on this thread
  * ("" if none).  The pointer stays valid until the next call on the thread. */
 const char *attn_last_error(void);

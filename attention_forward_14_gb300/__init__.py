@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     attn_fwd,
     attn_fwd_host,
     attn_fwd_splitkv,
+    attn_fwd_varlen,
     lib_path,
     load,
     status,

@@ -21,7 +21,7 @@ ERRORS = {
     -5: "ATTN_ERR_SCALE", -6: "ATTN_ERR_ALIGN", -7: "ATTN_ERR_ARCH", -8: "ATTN_ERR_CUDA", -9: "ATTN_ERR_WATCHDOG",
 }
 # Every function include/attn_fwd.h declares.
-EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
+EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_fwd_varlen", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
            "attn_fwd_splitkv_default_splits", "attn_fwd_splitkv_noalloc", "attn_last_error", "attn_fwd_status", "attn_fwd_status_clear",
            "attn_fwd_watchdog_selftest", "attn_version"]
 
@@ -43,6 +43,9 @@ def _bind(lib):
     lib.attn_fwd_host.restype = c_int
     lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                   i64, i64, i64, i64, i64, c_int, c_float, c_int, vp]
+    lib.attn_fwd_varlen.restype = c_int
+    lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, c_int, c_float,
+                                    c_int, vp]
     lib.attn_fwd_splitkv.restype = c_int
     lib.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_float, c_int, c_int,
                                      vp, i64, vp]
@@ -141,6 +144,38 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, 
                           lse.data_ptr() if lse is not None else None,
                           b, h, sq, sk, d, int(bool(causal)), float(scale), _dtype_code(q),
                           _stream_handle(stream, q.device))
+    _check(rc, lib)
+    return o, lse
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                    causal: bool = False, scale: float | None = None, o=None, lse=None, stream=None):
+    """Packed variable-length forward.  q: [total_q, h, d], k/v: [total_k,
+    h, d] CUDA tensors; cu_seqlens_*: int32 CUDA tensors [batch + 1].
+    Returns (o [total_q, h, d], lse [h, total_q])."""
+    import torch
+    lib = load()
+    total_q, h, d = q.shape
+    total_k = k.shape[0]
+    batch = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != batch + 1:
+        raise AttnError(-2, "cu_seqlens_q and cu_seqlens_k sizes differ")
+    for name, t in (("q", q), ("k", k), ("v", v), ("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise AttnError(-2, f"{name} must be a contiguous CUDA tensor")
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+        raise AttnError(-4, "cu_seqlens must be int32")
+    if scale is None:
+        scale = 1.0 / float(d) ** 0.5
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((h, total_q), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                 cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), batch, h, total_q, total_k,
+                                 int(max_seqlen_q), int(max_seqlen_k), d, int(bool(causal)), float(scale),
+                                 _dtype_code(q), _stream_handle(stream, q.device))
     _check(rc, lib)
     return o, lse
 

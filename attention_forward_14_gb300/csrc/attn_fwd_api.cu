@@ -116,6 +116,25 @@ int make_map(CUtensorMap *map, const void *ptr, int dtype, int64_t bh, int64_t s
 unsigned long long *g_trace_buf = nullptr;  // timeline builds only
 #endif
 
+// Packed [tokens, h, d] tensor seen as 3-D [tokens][h][d]: box = 64
+// elements x 1 head x 128 tokens, the same 128-row x 128-byte shared-memory
+// image as the dense map.  Rows past the last token are zero-filled.
+int make_map_packed(CUtensorMap *map, const void *ptr, int dtype, int64_t tokens, int64_t h, int64_t d)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    int rc = get_encode(&enc);
+    if (rc != ATTN_OK) return rc;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h), static_cast<cuuint64_t>(tokens)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2), static_cast<cuuint64_t>(h * d * 2)};
+    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                     const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (packed) failed (CUresult %d)", static_cast<int>(r));
+    return ATTN_OK;
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 constexpr int64_t kMaxSeq = int64_t(1) << 30;
@@ -195,6 +214,10 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_
     p.tiles_per_split = static_cast<int32_t>((kv_tiles(sk) + split.num_splits - 1) / split.num_splits);
     p.o_part = split.o_part;
     p.lse_part = split.lse_part;
+    p.cu_q = p.cu_k = nullptr;
+    p.heads = static_cast<int32_t>(h);
+    p.total_q = static_cast<int32_t>(sq);
+    p.total_k = static_cast<int32_t>(sk);
     const int64_t units = bh * p.num_mblk * split.num_splits;
     if (units > INT32_MAX) return fail(ATTN_ERR_SHAPE, "too many work units (%lld)", (long long)units);
     p.num_units = static_cast<int32_t>(units);
@@ -376,6 +399,75 @@ int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *
     // nothing in the scratch has to start at zero.
     return attn_fwd_splitkv(q, k, v, o, lse, b, h, sq, sk, d, causal, scale, dtype, num_splits, slot.ptr,
                             static_cast<int64_t>(ATTN_NOALLOC_SCRATCH_BYTES), stream);
+}
+
+int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse, const int32_t *cu_seqlens_q,
+                    const int32_t *cu_seqlens_k, int64_t batch, int64_t h, int64_t total_q, int64_t total_k,
+                    int64_t max_seqlen_q, int64_t max_seqlen_k, int64_t d, int causal, float scale, int dtype,
+                    void *stream)
+{
+    g_err.clear();
+    if (batch < 0 || h < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
+        return fail(ATTN_ERR_SHAPE, "negative varlen size");
+    if (total_q > INT32_MAX || total_k > INT32_MAX || max_seqlen_q > total_q || max_seqlen_k > total_k)
+        return fail(ATTN_ERR_SHAPE, "varlen totals above 2^31-1 or max lengths above the totals");
+    bool nothing = false;
+    // validate pointers/d/dtype/scale as a dense problem of total_q rows
+    int rc = validate(q, k, v, o, lse, 1, h, total_q, total_k, d, scale, dtype, &nothing);
+    if (rc != ATTN_OK || nothing || batch == 0 || max_seqlen_q == 0) return rc;
+    if (!cu_seqlens_q || !cu_seqlens_k) return fail(ATTN_ERR_NULL, "cu_seqlens_q / cu_seqlens_k is NULL");
+    if (!aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4)) return fail(ATTN_ERR_ALIGN, "cu_seqlens must be 4-byte aligned");
+    DeviceInfo *di = nullptr;
+    rc = device_info(&di);
+    if (rc != ATTN_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (total_k == 0) {  // no key anywhere: every row gets O = 0, LSE = -inf
+        e = (dtype == ATTN_BF16) ? launch_fill_empty<__nv_bfloat16>(o, lse, total_q * h, static_cast<int>(d), st)
+                                 : launch_fill_empty<__half>(o, lse, total_q * h, static_cast<int>(d), st);
+        return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "launch (empty keys)");
+    }
+    LaunchArgs a;
+    if ((rc = make_map_packed(&a.q, q, dtype, total_q, h, d)) != ATTN_OK) return rc;
+    if ((rc = make_map_packed(&a.k, k, dtype, total_k, h, d)) != ATTN_OK) return rc;
+    if ((rc = make_map_packed(&a.v, v, dtype, total_k, h, d)) != ATTN_OK) return rc;
+    FwdParams &p = a.p;
+    p.o = o;
+    p.lse = lse;
+    p.status = di->status;
+    const int64_t bh = batch * h;
+    if (bh > INT32_MAX) return fail(ATTN_ERR_SHAPE, "batch*h too large");
+    p.bh = static_cast<int32_t>(bh);
+    p.sq = static_cast<int32_t>(max_seqlen_q);
+    p.sk = static_cast<int32_t>(max_seqlen_k);
+    p.num_mblk = static_cast<int32_t>((max_seqlen_q + 255) / 256);
+    p.num_splits = 1;
+    p.tiles_per_split = static_cast<int32_t>(kv_tiles(max_seqlen_k > 0 ? max_seqlen_k : 1));
+    p.o_part = nullptr;
+    p.lse_part = nullptr;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.heads = static_cast<int32_t>(h);
+    p.total_q = static_cast<int32_t>(total_q);
+    p.total_k = static_cast<int32_t>(total_k);
+    const int64_t units = bh * p.num_mblk;
+    if (units > INT32_MAX) return fail(ATTN_ERR_SHAPE, "too many work units (%lld)", (long long)units);
+    p.num_units = static_cast<int32_t>(units);
+    p.sl2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    p.timeout_ns = kDefaultTimeoutNs;
+    p.withheld_load = -1;
+#ifdef ATTN_TRACE_ENABLE
+    p.trace = g_trace_buf;
+#endif
+    a.grid = static_cast<int>(units < di->sm_count ? units : di->sm_count);
+    a.stream = st;
+    const bool c = causal != 0;
+    if (d == 64)
+        e = (dtype == ATTN_BF16) ? dispatch_causal<64, __nv_bfloat16>(a, c) : dispatch_causal<64, __half>(a, c);
+    else
+        e = (dtype == ATTN_BF16) ? dispatch_causal<128, __nv_bfloat16>(a, c) : dispatch_causal<128, __half>(a, c);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch (varlen)");
+    return ATTN_OK;
 }
 
 const char *attn_last_error(void) { return g_err.c_str(); }

@@ -79,6 +79,14 @@ struct FwdParams {
     int32_t tiles_per_split;
     float *o_part;
     float *lse_part;
+    // Varlen (packed sequences): cu_q / cu_k are the batch+1 cumulative
+    // sequence offsets (device int32); Q, O are [total_q, heads, D], K, V
+    // [total_k, heads, D], LSE [heads, total_q].  bh is then batch * heads,
+    // sq / sk the maximum lengths.  nullptr: the dense [b, h, s, D] layout.
+    const int32_t *cu_q;
+    const int32_t *cu_k;
+    int32_t heads;
+    int32_t total_q, total_k;
 #ifdef ATTN_TRACE_ENABLE
     unsigned long long *trace;  // per-warp event records (timeline builds only)
 #endif
@@ -161,10 +169,14 @@ struct Ctl {
 static_assert(sizeof(Ctl) <= 1024, "control block");
 
 struct Unit {
-    int bh, row0;
-    int jb;     // first K/V tile of the unit
-    int n;      // number of K/V tiles (0: the rows see no key in this range)
-    int split;  // split index (0 without split-KV)
+    int bh;      // dense: b*h index of the head plane; varlen: head index
+    int row0;    // first query row of the unit within its sequence
+    int sq, sk;  // query / key length of the unit's sequence
+    int q_tok0;  // varlen: token of query row 0 of the sequence (else 0)
+    int k_tok0;  // varlen: token of key 0 of the sequence (else 0)
+    int jb;      // first K/V tile of the unit
+    int n;       // number of K/V tiles (0: the rows see no key in this range)
+    int split;   // split index (0 without split-KV)
 };
 
 template <int D, bool CAUSAL>
@@ -174,21 +186,53 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams &p)
     Unit un;
     un.split = u % p.num_splits;
     const int v = u / p.num_splits;  // (bh, row block) index
-    int mblk;
+    int mblk, bh;
     if (CAUSAL) {  // heaviest row blocks first
         mblk = p.num_mblk - 1 - v / p.bh;
-        un.bh = v % p.bh;
+        bh = v % p.bh;
     } else {       // consecutive units share a head (K/V reuse in L2)
-        un.bh = v / p.num_mblk;
+        bh = v / p.num_mblk;
         mblk = v % p.num_mblk;
     }
     un.row0 = mblk * C::UNIT_ROWS;
-    const int last = min(un.row0 + C::UNIT_ROWS - 1, p.sq - 1);
-    const int kend = CAUSAL ? min(p.sk, last + 1 + (p.sk - p.sq)) : p.sk;
-    const int n_all = kend > 0 ? (kend + C::BN - 1) / C::BN : 0;
+    if (p.cu_q != nullptr) {
+        const int seq = bh / p.heads;
+        un.bh = bh % p.heads;
+        un.q_tok0 = p.cu_q[seq];
+        un.sq = p.cu_q[seq + 1] - un.q_tok0;
+        un.k_tok0 = p.cu_k[seq];
+        un.sk = p.cu_k[seq + 1] - un.k_tok0;
+        // offsets outside the packed tensors: treat as an empty sequence
+        if (un.q_tok0 < 0 || un.sq < 0 || un.q_tok0 + un.sq > p.total_q || un.k_tok0 < 0 || un.sk < 0 ||
+            un.k_tok0 + un.sk > p.total_k)
+            un.sq = un.sk = 0;
+    } else {
+        un.bh = bh;
+        un.q_tok0 = un.k_tok0 = 0;
+        un.sq = p.sq;
+        un.sk = p.sk;
+    }
+    const int last = min(un.row0 + C::UNIT_ROWS - 1, un.sq - 1);
+    const int kend = CAUSAL ? min(un.sk, last + 1 + (un.sk - un.sq)) : un.sk;
+    const int n_all = (kend > 0 && un.row0 < un.sq) ? (kend + C::BN - 1) / C::BN : 0;
     un.jb = un.split * p.tiles_per_split;
     un.n = max(0, min(n_all, un.jb + p.tiles_per_split) - un.jb);
     return un;
+}
+
+// Element offset of query row `row` (within the unit's sequence) in O, and
+// its index in LSE, for either layout.
+__device__ __forceinline__ size_t o_row_offset(const FwdParams &p, const Unit &un, int row, int D)
+{
+    if (p.cu_q != nullptr)
+        return (static_cast<size_t>(un.q_tok0 + row) * p.heads + un.bh) * D;
+    return (static_cast<size_t>(un.bh) * p.sq + row) * D;
+}
+
+__device__ __forceinline__ size_t lse_index(const FwdParams &p, const Unit &un, int row)
+{
+    if (p.cu_q != nullptr) return static_cast<size_t>(un.bh) * p.total_q + un.q_tok0 + row;
+    return static_cast<size_t>(un.bh) * p.sq + row;
 }
 
 // The i-th work unit of this CTA.  Rounds of gridDim.x units are dealt out
@@ -380,20 +424,20 @@ __device__ __forceinline__ float2 exp_store_tile(const uint32_t (&sr)[128], int 
 }
 
 template <typename T>
-__device__ __forceinline__ void store_row_zero(const FwdParams &p, int bh, int row, int D, int split)
+__device__ __forceinline__ void store_row_zero(const FwdParams &p, const Unit &un, int row, int D)
 {
-    if (row >= p.sq) return;
+    if (row >= un.sq) return;
     if (p.num_splits > 1) {  // an empty split range: weight 0 in the combine
-        const size_t r = (static_cast<size_t>(split) * p.bh + bh) * p.sq + row;
+        const size_t r = (static_cast<size_t>(un.split) * p.bh + un.bh) * p.sq + row;
         float4 *dst = reinterpret_cast<float4 *>(p.o_part + r * D);
         for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
         p.lse_part[2 * r] = -INFINITY;
         p.lse_part[2 * r + 1] = -INFINITY;
         return;
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.o) + (static_cast<size_t>(bh) * p.sq + row) * D);
+    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.o) + o_row_offset(p, un, row, D));
     for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
-    if (p.lse) p.lse[static_cast<size_t>(bh) * p.sq + row] = -INFINITY;
+    if (p.lse) p.lse[lse_index(p, un, row)] = -INFINITY;
 }
 
 template <int D, typename T, bool CAUSAL>
@@ -471,6 +515,14 @@ __global__ void __launch_bounds__(384, 1)
             if (u >= p.num_units) continue;
             const Unit un = decode_unit<D, CAUSAL>(u, p);
             if (un.n == 0) continue;
+            // TMA coordinates (after the 64-column panel): dense maps are
+            // [bh][s][D] (row, plane = bh); varlen maps are [token][head][D]
+            // (row = head, plane = token).
+            const bool vl = p.cu_q != nullptr;
+            auto row_coord = [&](int r) { return vl ? un.bh : r; };
+            auto plane_coord = [&](int r) { return vl ? un.q_tok0 + r : un.bh; };
+            auto krow_coord = [&](int r) { return vl ? un.bh : r; };
+            auto kplane_coord = [&](int r) { return vl ? un.k_tok0 + r : un.bh; };
             for (int t = 0; t < C::QT && ok; ++t) {
                 ok = warp_wait(B(ctl->q_empty[t]), (q_it & 1u) ^ 1u, ctl, p, SITE_LOAD_Q_EMPTY);
                 if (!ok) break;
@@ -478,7 +530,8 @@ __global__ void __launch_bounds__(384, 1)
                     mbar_arrive_expect_tx(B(ctl->q_full[t]), C::TILE_BYTES);
                     for (int pn = 0; pn < C::NPANEL; ++pn)
                         tma_load_3d(sQ + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tmQ, B(ctl->q_full[t]),
-                                    pn * C::PANEL_ELEMS, un.row0 + t * C::BM, un.bh, pol_q);
+                                    pn * C::PANEL_ELEMS, row_coord(un.row0 + t * C::BM), plane_coord(un.row0 + t * C::BM),
+                                    pol_q);
                 }
                 __syncwarp();
             }
@@ -487,16 +540,20 @@ __global__ void __launch_bounds__(384, 1)
             if (ATTN_KV_PREFETCH > 0 && elect_one()) {
                 for (int jj = 0; jj < ATTN_KV_PREFETCH && jj < un.n; ++jj)
                     for (int pn = 0; pn < C::NPANEL; ++pn) {
-                        tma_prefetch_3d(&tmK, pn * C::PANEL_ELEMS, (un.jb + jj) * C::BN, un.bh);
-                        tma_prefetch_3d(&tmV, pn * C::PANEL_ELEMS, (un.jb + jj) * C::BN, un.bh);
+                        tma_prefetch_3d(&tmK, pn * C::PANEL_ELEMS, krow_coord((un.jb + jj) * C::BN),
+                                        kplane_coord((un.jb + jj) * C::BN));
+                        tma_prefetch_3d(&tmV, pn * C::PANEL_ELEMS, krow_coord((un.jb + jj) * C::BN),
+                                        kplane_coord((un.jb + jj) * C::BN));
                     }
             }
             __syncwarp();
             for (int j = 0; j < un.n && ok; ++j) {
                 if (ATTN_KV_PREFETCH > 0 && j + ATTN_KV_PREFETCH < un.n && elect_one()) {
                     for (int pn = 0; pn < C::NPANEL; ++pn) {
-                        tma_prefetch_3d(&tmK, pn * C::PANEL_ELEMS, (un.jb + j + ATTN_KV_PREFETCH) * C::BN, un.bh);
-                        tma_prefetch_3d(&tmV, pn * C::PANEL_ELEMS, (un.jb + j + ATTN_KV_PREFETCH) * C::BN, un.bh);
+                        tma_prefetch_3d(&tmK, pn * C::PANEL_ELEMS, krow_coord((un.jb + j + ATTN_KV_PREFETCH) * C::BN),
+                                        kplane_coord((un.jb + j + ATTN_KV_PREFETCH) * C::BN));
+                        tma_prefetch_3d(&tmV, pn * C::PANEL_ELEMS, krow_coord((un.jb + j + ATTN_KV_PREFETCH) * C::BN),
+                                        kplane_coord((un.jb + j + ATTN_KV_PREFETCH) * C::BN));
                     }
                 }
                 __syncwarp();
@@ -512,7 +569,8 @@ __global__ void __launch_bounds__(384, 1)
                         const CUtensorMap *m = which ? &tmV : &tmK;
                         for (int pn = 0; pn < C::NPANEL; ++pn)
                             tma_load_3d(sKV + slot * C::TILE_BYTES + pn * C::PANEL_BYTES, m, B(ctl->kv_full[slot]),
-                                        pn * C::PANEL_ELEMS, (un.jb + j) * C::BN, un.bh, pol_kv);
+                                        pn * C::PANEL_ELEMS, krow_coord((un.jb + j) * C::BN),
+                                        kplane_coord((un.jb + j) * C::BN), pol_kv);
                     }
                     __syncwarp();
                     ++kv_it;
@@ -676,11 +734,11 @@ __global__ void __launch_bounds__(384, 1)
             const Unit un = decode_unit<D, CAUSAL>(u, p);
             const int row = un.row0 + t * C::BM + r_in_tile;
             if (un.n == 0) {
-                store_row_zero<T>(p, un.bh, row, D, un.split);
+                store_row_zero<T>(p, un, row, D);
                 continue;
             }
             // keys visible to this row: [0, kend)
-            const int kend = CAUSAL ? min(p.sk, row + 1 + (p.sk - p.sq)) : p.sk;
+            const int kend = CAUSAL ? min(un.sk, row + 1 + (un.sk - un.sq)) : un.sk;
             // l: sum of p in fp32 (gives LSE); lr: sum of p as rounded for
             // the P.V product (normalises O, so its weights sum to one).
             float m = -INFINITY, l = 0.f, lr = 0.f;
@@ -748,7 +806,7 @@ __global__ void __launch_bounds__(384, 1)
                 o_ph ^= 1u;
                 tc_fence_after();
                 const float inv_l = (lr > 0.f) ? 1.f / lr : 0.f;
-                const bool valid = row < p.sq;
+                const bool valid = row < un.sq;
                 if (p.num_splits > 1) {
                     // split partial: O / lr in fp32, both log-sum-exps
                     const size_t r = (static_cast<size_t>(un.split) * p.bh + un.bh) * p.sq + (valid ? row : 0);
@@ -774,8 +832,7 @@ __global__ void __launch_bounds__(384, 1)
                     tc_fence_before();
                     continue;
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.o) +
-                                                       (static_cast<size_t>(un.bh) * p.sq + (valid ? row : 0)) * D);
+                uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.o) + o_row_offset(p, un, valid ? row : 0, D));
 #pragma unroll
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t orr[32];
@@ -794,7 +851,7 @@ __global__ void __launch_bounds__(384, 1)
                     }
                 }
                 if (valid && p.lse)
-                    p.lse[static_cast<size_t>(un.bh) * p.sq + row] =
+                    p.lse[lse_index(p, un, row)] =
                         (l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
                 ATTN_TRACE(EV_SM_EPI_DONE, u);
                 tc_fence_before();

@@ -109,3 +109,29 @@ def sample_heads(w: Workload, n: int = 4, seed: int = 7):
         if (bi, hi) not in pairs:
             pairs.append((bi, hi))
     return pairs
+
+
+def draw_varlen(lens_q, lens_k, h, d, dtype, seed, qk_std=1.0):
+    """Packed variable-length inputs: sequence s draws its own dense
+    [1, h, lens_q[s], d] / [1, h, lens_k[s], d] tensors (seed + s), which are
+    laid out token-major and concatenated.  Returns (q, k, v) packed
+    [total, h, d] CPU tensors, cu_seqlens_q, cu_seqlens_k (int32) and the
+    per-sequence dense tensors [(q_s, k_s, v_s), ...]."""
+    dense = [draw(1, h, int(a), int(b), d, dtype, seed + i, qk_std) for i, (a, b) in enumerate(zip(lens_q, lens_k))]
+
+    def pack(idx):
+        parts = [t[idx][0].transpose(0, 1).contiguous() for t in dense]  # [s, h, d]
+        return torch.cat(parts, 0) if parts else torch.empty(0, h, d, dtype=DTYPES[dtype])
+
+    cu_q = torch.zeros(len(lens_q) + 1, dtype=torch.int32)
+    cu_k = torch.zeros(len(lens_k) + 1, dtype=torch.int32)
+    cu_q[1:] = torch.cumsum(torch.tensor([int(x) for x in lens_q], dtype=torch.int64), 0).to(torch.int32)
+    cu_k[1:] = torch.cumsum(torch.tensor([int(x) for x in lens_k], dtype=torch.int64), 0).to(torch.int32)
+    return pack(0), pack(1), pack(2), cu_q, cu_k, dense
+
+
+def varlen_lengths(n, lo, hi, seed):
+    """Seeded sequence lengths, uniform in [lo, hi]."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=g)]

@@ -124,6 +124,33 @@ int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o,
                      int num_splits, void *workspace, int64_t workspace_bytes,
                      void *stream);
 
+/*
+ * Variable-length (packed) forward.  "05 · kernel 工程与四代演化" 6.1 lists
+ * varlen_fwd among the exported entry points; the operation is attn_fwd
+ * applied to each sequence of a batch of different lengths, with the
+ * sequences concatenated along the token axis.
+ *
+ *   q, o          : [total_q, h, d] of dtype (token-major, heads inside),
+ *                   16-byte aligned.
+ *   k, v          : [total_k, h, d] of dtype, 16-byte aligned.
+ *   lse           : fp32 [h, total_q], or NULL.
+ *   cu_seqlens_q  : device int32 [batch + 1]: sequence s owns query tokens
+ *                   cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1 (non-decreasing,
+ *                   cu_seqlens_q[0] = 0, cu_seqlens_q[batch] = total_q).
+ *   cu_seqlens_k  : the same for keys/values (total_k).
+ *   max_seqlen_q/k: upper bounds of the per-sequence lengths (they size the
+ *                   work grid; the host never reads the offsets).
+ * The causal mask is bottom-right per sequence.  A sequence whose offsets
+ * fall outside the totals is skipped (its outputs are not written).  Same
+ * error codes as attn_fwd.
+ */
+int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o,
+                    float *lse, const int32_t *cu_seqlens_q,
+                    const int32_t *cu_seqlens_k, int64_t batch, int64_t h,
+                    int64_t total_q, int64_t total_k, int64_t max_seqlen_q,
+                    int64_t max_seqlen_k, int64_t d, int causal, float scale,
+                    int dtype, void *stream);
+
 /* Bytes of workspace attn_fwd_splitkv needs (0 when num_splits == 1), or a
  * negative ATTN_ERR_* code for invalid sizes. */
 int64_t attn_fwd_splitkv_workspace_bytes(int64_t b, int64_t h, int64_t sq,

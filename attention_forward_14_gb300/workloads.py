@@ -111,6 +111,49 @@ def sample_heads(w: Workload, n: int = 4, seed: int = 7):
     return pairs
 
 
+@dataclass(frozen=True)
+class VarlenWorkload:
+    """Packed batch of sequences with seeded lengths in [lo, hi] (self
+    attention: query and key lengths equal per sequence)."""
+    name: str
+    n: int
+    lo: int
+    hi: int
+    h: int
+    d: int
+    dtype: str
+    causal: bool
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def lengths(self):
+        return varlen_lengths(self.n, self.lo, self.hi, self.seed)
+
+    def flops(self) -> float:
+        f = sum(4.0 * self.h * s * s * self.d for s in self.lengths())
+        return f * 0.5 if self.causal else f
+
+    def bytes(self) -> int:
+        t = sum(self.lengths())
+        return 2 * t * self.h * self.d * 4 + 4 * self.h * t
+
+
+VARLEN = {
+    w.name: w for w in [
+        VarlenWorkload("varlen_16seq_512to8192_h32_d128_bf16_causal", 16, 512, 8192, 32, 128, "bf16", True,
+                       20260006),
+    ]
+}
+
+
+def varlen_inputs(w: VarlenWorkload):
+    lens = w.lengths()
+    return draw_varlen(lens, lens, w.h, w.d, w.dtype, w.seed)
+
+
 def draw_varlen(lens_q, lens_k, h, d, dtype, seed, qk_std=1.0):
     """Packed variable-length inputs: sequence s draws its own dense
     [1, h, lens_q[s], d] / [1, h, lens_k[s], d] tensors (seed + s), which are

@@ -195,6 +195,59 @@ def bench_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def bench_varlen(args, w):
+    """Packed variable-length workload: one step = one attn_fwd_varlen call."""
+    import torch
+    import attention_forward_14_gb300 as af
+    from attention_forward_14_gb300 import workloads as W
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    q, k, v, cu_q, cu_k, _ = W.varlen_inputs(w)
+    lens = w.lengths()
+    qd, kd, vd, cqd, ckd = q.to(dev), k.to(dev), v.to(dev), cu_q.to(dev), cu_k.to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.h, q.shape[0]), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        af.attn_fwd_varlen(qd, kd, vd, cqd, ckd, max(lens), max(lens), causal=w.causal, scale=w.scale, o=o, lse=lse,
+                           stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    peaks = load_peaks()
+    value = w.flops() / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": w.name, "sequences": w.n, "lengths": lens, "total_tokens": int(q.shape[0]), "h": w.h,
+                   "d": w.d, "causal": w.causal, "flops_per_step": w.flops()},
+        "pct_of_peak": 100.0 * value / peaks["bf16"],
+        "roofline": {"bound": "tensor", "achieved": value, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                     "frac": value / peaks["bf16"], "traffic": profiled_traffic(w.name),
+                     "peak_kind": f"{peaks['source']} bf16 dense burst (cuBLAS)", "kernel": "attn_fwd_kernel",
+                     "algorithmic_bytes": w.bytes()},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -208,7 +261,10 @@ def main():
     args.warmup = max(3, args.warmup)
 
     from attention_forward_14_gb300 import workloads as W
-    w = W.WORKLOADS[args.workload or W.HEADLINE]
+    name = args.workload or W.HEADLINE
+    if name in W.VARLEN:
+        return bench_varlen(args, W.VARLEN[name])
+    w = W.WORKLOADS[name]
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -68,3 +68,27 @@ def test_varlen_matches_dense_for_equal_lengths():
     o_v = o_v.reshape(3, 384, 2, 128).transpose(1, 2)
     assert torch.equal(o_v.cpu(), o_d.cpu())
     assert torch.equal(l_v.reshape(2, 3, 384).transpose(0, 1).cpu(), l_d.cpu())
+
+
+@pytest.mark.parametrize("name", list(W.VARLEN))
+def test_varlen_workload_full_size(name):
+    """The benchmarked packed batch at full size; the shortest and the
+    longest sequence and one more are compared with the oracle on two heads."""
+    w = W.VARLEN[name]
+    q, k, v, cu_q, cu_k, dense = W.varlen_inputs(w)
+    lens = w.lengths()
+    dev = torch.device("cuda", 0)
+    o, lse = af.attn_fwd_varlen(q.to(dev), k.to(dev), v.to(dev), cu_q.to(dev), cu_k.to(dev), max(lens), max(lens),
+                                causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    o = o.float().cpu().double().numpy()
+    lse = lse.cpu().double().numpy()
+    assert np.isfinite(o).all()
+    picks = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 5})
+    for s in picks:
+        a, b = int(cu_q[s]), int(cu_q[s + 1])
+        qs, ks, vs = dense[s]
+        for hh in (0, w.h - 1):
+            o_ref, lse_ref = oracle.attn_fwd(qs[:, hh:hh + 1].double().numpy(), ks[:, hh:hh + 1].double().numpy(),
+                                             vs[:, hh:hh + 1].double().numpy(), w.causal, w.scale)
+            compare(o[a:b, hh][None, None], lse[hh, a:b][None, None], o_ref, lse_ref, w.dtype, f"seq {s} head {hh}")

@@ -21,7 +21,7 @@ ERRORS = {
     -5: "ATTN_ERR_SCALE", -6: "ATTN_ERR_ALIGN", -7: "ATTN_ERR_ARCH", -8: "ATTN_ERR_CUDA", -9: "ATTN_ERR_WATCHDOG",
 }
 # Every function include/attn_fwd.h declares.
-EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_fwd_varlen", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
+EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_fwd_varlen", "attn_fwd_fp8", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
            "attn_fwd_splitkv_default_splits", "attn_fwd_splitkv_noalloc", "attn_last_error", "attn_fwd_status", "attn_fwd_status_clear",
            "attn_fwd_watchdog_selftest", "attn_version"]
 
@@ -43,6 +43,9 @@ def _bind(lib):
     lib.attn_fwd_host.restype = c_int
     lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                   i64, i64, i64, i64, i64, c_int, c_float, c_int, vp]
+    lib.attn_fwd_fp8.restype = c_int
+    lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_float, c_float, c_float,
+                                 c_float, vp]
     lib.attn_fwd_varlen.restype = c_int
     lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, c_int, c_float,
                                     c_int, vp]
@@ -144,6 +147,31 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, 
                           lse.data_ptr() if lse is not None else None,
                           b, h, sq, sk, d, int(bool(causal)), float(scale), _dtype_code(q),
                           _stream_handle(stream, q.device))
+    _check(rc, lib)
+    return o, lse
+
+
+def attn_fwd_fp8(q, k, v, causal: bool = False, scale: float | None = None, descale_q: float = 1.0,
+                 descale_k: float = 1.0, descale_v: float = 1.0, o=None, lse=None, stream=None):
+    """e4m3 inputs [b, h, s, 128] (torch.float8_e4m3fn CUDA tensors) with
+    per-tensor descales; returns (o bf16 [b, h, sq, 128], lse fp32)."""
+    import torch
+    lib = load()
+    b, h, sq, d = q.shape
+    sk = k.shape[2]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.float8_e4m3fn:
+            raise AttnError(-4, f"{name} must be a contiguous CUDA float8_e4m3fn tensor")
+    if scale is None:
+        scale = 1.0 / float(d) ** 0.5
+    if o is None:
+        o = torch.empty((b, h, sq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((b, h, sq), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), b, h, sq, sk,
+                              d, int(bool(causal)), float(scale), float(descale_q), float(descale_k),
+                              float(descale_v), _stream_handle(stream, q.device))
     _check(rc, lib)
     return o, lse
 

@@ -96,25 +96,23 @@ int get_encode(PFN_cuTensorMapEncodeTiled_v12000 *fn)
 // 3-D view [bh, s, d] of a contiguous [b, h, s, d] tensor; box = 128 rows x
 // 64 elements (one 128-byte swizzle panel), so rows past s of each head are
 // zero-filled by the copy engine rather than read from the next head.
-int make_map(CUtensorMap *map, const void *ptr, int dtype, int64_t bh, int64_t s, int64_t d)
+int make_map(CUtensorMap *map, const void *ptr, int dtype, int64_t bh, int64_t s, int64_t d, int elem_bytes = 2)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     int rc = get_encode(&enc);
     if (rc != ATTN_OK) return rc;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(s), static_cast<cuuint64_t>(bh)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2), static_cast<cuuint64_t>(s * d * 2)};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * elem_bytes), static_cast<cuuint64_t>(s * d * elem_bytes)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), 128, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                     const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = enc(map, dt, 3, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
     return ATTN_OK;
 }
-
-#ifdef ATTN_TRACE_ENABLE
-unsigned long long *g_trace_buf = nullptr;  // timeline builds only
-#endif
 
 // Packed [tokens, h, d] tensor seen as 3-D [tokens][h][d]: box = 64
 // elements x 1 head x 128 tokens, the same 128-row x 128-byte shared-memory
@@ -222,6 +220,7 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_
     if (units > INT32_MAX) return fail(ATTN_ERR_SHAPE, "too many work units (%lld)", (long long)units);
     p.num_units = static_cast<int32_t>(units);
     p.sl2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    p.o_scale = 1.f;
     p.timeout_ns = timeout_ns;
     p.withheld_load = withheld_load;
 #ifdef ATTN_TRACE_ENABLE
@@ -454,6 +453,7 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float 
     if (units > INT32_MAX) return fail(ATTN_ERR_SHAPE, "too many work units (%lld)", (long long)units);
     p.num_units = static_cast<int32_t>(units);
     p.sl2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    p.o_scale = 1.f;
     p.timeout_ns = kDefaultTimeoutNs;
     p.withheld_load = -1;
 #ifdef ATTN_TRACE_ENABLE
@@ -467,6 +467,68 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float 
     else
         e = (dtype == ATTN_BF16) ? dispatch_causal<128, __nv_bfloat16>(a, c) : dispatch_causal<128, __half>(a, c);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch (varlen)");
+    return ATTN_OK;
+}
+
+int attn_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse, int64_t b, int64_t h, int64_t sq,
+                 int64_t sk, int64_t d, int causal, float scale, float descale_q, float descale_k, float descale_v,
+                 void *stream)
+{
+    g_err.clear();
+    if (d != 128) return fail(ATTN_ERR_HEADDIM, "the e4m3 forward supports head dim 128 only (got %lld)", (long long)d);
+    if (!std::isfinite(descale_q) || !std::isfinite(descale_k) || !std::isfinite(descale_v))
+        return fail(ATTN_ERR_SCALE, "descale factors must be finite");
+    const double sqk = static_cast<double>(scale) * descale_q * descale_k;
+    if (!std::isfinite(sqk) || !std::isfinite(static_cast<float>(sqk)))
+        return fail(ATTN_ERR_SCALE, "scale * descale_q * descale_k is not finite in fp32");
+    bool nothing = false;
+    // pointer, size and alignment checks as for a bf16 problem (O is bf16)
+    int rc = validate(q, k, v, o, lse, b, h, sq, sk, d, scale, ATTN_BF16, &nothing);
+    if (rc != ATTN_OK || nothing) return rc;
+    DeviceInfo *di = nullptr;
+    rc = device_info(&di);
+    if (rc != ATTN_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t bh = b * h;
+    cudaError_t e;
+    if (sk == 0) {
+        e = launch_fill_empty<__nv_bfloat16>(o, lse, bh * sq, static_cast<int>(d), st);
+        return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "launch (empty keys)");
+    }
+    LaunchArgs a;
+    if ((rc = make_map(&a.q, q, ATTN_BF16, bh, sq, d, 1)) != ATTN_OK) return rc;
+    if ((rc = make_map(&a.k, k, ATTN_BF16, bh, sk, d, 1)) != ATTN_OK) return rc;
+    if ((rc = make_map(&a.v, v, ATTN_BF16, bh, sk, d, 1)) != ATTN_OK) return rc;
+    FwdParams &p = a.p;
+    p.o = o;
+    p.lse = lse;
+    p.status = di->status;
+    p.bh = static_cast<int32_t>(bh);
+    p.sq = static_cast<int32_t>(sq);
+    p.sk = static_cast<int32_t>(sk);
+    p.num_mblk = static_cast<int32_t>((sq + 255) / 256);
+    p.num_splits = 1;
+    p.tiles_per_split = static_cast<int32_t>(kv_tiles(sk));
+    p.o_part = nullptr;
+    p.lse_part = nullptr;
+    p.cu_q = p.cu_k = nullptr;
+    p.heads = static_cast<int32_t>(h);
+    p.total_q = static_cast<int32_t>(sq);
+    p.total_k = static_cast<int32_t>(sk);
+    const int64_t units = bh * p.num_mblk;
+    if (units > INT32_MAX) return fail(ATTN_ERR_SHAPE, "too many work units (%lld)", (long long)units);
+    p.num_units = static_cast<int32_t>(units);
+    p.sl2e = static_cast<float>(sqk * 1.4426950408889634074);
+    p.o_scale = descale_v;
+    p.timeout_ns = kDefaultTimeoutNs;
+    p.withheld_load = -1;
+#ifdef ATTN_TRACE_ENABLE
+    p.trace = g_trace_buf;
+#endif
+    a.grid = static_cast<int>(units < di->sm_count ? units : di->sm_count);
+    a.stream = st;
+    e = causal ? launch_fwd<128, __nv_fp8_e4m3, true>(a) : launch_fwd<128, __nv_fp8_e4m3, false>(a);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch (e4m3)");
     return ATTN_OK;
 }
 

@@ -44,6 +44,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <type_traits>
 
 #include "ptx.cuh"
@@ -66,7 +67,8 @@ struct FwdParams {
     int32_t sq, sk;
     int32_t num_mblk;      // ceil(sq / 256)
     int32_t num_units;     // bh * num_mblk
-    float sl2e;            // scale * log2(e)
+    float sl2e;            // scale * log2(e) (e4m3: times the Q and K descales)
+    float o_scale;         // multiplier of O (e4m3: the V descale; else 1)
     uint64_t timeout_ns;   // bound of every wait
     int32_t withheld_load; // K/V load index never issued (watchdog self-test), -1 = none
     // Split-KV: each (bh, row block) is cut into num_splits ranges of
@@ -131,18 +133,55 @@ enum : uint32_t {
     SITE_DRAIN = 8,
 };
 
-template <int D_>
+// Input element types: fp16, bf16 (16-bit, kind::f16 MMAs, P two per
+// tensor-memory column) and e4m3 (8-bit, kind::f8f6f4 MMAs, P four per
+// column, output in bf16).  SHIFT is the log2 offset of the exp reference
+// and TAU the lazy-rescale threshold (both log2 units).  For e4m3 the
+// reference sits 8 below the row max, so P spans [0, 256] and uses the
+// 8-bit range instead of flushing small values ("05 · kernel 工程与四代演化"
+// 4.4); TAU = 0.5 keeps P <= 2^8.5 < 448, the e4m3 maximum.
+template <typename T>
+struct Elem;
+template <>
+struct Elem<__half> {
+    static constexpr int BYTES = 2;
+    static constexpr bool FP8 = false;
+    static constexpr bool BF16 = false;
+    static constexpr float SHIFT = 0.f, TAU = 8.f;
+    using Out = __half;
+};
+template <>
+struct Elem<__nv_bfloat16> {
+    static constexpr int BYTES = 2;
+    static constexpr bool FP8 = false;
+    static constexpr bool BF16 = true;
+    static constexpr float SHIFT = 0.f, TAU = 8.f;
+    using Out = __nv_bfloat16;
+};
+template <>
+struct Elem<__nv_fp8_e4m3> {
+    static constexpr int BYTES = 1;
+    static constexpr bool FP8 = true;
+    static constexpr bool BF16 = false;  // format code 0 = e4m3 in kind::f8f6f4
+    static constexpr float SHIFT = 8.f, TAU = 0.5f;
+    using Out = __nv_bfloat16;
+};
+
+template <int D_, int EB = 2>
 struct Cfg {
     static constexpr int D = D_;
     static constexpr int BM = 128;                 // rows per Q tile = TMEM lanes
     static constexpr int QT = 2;                   // Q tiles per unit
     static constexpr int UNIT_ROWS = BM * QT;      // 256
     static constexpr int BN = 128;                 // keys per K/V tile
-    static constexpr int PANEL_ELEMS = 64;         // 128-byte swizzle panel (16-bit elems)
-    static constexpr int NPANEL = D / PANEL_ELEMS;
+    static constexpr int PANEL_ELEMS = 128 / EB;   // one 128-byte swizzle panel
+    static constexpr int NPANEL = D * EB / 128;
     static constexpr int PANEL_BYTES = 128 * 128;  // 128 rows x 128 B
     static constexpr int TILE_BYTES = NPANEL * PANEL_BYTES;  // one Q, K or V tile
-    static constexpr int NSLOT = (D == 128) ? 5 : 8;
+    static constexpr int NSLOT = (TILE_BYTES == 2 * PANEL_BYTES) ? 5 : 8;
+    static constexpr int QK_STEPS = D * EB / 32;   // 32-byte k-steps of S = Q K^T
+    static constexpr int PV_KEYS = 32 / EB;        // keys per k-step of O += P V
+    static constexpr int PV_STEPS = BN / PV_KEYS;
     static constexpr int CTL_BYTES = 1024;
     static constexpr int Q_OFF = CTL_BYTES;
     static constexpr int KV_OFF = Q_OFF + QT * TILE_BYTES;
@@ -153,7 +192,6 @@ struct Cfg {
     static constexpr int THREADS = 384;
     static constexpr int REGS_SOFTMAX = 216;
     static constexpr int REGS_OTHER = 72;
-    static constexpr float TAU = 8.0f;             // lazy-rescale threshold (log2 units)
     static_assert(TMEM_O + QT * D <= TMEM_COLS, "tensor memory budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -393,31 +431,65 @@ __device__ __forceinline__ float2 exp_store_tile(const uint32_t (&sr)[128], int 
         l4[i] = make_float2(0.f, 0.f);
         lr4[i] = 0.f;
     }
-    uint32_t pa[32], pb[32];
+    if constexpr (!Elem<T>::FP8) {
+        uint32_t pa[32], pb[32];
 #pragma unroll
-    for (int c = 0; c < 64; ++c) {
-        float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sc2, nm2);
-        if (MASKED) {
-            x.x = (2 * c < lim) ? x.x : -INFINITY;
-            x.y = (2 * c + 1 < lim) ? x.y : -INFINITY;
+        for (int c = 0; c < 64; ++c) {
+            float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sc2, nm2);
+            if (MASKED) {
+                x.x = (2 * c < lim) ? x.x : -INFINITY;
+                x.y = (2 * c + 1 < lim) ? x.y : -INFINITY;
+            }
+            const float p0 = ex2_approx(x.x);
+            const float p1 = ex2_approx(x.y);
+            l4[c & 3] = __fadd2_rn(l4[c & 3], make_float2(p0, p1));
+            const uint32_t pk = pack2<T>(p0, p1);
+            lr4[c & 3] = add_halves<T>(pk, lr4[c & 3]);
+            if (c < 32)
+                pa[c] = pk;
+            else
+                pb[c - 32] = pk;
+            if (c == 31) {
+                tmem_st32(tS, pa);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(half_bar);
+            }
         }
-        const float p0 = ex2_approx(x.x);
-        const float p1 = ex2_approx(x.y);
-        l4[c & 3] = __fadd2_rn(l4[c & 3], make_float2(p0, p1));
-        const uint32_t pk = pack2<T>(p0, p1);
-        lr4[c & 3] = add_halves<T>(pk, lr4[c & 3]);
-        if (c < 32)
-            pa[c] = pk;
-        else
-            pb[c - 32] = pk;
-        if (c == 31) {
-            tmem_st32(tS, pa);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(half_bar);
+        tmem_st32(tS + 32, pb);
+    } else {
+        // e4m3: four per 32-bit column; 32 columns for the 128 keys
+        uint32_t pa[16], pb[16];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sr[4 * c]), __uint_as_float(sr[4 * c + 1])), sc2, nm2);
+            float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sr[4 * c + 2]), __uint_as_float(sr[4 * c + 3])), sc2, nm2);
+            if (MASKED) {
+                x0.x = (4 * c < lim) ? x0.x : -INFINITY;
+                x0.y = (4 * c + 1 < lim) ? x0.y : -INFINITY;
+                x1.x = (4 * c + 2 < lim) ? x1.x : -INFINITY;
+                x1.y = (4 * c + 3 < lim) ? x1.y : -INFINITY;
+            }
+            const float p0 = ex2_approx(x0.x), p1 = ex2_approx(x0.y);
+            const float p2 = ex2_approx(x1.x), p3 = ex2_approx(x1.y);
+            l4[c & 3] = __fadd2_rn(l4[c & 3], __fadd2_rn(make_float2(p0, p1), make_float2(p2, p3)));
+            const uint32_t lo = pack_e4m3x2(p0, p1), hi = pack_e4m3x2(p2, p3);
+            lr4[c & 3] = add_halves_f16(e4m3x2_to_f16x2(lo), lr4[c & 3]);
+            lr4[c & 3] = add_halves_f16(e4m3x2_to_f16x2(hi), lr4[c & 3]);
+            const uint32_t pk = lo | (hi << 16);
+            if (c < 16)
+                pa[c] = pk;
+            else
+                pb[c - 16] = pk;
+            if (c == 15) {
+                tmem_st16(tS, pa);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(half_bar);
+            }
         }
+        tmem_st16(tS + 16, pb);
     }
-    tmem_st32(tS + 32, pb);
     const float2 a = __fadd2_rn(l4[0], l4[1]);
     const float2 b = __fadd2_rn(l4[2], l4[3]);
     return make_float2((a.x + a.y) + (b.x + b.y), (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]));
@@ -435,7 +507,7 @@ __device__ __forceinline__ void store_row_zero(const FwdParams &p, const Unit &u
         p.lse_part[2 * r + 1] = -INFINITY;
         return;
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.o) + o_row_offset(p, un, row, D));
+    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<typename Elem<T>::Out *>(p.o) + o_row_offset(p, un, row, D));
     for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
     if (p.lse) p.lse[lse_index(p, un, row)] = -INFINITY;
 }
@@ -445,10 +517,12 @@ __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p)
 {
-    using C = Cfg<D>;
-    constexpr bool BF16 = std::is_same<T, __nv_bfloat16>::value;
-    constexpr uint32_t IDESC_QK = idesc_f16(128, C::BN, BF16, false);
-    constexpr uint32_t IDESC_PV = idesc_f16(128, D, BF16, true);
+    using E = Elem<T>;
+    using C = Cfg<D, E::BYTES>;
+    using TO = typename E::Out;
+    // format code 1 = bf16 in kind::f16; 0 = f16, or e4m3 in kind::f8f6f4
+    constexpr uint32_t IDESC_QK = idesc_f16(128, C::BN, E::BF16, false);
+    constexpr uint32_t IDESC_PV = idesc_f16(128, D, E::BF16, true);
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -618,20 +692,27 @@ __global__ void __launch_bounds__(384, 1)
             const uint32_t b0 = dk0 + ((kslot * C::TILE_BYTES) >> 4);
             const uint32_t d = tmem + C::TMEM_S + t * C::BN;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
+            for (int kk = 0; kk < C::QK_STEPS; ++kk) {  // 32 bytes of the head dim per step
                 const uint32_t off = ((kk / 4) * C::PANEL_BYTES + (kk % 4) * 32) >> 4;
-                mma_ss(d, a0 + off, b0 + off, IDESC_QK, kk > 0 ? 1u : 0u);
+                if constexpr (E::FP8)
+                    mma_ss_f8(d, a0 + off, b0 + off, IDESC_QK, kk > 0 ? 1u : 0u);
+                else
+                    mma_ss(d, a0 + off, b0 + off, IDESC_QK, kk > 0 ? 1u : 0u);
             }
         };
         // O_t (+)= P_t V over keys [64*half, 64*half + 64) of the tile.
         auto issue_pv = [&](int t, uint32_t vslot, bool accumulate, int half) {
             const uint32_t b0 = dv0 + ((vslot * C::TILE_BYTES) >> 4);
-            const uint32_t a = tmem + C::TMEM_S + t * C::BN;  // P_t, 2 elements per column
+            const uint32_t a = tmem + C::TMEM_S + t * C::BN;  // P_t, 32 bits of keys per column
             const uint32_t d = tmem + C::TMEM_O + t * D;
 #pragma unroll
-            for (int k2 = 0; k2 < C::BN / 32; ++k2) {
-                const int kk = half * (C::BN / 32) + k2;
-                mma_ts(d, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+            for (int k2 = 0; k2 < C::PV_STEPS / 2; ++k2) {
+                const int kk = half * (C::PV_STEPS / 2) + k2;
+                const uint32_t bo = (kk * C::PV_KEYS * 128) >> 4;  // PV_KEYS rows of 128 B
+                if constexpr (E::FP8)
+                    mma_ts_f8(d, a + kk * 8, b0 + bo, IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+                else
+                    mma_ts(d, a + kk * 8, b0 + bo, IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
             }
         };
         for (int i = 0; i * static_cast<int>(gridDim.x) < p.num_units && ok; ++i) {
@@ -768,7 +849,7 @@ __global__ void __launch_bounds__(384, 1)
                 const float mx = (mraw == (neg ? INFINITY : -INFINITY)) ? -INFINITY : mraw * sl2e;
                 const float m_new = fmaxf(m, mx);
                 if (j > 0) {
-                    const bool need = (m_new - m) > C::TAU;
+                    const bool need = (m_new - m) > E::TAU;
                     if (__any_sync(0xffffffffu, need)) {
                         const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m - m_new);
                         rescale_rows<D>(tO, alpha);
@@ -781,7 +862,7 @@ __global__ void __launch_bounds__(384, 1)
                     m = m_new;
                 }
                 ATTN_TRACE(EV_SM_MAX, j);
-                const float m_use = (m == -INFINITY) ? 0.f : m;
+                const float m_use = ((m == -INFINITY) ? 0.f : m) - E::SHIFT;  // exp reference
                 float2 sums;  // {sum of p, sum of p as rounded}
                 if (masked)
                     sums = exp_store_tile<T, true>(sr, lim, sl2e, m_use, tS, B(ctl->p_half[t]));
@@ -805,7 +886,8 @@ __global__ void __launch_bounds__(384, 1)
                 ATTN_TRACE(EV_SM_EPI_GOT, u);
                 o_ph ^= 1u;
                 tc_fence_after();
-                const float inv_l = (lr > 0.f) ? 1.f / lr : 0.f;
+                const float inv_l = (lr > 0.f) ? p.o_scale / lr : 0.f;
+                const float m_ref = m - E::SHIFT;  // reference of l and lr
                 const bool valid = row < un.sq;
                 if (p.num_splits > 1) {
                     // split partial: O / lr in fp32, both log-sum-exps
@@ -825,14 +907,14 @@ __global__ void __launch_bounds__(384, 1)
                         }
                     }
                     if (valid) {
-                        p.lse_part[2 * r] = (l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
-                        p.lse_part[2 * r + 1] = (lr > 0.f) ? (m + log2f(lr)) * 0.69314718055994531f : -INFINITY;
+                        p.lse_part[2 * r] = (l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                        p.lse_part[2 * r + 1] = (lr > 0.f) ? (m_ref + log2f(lr)) * 0.69314718055994531f : -INFINITY;
                     }
                     ATTN_TRACE(EV_SM_EPI_DONE, u);
                     tc_fence_before();
                     continue;
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.o) + o_row_offset(p, un, valid ? row : 0, D));
+                uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<TO *>(p.o) + o_row_offset(p, un, valid ? row : 0, D));
 #pragma unroll
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t orr[32];
@@ -842,7 +924,7 @@ __global__ void __launch_bounds__(384, 1)
                     for (int c = 0; c < 16; ++c) {
                         const float2 v = __fmul2_rn(make_float2(__uint_as_float(orr[2 * c]), __uint_as_float(orr[2 * c + 1])),
                                                     make_float2(inv_l, inv_l));
-                        pk[c] = pack2<T>(v.x, v.y);
+                        pk[c] = pack2<TO>(v.x, v.y);
                     }
                     if (valid) {
 #pragma unroll
@@ -852,7 +934,7 @@ __global__ void __launch_bounds__(384, 1)
                 }
                 if (valid && p.lse)
                     p.lse[lse_index(p, un, row)] =
-                        (l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                        (l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
                 ATTN_TRACE(EV_SM_EPI_DONE, u);
                 tc_fence_before();
             }

@@ -24,7 +24,7 @@ struct LaunchArgs {
 template <int D, typename T, bool CAUSAL>
 cudaError_t launch_fwd(const LaunchArgs &a)
 {
-    constexpr int smem = Cfg<D>::SMEM_BYTES;
+    constexpr int smem = Cfg<D, Elem<T>::BYTES>::SMEM_BYTES;
     constexpr int kMaxDev = 64;
     static std::atomic<int> ready[kMaxDev];
     auto kern = attn_fwd_kernel<D, T, CAUSAL>;
@@ -36,7 +36,7 @@ cudaError_t launch_fwd(const LaunchArgs &a)
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < kMaxDev) ready[dev].store(1, std::memory_order_release);
     }
-    kern<<<a.grid, Cfg<D>::THREADS, smem, a.stream>>>(a.q, a.k, a.v, a.p);
+    kern<<<a.grid, Cfg<D, Elem<T>::BYTES>::THREADS, smem, a.stream>>>(a.q, a.k, a.v, a.p);
     return cudaGetLastError();
 }
 
@@ -75,5 +75,7 @@ ATTN_DECLARE_INSTANCE(128, __half, false)
 ATTN_DECLARE_INSTANCE(128, __half, true)
 ATTN_DECLARE_INSTANCE(128, __nv_bfloat16, false)
 ATTN_DECLARE_INSTANCE(128, __nv_bfloat16, true)
+ATTN_DECLARE_INSTANCE(128, __nv_fp8_e4m3, false)
+ATTN_DECLARE_INSTANCE(128, __nv_fp8_e4m3, true)
 
 }  // namespace attn

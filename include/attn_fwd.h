@@ -151,6 +151,24 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o,
                     int64_t max_seqlen_k, int64_t d, int causal, float scale,
                     int dtype, void *stream);
 
+/*
+ * FP8 forward.  "05 · kernel 工程与四代演化" 4.4 describes an FP8 forward that
+ * subtracts an extra 8 from the softmax maximum so that exp2 lands in
+ * [0, 256] and uses more of the 8-bit range.  Here q, k, v are e4m3 (1 byte
+ * per element, [b, h, s, d] contiguous, 16-byte aligned) with per-tensor
+ * descale factors, so the operation is attn_fwd on the real-valued inputs
+ * Q = descale_q*q, K = descale_k*k, V = descale_v*v:
+ *   O = softmax(scale * descale_q * descale_k * q.k^T [+ causal]) (descale_v * v)
+ * Both products run on the 8-bit tensor cores; P is rounded to e4m3 (its
+ * reference sits 8 below the row maximum, so P <= 2^8.5 < 448) and O is
+ * written as bf16 [b, h, sq, d]; LSE as for attn_fwd.  d must be 128.
+ * Returns ATTN_OK or a negative ATTN_ERR_* code.
+ */
+int attn_fwd_fp8(const void *q, const void *k, const void *v, void *o,
+                 float *lse, int64_t b, int64_t h, int64_t sq, int64_t sk,
+                 int64_t d, int causal, float scale, float descale_q,
+                 float descale_k, float descale_v, void *stream);
+
 /* Bytes of workspace attn_fwd_splitkv needs (0 when num_splits == 1), or a
  * negative ATTN_ERR_* code for invalid sizes. */
 int64_t attn_fwd_splitkv_workspace_bytes(int64_t b, int64_t h, int64_t sq,

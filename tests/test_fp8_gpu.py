@@ -1,0 +1,80 @@
+"""e4m3 forward against the fp64 oracle evaluated on the same 8-bit inputs
+(upcast exactly, times the descales).
+
+Tolerance (derived, not tuned): P is rounded to e4m3, 3 mantissa bits, so
+each weight carries a relative error of at most 2^-4 (RMS 2^-4/sqrt(3) =
+3.6% for round-to-nearest).  O is normalised by the sum of the rounded P, so
+the weights still sum to one and the error of O is
+sum_j w_j d_j (v_j - O): an incoherent sum of 3.6% perturbations, i.e. about
+3.6% of the spread of V seen by the row.  The bounds below allow that plus
+bf16 output rounding: rel-L2 <= 5e-2, max-abs <= 6e-2 for N(0,1) inputs.
+LSE uses the unrounded fp32 sum and keeps the 1e-3 bound."""
+import math
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import attention_forward_14_gb300 as af
+from attention_forward_14_gb300 import workloads as W
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+FP8_TOL = dict(max_abs=6e-2, rel_l2=5e-2)
+
+
+def _fp8_inputs(b, h, sq, sk, d, seed, qk_std=1.0):
+    q, k, v = W.draw(b, h, sq, sk, d, "bf16", seed, qk_std)  # seeded draw, then rounded to e4m3
+    return (t.float().to(torch.float8_e4m3fn) for t in (q, k, v))
+
+
+def _check(b, h, sq, sk, causal, seed, dq=1.0, dk=1.0, dv=1.0, qk_std=1.0, what=""):
+    d = 128
+    q8, k8, v8 = _fp8_inputs(b, h, sq, sk, d, seed, qk_std)
+    dev = torch.device("cuda", 0)
+    scale = 1 / math.sqrt(d)
+    o = torch.full((b, h, sq, d), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((b, h, sq), float("nan"), dtype=torch.float32, device=dev)
+    af.attn_fwd_fp8(q8.to(dev), k8.to(dev), v8.to(dev), causal=causal, scale=scale, descale_q=dq, descale_k=dk,
+                    descale_v=dv, o=o, lse=lse)
+    torch.cuda.synchronize()
+    o = o.float().cpu().double().numpy()
+    lse = lse.cpu().double().numpy()
+    qf, kf, vf = (t.float().double().numpy() for t in (q8, k8, v8))
+    o_ref, lse_ref = oracle.attn_fwd(qf * dq, kf * dk, vf * dv, causal, scale)
+    assert np.isfinite(o).all(), what
+    err = np.abs(o - o_ref)
+    rel = float(np.linalg.norm(o - o_ref) / np.linalg.norm(o_ref))
+    inf = np.isinf(lse_ref)
+    assert (np.isinf(lse) == inf).all(), what
+    lerr = float(np.abs(lse[~inf] - lse_ref[~inf]).max()) if (~inf).any() else 0.0
+    print(f"{what}: max-abs {err.max():.3e} rel-L2 {rel:.3e} lse {lerr:.3e}")
+    assert err.max() <= FP8_TOL["max_abs"], (what, err.max())
+    assert rel <= FP8_TOL["rel_l2"], (what, rel)
+    assert lerr <= 1e-3, (what, lerr)
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 256, 256), (2, 3, 300, 300), (1, 2, 1, 1000), (1, 1, 513, 100),
+                                   (1, 2, 1024, 1024)], ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_matches_oracle(shape, causal):
+    b, h, sq, sk = shape
+    _check(b, h, sq, sk, causal, seed=zlib.crc32(repr((shape, causal)).encode()), what=f"{shape} c{causal}")
+
+
+def test_fp8_descales():
+    _check(1, 2, 300, 500, True, seed=4, dq=0.5, dk=2.0, dv=0.25, what="descales")
+
+
+def test_fp8_large_logits():
+    """Q, K ~ N(0, 4) before the e4m3 rounding: sharper softmax rows."""
+    _check(1, 2, 512, 2048, True, seed=8, qk_std=2.0, what="qk2")
+
+
+def test_fp8_rejects_other_head_dims():
+    dev = torch.device("cuda", 0)
+    x = torch.zeros(1, 1, 4, 64, device=dev).to(torch.float8_e4m3fn)
+    with pytest.raises(af.AttnError):
+        af.attn_fwd_fp8(x, x, x)

@@ -1,14 +1,17 @@
 """e4m3 forward against the fp64 oracle evaluated on the same 8-bit inputs
 (upcast exactly, times the descales).
 
-Tolerance (derived, not tuned): P is rounded to e4m3, 3 mantissa bits, so
-each weight carries a relative error of at most 2^-4 (RMS 2^-4/sqrt(3) =
-3.6% for round-to-nearest).  O is normalised by the sum of the rounded P, so
-the weights still sum to one and the error of O is
-sum_j w_j d_j (v_j - O): an incoherent sum of 3.6% perturbations, i.e. about
-3.6% of the spread of V seen by the row.  The bounds below allow that plus
-bf16 output rounding: rel-L2 <= 5e-2, max-abs <= 6e-2 for N(0,1) inputs.
-LSE uses the unrounded fp32 sum and keeps the 1e-3 bound."""
+Tolerance, derived from the arithmetic rather than tuned: P is rounded to
+e4m3 (3 mantissa bits, round to nearest), so each weight carries a relative
+error |d_j| <= 2^-4.  O is divided by the sum of the rounded P, so the
+weights still sum to one and, to first order,
+    O_i - O_exact_i = sum_j w_j (d_j - dbar) (v_j - O_i),
+which is bounded per element by 2^-4 * max_j |v_j - O_i| over the keys the
+row sees (the bound is reached only when few keys share the weight, e.g.
+near the causal diagonal).  The check is that bound (+ 1/8 for the second
+order term) plus bf16 output rounding, per element; in addition the
+incoherent average must stay small: rel-L2 <= 5e-2.  LSE uses the unrounded
+fp32 sum: 1e-3."""
 import math
 import zlib
 
@@ -22,7 +25,25 @@ import oracle
 
 pytestmark = pytest.mark.gpu
 
-FP8_TOL = dict(max_abs=6e-2, rel_l2=5e-2)
+REL_L2 = 5e-2
+
+
+def _row_bound(o_ref, v, causal, sq, sk):
+    """2^-4 * max over visible keys j of |v_j - O_i| (per element), for
+    [b, h, sq, d] O and [b, h, sk, d] V."""
+    vmax = np.maximum.accumulate(v, axis=2)  # prefix max / min over keys
+    vmin = np.minimum.accumulate(v, axis=2)
+    last = np.full(sq, sk - 1)
+    if causal:
+        last = np.minimum(np.arange(sq) + (sk - sq), sk - 1)
+    bound = np.zeros_like(o_ref)
+    ok = last >= 0
+    idx = np.clip(last, 0, sk - 1)
+    hi = vmax[:, :, idx, :]
+    lo = vmin[:, :, idx, :]
+    spread = np.maximum(hi - o_ref, o_ref - lo)
+    bound[:, :, ok, :] = spread[:, :, ok, :]
+    return 2.0 ** -4 * bound * (1 + 2.0 ** -3)
 
 
 def _fp8_inputs(b, h, sq, sk, d, seed, qk_std=1.0):
@@ -47,12 +68,14 @@ def _check(b, h, sq, sk, causal, seed, dq=1.0, dk=1.0, dv=1.0, qk_std=1.0, what=
     assert np.isfinite(o).all(), what
     err = np.abs(o - o_ref)
     rel = float(np.linalg.norm(o - o_ref) / np.linalg.norm(o_ref))
+    bound = _row_bound(o_ref, vf * dv, causal, sq, sk) + 2.0 ** -8 * np.abs(o_ref) + 1e-6
     inf = np.isinf(lse_ref)
     assert (np.isinf(lse) == inf).all(), what
     lerr = float(np.abs(lse[~inf] - lse_ref[~inf]).max()) if (~inf).any() else 0.0
-    print(f"{what}: max-abs {err.max():.3e} rel-L2 {rel:.3e} lse {lerr:.3e}")
-    assert err.max() <= FP8_TOL["max_abs"], (what, err.max())
-    assert rel <= FP8_TOL["rel_l2"], (what, rel)
+    worst = float((err / bound).max())
+    print(f"{what}: max-abs {err.max():.3e} rel-L2 {rel:.3e} lse {lerr:.3e} worst err/bound {worst:.3f}")
+    assert worst <= 1.0, (what, worst)
+    assert rel <= REL_L2, (what, rel)
     assert lerr <= 1e-3, (what, lerr)
 
 

@@ -19,7 +19,7 @@ from dataclasses import dataclass
 
 import torch
 
-DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16}
+DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}
 
 
 @dataclass(frozen=True)
@@ -51,6 +51,9 @@ class Workload:
 
     def bytes(self) -> int:
         """Algorithmic HBM bytes: Q, K, V read once, O written once, fp32 LSE."""
+        if self.dtype == "e4m3":  # 1-byte Q, K, V; bf16 O
+            return (self.b * self.h * (self.sq * self.d + 2 * self.sk * self.d) + 2 * self.b * self.h * self.sq * self.d
+                    + 4 * self.b * self.h * self.sq)
         e = 2
         return (e * self.b * self.h * (2 * self.sq * self.d + 2 * self.sk * self.d)
                 + 4 * self.b * self.h * self.sq)
@@ -64,12 +67,15 @@ WORKLOADS = {
         Workload("noncausal_b8_h16_s1000_d64_bf16", 8, 16, 1000, 1000, 64, "bf16", False, 1.0, 20260002),
         Workload("causal_b2_h32_s4096_d128_bf16", 2, 32, 4096, 4096, 128, "bf16", True, 1.0, 20260003),
         Workload("causal_b1_h32_s16384_d128_bf16_qk3", 1, 32, 16384, 16384, 128, "bf16", True, 3.0, 20260004),
+        # the long causal problem with 8-bit (e4m3) inputs
+        Workload("causal_b1_h32_s16384_d128_e4m3", 1, 32, 16384, 16384, 128, "e4m3", True, 1.0, 20260007),
         # decode step: one query row per (batch, head) against a 16k-key cache
         Workload("decode_b8_h32_q1_s16384_d128_bf16", 8, 32, 1, 16384, 128, "bf16", False, 1.0, 20260005,
                  splitkv=True),
     ]
 }
-ORDER = [n for n in WORKLOADS if not WORKLOADS[n].splitkv]
+ORDER = [n for n in WORKLOADS if not WORKLOADS[n].splitkv and WORKLOADS[n].dtype != "e4m3"]
+FP8 = [n for n in WORKLOADS if WORKLOADS[n].dtype == "e4m3"]
 DECODE = [n for n in WORKLOADS if WORKLOADS[n].splitkv]
 HEADLINE = "causal_b1_h32_s16384_d128_bf16_qk3"
 

@@ -248,6 +248,53 @@ def bench_varlen(args, w):
     print(json.dumps(line), flush=True)
 
 
+def _finish_fp8(args, w, world, rank, dist, dev, q, k, v, qd, kd, vd, o, lse, stream, t_all0, t_all1, total_ms,
+                launch_ms, sampler, step):
+    """e4m3 line: roofline against the 8-bit tensor peak (measured bf16 peak
+    x the nominal fp8/bf16 ratio 2); e2e = H2D of q, k, v (pinned), the
+    forward, D2H of O and LSE, each step."""
+    import torch
+    ms = total_ms / args.steps
+    value = world * w.flops() / (ms * 1e-3) / 1e12
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        step()
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, dist, dev)
+    if rank == 0:
+        peaks = load_peaks()
+        peak8 = 2.0 * peaks["bf16"]
+        kern_ms = statistics.mean(launch_ms)
+        achieved = w.flops() / (kern_ms * 1e-3) / 1e12
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+            "config": {"workload": w.name, "b": w.b, "h": w.h, "sq": w.sq, "sk": w.sk, "d": w.d, "causal": w.causal,
+                       "flops_per_step": w.flops(), "output": "bf16"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak8, "unit": "TFLOP/s",
+                         "frac": achieved / peak8, "traffic": profiled_traffic(w.name),
+                         "peak_kind": f"{peaks['source']} bf16 burst x 2 (nominal fp8/bf16 ratio)",
+                         "kernel": "attn_fwd_kernel<128, e4m3>", "algorithmic_bytes": w.bytes()},
+            "e2e": {"value": world * w.flops() / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+                    "h2d_bytes_per_step": 3 * q.numel(), "d2h_bytes_per_step": 2 * o.numel() + 4 * lse.numel(),
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps,
+            "clocks": sampler.summary(),
+        }
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -301,6 +348,12 @@ def main():
         def step():
             af.attn_fwd_splitkv(qd, kd, vd, causal=w.causal, scale=w.scale, num_splits=splits, o=o, lse=lse,
                                 workspace=ws, stream=stream)
+    elif w.dtype == "e4m3":
+        splits = 1
+        o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+
+        def step():
+            af.attn_fwd_fp8(qd, kd, vd, causal=w.causal, scale=w.scale, o=o, lse=lse, stream=stream)
     else:
         splits = 1
 
@@ -337,6 +390,9 @@ def main():
 
     # end to end through the host-buffer entry point: H2D of Q, K, V from
     # pinned memory, the forward, D2H of O and LSE, every step.
+    if w.dtype == "e4m3":  # the host-buffer entry point takes 16-bit inputs; time the same calls with copies
+        return _finish_fp8(args, w, world, rank, dist, dev, q, k, v, qd, kd, vd, o, lse, stream, t_all0, t_all1,
+                           total_ms, launch_ms, sampler, step)
     qh, kh, vh = (t.pin_memory() for t in (q, k, v))
     oh = torch.empty_like(qh).pin_memory()
     lh = torch.empty(q.shape[:3], dtype=torch.float32).pin_memory()

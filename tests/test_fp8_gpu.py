@@ -101,3 +101,27 @@ def test_fp8_rejects_other_head_dims():
     x = torch.zeros(1, 1, 4, 64, device=dev).to(torch.float8_e4m3fn)
     with pytest.raises(af.AttnError):
         af.attn_fwd_fp8(x, x, x)
+
+
+@pytest.mark.parametrize("name", W.FP8)
+def test_fp8_workload_sampled(name):
+    """The benchmarked e4m3 problem at full size; two whole heads and sampled
+    rows of two more against the oracle under the same bound."""
+    w = W.WORKLOADS[name]
+    q8, k8, v8 = W.inputs(w)
+    dev = torch.device("cuda", 0)
+    o, lse = af.attn_fwd_fp8(q8.to(dev), k8.to(dev), v8.to(dev), causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    o = o.float().cpu().double().numpy()
+    lse = lse.cpu().double().numpy()
+    assert np.isfinite(o).all()
+    qf, kf, vf = (t.float().double().numpy() for t in (q8, k8, v8))
+    for bi, hi in W.sample_heads(w, n=2):
+        o_ref, lse_ref = oracle.attn_fwd(qf[bi:bi + 1, hi:hi + 1], kf[bi:bi + 1, hi:hi + 1], vf[bi:bi + 1, hi:hi + 1],
+                                         w.causal, w.scale)
+        oo = o[bi:bi + 1, hi:hi + 1]
+        err = np.abs(oo - o_ref)
+        bound = _row_bound(o_ref, vf[bi:bi + 1, hi:hi + 1], w.causal, w.sq, w.sk) + 2.0 ** -8 * np.abs(o_ref) + 1e-6
+        assert float((err / bound).max()) <= 1.0
+        assert float(np.linalg.norm(oo - o_ref) / np.linalg.norm(o_ref)) <= REL_L2
+        assert float(np.abs(lse[bi:bi + 1, hi:hi + 1] - lse_ref).max()) <= 1e-3

@@ -63,6 +63,8 @@ def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_forward_14_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
+        if f.startswith("attn_bwd"):  # backward sources do not change the forward kernel
+            continue
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]

@@ -199,7 +199,7 @@ int attn_fwd_splitkv_default_splits(int64_t b, int64_t h, int64_t sq,
  *                ATTN_ERR_SHAPE and a message saying how much they need.
  *
  * The first call on each device looks up the array's device address on that
- * device; make that first call before any stream capture.  All calls on a
+ * device.  All calls on a
  * device share the one array, and it keeps the last call's contents (nothing
  * in it needs to start at zero: each call writes what it reads).  Calls that
  * overlap on the GPU -- on different streams, or from different host threads

@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for the fused attention forward -- TEST INFRASTRUCTURE ONLY.
+"""fp64 CPU oracle for the fused attention forward and its gradients -- TEST
+INFRASTRUCTURE ONLY.
 
 Only the tests, the smoke check and the benchmark's CPU-baseline leg may load
 this package.  It shares no code with the CUDA library and imports nothing
@@ -52,6 +53,20 @@ def _bind(lib):
     lib.oracle_attn_head_rows_f64.argtypes = [dp, dp, dp, i64, i64, i64, ctypes.c_int,
                                               ctypes.c_double,
                                               ctypes.POINTER(ctypes.c_int64), i64, dp, dp]
+    lib.oracle_attn_probs_f64.restype = ctypes.c_int
+    lib.oracle_attn_probs_f64.argtypes = [dp, dp, dp, i64, i64, i64, i64, i64, ctypes.c_int,
+                                          ctypes.c_double]
+    lib.oracle_attn_bwd_f64.restype = ctypes.c_int
+    lib.oracle_attn_bwd_f64.argtypes = [dp, dp, dp, dp, dp, dp, dp, i64, i64, i64, i64, i64,
+                                        ctypes.c_int, ctypes.c_double]
+    lib.oracle_attn_bwd_dq_rows_f64.restype = ctypes.c_int
+    lib.oracle_attn_bwd_dq_rows_f64.argtypes = [dp, dp, dp, dp, i64, i64, i64, ctypes.c_int,
+                                                ctypes.c_double, ctypes.POINTER(ctypes.c_int64),
+                                                i64, dp]
+    lib.oracle_attn_bwd_dkv_cols_f64.restype = ctypes.c_int
+    lib.oracle_attn_bwd_dkv_cols_f64.argtypes = [dp, dp, dp, dp, i64, i64, i64, ctypes.c_int,
+                                                 ctypes.c_double, ctypes.POINTER(ctypes.c_int64),
+                                                 i64, dp, dp]
     return lib
 
 
@@ -133,3 +148,69 @@ def attn_head_rows(q_head, k_head, v_head, rows, causal: bool, scale: float, lib
     if rc != 0:
         raise RuntimeError(f"oracle_attn_head_rows_f64 failed: {rc}")
     return o, lse
+
+
+def attn_probs(q, k, causal: bool, scale: float, lib=None):
+    """P = softmax(scale * Q K^T [+ causal]) as [b, h, sq, sk] fp64."""
+    lib = lib or _load()
+    q, k = _f64(q), _f64(k)
+    b, h, sq, d = q.shape
+    sk = k.shape[2]
+    p = np.zeros((b, h, sq, sk), np.float64)
+    rc = lib.oracle_attn_probs_f64(_ptr(q), _ptr(k), _ptr(p), b, h, sq, sk, d,
+                                   int(bool(causal)), float(scale))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_probs_f64 failed: {rc}")
+    return p
+
+
+def attn_bwd(q, k, v, dout, causal: bool, scale: float, lib=None):
+    """Gradients (dq, dk, dv) of the forward for the output gradient
+    ``dout`` [b, h, sq, d], by the chain rule through the definition."""
+    lib = lib or _load()
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    b, h, sq, d = q.shape
+    sk = k.shape[2]
+    assert k.shape == (b, h, sk, d) and v.shape == (b, h, sk, d) and dout.shape == q.shape
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    rc = lib.oracle_attn_bwd_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), b, h, sq, sk, d, int(bool(causal)), float(scale))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_bwd_f64 failed: {rc}")
+    return dq, dk, dv
+
+
+def attn_bwd_dq_rows(q_head, k_head, v_head, do_head, rows, causal: bool, scale: float, lib=None):
+    """dQ of selected query rows of one head ([sq, d] / [sk, d] inputs)."""
+    lib = lib or _load()
+    q_head, k_head, v_head, do_head = _f64(q_head), _f64(k_head), _f64(v_head), _f64(do_head)
+    sq, d = q_head.shape
+    sk = k_head.shape[0]
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    dq = np.zeros((rows.size, d), np.float64)
+    rc = lib.oracle_attn_bwd_dq_rows_f64(
+        _ptr(q_head), _ptr(k_head), _ptr(v_head), _ptr(do_head), sq, sk, d, int(bool(causal)),
+        float(scale), rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), rows.size, _ptr(dq))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_bwd_dq_rows_f64 failed: {rc}")
+    return dq
+
+
+def attn_bwd_dkv_cols(q_head, k_head, v_head, do_head, cols, causal: bool, scale: float, lib=None):
+    """dK and dV of selected keys of one head ([sq, d] / [sk, d] inputs)."""
+    lib = lib or _load()
+    q_head, k_head, v_head, do_head = _f64(q_head), _f64(k_head), _f64(v_head), _f64(do_head)
+    sq, d = q_head.shape
+    sk = k_head.shape[0]
+    cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+    dk = np.zeros((cols.size, d), np.float64)
+    dv = np.zeros((cols.size, d), np.float64)
+    rc = lib.oracle_attn_bwd_dkv_cols_f64(
+        _ptr(q_head), _ptr(k_head), _ptr(v_head), _ptr(do_head), sq, sk, d, int(bool(causal)),
+        float(scale), cols.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), cols.size, _ptr(dk),
+        _ptr(dv))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_bwd_dkv_cols_f64 failed: {rc}")
+    return dk, dv

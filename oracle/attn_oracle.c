@@ -31,8 +31,13 @@
  *     over K/V tiles of Bc keys, running m and l, O rescaled on every tile),
  *     restated in fp64 so that its algebra can be checked against the
  *     definition.
- * Parity is pinned by the CPU tests (brute force, closed forms, invariants);
- * nothing here is "parity unpinned".
+ * and, for the backward pass (end of the file): the gradients dQ, dK, dV of
+ * the forward by definition (oracle_attn_bwd_f64), the same for selected
+ * query rows or keys of one head (for spot checks of large problems), and
+ * the probabilities P themselves (used to size error bounds).
+ * Parity is pinned by the CPU tests (brute force, closed forms, invariants,
+ * finite differences of the forward for the gradients); nothing here is
+ * "parity unpinned".
  */
 #include <math.h>
 #include <stdint.h>
@@ -264,4 +269,269 @@ int oracle_attn_online_f64(const double *q, const double *k, const double *v,
         free(pv);
     }
     return err;
+}
+
+/* ================================================================ backward
+ *
+ * Gradients of the forward above.  The pages name a backward pass (the
+ * exported bwd / varlen_bwd entry points of "05 · kernel 工程与四代演化"
+ * 6.1) but do not state it, so this is the chain rule through the
+ * definition.  For a scalar loss L with dO = dL/dO given:
+ *   O = P V                  ->  dV = P^T dO,   dP = dO V^T
+ *   P[i, :] = softmax(S[i, :])
+ *                            ->  dS[i, j] = P[i, j] (dP[i, j] - D[i]),
+ *                                D[i] = sum_t P[i, t] dP[i, t]
+ *   S = scale Q K^T          ->  dQ = scale dS K,   dK = scale dS^T Q
+ * Masked keys have P = 0 and take no part; a row that sees no key has P = 0
+ * throughout, so its dQ is 0 and it adds nothing to dK or dV.
+ */
+
+/* P[i, 0..sk) of one query row by definition (two-pass softmax); masked
+ * keys get 0.  Returns the number of visible keys (0: the row is all 0). */
+static int64_t probs_row_by_definition(const double *qi, const double *K, int64_t i,
+                                       int64_t sq, int64_t sk, int64_t d, int causal,
+                                       double scale, double *prow)
+{
+    int64_t last = last_visible_key(i, sq, sk, causal);
+    for (int64_t j = 0; j < sk; ++j) prow[j] = 0.0;
+    if (last < 0) return 0;
+    int64_t n = 1 + last; /* visible keys 0..last */
+    double m = -INFINITY;
+    for (int64_t j = 0; j < n; ++j) {
+        const double *kj = K + j * d;
+        double dot = 0.0;
+        for (int64_t c = 0; c < d; ++c) dot += qi[c] * kj[c];
+        prow[j] = dot * scale;
+        if (prow[j] > m) m = prow[j];
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        prow[j] = exp(prow[j] - m);
+        l += prow[j];
+    }
+    for (int64_t j = 0; j < n; ++j) prow[j] /= l;
+    return n;
+}
+
+/* The probabilities P = softmax(scale Q K^T [+ causal]) themselves:
+ * p [b, h, sq, sk] (used to size error bounds of the gradients). */
+int oracle_attn_probs_f64(const double *q, const double *k, double *p, int64_t b,
+                          int64_t h, int64_t sq, int64_t sk, int64_t d, int causal,
+                          double scale)
+{
+    if (check_dims(b, h, sq, sk, d) != ORACLE_OK) return ORACLE_ERR_ARG;
+    int64_t total = b * h * sq;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t r = 0; r < total; ++r) {
+        int64_t head = r / sq, i = r % sq;
+        probs_row_by_definition(q + r * d, k + head * sk * d, i, sq, sk, d, causal, scale,
+                                p + r * sk);
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Full backward by definition.  q, dout, dq: [b, h, sq, d]; k, v, dk, dv:
+ * [b, h, sk, d].  P and dP are materialised per head ([sq, sk] each).
+ */
+int oracle_attn_bwd_f64(const double *q, const double *k, const double *v,
+                        const double *dout, double *dq, double *dk, double *dv,
+                        int64_t b, int64_t h, int64_t sq, int64_t sk, int64_t d,
+                        int causal, double scale)
+{
+    if (check_dims(b, h, sq, sk, d) != ORACLE_OK) return ORACLE_ERR_ARG;
+    int64_t bh = b * h;
+    for (int64_t x = 0; x < bh * sq * d; ++x) dq[x] = 0.0;
+    for (int64_t x = 0; x < bh * sk * d; ++x) dk[x] = dv[x] = 0.0;
+    if (sq == 0 || sk == 0) return ORACLE_OK;
+    double *P = (double *)malloc(sizeof(double) * (size_t)(sq * sk));
+    double *dP = (double *)malloc(sizeof(double) * (size_t)(sq * sk));
+    if (!P || !dP) {
+        free(P);
+        free(dP);
+        return ORACLE_ERR_NOMEM;
+    }
+    for (int64_t hd = 0; hd < bh; ++hd) {
+        const double *Q = q + hd * sq * d, *K = k + hd * sk * d, *V = v + hd * sk * d;
+        const double *dO = dout + hd * sq * d;
+        double *dQ = dq + hd * sq * d, *dK = dk + hd * sk * d, *dV = dv + hd * sk * d;
+#pragma omp parallel for schedule(dynamic, 8)
+        for (int64_t i = 0; i < sq; ++i) {
+            probs_row_by_definition(Q + i * d, K, i, sq, sk, d, causal, scale, P + i * sk);
+            /* dP = dO V^T */
+            for (int64_t j = 0; j < sk; ++j) {
+                double acc = 0.0;
+                for (int64_t c = 0; c < d; ++c) acc += dO[i * d + c] * V[j * d + c];
+                dP[i * sk + j] = acc;
+            }
+            /* D[i] = sum_t P[i, t] dP[i, t];  dS (kept in dP) = P (dP - D) */
+            double Di = 0.0;
+            for (int64_t t = 0; t < sk; ++t) Di += P[i * sk + t] * dP[i * sk + t];
+            for (int64_t j = 0; j < sk; ++j) dP[i * sk + j] = P[i * sk + j] * (dP[i * sk + j] - Di);
+            /* dQ = scale dS K */
+            for (int64_t c = 0; c < d; ++c) {
+                double acc = 0.0;
+                for (int64_t j = 0; j < sk; ++j) acc += dP[i * sk + j] * K[j * d + c];
+                dQ[i * d + c] = scale * acc;
+            }
+        }
+#pragma omp parallel for schedule(dynamic, 8)
+        for (int64_t j = 0; j < sk; ++j) {
+            /* dV = P^T dO,  dK = scale dS^T Q */
+            for (int64_t c = 0; c < d; ++c) {
+                double av = 0.0, ak = 0.0;
+                for (int64_t i = 0; i < sq; ++i) {
+                    av += P[i * sk + j] * dO[i * d + c];
+                    ak += dP[i * sk + j] * Q[i * d + c];
+                }
+                dV[j * d + c] = av;
+                dK[j * d + c] = scale * ak;
+            }
+        }
+    }
+    free(P);
+    free(dP);
+    return ORACLE_OK;
+}
+
+/*
+ * dQ for selected query rows of one head (for spot checks of large
+ * problems): the same definition, one row at a time.  q_head, do_head:
+ * [sq, d]; k_head, v_head: [sk, d]; dq_rows: [nrows, d].
+ */
+int oracle_attn_bwd_dq_rows_f64(const double *q_head, const double *k_head,
+                                const double *v_head, const double *do_head,
+                                int64_t sq, int64_t sk, int64_t d, int causal,
+                                double scale, const int64_t *rows, int64_t nrows,
+                                double *dq_rows)
+{
+    if (check_dims(1, 1, sq, sk, d) != ORACLE_OK || nrows < 0) return ORACLE_ERR_ARG;
+    for (int64_t t = 0; t < nrows; ++t)
+        if (rows[t] < 0 || rows[t] >= sq) return ORACLE_ERR_ARG;
+    int err = ORACLE_OK;
+#pragma omp parallel
+    {
+        double *prow = (double *)malloc(sizeof(double) * (size_t)(sk > 0 ? sk : 1));
+        double *dprow = (double *)malloc(sizeof(double) * (size_t)(sk > 0 ? sk : 1));
+        if (!prow || !dprow) {
+#pragma omp atomic write
+            err = ORACLE_ERR_NOMEM;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t t = 0; t < nrows; ++t) {
+                int64_t i = rows[t];
+                const double *dOi = do_head + i * d;
+                probs_row_by_definition(q_head + i * d, k_head, i, sq, sk, d, causal, scale, prow);
+                double Di = 0.0;
+                for (int64_t j = 0; j < sk; ++j) {
+                    double acc = 0.0;
+                    for (int64_t c = 0; c < d; ++c) acc += dOi[c] * v_head[j * d + c];
+                    dprow[j] = acc;
+                    Di += prow[j] * acc;
+                }
+                for (int64_t c = 0; c < d; ++c) {
+                    double acc = 0.0;
+                    for (int64_t j = 0; j < sk; ++j)
+                        acc += prow[j] * (dprow[j] - Di) * k_head[j * d + c];
+                    dq_rows[t * d + c] = scale * acc;
+                }
+            }
+        }
+        free(prow);
+        free(dprow);
+    }
+    return err;
+}
+
+/*
+ * dK and dV for selected keys of one head.  Every query row's softmax
+ * (its max m[i] and sum l[i]) and D[i] are computed first, by definition;
+ * then for each selected key j and each row i that sees it:
+ *   P[i, j] = exp(S[i, j] - m[i]) / l[i],  dP[i, j] = dO[i] . V[j],
+ *   dV[j] += P[i, j] dO[i],  dK[j] += scale P[i, j] (dP[i, j] - D[i]) Q[i].
+ * dk_cols, dv_cols: [ncols, d].
+ */
+int oracle_attn_bwd_dkv_cols_f64(const double *q_head, const double *k_head,
+                                 const double *v_head, const double *do_head,
+                                 int64_t sq, int64_t sk, int64_t d, int causal,
+                                 double scale, const int64_t *cols, int64_t ncols,
+                                 double *dk_cols, double *dv_cols)
+{
+    if (check_dims(1, 1, sq, sk, d) != ORACLE_OK || ncols < 0) return ORACLE_ERR_ARG;
+    for (int64_t t = 0; t < ncols; ++t)
+        if (cols[t] < 0 || cols[t] >= sk) return ORACLE_ERR_ARG;
+    double *m = (double *)malloc(sizeof(double) * (size_t)(sq > 0 ? sq : 1));
+    double *l = (double *)malloc(sizeof(double) * (size_t)(sq > 0 ? sq : 1));
+    double *D = (double *)malloc(sizeof(double) * (size_t)(sq > 0 ? sq : 1));
+    if (!m || !l || !D) {
+        free(m);
+        free(l);
+        free(D);
+        return ORACLE_ERR_NOMEM;
+    }
+    int err = ORACLE_OK;
+#pragma omp parallel
+    {
+        double *srow = (double *)malloc(sizeof(double) * (size_t)(sk > 0 ? sk : 1));
+        if (!srow) {
+#pragma omp atomic write
+            err = ORACLE_ERR_NOMEM;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t i = 0; i < sq; ++i) {
+                const double *qi = q_head + i * d, *dOi = do_head + i * d;
+                int64_t n = last_visible_key(i, sq, sk, causal) + 1;
+                double mi = -INFINITY;
+                for (int64_t j = 0; j < n; ++j) {
+                    double dot = 0.0;
+                    for (int64_t c = 0; c < d; ++c) dot += qi[c] * k_head[j * d + c];
+                    srow[j] = scale * dot;
+                    if (srow[j] > mi) mi = srow[j];
+                }
+                double li = 0.0, Di = 0.0;
+                for (int64_t j = 0; j < n; ++j) li += exp(srow[j] - mi);
+                for (int64_t j = 0; j < n; ++j) {
+                    double acc = 0.0;
+                    for (int64_t c = 0; c < d; ++c) acc += dOi[c] * v_head[j * d + c];
+                    Di += exp(srow[j] - mi) / li * acc;
+                }
+                m[i] = mi;
+                l[i] = li;
+                D[i] = Di;
+            }
+        }
+        free(srow);
+    }
+    if (err != ORACLE_OK) {
+        free(m);
+        free(l);
+        free(D);
+        return err;
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < ncols; ++t) {
+        int64_t j = cols[t];
+        const double *kj = k_head + j * d, *vj = v_head + j * d;
+        double *dKj = dk_cols + t * d, *dVj = dv_cols + t * d;
+        for (int64_t c = 0; c < d; ++c) dKj[c] = dVj[c] = 0.0;
+        for (int64_t i = 0; i < sq; ++i) {
+            if (j > last_visible_key(i, sq, sk, causal)) continue;
+            const double *qi = q_head + i * d, *dOi = do_head + i * d;
+            double s = 0.0, dp = 0.0;
+            for (int64_t c = 0; c < d; ++c) {
+                s += qi[c] * kj[c];
+                dp += dOi[c] * vj[c];
+            }
+            double p = exp(s * scale - m[i]) / l[i];
+            double ds = p * (dp - D[i]);
+            for (int64_t c = 0; c < d; ++c) {
+                dVj[c] += p * dOi[c];
+                dKj[c] += scale * ds * qi[c];
+            }
+        }
+    }
+    free(m);
+    free(l);
+    free(D);
+    return ORACLE_OK;
 }

@@ -309,6 +309,179 @@ def pin_empty(lib):
     return fails
 
 
+# ---------------------------------------------------------------- backward pins
+#
+# The gradients are pinned by the forward: dL/dQ, dL/dK, dL/dV of the scalar
+# L = sum(O * dO) by central differences, in 40-digit arithmetic on tiny
+# inputs (textbook softmax, nothing shared with the oracle) and in fp64 on
+# the already-pinned forward oracle for larger ones; plus what the chain rule
+# fixes without computing it (rows of dS sum to zero, so the key gradients
+# sum to zero; rows of P sum to one, so the value gradients sum to the
+# output gradients of the rows that see a key; identical keys or a zero
+# scale make the query gradient vanish).
+
+
+def _loss_mp(q, k, v, do, causal, scale):
+    """L = sum_i sum_c O[i, c] dO[i, c] for one head, textbook softmax in
+    mpmath (q, k, v, do: nested lists of mpf)."""
+    sq, sk, d = len(q), len(k), len(k[0]) if k else 0
+    total = mpmath.mpf(0)
+    for i in range(sq):
+        vis = [j for j in range(sk) if (not causal) or j <= i + sk - sq]
+        if not vis:
+            continue
+        e = [mpmath.exp(scale * mpmath.fsum(q[i][c] * k[j][c] for c in range(d))) for j in vis]
+        z = mpmath.fsum(e)
+        for c in range(d):
+            total += do[i][c] * mpmath.fsum(e[t] * v[j][c] for t, j in enumerate(vis)) / z
+    return total
+
+
+def pin_bwd_finite_difference_mp(lib):
+    """Every entry of dQ, dK, dV on tiny inputs against central differences
+    of the 40-digit textbook loss (step 1e-12: truncation ~1e-24)."""
+    fails = []
+    mpmath.mp.dps = 40
+    hstep = mpmath.mpf("1e-12")
+    for t, (sq, sk, d) in enumerate([(1, 1, 1), (2, 3, 2), (3, 2, 2), (3, 3, 1)]):
+        r = _rng(7000 + t)
+        q, k, v, do = (r.standard_normal(shape) for shape in ((sq, d), (sk, d), (sk, d), (sq, d)))
+        scale = 0.7 + 0.1 * t
+        for causal in (False, True):
+            dq, dk, dv = oracle.attn_bwd(q[None, None], k[None, None], v[None, None], do[None, None],
+                                         causal, scale, lib=lib)
+            mp = [[[mpmath.mpf(float(x)) for x in row] for row in a] for a in (q, k, v, do)]
+            sc = mpmath.mpf(scale)
+            for which, got in ((0, dq[0, 0]), (1, dk[0, 0]), (2, dv[0, 0])):
+                want = np.zeros_like(got)
+                for (a, c) in np.ndindex(got.shape):
+                    plus = [[row[:] for row in m] for m in mp]
+                    minus = [[row[:] for row in m] for m in mp]
+                    plus[which][a][c] += hstep
+                    minus[which][a][c] -= hstep
+                    want[a, c] = float((_loss_mp(*plus, causal, sc) - _loss_mp(*minus, causal, sc)) / (2 * hstep))
+                fails += _cmp(f"bwd-fd-mp sq{sq} sk{sk} d{d} c{int(causal)} grad{which}", got, want, 1e-11)
+    return fails
+
+
+def pin_bwd_finite_difference_f64(lib):
+    """Larger inputs (several heads, sq != sk both ways): sampled entries of
+    every gradient against central differences of the fp64 forward oracle
+    (step 1e-5: error ~1e-10)."""
+    fails = []
+    for t, (sq, sk, d) in enumerate([(6, 9, 5), (9, 6, 5), (8, 8, 16)]):
+        r = _rng(7100 + t)
+        q = r.standard_normal((1, 2, sq, d))
+        k = r.standard_normal((1, 2, sk, d))
+        v = r.standard_normal((1, 2, sk, d))
+        do = r.standard_normal((1, 2, sq, d))
+        scale = 1.0 / math.sqrt(d)
+        for causal in (False, True):
+            grads = oracle.attn_bwd(q, k, v, do, causal, scale, lib=lib)
+
+            def loss(a, b, c):
+                o, _ = oracle.attn_fwd(a, b, c, causal, scale, lib=lib)
+                return float((o * do).sum())
+
+            for which in range(3):
+                base = (q, k, v)[which]
+                for idx in [tuple(int(r.integers(0, n)) for n in base.shape) for _ in range(12)]:
+                    h = 1e-5
+                    args_p = [x.copy() for x in (q, k, v)]
+                    args_m = [x.copy() for x in (q, k, v)]
+                    args_p[which][idx] += h
+                    args_m[which][idx] -= h
+                    want = (loss(*args_p) - loss(*args_m)) / (2 * h)
+                    got = grads[which][idx]
+                    if not abs(got - want) <= 1e-7:
+                        fails.append(f"bwd-fd-f64 sq{sq} sk{sk} c{int(causal)} grad{which}{idx}: "
+                                     f"{got:.12f} vs {want:.12f}")
+    return fails
+
+
+def pin_bwd_sums(lib):
+    """Sum over keys of dK is 0 (each row of dS sums to 0); sum over keys of
+    dV is the sum of dO over the rows that see at least one key."""
+    fails = []
+    for t, (sq, sk, d) in enumerate([(5, 5, 4), (7, 4, 3), (4, 7, 3), (33, 40, 8)]):
+        r = _rng(7200 + t)
+        q, do = r.standard_normal((1, 2, sq, d)), r.standard_normal((1, 2, sq, d))
+        k, v = r.standard_normal((1, 2, sk, d)), r.standard_normal((1, 2, sk, d))
+        for causal in (False, True):
+            _, dk, dv = oracle.attn_bwd(q, k, v, do, causal, 0.8, lib=lib)
+            sees = np.array([(not causal) or (i + sk - sq >= 0) for i in range(sq)])
+            fails += _cmp(f"bwd-sum-dk sq{sq} sk{sk} c{int(causal)}", dk.sum(axis=2), np.zeros((1, 2, d)))
+            fails += _cmp(f"bwd-sum-dv sq{sq} sk{sk} c{int(causal)}", dv.sum(axis=2),
+                          do[:, :, sees].sum(axis=2))
+    return fails
+
+
+def pin_bwd_identical_keys_and_zero_scale(lib):
+    """Identical key rows: the logits of a row are all equal whatever Q is,
+    so dQ = 0.  Zero scale: dQ = dK = 0 and attention is uniform over the
+    visible keys, so dV[j] = sum over rows i that see j of dO[i] / n_i."""
+    fails = []
+    r = _rng(7300)
+    sq, sk, d = 6, 8, 4
+    q, do = r.standard_normal((1, 1, sq, d)), r.standard_normal((1, 1, sq, d))
+    k1 = np.repeat(r.standard_normal((1, 1, 1, d)), sk, axis=2)
+    k, v = r.standard_normal((1, 1, sk, d)), r.standard_normal((1, 1, sk, d))
+    for causal in (False, True):
+        dq, _, _ = oracle.attn_bwd(q, k1, v, do, causal, 0.9, lib=lib)
+        fails += _cmp(f"bwd-identical-keys c{int(causal)} dq", dq, np.zeros_like(dq))
+        dq, dk, dv = oracle.attn_bwd(q, k, v, do, causal, 0.0, lib=lib)
+        fails += _cmp(f"bwd-scale0 c{int(causal)} dq", dq, np.zeros_like(dq))
+        fails += _cmp(f"bwd-scale0 c{int(causal)} dk", dk, np.zeros_like(dk))
+        want = np.zeros_like(dv)
+        for i in range(sq):
+            vis = [j for j in range(sk) if (not causal) or j <= i + sk - sq]
+            for j in vis:
+                want[0, 0, j] += do[0, 0, i] / len(vis)
+        fails += _cmp(f"bwd-scale0 c{int(causal)} dv", dv, want)
+    return fails
+
+
+def pin_bwd_rows_cols_and_probs(lib):
+    """The single-head row / key variants agree with the full gradients, and
+    the probabilities reproduce the pinned forward (P V = O, rows sum to 1)."""
+    fails = []
+    r = _rng(7400)
+    sq, sk, d = 37, 29, 6
+    q, do = r.standard_normal((2, 2, sq, d)), r.standard_normal((2, 2, sq, d))
+    k, v = r.standard_normal((2, 2, sk, d)), r.standard_normal((2, 2, sk, d))
+    rows, cols = [0, 5, 17, 36], [0, 3, 19, 28]
+    for causal in (False, True):
+        dq, dk, dv = oracle.attn_bwd(q, k, v, do, causal, 0.6, lib=lib)
+        dq_r = oracle.attn_bwd_dq_rows(q[1, 0], k[1, 0], v[1, 0], do[1, 0], rows, causal, 0.6, lib=lib)
+        dk_c, dv_c = oracle.attn_bwd_dkv_cols(q[1, 0], k[1, 0], v[1, 0], do[1, 0], cols, causal, 0.6, lib=lib)
+        fails += _cmp(f"bwd-rows c{int(causal)}", dq_r, dq[1, 0, rows])
+        fails += _cmp(f"bwd-cols-dk c{int(causal)}", dk_c, dk[1, 0, cols])
+        fails += _cmp(f"bwd-cols-dv c{int(causal)}", dv_c, dv[1, 0, cols])
+        p = oracle.attn_probs(q, k, causal, 0.6, lib=lib)
+        o, _ = oracle.attn_fwd(q, k, v, causal, 0.6, lib=lib)
+        fails += _cmp(f"probs c{int(causal)} PV", np.einsum("bhij,bhjc->bhic", p, v), o)
+        sees = np.array([(not causal) or (i + sk - sq >= 0) for i in range(sq)], np.float64)
+        fails += _cmp(f"probs c{int(causal)} rows", p.sum(-1), np.broadcast_to(sees, p.shape[:3]))
+    return fails
+
+
+def pin_bwd_empty(lib):
+    """No keys: dQ = 0 (and dK, dV are empty); no queries: dK = dV = 0."""
+    fails = []
+    r = _rng(7500)
+    q, do = r.standard_normal((1, 2, 3, 4)), r.standard_normal((1, 2, 3, 4))
+    k0 = np.zeros((1, 2, 0, 4))
+    for causal in (False, True):
+        dq, dk, dv = oracle.attn_bwd(q, k0, k0, do, causal, 1.0, lib=lib)
+        fails += _cmp(f"bwd-empty-k c{int(causal)} dq", dq, np.zeros_like(q))
+        k, v = r.standard_normal((1, 2, 5, 4)), r.standard_normal((1, 2, 5, 4))
+        q0 = np.zeros((1, 2, 0, 4))
+        _, dk, dv = oracle.attn_bwd(q0, k, v, q0, causal, 1.0, lib=lib)
+        fails += _cmp(f"bwd-empty-q c{int(causal)} dk", dk, np.zeros_like(k))
+        fails += _cmp(f"bwd-empty-q c{int(causal)} dv", dv, np.zeros_like(v))
+    return fails
+
+
 ALL_PINS = [
     pin_worked_examples,
     pin_bruteforce,
@@ -321,4 +494,10 @@ ALL_PINS = [
     pin_online_matches_definition,
     pin_head_rows,
     pin_empty,
+    pin_bwd_finite_difference_mp,
+    pin_bwd_finite_difference_f64,
+    pin_bwd_sums,
+    pin_bwd_identical_keys_and_zero_scale,
+    pin_bwd_rows_cols_and_probs,
+    pin_bwd_empty,
 ]

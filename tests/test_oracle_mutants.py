@@ -29,6 +29,20 @@ MUTANTS = [
      "for (int64_t j0 = 0; j0 < sk; j0 += (bc > 1 ? bc - 1 : 1)) {"),
     ("head_stride_wrong", "const double *Kh = k + head * sk * d;\n                const double *Vh = v + head * sk * d;\n                double l_out;",
      "const double *Kh = k; /* head offset forgotten */\n                const double *Vh = v + head * sk * d;\n                double l_out;"),
+    # backward
+    ("bwd_D_dropped", "dP[i * sk + j] = P[i * sk + j] * (dP[i * sk + j] - Di);",
+     "dP[i * sk + j] = P[i * sk + j] * dP[i * sk + j];"),
+    ("bwd_dk_scale_dropped", "dK[j * d + c] = scale * ak;", "dK[j * d + c] = ak;"),
+    ("bwd_dv_uses_ds", "av += P[i * sk + j] * dO[i * d + c];", "av += dP[i * sk + j] * dO[i * d + c];"),
+    ("bwd_dq_uses_v", "acc += dP[i * sk + j] * K[j * d + c];", "acc += dP[i * sk + j] * V[j * d + c];"),
+    ("bwd_dp_indices_swapped", "for (int64_t c = 0; c < d; ++c) acc += dO[i * d + c] * V[j * d + c];",
+     "for (int64_t c = 0; c < d; ++c) acc += dO[(j % sq) * d + c] * V[(i % sk) * d + c];"),
+    ("bwd_rows_D_dropped", "acc += prow[j] * (dprow[j] - Di) * k_head[j * d + c];",
+     "acc += prow[j] * dprow[j] * k_head[j * d + c];"),
+    ("bwd_cols_scale_dropped", "dKj[c] += scale * ds * qi[c];", "dKj[c] += ds * qi[c];"),
+    ("bwd_cols_mask_ignored", "if (j > last_visible_key(i, sq, sk, causal)) continue;", ""),
+    ("bwd_probs_strict_mask", "int64_t n = 1 + last; /* visible keys 0..last */",
+     "int64_t n = last; /* visible keys 0..last-1 */"),
 ]
 
 

@@ -1,4 +1,4 @@
-"""GB300-native fused attention forward (sm_103a).
+"""GB300-native fused attention forward and backward (sm_103a).
 
 The compute path is the C-ABI library ``libattn_fwd.so`` built from ``csrc/``;
 ``attn_fwd`` and friends (in ``binding``) only marshal arguments to it.  The
@@ -7,11 +7,13 @@ is no fallback path.
 """
 from .binding import (  # noqa: F401
     AttnError,
+    attn_bwd,
     attn_fwd,
     attn_fwd_fp8,
     attn_fwd_host,
     attn_fwd_splitkv,
     attn_fwd_varlen,
+    bwd_workspace_bytes,
     lib_path,
     load,
     status,

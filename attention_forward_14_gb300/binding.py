@@ -1,7 +1,7 @@
 """ctypes binding of libattn_fwd.so (the C ABI in include/attn_fwd.h).
 
-Argument marshalling only: every step of the forward runs in the library's
-CUDA kernels.  PyTorch provides device memory and streams.  If the library is
+Argument marshalling only: every step of the forward and backward runs in the
+library's CUDA kernels.  PyTorch provides device memory and streams.  If the library is
 missing or cannot be loaded, every call raises -- there is no fallback.
 """
 from __future__ import annotations
@@ -23,7 +23,7 @@ ERRORS = {
 # Every function include/attn_fwd.h declares.
 EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_fwd_varlen", "attn_fwd_fp8", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
            "attn_fwd_splitkv_default_splits", "attn_fwd_splitkv_noalloc", "attn_last_error", "attn_fwd_status", "attn_fwd_status_clear",
-           "attn_fwd_watchdog_selftest", "attn_version"]
+           "attn_fwd_watchdog_selftest", "attn_version", "attn_bwd", "attn_bwd_workspace_bytes"]
 
 
 class AttnError(RuntimeError):
@@ -70,6 +70,11 @@ def _bind(lib):
                                                c_int, c_int, c_int, vp]
     lib.attn_version.restype = ctypes.c_char_p
     lib.attn_version.argtypes = []
+    lib.attn_bwd.restype = c_int
+    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_float, c_int,
+                             vp, i64, vp]
+    lib.attn_bwd_workspace_bytes.restype = i64
+    lib.attn_bwd_workspace_bytes.argtypes = [i64, i64, i64, i64]
     return lib
 
 
@@ -298,3 +303,52 @@ def watchdog_selftest(q, k, v, o, lse, causal, scale, withheld_load: int, timeou
                                             int(withheld_load), int(timeout_ms),
                                             _stream_handle(None, q.device))
     return _check(rc, lib)
+
+
+def bwd_workspace_bytes(b: int, h: int, sq: int, d: int) -> int:
+    lib = load()
+    return _check(int(lib.attn_bwd_workspace_bytes(b, h, sq, d)), lib)
+
+
+def attn_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of attn_fwd for the output gradient ``dout``.
+
+    q, o, dout: [b, h, sq, 128]; k, v: [b, h, sk, 128] contiguous CUDA
+    tensors of one dtype (fp16 or bf16); lse: fp32 [b, h, sq] from the
+    forward.  Outputs and the workspace (a CUDA uint8 tensor of at least
+    bwd_workspace_bytes bytes) are allocated with torch when not given."""
+    import torch
+    lib = load()
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise AttnError(-2, "q, k, v must be 4-D [b, h, s, d]")
+    b, h, sq, d = q.shape
+    sk = k.shape[2]
+    if tuple(k.shape) != (b, h, sk, d) or tuple(v.shape) != (b, h, sk, d) or o.shape != q.shape or \
+            dout.shape != q.shape or tuple(lse.shape) != (b, h, sq):
+        raise AttnError(-2, "shape mismatch among q, k, v, o, dout, lse")
+    if not (q.dtype == k.dtype == v.dtype == o.dtype == dout.dtype) or lse.dtype != torch.float32:
+        raise AttnError(-4, "q, k, v, o, dout must share a dtype; lse must be fp32")
+    if scale is None:
+        scale = 1.0 / float(d) ** 0.5
+    if dq is None:
+        dq = torch.empty_like(q)
+    if dk is None:
+        dk = torch.empty_like(k)
+    if dv is None:
+        dv = torch.empty_like(v)
+    if workspace is None:
+        with torch.cuda.device(q.device):
+            need = bwd_workspace_bytes(b, h, sq, d)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout), ("lse", lse), ("dq", dq), ("dk", dk),
+                    ("dv", dv), ("workspace", workspace)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise AttnError(-2, f"{name} must be a contiguous CUDA tensor")
+    with torch.cuda.device(q.device):
+        rc = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), b, h, sq, sk, d, int(bool(causal)),
+                          float(scale), _dtype_code(q), workspace.data_ptr(),
+                          workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
+    _check(rc, lib)
+    return dq, dk, dv

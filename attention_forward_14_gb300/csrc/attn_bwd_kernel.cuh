@@ -1,0 +1,777 @@
+// Attention backward for sm_103a (GB300): gradients dQ, dK, dV of
+// O = softmax(scale * Q K^T [+ causal]) V for a given dO, from the forward's
+// O and natural log-sum-exp LSE.
+//
+// What is computed (the chain rule through the forward's definition; the
+// pages name the backward -- the bwd / varlen_bwd entry points of
+// "05 · kernel 工程与四代演化" 6.1 -- without stating it):
+//   P = exp(scale * Q K^T - LSE)   (recomputed; masked keys give 0)
+//   dV = P^T dO,   dP = dO V^T,   D = rowsum(dO * O)  ( = rowsum(P * dP) )
+//   dS = P * (dP - D),   dQ = scale dS K,   dK = scale dS^T Q
+//
+// Three launches on the caller's stream:
+//   attn_bwd_prep_kernel    D per query row, LSE * log2(e) per row (+inf for
+//                           padding and rows that see no key), and a zeroed
+//                           fp32 dQ accumulator;
+//   attn_bwd_kernel         one persistent CTA per SM; a work unit is one
+//                           block of 128 keys of one head.  K and V stay in
+//                           shared memory while the unit streams 128-query
+//                           tiles of Q, dO (and their LSE, D) through a
+//                           two-stage TMA ring.  Per tile, on the tensor
+//                           cores (tcgen05.mma, accumulators in TMEM):
+//                             S^T  = K Q^T           [keys x queries]
+//                             dP^T = V dO^T
+//                             dV  += P^T dO          (P^T read from TMEM)
+//                             dK  += dS^T Q          (dS^T read from TMEM)
+//                             dQ^T = K^T dS^T        (both from shared)
+//                           dV and dK accumulate in TMEM over the tiles of
+//                           the unit; each tile's dQ^T is added into the
+//                           fp32 accumulator with coalesced red.global.add;
+//   attn_bwd_dq_convert_kernel  dQ = accumulator cast to the input type.
+//
+// CTA of 16 warps:
+//   warps 0-3 / 4-7   softmax groups: each thread owns one key row (a TMEM
+//                     lane) and 64 of the tile's 128 query columns; it
+//                     turns S^T into P^T (kept in fp32 registers, stored to
+//                     TMEM as 16-bit for the dV product) and dP^T into dS^T
+//                     (stored to TMEM for dK and to shared memory for dQ)
+//   warps 8-11        dQ drain (TMEM -> red.global.add) and the dK / dV
+//                     epilogue of each unit
+//   warp 12           MMA issuer, tensor-memory owner
+//   warp 13           TMA producer
+//   warps 14-15       no work (they complete warpgroup 3)
+// Tensor memory (512 columns): dV [0,128), dK [128,256), S^T/P^T [256,384),
+// dP^T/dS^T then dQ^T [384,512).
+//
+// Every wait is bounded, as in the forward: a wait that runs out records
+// where in the status word, raises the CTA's abort flag, and the CTA winds
+// down (copies and MMAs drained, tensor memory freed) and returns.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <type_traits>
+
+#include "ptx.cuh"
+
+namespace attn {
+namespace bwd {
+
+struct BwdParams {
+    const void *o;         // forward output [bh, sq, D] of T   (prep)
+    const void *dout;      // dO [bh, sq, D] of T                (prep)
+    const float *lse;      // forward LSE [bh, sq] (natural log)  (prep)
+    float *lse2;           // [bh, sq_pad]: LSE * log2(e); +inf for padding / no key
+    float *dsum;           // [bh, sq_pad]: D = rowsum(dO * O); 0 for padding
+    float *dq_acc;         // [bh, sq, D] fp32 accumulator of dQ
+    void *dq;              // [bh, sq, D] of T                   (convert)
+    void *dk, *dv;         // [bh, sk, D] of T
+    uint32_t *status;      // watchdog status word (4 x u32)
+    int32_t bh, sq, sk, sq_pad;
+    int32_t num_kblk;      // ceil(sk / 128)
+    int32_t num_units;     // bh * num_kblk
+    float sl2e;            // scale * log2(e)
+    float scale;           // folded into dS
+    uint64_t timeout_ns;
+};
+
+enum : uint32_t {
+    SITE_BWD_LOAD_KV_EMPTY = 21,
+    SITE_BWD_LOAD_Q_EMPTY = 22,
+    SITE_BWD_MMA_KV_FULL = 23,
+    SITE_BWD_MMA_Q_FULL = 24,
+    SITE_BWD_MMA_P_FULL = 25,
+    SITE_BWD_MMA_DS_FULL = 26,
+    SITE_BWD_MMA_DQ_EMPTY = 27,
+    SITE_BWD_MMA_DKV_EMPTY = 28,
+    SITE_BWD_SM_S_FULL = 29,
+    SITE_BWD_SM_DP_FULL = 30,
+    SITE_BWD_DRAIN_DQ_FULL = 31,
+    SITE_BWD_DRAIN_DKV_FULL = 32,
+    SITE_BWD_SMEM_ALIGN = 33,
+};
+
+struct Cfg {
+    static constexpr int D = 128;
+    static constexpr int BN = 128;                  // keys per unit = TMEM lanes
+    static constexpr int BM = 128;                  // queries per tile
+    static constexpr int PANEL_BYTES = 128 * 128;   // 128 rows x 128 B (64 elements)
+    static constexpr int TILE_BYTES = 2 * PANEL_BYTES;  // [128 rows][128 elements] of 16 bits
+    static constexpr int NSTAGE = 2;
+    // shared memory (offsets from a 1024-byte aligned base)
+    static constexpr int CTL_OFF = 0;               // barriers, TMEM address, abort flag
+    static constexpr int LD_OFF = 1024;             // per stage: lse2[128], dsum[128]
+    static constexpr int LD_STAGE_BYTES = 1024;
+    static constexpr int K_OFF = 3072;
+    static constexpr int V_OFF = K_OFF + TILE_BYTES;
+    static constexpr int Q_OFF = V_OFF + TILE_BYTES;  // stage s: Q at Q_OFF + s*2*TILE, dO after it
+    static constexpr int DS_OFF = Q_OFF + NSTAGE * 2 * TILE_BYTES;
+    static constexpr int SMEM_BYTES = DS_OFF + TILE_BYTES;
+    // tensor memory columns
+    static constexpr int TM_DV = 0, TM_DK = 128, TM_S = 256, TM_DP = 384;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int THREADS = 512;
+    // setmaxnreg budgets: 2 x 128 softmax threads, 128 drain threads, 128
+    // others; (168 + 168 + 96 + 80) * 128 = 512 * 128 registers at launch.
+    static constexpr int REGS_SOFTMAX = 168, REGS_DRAIN = 96, REGS_OTHER = 80;
+    static_assert(LD_OFF + NSTAGE * LD_STAGE_BYTES <= K_OFF, "control / LSE area");
+    static_assert(K_OFF % 1024 == 0 && Q_OFF % 1024 == 0 && DS_OFF % 1024 == 0, "swizzle atoms need 1 KiB alignment");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(REGS_SOFTMAX * 2 + REGS_DRAIN + REGS_OTHER == 4 * 128, "register split");
+};
+
+struct Ctl {
+    uint64_t kv_full, kv_empty;
+    uint64_t q_full[2], q_empty[2];
+    uint64_t s_full, dp_full, p_full, ds_full;
+    uint64_t dq_full, dq_empty;
+    uint64_t dkv_full, dkv_empty;
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    uint32_t abort;
+};
+static_assert(sizeof(Ctl) <= 1024, "control block");
+
+// ---------------------------------------------------------------- PTX used only here
+
+// 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
+// Both addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the
+// async proxy (the tensor cores reading an operand).
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// 16 columns of 32-bit from this thread's lane.
+__device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Instruction descriptor, kind::f16, fp32 accumulate, with the major-ness
+// of both operands (bit 15: A MN-major, bit 16: B MN-major).
+__host__ __device__ constexpr uint32_t idesc(int M, int N, bool bf16, bool a_mn, bool b_mn)
+{
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn ? 1u : 0u) << 15) |
+           ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- waits
+
+// Forced inline: the callers run under different setmaxnreg budgets.
+__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl *ctl, const BwdParams &p, uint32_t site)
+{
+    volatile uint32_t *abort_flag = &ctl->abort;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > p.timeout_ns) {
+            *abort_flag = 1u;
+            if (atomicCAS(&p.status[0], 0u, 1u) == 0u) {
+                p.status[1] = blockIdx.x;
+                p.status[2] = threadIdx.x >> 5;
+                p.status[3] = site;
+                __threadfence();
+            }
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, Ctl *ctl, const BwdParams &p, uint32_t site)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, ctl, p, site);
+}
+
+// bar_wait by every lane of a warp, with a warp-uniform result.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Ctl *ctl, const BwdParams &p, uint32_t site)
+{
+    const bool w = bar_wait(bar, parity, ctl, p, site);
+    return __all_sync(0xffffffffu, w);
+}
+
+// Bounded wait that ignores the abort flag (lets this thread's own copies
+// and MMAs land before the CTA frees its resources).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
+{
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - t0 > timeout_ns) break;
+}
+
+// ---------------------------------------------------------------- schedule
+
+struct Unit {
+    int bh;   // head plane
+    int kb;   // key block (keys 128*kb ..)
+    int t0;   // first query tile that sees a key of the block
+    int n;    // number of query tiles
+};
+
+// Causal: units ordered by key block (block 0 sees every query tile: the
+// heaviest first), heads fastest.  Non-causal: all units are equal; the
+// blocks of one head are consecutive so that CTAs running together share
+// that head's Q and dO in L2.  Key j sees query i iff j <= i + (sk - sq)
+// (bottom-right alignment, as in the forward).
+template <bool CAUSAL>
+__device__ __forceinline__ Unit decode_unit(int u, const BwdParams &p)
+{
+    Unit un;
+    if (CAUSAL) {
+        un.kb = u / p.bh;
+        un.bh = u % p.bh;
+    } else {
+        un.bh = u / p.num_kblk;
+        un.kb = u % p.num_kblk;
+    }
+    const int n_tiles = (p.sq + Cfg::BM - 1) / Cfg::BM;
+    int t0 = 0;
+    if (CAUSAL) {
+        const int first_q = un.kb * Cfg::BN - (p.sk - p.sq);  // smallest query that sees key 128*kb
+        t0 = first_q > 0 ? first_q / Cfg::BM : 0;
+    }
+    un.t0 = min(t0, n_tiles);
+    un.n = n_tiles - un.t0;
+    return un;
+}
+
+// The i-th work unit of this CTA: rounds of gridDim.x units dealt out in
+// alternating directions (see the forward's scheduler).
+__device__ __forceinline__ int unit_at(int i)
+{
+    const int g = static_cast<int>(gridDim.x);
+    const int c = (i & 1) ? (g - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+    return i * g + c;
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi)
+{
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+template <typename T>
+__device__ __forceinline__ float2 unpack2(uint32_t u);
+
+template <>
+__device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t u)
+{
+    return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&u));
+}
+
+template <>
+__device__ __forceinline__ float2 unpack2<__half>(uint32_t u)
+{
+    return __half22float2(*reinterpret_cast<__half2 *>(&u));
+}
+
+// ---------------------------------------------------------------- prep
+
+// One query row per 16 threads: D = sum_c dO[c] O[c] (fp32), the row's
+// LSE in base 2, and a zeroed accumulator row.  Rows sq..sq_pad-1 get the
+// padding values (LSE2 = +inf, so that P = 0 there, and D = 0).
+template <typename T>
+__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p)
+{
+    constexpr int D = Cfg::D;
+    // rows is even (sq_pad is a multiple of 128) and the two rows of a warp
+    // are 2k and 2k+1, so both halves of a warp run the same iterations and
+    // the 16-wide shuffles below always have their whole warp.
+    const int64_t rows = static_cast<int64_t>(p.bh) * p.sq_pad;
+    const int sub = threadIdx.x & 15;
+    for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4; r < rows;
+         r += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 4) {
+        const int64_t head = r / p.sq_pad;
+        const int i = static_cast<int>(r - head * p.sq_pad);
+        float acc = 0.f;
+        if (i < p.sq) {
+            const int64_t off = (head * p.sq + i) * D + sub * 8;
+            const uint4 a = *reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.o) + off);
+            const uint4 b = *reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.dout) + off);
+            const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float2 x = unpack2<T>(av[c]), y = unpack2<T>(bv[c]);
+                acc = fmaf(x.x, y.x, acc);
+                acc = fmaf(x.y, y.y, acc);
+            }
+            float4 *z = reinterpret_cast<float4 *>(p.dq_acc + off);
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, 16);
+        if (sub == 0) {
+            float l2 = INFINITY;
+            if (i < p.sq) {
+                const float l = p.lse[head * p.sq + i];
+                l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+            }
+            p.lse2[r] = l2;
+            p.dsum[r] = (i < p.sq) ? acc : 0.f;
+        }
+    }
+}
+
+// dQ = accumulator (fp32, scale already applied) rounded to T, 8 elements
+// per thread and step.
+template <typename T>
+__global__ void __launch_bounds__(256) attn_bwd_dq_convert_kernel(const float *acc, T *dq, int64_t n8)
+{
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const float4 a = reinterpret_cast<const float4 *>(acc)[2 * i];
+        const float4 b = reinterpret_cast<const float4 *>(acc)[2 * i + 1];
+        reinterpret_cast<uint4 *>(dq)[i] =
+            make_uint4(pack2<T>(a.x, a.y), pack2<T>(a.z, a.w), pack2<T>(b.x, b.y), pack2<T>(b.z, b.w));
+    }
+}
+
+// ---------------------------------------------------------------- main kernel
+
+template <typename T, bool CAUSAL>
+__global__ void __launch_bounds__(512, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                    const BwdParams p)
+{
+    using C = Cfg;
+    constexpr bool BF16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t IDESC_S = idesc(128, C::BM, BF16, false, false);   // S^T, dP^T: [keys x queries]
+    constexpr uint32_t IDESC_ACC = idesc(128, C::D, BF16, false, true);   // dV, dK: A from TMEM, B MN-major
+    constexpr uint32_t IDESC_DQ = idesc(C::D, C::BM, BF16, true, true);   // dQ^T: both MN-major
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t base_addr = smem_addr(smem_raw);
+    // The whole budget is used, with no room to realign: the dynamic shared
+    // window starts 1 KiB aligned.  Should it not, report and do nothing.
+    if ((base_addr & 1023u) != 0u) {
+        if (threadIdx.x == 0 && atomicCAS(&p.status[0], 0u, 2u) == 0u) {
+            p.status[1] = blockIdx.x;
+            p.status[2] = 0u;
+            p.status[3] = SITE_BWD_SMEM_ALIGN;
+        }
+        return;
+    }
+    Ctl *ctl = reinterpret_cast<Ctl *>(smem_raw + C::CTL_OFF);
+    const uint32_t sLD = base_addr + C::LD_OFF;
+    const uint32_t sK = base_addr + C::K_OFF;
+    const uint32_t sV = base_addr + C::V_OFF;
+    const uint32_t sQ = base_addr + C::Q_OFF;  // stage s: Q at sQ + s*2*TILE, dO at + TILE
+    const uint32_t sDS = base_addr + C::DS_OFF;
+    const float *ld_smem = reinterpret_cast<const float *>(smem_raw + C::LD_OFF);
+
+    auto B = [&](const uint64_t &bar) { return smem_addr(&bar); };
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(B(ctl->kv_full), 1);
+        mbar_init(B(ctl->kv_empty), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(B(ctl->q_full[s]), 1);
+            mbar_init(B(ctl->q_empty[s]), 1);
+        }
+        mbar_init(B(ctl->s_full), 1);
+        mbar_init(B(ctl->dp_full), 1);
+        mbar_init(B(ctl->p_full), 8);   // one arrive per softmax warp
+        mbar_init(B(ctl->ds_full), 8);
+        mbar_init(B(ctl->dq_full), 1);
+        mbar_init(B(ctl->dq_empty), 4);  // one arrive per drain warp
+        mbar_init(B(ctl->dkv_full), 1);
+        mbar_init(B(ctl->dkv_empty), 4);
+        mbar_init(B(ctl->mma_done), 1);
+        ctl->abort = 0u;
+        fence_barrier_init();
+    }
+    if (warp == 12) {
+        tmem_alloc(smem_addr(&ctl->tmem_base), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 13 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmdO);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    const int n_rounds_end = p.num_units;
+
+    if (warp >= 12) {
+        regs_dec<C::REGS_OTHER>();
+        if (warp == 13) {
+            // ------------------------------------------------------------ producer
+            const uint64_t pol = l2_evict_normal();
+            uint32_t un_it = 0, q_it = 0;
+            bool ok = true;
+            for (int i = 0; i * static_cast<int>(gridDim.x) < n_rounds_end && ok; ++i) {
+                const int u = unit_at(i);
+                if (u >= p.num_units) continue;
+                const Unit un = decode_unit<CAUSAL>(u, p);
+                if (un.n == 0) continue;
+                ok = warp_wait(B(ctl->kv_empty), (un_it & 1u) ^ 1u, ctl, p, SITE_BWD_LOAD_KV_EMPTY);
+                if (!ok) break;
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(B(ctl->kv_full), 2 * C::TILE_BYTES);
+                    for (int pn = 0; pn < 2; ++pn) {
+                        tma_load_3d(sK + pn * C::PANEL_BYTES, &tmK, B(ctl->kv_full), pn * 64, un.kb * C::BN, un.bh, pol);
+                        tma_load_3d(sV + pn * C::PANEL_BYTES, &tmV, B(ctl->kv_full), pn * 64, un.kb * C::BN, un.bh, pol);
+                    }
+                }
+                __syncwarp();
+                ++un_it;
+                for (int t = 0; t < un.n && ok; ++t) {
+                    const uint32_t st = q_it & 1u;
+                    ok = warp_wait(B(ctl->q_empty[st]), ((q_it >> 1) & 1u) ^ 1u, ctl, p, SITE_BWD_LOAD_Q_EMPTY);
+                    if (!ok) break;
+                    const int q0 = (un.t0 + t) * C::BM;
+                    if (elect_one()) {
+                        const uint32_t bar = B(ctl->q_full[st]);
+                        mbar_arrive_expect_tx(bar, 2 * C::TILE_BYTES + 2 * C::BM * 4);
+                        const uint32_t dq_tile = sQ + st * 2 * C::TILE_BYTES;
+                        for (int pn = 0; pn < 2; ++pn) {
+                            tma_load_3d(dq_tile + pn * C::PANEL_BYTES, &tmQ, bar, pn * 64, q0, un.bh, pol);
+                            tma_load_3d(dq_tile + C::TILE_BYTES + pn * C::PANEL_BYTES, &tmdO, bar, pn * 64, q0, un.bh,
+                                        pol);
+                        }
+                        const size_t row = static_cast<size_t>(un.bh) * p.sq_pad + q0;
+                        bulk_load(sLD + st * C::LD_STAGE_BYTES, p.lse2 + row, C::BM * 4, bar);
+                        bulk_load(sLD + st * C::LD_STAGE_BYTES + C::BM * 4, p.dsum + row, C::BM * 4, bar);
+                    }
+                    __syncwarp();
+                    ++q_it;
+                }
+            }
+            // Wind-down: let the last copies land before the CTA exits.
+            if (un_it > 0) drain_wait(B(ctl->kv_full), (un_it - 1) & 1u, p.timeout_ns);
+            for (uint32_t k = (q_it > 2 ? q_it - 2 : 0u); k < q_it; ++k)
+                drain_wait(B(ctl->q_full[k & 1u]), (k >> 1) & 1u, p.timeout_ns);
+            __syncwarp();
+        } else if (warp == 12) {
+            // ------------------------------------------------------------ MMA issuer
+            uint32_t un_it = 0, q_it = 0, tile_it = 0;  // tile_it: tiles issued so far (all units)
+            bool ok = true;
+            const uint32_t dK0 = desc_lo(sK, 16);              // K, K-major (A of S^T)
+            const uint32_t dV0 = desc_lo(sV, 16);              // V, K-major (A of dP^T)
+            const uint32_t dKt0 = desc_lo(sK, C::PANEL_BYTES); // K^T, MN-major (A of dQ^T)
+            const uint32_t dDS0 = desc_lo(sDS, C::PANEL_BYTES);// dS^T, MN-major (B of dQ^T)
+            auto kmajor_step = [](int kk) { return static_cast<uint32_t>(((kk >> 2) * C::PANEL_BYTES + (kk & 3) * 32) >> 4); };
+            // [keys x queries] = A(K or V) . B(Q or dO)^T over the head dim
+            auto issue_kq = [&](uint32_t a0, uint32_t b0, uint32_t d) {
+#pragma unroll
+                for (int kk = 0; kk < C::D / 16; ++kk)
+                    mma_ss(d, a0 + kmajor_step(kk), b0 + kmajor_step(kk), IDESC_S, kk > 0 ? 1u : 0u);
+            };
+            // acc += A(TMEM, [keys x queries] 16-bit) . B([queries x D], MN-major) over the tile's queries
+            auto issue_acc = [&](uint32_t d, uint32_t a_tm, uint32_t b0, bool accumulate) {
+#pragma unroll
+                for (int s = 0; s < C::BM / 16; ++s)
+                    mma_ts(d, a_tm + 64 * (s >> 2) + 8 * (s & 3), b0 + ((s * 16 * 128) >> 4), IDESC_ACC,
+                           (accumulate || s > 0) ? 1u : 0u);
+            };
+            // dQ^T [D x queries] = K^T . dS^T over the unit's keys
+            auto issue_dq = [&](uint32_t d) {
+#pragma unroll
+                for (int s = 0; s < C::BN / 16; ++s)
+                    mma_ss(d, dKt0 + ((s * 16 * 128) >> 4), dDS0 + ((s * 16 * 128) >> 4), IDESC_DQ, s > 0 ? 1u : 0u);
+            };
+            auto q_desc = [&](uint32_t st, bool dout, uint32_t lbo) {
+                return desc_lo(sQ + st * 2 * C::TILE_BYTES + (dout ? C::TILE_BYTES : 0), lbo);
+            };
+            uint32_t dq_pending = 0u;  // 1 when a dQ^T in TMEM has not been drained yet
+            for (int i = 0; i * static_cast<int>(gridDim.x) < n_rounds_end && ok; ++i) {
+                const int u = unit_at(i);
+                if (u >= p.num_units) continue;
+                const Unit un = decode_unit<CAUSAL>(u, p);
+                if (un.n == 0) continue;
+                if (!(ok = warp_wait(B(ctl->kv_full), un_it & 1u, ctl, p, SITE_BWD_MMA_KV_FULL))) break;
+                if (!(ok = warp_wait(B(ctl->q_full[q_it & 1u]), (q_it >> 1) & 1u, ctl, p, SITE_BWD_MMA_Q_FULL))) break;
+                tc_fence_after();
+                if (elect_one()) {
+                    issue_kq(dK0, q_desc(q_it & 1u, false, 16), tmem + C::TM_S);
+                    tc_commit(B(ctl->s_full));
+                }
+                __syncwarp();
+                if (dq_pending) {  // the previous unit's last dQ^T still occupies the dP^T columns
+                    if (!(ok = warp_wait(B(ctl->dq_empty), (tile_it - 1) & 1u, ctl, p, SITE_BWD_MMA_DQ_EMPTY))) break;
+                    dq_pending = 0u;
+                }
+                tc_fence_after();
+                if (elect_one()) {
+                    issue_kq(dV0, q_desc(q_it & 1u, true, 16), tmem + C::TM_DP);
+                    tc_commit(B(ctl->dp_full));
+                }
+                __syncwarp();
+                for (int t = 0; t < un.n && ok; ++t) {
+                    const uint32_t st = q_it & 1u;
+                    // dV += P^T dO
+                    if (!(ok = warp_wait(B(ctl->p_full), tile_it & 1u, ctl, p, SITE_BWD_MMA_P_FULL))) break;
+                    if (t == 0 && un_it > 0 &&
+                        !(ok = warp_wait(B(ctl->dkv_empty), (un_it - 1) & 1u, ctl, p, SITE_BWD_MMA_DKV_EMPTY)))
+                        break;
+                    tc_fence_after();
+                    if (elect_one()) issue_acc(tmem + C::TM_DV, tmem + C::TM_S, q_desc(st, true, C::PANEL_BYTES), t > 0);
+                    __syncwarp();
+                    // S^T of the next tile (its P^T columns were just consumed, in order)
+                    const bool more = t + 1 < un.n;
+                    if (more) {
+                        if (!(ok = warp_wait(B(ctl->q_full[(q_it + 1) & 1u]), ((q_it + 1) >> 1) & 1u, ctl, p,
+                                             SITE_BWD_MMA_Q_FULL)))
+                            break;
+                        tc_fence_after();
+                        if (elect_one()) {
+                            issue_kq(dK0, q_desc((q_it + 1) & 1u, false, 16), tmem + C::TM_S);
+                            tc_commit(B(ctl->s_full));
+                        }
+                        __syncwarp();
+                    }
+                    // dK += dS^T Q, then dQ^T = K^T dS^T into the dP^T columns
+                    if (!(ok = warp_wait(B(ctl->ds_full), tile_it & 1u, ctl, p, SITE_BWD_MMA_DS_FULL))) break;
+                    tc_fence_after();
+                    if (elect_one()) {
+                        issue_acc(tmem + C::TM_DK, tmem + C::TM_DP, q_desc(st, false, C::PANEL_BYTES), t > 0);
+                        issue_dq(tmem + C::TM_DP);
+                        tc_commit(B(ctl->dq_full));
+                        tc_commit(B(ctl->q_empty[st]));
+                        if (!more) {
+                            tc_commit(B(ctl->kv_empty));
+                            tc_commit(B(ctl->dkv_full));
+                        }
+                    }
+                    __syncwarp();
+                    dq_pending = 1u;
+                    ++tile_it;
+                    ++q_it;
+                    // dP^T of the next tile, once dQ^T has been drained
+                    if (more) {
+                        if (!(ok = warp_wait(B(ctl->dq_empty), (tile_it - 1) & 1u, ctl, p, SITE_BWD_MMA_DQ_EMPTY)))
+                            break;
+                        dq_pending = 0u;
+                        tc_fence_after();
+                        if (elect_one()) {
+                            issue_kq(dV0, q_desc(q_it & 1u, true, 16), tmem + C::TM_DP);
+                            tc_commit(B(ctl->dp_full));
+                        }
+                        __syncwarp();
+                    }
+                }
+                ++un_it;
+            }
+            // Every MMA issued must complete before tensor memory is freed.
+            if (elect_one()) tc_commit(B(ctl->mma_done));
+            __syncwarp();
+            drain_wait(B(ctl->mma_done), 0u, p.timeout_ns);
+            __syncwarp();
+        }
+    } else if (warp >= 8) {
+        regs_dec<C::REGS_DRAIN>();
+        // ---------------------------------------------------------------- dQ drain + dK/dV epilogue
+        const int quad = warp & 3;
+        const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+        const int dcol = quad * 32 + lane;  // head-dim column of dQ^T this thread drains
+        uint32_t tile_it = 0, un_it = 0;
+        bool ok = true;
+        for (int i = 0; i * static_cast<int>(gridDim.x) < n_rounds_end && ok; ++i) {
+            const int u = unit_at(i);
+            if (u >= p.num_units) continue;
+            const Unit un = decode_unit<CAUSAL>(u, p);
+            if (un.n == 0) continue;
+            for (int t = 0; t < un.n && ok; ++t) {
+                if (!(ok = warp_wait(B(ctl->dq_full), tile_it & 1u, ctl, p, SITE_BWD_DRAIN_DQ_FULL))) break;
+                ++tile_it;
+                tc_fence_after();
+                const int q0 = (un.t0 + t) * C::BM;
+                float *dst = p.dq_acc + (static_cast<size_t>(un.bh) * p.sq + q0) * C::D + dcol;
+                const int nq = min(C::BM, p.sq - q0);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t v[64];
+                    tmem_ld32_wait(tmem + lane_off + C::TM_DP + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(v));
+                    tmem_ld32_wait(tmem + lane_off + C::TM_DP + 64 * h + 32,
+                                   *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+                    if (h == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(B(ctl->dq_empty));
+                    }
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (64 * h + c < nq) atomicAdd(dst + static_cast<size_t>(64 * h + c) * C::D, __uint_as_float(v[c]));
+                }
+            }
+            if (!ok) break;
+            // dK, dV of the unit: this thread's key row, D columns each
+            if (!(ok = warp_wait(B(ctl->dkv_full), un_it & 1u, ctl, p, SITE_BWD_DRAIN_DKV_FULL))) break;
+            ++un_it;
+            tc_fence_after();
+            const int key = un.kb * C::BN + quad * 32 + lane;
+            const bool valid = key < p.sk;
+            const size_t roff = (static_cast<size_t>(un.bh) * p.sk + (valid ? key : 0)) * C::D;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                uint4 *out = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(which ? p.dk : p.dv) + roff);
+                const uint32_t src = tmem + lane_off + (which ? C::TM_DK : C::TM_DV);
+#pragma unroll
+                for (int ch = 0; ch < C::D / 32; ++ch) {
+                    uint32_t v[32];
+                    tmem_ld32_wait(src + 32 * ch, v);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) pk[c] = pack2<T>(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]));
+                    if (valid) {
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            out[ch * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B(ctl->dkv_empty));
+        }
+    } else {
+        regs_inc<C::REGS_SOFTMAX>();
+        // ---------------------------------------------------------------- softmax groups
+        const int g = warp >> 2;     // query half of the tile: columns 64g .. 64g+63
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;  // key row within the unit's block
+        const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tS = tmem + lane_off + C::TM_S + 64 * g;
+        const uint32_t tDP = tmem + lane_off + C::TM_DP + 64 * g;
+        const float sl2e = p.sl2e, scale = p.scale;
+        uint32_t tile_it = 0, q_it = 0;
+        bool ok = true;
+        for (int i = 0; i * static_cast<int>(gridDim.x) < n_rounds_end && ok; ++i) {
+            const int u = unit_at(i);
+            if (u >= p.num_units) continue;
+            const Unit un = decode_unit<CAUSAL>(u, p);
+            if (un.n == 0) continue;
+            const int key = un.kb * C::BN + r;
+            const bool row_ok = key < p.sk;
+            for (int t = 0; t < un.n && ok; ++t) {
+                const uint32_t st = q_it & 1u;
+                // the tile's LSE / D vectors arrive with Q and dO
+                if (!(ok = warp_wait(B(ctl->q_full[st]), (q_it >> 1) & 1u, ctl, p, SITE_BWD_SM_S_FULL))) break;
+                if (!(ok = warp_wait(B(ctl->s_full), tile_it & 1u, ctl, p, SITE_BWD_SM_S_FULL))) break;
+                tc_fence_after();
+                const int q0 = (un.t0 + t) * C::BM + 64 * g;  // first query of this thread's columns
+                // columns c < lim are masked for this key row (key j sees query i iff i >= j - (sk - sq))
+                int lim = CAUSAL ? key - (p.sk - p.sq) - q0 : 0;
+                if (!row_ok) lim = 64;
+                const bool masked = __any_sync(0xffffffffu, lim > 0);
+                const float *l2 = ld_smem + st * (C::LD_STAGE_BYTES / 4) + 64 * g;
+                const float *dsv = l2 + C::BM;
+                float pr[64];
+#pragma unroll
+                for (int ch = 0; ch < 2; ++ch) {
+                    uint32_t sr[32];
+                    tmem_ld32_wait(tS + 32 * ch, sr);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                        const float4 lv = *reinterpret_cast<const float4 *>(l2 + 32 * ch + c);
+                        const float lvv[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float x = ex2_approx(fmaf(__uint_as_float(sr[c + e]), sl2e, -lvv[e]));
+                            if (masked && (32 * ch + c + e) < lim) x = 0.f;
+                            pr[32 * ch + c + e] = x;
+                        }
+                    }
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) pk[c] = pack2<T>(pr[32 * ch + 2 * c], pr[32 * ch + 2 * c + 1]);
+                    tmem_st16(tS + 16 * ch, pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(B(ctl->p_full));
+                // dS^T = scale * P^T (dP^T - D)
+                if (!(ok = warp_wait(B(ctl->dp_full), tile_it & 1u, ctl, p, SITE_BWD_SM_DP_FULL))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ch = 0; ch < 2; ++ch) {
+                    uint32_t dr[32];
+                    tmem_ld32_wait(tDP + 32 * ch, dr);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                        const float4 dv4 = *reinterpret_cast<const float4 *>(dsv + 32 * ch + c);
+                        const float dvv[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
+                        float ds[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            ds[e] = scale * pr[32 * ch + c + e] * (__uint_as_float(dr[c + e]) - dvv[e]);
+                        pk[c / 2] = pack2<T>(ds[0], ds[1]);
+                        pk[c / 2 + 1] = pack2<T>(ds[2], ds[3]);
+                    }
+                    tmem_st16(tDP + 16 * ch, pk);
+                    // shared copy for dQ^T: MN-major B, panel g (queries 64g..), row r,
+                    // 16-byte chunks 4*ch .. 4*ch+3 of the row, 128-byte swizzle
+#pragma unroll
+                    for (int k8 = 0; k8 < 4; ++k8) {
+                        const uint32_t chunk = static_cast<uint32_t>((4 * ch + k8) ^ (r & 7));
+                        st_shared_v4(sDS + g * C::PANEL_BYTES + r * 128 + chunk * 16, pk[4 * k8], pk[4 * k8 + 1],
+                                     pk[4 * k8 + 2], pk[4 * k8 + 3]);
+                    }
+                }
+                tmem_wait_st();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(B(ctl->ds_full));
+                ++tile_it;
+                ++q_it;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 12) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+}  // namespace bwd
+}  // namespace attn

@@ -1,6 +1,7 @@
-// C ABI of the fused attention forward (declared in include/attn_fwd.h):
-// argument validation, TMA tensor maps, persistent grid sizing, dispatch to
-// the <head_dim, dtype, causal> instances, device watchdog status.
+// C ABI of the fused attention forward and backward (declared in
+// include/attn_fwd.h): argument validation, TMA tensor maps, persistent grid
+// sizing, dispatch to the <head_dim, dtype, causal> instances, device
+// watchdog status.
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -12,6 +13,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include "attn_bwd_launch.h"
 #include "attn_fwd.h"
 #include "launch.h"
 
@@ -252,6 +254,94 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_
 }
 
 constexpr uint64_t kDefaultTimeoutNs = 2000ull * 1000ull * 1000ull;  // 2 s per wait
+
+// ---------------------------------------------------------------- backward
+
+int64_t bwd_sq_pad(int64_t sq) { return (sq + 127) / 128 * 128; }
+
+int64_t bwd_workspace_bytes(int64_t bh, int64_t sq, int64_t d)
+{
+    return bh * sq * d * 4 + 2 * bh * bwd_sq_pad(sq) * 4;
+}
+
+int run_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse, void *dq,
+            void *dk, void *dv, int64_t b, int64_t h, int64_t sq, int64_t sk, int64_t d, int causal, float scale,
+            int dtype, void *workspace, int64_t workspace_bytes, cudaStream_t stream)
+{
+    if (b < 0 || h < 0 || sq < 0 || sk < 0)
+        return fail(ATTN_ERR_SHAPE, "negative size: b=%lld h=%lld sq=%lld sk=%lld", (long long)b, (long long)h,
+                    (long long)sq, (long long)sk);
+    if (sq > kMaxSeq || sk > kMaxSeq)
+        return fail(ATTN_ERR_SHAPE, "sequence length above 2^30: sq=%lld sk=%lld", (long long)sq, (long long)sk);
+    if (b > 0 && h >= (int64_t(1) << 31) / b)
+        return fail(ATTN_ERR_SHAPE, "b*h not below 2^31: b=%lld h=%lld", (long long)b, (long long)h);
+    if (d != 128) return fail(ATTN_ERR_HEADDIM, "backward: head dim %lld not supported (128)", (long long)d);
+    if (dtype != ATTN_FP16 && dtype != ATTN_BF16) return fail(ATTN_ERR_DTYPE, "dtype %d is not fp16 (0) or bf16 (1)", dtype);
+    if (!std::isfinite(scale)) return fail(ATTN_ERR_SCALE, "scale is not finite");
+    const int64_t bh = b * h;
+    if (bh == 0) return ATTN_OK;
+    if (bh * ((sq + 127) / 128) * ((sk + 127) / 128) > INT32_MAX)
+        return fail(ATTN_ERR_SHAPE, "too many work units");
+    const bool rows = sq > 0, keys = sk > 0;
+    if ((rows && !dq) || (keys && (!dk || !dv))) return fail(ATTN_ERR_NULL, "dq, dk or dv is NULL");
+    if ((rows && !aligned(dq, 16)) || (keys && (!aligned(dk, 16) || !aligned(dv, 16))))
+        return fail(ATTN_ERR_ALIGN, "dq, dk and dv must be 16-byte aligned");
+    DeviceInfo *di = nullptr;
+    int rc = device_info(&di);
+    if (rc != ATTN_OK) return rc;
+    const size_t qbytes = static_cast<size_t>(bh * sq * d) * 2, kbytes = static_cast<size_t>(bh * sk * d) * 2;
+    cudaError_t e;
+    if (!rows || !keys) {  // no queries: dK = dV = 0; no keys: dQ = 0
+        if (rows && (e = cudaMemsetAsync(dq, 0, qbytes, stream)) != cudaSuccess) return cuda_fail(e, "zero dq");
+        if (keys && (e = cudaMemsetAsync(dk, 0, kbytes, stream)) != cudaSuccess) return cuda_fail(e, "zero dk");
+        if (keys && (e = cudaMemsetAsync(dv, 0, kbytes, stream)) != cudaSuccess) return cuda_fail(e, "zero dv");
+        return ATTN_OK;
+    }
+    if (!q || !k || !v || !o || !dout || !lse) return fail(ATTN_ERR_NULL, "q, k, v, o, dout or lse is NULL");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16))
+        return fail(ATTN_ERR_ALIGN, "q, k, v, o and dout must be 16-byte aligned");
+    if (!aligned(lse, 4)) return fail(ATTN_ERR_ALIGN, "lse must be 4-byte aligned");
+    const int64_t need = bwd_workspace_bytes(bh, sq, d);
+    if (!workspace) return fail(ATTN_ERR_NULL, "workspace is NULL");
+    if (!aligned(workspace, 16)) return fail(ATTN_ERR_ALIGN, "workspace must be 16-byte aligned");
+    if (workspace_bytes < need)
+        return fail(ATTN_ERR_SHAPE, "workspace too small: %lld bytes, need %lld", (long long)workspace_bytes,
+                    (long long)need);
+    bwd::BwdLaunchArgs a;
+    if ((rc = make_map(&a.q, q, dtype, bh, sq, d)) != ATTN_OK) return rc;
+    if ((rc = make_map(&a.dout, dout, dtype, bh, sq, d)) != ATTN_OK) return rc;
+    if ((rc = make_map(&a.k, k, dtype, bh, sk, d)) != ATTN_OK) return rc;
+    if ((rc = make_map(&a.v, v, dtype, bh, sk, d)) != ATTN_OK) return rc;
+    bwd::BwdParams &p = a.p;
+    const int64_t sq_pad = bwd_sq_pad(sq);
+    p.o = o;
+    p.dout = dout;
+    p.lse = lse;
+    p.dq_acc = static_cast<float *>(workspace);
+    p.lse2 = p.dq_acc + bh * sq * d;
+    p.dsum = p.lse2 + bh * sq_pad;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.status = di->status;
+    p.bh = static_cast<int32_t>(bh);
+    p.sq = static_cast<int32_t>(sq);
+    p.sk = static_cast<int32_t>(sk);
+    p.sq_pad = static_cast<int32_t>(sq_pad);
+    p.num_kblk = static_cast<int32_t>((sk + 127) / 128);
+    p.num_units = static_cast<int32_t>(bh * p.num_kblk);
+    p.sl2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    p.scale = scale;
+    p.timeout_ns = kDefaultTimeoutNs;
+    a.grid = p.num_units < di->sm_count ? p.num_units : di->sm_count;
+    a.sm_count = di->sm_count;
+    a.stream = stream;
+    if (dtype == ATTN_BF16)
+        e = causal ? bwd::launch_bwd<__nv_bfloat16, true>(a) : bwd::launch_bwd<__nv_bfloat16, false>(a);
+    else
+        e = causal ? bwd::launch_bwd<__half, true>(a) : bwd::launch_bwd<__half, false>(a);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "backward launch");
+}
 
 // Scratch of attn_fwd_splitkv_noalloc: a fixed device array that every GPU
 // loading this library holds until the process exits.  In host code the name
@@ -575,6 +665,24 @@ int attn_fwd_watchdog_selftest(const void *q, const void *k, const void *v, void
              static_cast<uint64_t>(timeout_ms) * 1000000ull);
     if (rc != ATTN_OK) return rc;
     return attn_fwd_status(nullptr);
+}
+
+int attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse, void *dq,
+             void *dk, void *dv, int64_t b, int64_t h, int64_t sq, int64_t sk, int64_t d, int causal, float scale,
+             int dtype, void *workspace, int64_t workspace_bytes, void *stream)
+{
+    g_err.clear();
+    return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, b, h, sq, sk, d, causal, scale, dtype, workspace,
+                   workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int64_t attn_bwd_workspace_bytes(int64_t b, int64_t h, int64_t sq, int64_t d)
+{
+    g_err.clear();
+    if (b < 0 || h < 0 || sq < 0 || sq > kMaxSeq || (b > 0 && h >= (int64_t(1) << 31) / b))
+        return fail(ATTN_ERR_SHAPE, "invalid backward workspace query");
+    if (d != 128) return fail(ATTN_ERR_HEADDIM, "backward: head dim %lld not supported (128)", (long long)d);
+    return bwd_workspace_bytes(b * h, sq, d);
 }
 
 const char *attn_version(void) { return "attn_fwd sm_103a 0.1"; }

@@ -96,6 +96,14 @@ def draw(b, h, sq, sk, d, dtype, seed, qk_std=1.0, v_std=1.0):
     return q.to(tdt), k.to(tdt), v.to(tdt)
 
 
+def draw_grad(b, h, sq, d, dtype, seed):
+    """Seeded output gradient dO [b, h, sq, d] ~ N(0, 1) as a CPU tensor."""
+    tdt = DTYPES[dtype] if isinstance(dtype, str) else dtype
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return torch.randn((b, h, sq, d), generator=g, dtype=torch.float32).to(tdt)
+
+
 def inputs(w: Workload):
     """CPU tensors (q, k, v) of the workload."""
     return draw(w.b, w.h, w.sq, w.sk, w.d, w.dtype, w.seed, w.qk_std)
@@ -184,3 +192,36 @@ def varlen_lengths(n, lo, hi, seed):
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
     return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=g)]
+
+
+# Backward workloads: the forward's problem plus a seeded dO.  One step is
+# one attn_bwd call; its work is the five products of the gradient (S, dP,
+# dV, dK, dQ), 2.5x the forward's FLOPs.
+@dataclass(frozen=True)
+class BwdWorkload:
+    fwd: str        # the forward workload whose q, k, v are used
+    grad_seed: int
+
+    @property
+    def w(self) -> Workload:
+        return WORKLOADS[self.fwd]
+
+    @property
+    def name(self) -> str:
+        return "bwd_" + self.fwd
+
+    def flops(self) -> float:
+        return 2.5 * self.w.flops()
+
+    def bytes(self) -> int:
+        w = self.w
+        e = 2
+        # read q, k, v, o, dO, lse; write dq, dk, dv
+        return (e * w.b * w.h * (3 * w.sq * w.d + 2 * w.sk * w.d) + 4 * w.b * w.h * w.sq
+                + e * w.b * w.h * (w.sq * w.d + 2 * w.sk * w.d))
+
+
+BWD = {bw.name: bw for bw in [
+    BwdWorkload("causal_b1_h32_s16384_d128_bf16_qk3", 20260008),
+    BwdWorkload("causal_b2_h32_s4096_d128_bf16", 20260009),
+]}

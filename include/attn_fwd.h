@@ -212,6 +212,45 @@ int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v,
                              float scale, int dtype, int num_splits,
                              void *stream);
 
+/*
+ * Backward pass: the gradients of attn_fwd.  "05 · kernel 工程与四代演化" 6.1
+ * lists bwd among the exported entry points (and chapter 04 of that series
+ * as its implementation, which is not among the pages); the operation is the
+ * chain rule through attn_fwd's definition.  For the loss gradient dO:
+ *   P  = softmax(scale * Q K^T [+ causal])   recomputed from LSE:
+ *        P[i, j] = exp(scale * q_i . k_j - lse[i])
+ *   dV = P^T dO
+ *   dS = P * (dO V^T - D),  D[i] = sum_c dO[i, c] * O[i, c]
+ *   dQ = scale * dS K,      dK = scale * dS^T Q
+ * with the causal mask of attn_fwd (bottom-right aligned).
+ *
+ *   q, o, dout, dq : [b, h, sq, d] of dtype, contiguous, 16-byte aligned.
+ *   k, v, dk, dv   : [b, h, sk, d] of dtype, contiguous, 16-byte aligned.
+ *   lse            : fp32 [b, h, sq] as written by attn_fwd (natural log;
+ *                    -inf for a row that sees no key).
+ *   o, lse         : the forward's outputs for these q, k, v; D is computed
+ *                    from o (so an o rounded to dtype carries that rounding
+ *                    into D).
+ *   d              : 128 only (ATTN_ERR_HEADDIM otherwise).
+ *   workspace      : caller-owned device scratch, 16-byte aligned, of at
+ *                    least attn_bwd_workspace_bytes(b, h, sq, d) bytes (an
+ *                    fp32 dQ accumulator and two fp32 values per query
+ *                    row); its contents on entry do not matter.  Calls on
+ *                    different streams need different workspaces.
+ * Outputs dq, dk, dv are written in full (zeros where the gradient is zero,
+ * e.g. dq of rows that see no key, or everything when sq or sk is 0).
+ * Three kernels run on `stream`, asynchronously; the library allocates
+ * nothing.  Returns ATTN_OK or a negative ATTN_ERR_* code.
+ */
+int attn_bwd(const void *q, const void *k, const void *v, const void *o,
+             const void *dout, const float *lse, void *dq, void *dk, void *dv,
+             int64_t b, int64_t h, int64_t sq, int64_t sk, int64_t d,
+             int causal, float scale, int dtype, void *workspace,
+             int64_t workspace_bytes, void *stream);
+
+/* Bytes of workspace attn_bwd needs, or a negative ATTN_ERR_* code. */
+int64_t attn_bwd_workspace_bytes(int64_t b, int64_t h, int64_t sq, int64_t d);
+
 /* Thread-local message describing the last non-OK return on this thread
  * ("" if none).  The pointer stays valid until the next call on the thread. */
 const char *attn_last_error(void);

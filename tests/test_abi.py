@@ -102,3 +102,30 @@ def test_splitkv_workspace_size(lib):
 def test_splitkv_argument_errors(lib, splits, ws, ws_bytes, code):
     rc = lib.attn_fwd_splitkv(P, P, P, P, None, 1, 2, 3, 1000, 128, 0, 0.1, 1, splits, ws, ws_bytes, None)
     assert rc == code, (rc, lib.attn_last_error())
+
+
+def call_bwd(lib, b=1, h=1, sq=4, sk=4, d=128, causal=0, scale=0.1, dtype=1, ws=P, ws_bytes=1 << 20, ptr=P):
+    rc = lib.attn_bwd(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, b, h, sq, sk, d, causal, scale, dtype, ws, ws_bytes,
+                      None)
+    return rc, lib.attn_last_error().decode()
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    assert call_bwd(lib, d=64)[0] == -3
+    assert call_bwd(lib, dtype=7)[0] == -4
+    assert call_bwd(lib, b=-1)[0] == -2
+    assert call_bwd(lib, sq=(1 << 30) + 1)[0] == -2
+    assert call_bwd(lib, scale=math.nan)[0] == -5
+    assert call_bwd(lib, scale=math.inf)[0] == -5
+    assert call_bwd(lib, ptr=None)[0] == -1
+    assert call_bwd(lib, ptr=P + 4)[0] == -6
+    rc, msg = call_bwd(lib, b=0)
+    assert rc == 0, msg  # nothing to do
+
+
+def test_bwd_workspace_bytes(lib):
+    # fp32 dQ accumulator + two fp32 values per query row padded to 128 rows
+    assert lib.attn_bwd_workspace_bytes(2, 3, 300, 128) == 6 * 300 * 128 * 4 + 2 * 6 * 384 * 4
+    assert lib.attn_bwd_workspace_bytes(1, 1, 0, 128) == 0
+    assert lib.attn_bwd_workspace_bytes(1, 1, 4, 64) == -3
+    assert lib.attn_bwd_workspace_bytes(-1, 1, 4, 128) == -2

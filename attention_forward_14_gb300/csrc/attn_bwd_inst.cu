@@ -28,7 +28,7 @@ cudaError_t launch_bwd(const BwdLaunchArgs &a)
     if (prep_blocks > 8 * a.sm_count) prep_blocks = 8 * a.sm_count;
     attn_bwd_prep_kernel<T><<<prep_blocks, 256, 0, a.stream>>>(a.p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    attn_bwd_kernel<T, CAUSAL><<<a.grid, Cfg::THREADS, Cfg::SMEM_BYTES, a.stream>>>(a.q, a.k, a.v, a.dout, a.p);
+    attn_bwd_kernel<T, CAUSAL><<<a.grid, Cfg::THREADS, Cfg::SMEM_BYTES, a.stream>>>(a.q, a.k, a.v, a.dout, a.dq_acc, a.p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t n8 = static_cast<int64_t>(a.p.bh) * a.p.sq * Cfg::D / 8;
     int cv_blocks = static_cast<int>((n8 + 255) / 256);

@@ -25,8 +25,9 @@
 //                             dK  += dS^T Q          (dS^T read from TMEM)
 //                             dQ^T = K^T dS^T        (both from shared)
 //                           dV and dK accumulate in TMEM over the tiles of
-//                           the unit; each tile's dQ^T is added into the
-//                           fp32 accumulator with coalesced red.global.add;
+//                           the unit; each tile's dQ is staged in shared
+//                           memory and added into the fp32 accumulator by
+//                           the copy engine (a TMA reduce-add);
 //   attn_bwd_dq_convert_kernel  dQ = accumulator cast to the input type.
 //
 // CTA of 16 warps:
@@ -35,7 +36,7 @@
 //                     turns S^T into P^T (kept in fp32 registers, stored to
 //                     TMEM as 16-bit for the dV product) and dP^T into dS^T
 //                     (stored to TMEM for dK and to shared memory for dQ)
-//   warps 8-11        dQ drain (TMEM -> red.global.add) and the dK / dV
+//   warps 8-11        dQ drain (TMEM -> shared -> TMA reduce-add) and the dK / dV
 //                     epilogue of each unit
 //   warp 12           MMA issuer, tensor-memory owner
 //   warp 13           TMA producer
@@ -72,9 +73,42 @@ struct BwdParams {
     int32_t bh, sq, sk, sq_pad;
     int32_t num_kblk;      // ceil(sk / 128)
     int32_t num_units;     // bh * num_kblk
+    int32_t group;         // heads per scheduling group (see decode_unit)
+    int32_t *counter;      // next unit to hand out (zeroed by the prep kernel)
     float sl2e;            // scale * log2(e)
     float scale;           // folded into dS
     uint64_t timeout_ns;
+#ifdef ATTN_TRACE_ENABLE
+    unsigned long long *trace;  // per-warp event records (timeline builds only)
+#endif
+};
+
+// Pipeline timeline hooks, compiled out unless ATTN_TRACE_ENABLE is defined
+// (a separate diagnostic build recording {clock, event, arg} per warp).
+#ifdef ATTN_TRACE_ENABLE
+#define BWD_TRACE_DECL uint32_t bwd_trace_n = 0;
+#define BWD_TRACE(ev, arg) bwd_trace_record(p, bwd_trace_n, (ev), (arg))
+__device__ __forceinline__ void bwd_trace_record(const BwdParams &p, uint32_t &n, uint32_t ev, uint32_t arg)
+{
+    constexpr uint32_t kCtas = 4, kWarps = 16, kEvents = 16384;
+    if (p.trace == nullptr || blockIdx.x >= kCtas || (threadIdx.x & 31) != 0 || n >= kEvents) return;
+    const uint32_t w = threadIdx.x >> 5;
+    unsigned long long *rec = p.trace + 2ull * ((blockIdx.x * kWarps + w) * kEvents + n);
+    rec[0] = clock64();
+    rec[1] = (static_cast<unsigned long long>(ev) << 32) | arg;
+    ++n;
+}
+#else
+#define BWD_TRACE_DECL
+#define BWD_TRACE(ev, arg) ((void)0)
+#endif
+
+enum : uint32_t {
+    BEV_MMA_WAIT_P = 1, BEV_MMA_GOT_P, BEV_MMA_WAIT_DS, BEV_MMA_GOT_DS, BEV_MMA_WAIT_DQE, BEV_MMA_GOT_DQE,
+    BEV_MMA_WAIT_Q, BEV_MMA_GOT_Q, BEV_MMA_ISSUED_DV, BEV_MMA_ISSUED_S, BEV_MMA_ISSUED_DKDQ, BEV_MMA_ISSUED_DP,
+    BEV_SM_WAIT_S = 20, BEV_SM_GOT_S, BEV_SM_P_DONE, BEV_SM_WAIT_DP, BEV_SM_GOT_DP, BEV_SM_DS_DONE,
+    BEV_DR_WAIT = 40, BEV_DR_GOT, BEV_DR_RELEASED, BEV_DR_DONE,
+    BEV_LD_WAIT = 60, BEV_LD_GOT,
 };
 
 enum : uint32_t {
@@ -91,6 +125,11 @@ enum : uint32_t {
     SITE_BWD_DRAIN_DQ_FULL = 31,
     SITE_BWD_DRAIN_DKV_FULL = 32,
     SITE_BWD_SMEM_ALIGN = 33,
+    SITE_BWD_UNIT_FULL = 34,
+    SITE_BWD_UNIT_EMPTY = 35,
+    SITE_BWD_LOAD_DO_EMPTY = 36,
+    SITE_BWD_MMA_DO_FULL = 37,
+    SITE_BWD_DRAIN_SYNC = 38,
 };
 
 struct Cfg {
@@ -113,9 +152,10 @@ struct Cfg {
     static constexpr int TM_DV = 0, TM_DK = 128, TM_S = 256, TM_DP = 384;
     static constexpr int TMEM_COLS = 512;
     static constexpr int THREADS = 512;
-    // setmaxnreg budgets: 2 x 128 softmax threads, 128 drain threads, 128
-    // others; (168 + 168 + 96 + 80) * 128 = 512 * 128 registers at launch.
-    static constexpr int REGS_SOFTMAX = 168, REGS_DRAIN = 96, REGS_OTHER = 80;
+    // setmaxnreg budgets: 2 x 128 softmax threads, 128 drain threads (all
+    // 128 dQ^T columns of a row in registers), 128 others;
+    // (144 + 144 + 136 + 88) * 128 = 512 * 128 registers at launch.
+    static constexpr int REGS_SOFTMAX = 144, REGS_DRAIN = 136, REGS_OTHER = 88;
     static_assert(LD_OFF + NSTAGE * LD_STAGE_BYTES <= K_OFF, "control / LSE area");
     static_assert(K_OFF % 1024 == 0 && Q_OFF % 1024 == 0 && DS_OFF % 1024 == 0, "swizzle atoms need 1 KiB alignment");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -124,15 +164,21 @@ struct Cfg {
 
 struct Ctl {
     uint64_t kv_full, kv_empty;
-    uint64_t q_full[2], q_empty[2];
+    uint64_t q_full[2], q_empty[2];    // Q and the LSE / D vectors of a stage
+    uint64_t do_full[2], do_empty[2];  // dO of a stage (its slot also stages dQ)
     uint64_t s_full, dp_full, p_full, ds_full;
     uint64_t dq_full, dq_empty;
     uint64_t dkv_full, dkv_empty;
     uint64_t mma_done;
+    uint64_t dr_sync;                      // the four drain warps meet here
+    uint64_t unit_full[4], unit_empty[4];  // ring of claimed unit indices
+    int32_t unit_idx[4];
     uint32_t tmem_base;
     uint32_t abort;
 };
 static_assert(sizeof(Ctl) <= 1024, "control block");
+constexpr int kUnitRing = 4;
+constexpr int kUnitReaders = 13;  // MMA warp + 8 softmax warps + 4 drain warps
 
 // ---------------------------------------------------------------- PTX used only here
 
@@ -157,6 +203,29 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+// Tile reduce-add shared -> global through the copy engine (the adds are
+// done at L2), tracked as a bulk group of this thread.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap *map, uint32_t src, int32_t c0, int32_t c1, int32_t c2)
+{
+    asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// This thread's bulk groups have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// ... and have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 // 16 columns of 32-bit from this thread's lane.
 __device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&r)[16])
 {
@@ -168,6 +237,25 @@ __device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&r)[16]
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
+}
+
+// 64 columns of 32-bit from this thread's lane (two loads, one wait).
+__device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&r)[64])
+{
+#define BWD_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), \
+                  "=r"(r[i + 6]), "=r"(r[i + 7])
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : BWD_R8(0), BWD_R8(8), BWD_R8(16), BWD_R8(24), BWD_R8(32), BWD_R8(40), BWD_R8(48), BWD_R8(56)
+        : "r"(taddr), "r"(taddr + 32)
+        : "memory");
+#undef BWD_R8
 }
 
 // Instruction descriptor, kind::f16, fp32 accumulate, with the major-ness
@@ -233,22 +321,24 @@ struct Unit {
     int n;    // number of query tiles
 };
 
-// Causal: units ordered by key block (block 0 sees every query tile: the
-// heaviest first), heads fastest.  Non-causal: all units are equal; the
-// blocks of one head are consecutive so that CTAs running together share
-// that head's Q and dO in L2.  Key j sees query i iff j <= i + (sk - sq)
+// Units are handed out in order from a global counter (dynamic
+// scheduling).  The order is by groups of `group` heads; within a group, by
+// key block (block 0 sees every query tile when causal: the heaviest
+// first), then head.  A group's fp32 dQ accumulator, Q and dO are sized on
+// the host to stay in L2 while its units run, and the light blocks of the
+// last group fill the tail.  Key j sees query i iff j <= i + (sk - sq)
 // (bottom-right alignment, as in the forward).
 template <bool CAUSAL>
 __device__ __forceinline__ Unit decode_unit(int u, const BwdParams &p)
 {
     Unit un;
-    if (CAUSAL) {
-        un.kb = u / p.bh;
-        un.bh = u % p.bh;
-    } else {
-        un.bh = u / p.num_kblk;
-        un.kb = u % p.num_kblk;
-    }
+    const int per_group = p.group * p.num_kblk;
+    const int g = u / per_group;
+    const int r = u - g * per_group;
+    const int h0 = g * p.group;
+    const int gsz = min(p.group, p.bh - h0);
+    un.kb = r / gsz;
+    un.bh = h0 + (r - un.kb * gsz);
     const int n_tiles = (p.sq + Cfg::BM - 1) / Cfg::BM;
     int t0 = 0;
     if (CAUSAL) {
@@ -260,13 +350,17 @@ __device__ __forceinline__ Unit decode_unit(int u, const BwdParams &p)
     return un;
 }
 
-// The i-th work unit of this CTA: rounds of gridDim.x units dealt out in
-// alternating directions (see the forward's scheduler).
-__device__ __forceinline__ int unit_at(int i)
+// The k-th unit index of this CTA from the ring (-1: no more work), read by
+// a whole warp; lane 0 then releases the slot.
+__device__ __forceinline__ bool next_unit(uint32_t k, int &u, Ctl *ctl, const BwdParams &p)
 {
-    const int g = static_cast<int>(gridDim.x);
-    const int c = (i & 1) ? (g - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
-    return i * g + c;
+    const uint32_t slot = k % kUnitRing;
+    const uint32_t full = smem_addr(&ctl->unit_full[slot]);
+    if (!warp_wait(full, (k / kUnitRing) & 1u, ctl, p, SITE_BWD_UNIT_FULL)) return false;
+    u = *reinterpret_cast<volatile int32_t *>(&ctl->unit_idx[slot]);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(smem_addr(&ctl->unit_empty[slot]));
+    return true;
 }
 
 template <typename T>
@@ -315,6 +409,7 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p)
     // the 16-wide shuffles below always have their whole warp.
     const int64_t rows = static_cast<int64_t>(p.bh) * p.sq_pad;
     const int sub = threadIdx.x & 15;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *p.counter = 0;
     for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4; r < rows;
          r += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 4) {
         const int64_t head = r / p.sq_pad;
@@ -369,7 +464,7 @@ template <typename T, bool CAUSAL>
 __global__ void __launch_bounds__(512, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                    const BwdParams p)
+                    const __grid_constant__ CUtensorMap tmdQacc, const BwdParams p)
 {
     using C = Cfg;
     constexpr bool BF16 = std::is_same<T, __nv_bfloat16>::value;
@@ -400,6 +495,7 @@ __global__ void __launch_bounds__(512, 1)
     auto B = [&](const uint64_t &bar) { return smem_addr(&bar); };
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    BWD_TRACE_DECL
 
     if (threadIdx.x == 0) {
         mbar_init(B(ctl->kv_full), 1);
@@ -407,6 +503,8 @@ __global__ void __launch_bounds__(512, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(B(ctl->q_full[s]), 1);
             mbar_init(B(ctl->q_empty[s]), 1);
+            mbar_init(B(ctl->do_full[s]), 1);
+            mbar_init(B(ctl->do_empty[s]), 1);
         }
         mbar_init(B(ctl->s_full), 1);
         mbar_init(B(ctl->dp_full), 1);
@@ -417,6 +515,11 @@ __global__ void __launch_bounds__(512, 1)
         mbar_init(B(ctl->dkv_full), 1);
         mbar_init(B(ctl->dkv_empty), 4);
         mbar_init(B(ctl->mma_done), 1);
+        mbar_init(B(ctl->dr_sync), 4);
+        for (int s = 0; s < kUnitRing; ++s) {
+            mbar_init(B(ctl->unit_full[s]), 1);
+            mbar_init(B(ctl->unit_empty[s]), kUnitReaders);
+        }
         ctl->abort = 0u;
         fence_barrier_init();
     }
@@ -429,12 +532,12 @@ __global__ void __launch_bounds__(512, 1)
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         tma_prefetch_desc(&tmdO);
+        tma_prefetch_desc(&tmdQacc);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
-    const int n_rounds_end = p.num_units;
 
     if (warp >= 12) {
         regs_dec<C::REGS_OTHER>();
@@ -443,9 +546,20 @@ __global__ void __launch_bounds__(512, 1)
             const uint64_t pol = l2_evict_normal();
             uint32_t un_it = 0, q_it = 0;
             bool ok = true;
-            for (int i = 0; i * static_cast<int>(gridDim.x) < n_rounds_end && ok; ++i) {
-                const int u = unit_at(i);
-                if (u >= p.num_units) continue;
+            for (uint32_t kq = 0; ok; ++kq) {
+                // claim the next unit and publish it to the other warps
+                const uint32_t slot = kq % kUnitRing;
+                ok = warp_wait(B(ctl->unit_empty[slot]), ((kq / kUnitRing) & 1u) ^ 1u, ctl, p, SITE_BWD_UNIT_EMPTY);
+                if (!ok) break;
+                int u = -1;
+                if (lane == 0) {
+                    u = atomicAdd(p.counter, 1);
+                    if (u >= p.num_units) u = -1;
+                    ctl->unit_idx[slot] = u;
+                    mbar_arrive(B(ctl->unit_full[slot]));
+                }
+                u = __shfl_sync(0xffffffffu, u, 0);
+                if (u < 0) break;
                 const Unit un = decode_unit<CAUSAL>(u, p);
                 if (un.n == 0) continue;
                 ok = warp_wait(B(ctl->kv_empty), (un_it & 1u) ^ 1u, ctl, p, SITE_BWD_LOAD_KV_EMPTY);
@@ -461,21 +575,32 @@ __global__ void __launch_bounds__(512, 1)
                 ++un_it;
                 for (int t = 0; t < un.n && ok; ++t) {
                     const uint32_t st = q_it & 1u;
+                    BWD_TRACE(BEV_LD_WAIT, q_it);
                     ok = warp_wait(B(ctl->q_empty[st]), ((q_it >> 1) & 1u) ^ 1u, ctl, p, SITE_BWD_LOAD_Q_EMPTY);
+                    BWD_TRACE(BEV_LD_GOT, q_it);
                     if (!ok) break;
                     const int q0 = (un.t0 + t) * C::BM;
+                    const uint32_t q_tile = sQ + st * 2 * C::TILE_BYTES;
                     if (elect_one()) {
                         const uint32_t bar = B(ctl->q_full[st]);
-                        mbar_arrive_expect_tx(bar, 2 * C::TILE_BYTES + 2 * C::BM * 4);
-                        const uint32_t dq_tile = sQ + st * 2 * C::TILE_BYTES;
-                        for (int pn = 0; pn < 2; ++pn) {
-                            tma_load_3d(dq_tile + pn * C::PANEL_BYTES, &tmQ, bar, pn * 64, q0, un.bh, pol);
-                            tma_load_3d(dq_tile + C::TILE_BYTES + pn * C::PANEL_BYTES, &tmdO, bar, pn * 64, q0, un.bh,
-                                        pol);
-                        }
+                        mbar_arrive_expect_tx(bar, C::TILE_BYTES + 2 * C::BM * 4);
+                        for (int pn = 0; pn < 2; ++pn)
+                            tma_load_3d(q_tile + pn * C::PANEL_BYTES, &tmQ, bar, pn * 64, q0, un.bh, pol);
                         const size_t row = static_cast<size_t>(un.bh) * p.sq_pad + q0;
                         bulk_load(sLD + st * C::LD_STAGE_BYTES, p.lse2 + row, C::BM * 4, bar);
                         bulk_load(sLD + st * C::LD_STAGE_BYTES + C::BM * 4, p.dsum + row, C::BM * 4, bar);
+                    }
+                    __syncwarp();
+                    // dO's slot is also where the previous user of the stage
+                    // staged its dQ: wait for that to be read out
+                    ok = warp_wait(B(ctl->do_empty[st]), ((q_it >> 1) & 1u) ^ 1u, ctl, p, SITE_BWD_LOAD_DO_EMPTY);
+                    if (!ok) break;
+                    if (elect_one()) {
+                        const uint32_t bar = B(ctl->do_full[st]);
+                        mbar_arrive_expect_tx(bar, C::TILE_BYTES);
+                        for (int pn = 0; pn < 2; ++pn)
+                            tma_load_3d(q_tile + C::TILE_BYTES + pn * C::PANEL_BYTES, &tmdO, bar, pn * 64, q0, un.bh,
+                                        pol);
                     }
                     __syncwarp();
                     ++q_it;
@@ -483,8 +608,10 @@ __global__ void __launch_bounds__(512, 1)
             }
             // Wind-down: let the last copies land before the CTA exits.
             if (un_it > 0) drain_wait(B(ctl->kv_full), (un_it - 1) & 1u, p.timeout_ns);
-            for (uint32_t k = (q_it > 2 ? q_it - 2 : 0u); k < q_it; ++k)
+            for (uint32_t k = (q_it > 2 ? q_it - 2 : 0u); k < q_it; ++k) {
                 drain_wait(B(ctl->q_full[k & 1u]), (k >> 1) & 1u, p.timeout_ns);
+                drain_wait(B(ctl->do_full[k & 1u]), (k >> 1) & 1u, p.timeout_ns);
+            }
             __syncwarp();
         } else if (warp == 12) {
             // ------------------------------------------------------------ MMA issuer
@@ -518,9 +645,10 @@ __global__ void __launch_bounds__(512, 1)
                 return desc_lo(sQ + st * 2 * C::TILE_BYTES + (dout ? C::TILE_BYTES : 0), lbo);
             };
             uint32_t dq_pending = 0u;  // 1 when a dQ^T in TMEM has not been drained yet
-            for (int i = 0; i * static_cast<int>(gridDim.x) < n_rounds_end && ok; ++i) {
-                const int u = unit_at(i);
-                if (u >= p.num_units) continue;
+            for (uint32_t kq = 0; ok; ++kq) {
+                int u;
+                if (!(ok = next_unit(kq, u, ctl, p))) break;
+                if (u < 0) break;
                 const Unit un = decode_unit<CAUSAL>(u, p);
                 if (un.n == 0) continue;
                 if (!(ok = warp_wait(B(ctl->kv_full), un_it & 1u, ctl, p, SITE_BWD_MMA_KV_FULL))) break;
@@ -535,6 +663,7 @@ __global__ void __launch_bounds__(512, 1)
                     if (!(ok = warp_wait(B(ctl->dq_empty), (tile_it - 1) & 1u, ctl, p, SITE_BWD_MMA_DQ_EMPTY))) break;
                     dq_pending = 0u;
                 }
+                if (!(ok = warp_wait(B(ctl->do_full[q_it & 1u]), (q_it >> 1) & 1u, ctl, p, SITE_BWD_MMA_DO_FULL))) break;
                 tc_fence_after();
                 if (elect_one()) {
                     issue_kq(dV0, q_desc(q_it & 1u, true, 16), tmem + C::TM_DP);
@@ -544,19 +673,24 @@ __global__ void __launch_bounds__(512, 1)
                 for (int t = 0; t < un.n && ok; ++t) {
                     const uint32_t st = q_it & 1u;
                     // dV += P^T dO
+                    BWD_TRACE(BEV_MMA_WAIT_P, tile_it);
                     if (!(ok = warp_wait(B(ctl->p_full), tile_it & 1u, ctl, p, SITE_BWD_MMA_P_FULL))) break;
+                    BWD_TRACE(BEV_MMA_GOT_P, tile_it);
                     if (t == 0 && un_it > 0 &&
                         !(ok = warp_wait(B(ctl->dkv_empty), (un_it - 1) & 1u, ctl, p, SITE_BWD_MMA_DKV_EMPTY)))
                         break;
                     tc_fence_after();
                     if (elect_one()) issue_acc(tmem + C::TM_DV, tmem + C::TM_S, q_desc(st, true, C::PANEL_BYTES), t > 0);
                     __syncwarp();
+                    BWD_TRACE(BEV_MMA_ISSUED_DV, tile_it);
                     // S^T of the next tile (its P^T columns were just consumed, in order)
                     const bool more = t + 1 < un.n;
                     if (more) {
+                        BWD_TRACE(BEV_MMA_WAIT_Q, tile_it);
                         if (!(ok = warp_wait(B(ctl->q_full[(q_it + 1) & 1u]), ((q_it + 1) >> 1) & 1u, ctl, p,
                                              SITE_BWD_MMA_Q_FULL)))
                             break;
+                        BWD_TRACE(BEV_MMA_GOT_Q, tile_it);
                         tc_fence_after();
                         if (elect_one()) {
                             issue_kq(dK0, q_desc((q_it + 1) & 1u, false, 16), tmem + C::TM_S);
@@ -565,7 +699,9 @@ __global__ void __launch_bounds__(512, 1)
                         __syncwarp();
                     }
                     // dK += dS^T Q, then dQ^T = K^T dS^T into the dP^T columns
+                    BWD_TRACE(BEV_MMA_WAIT_DS, tile_it);
                     if (!(ok = warp_wait(B(ctl->ds_full), tile_it & 1u, ctl, p, SITE_BWD_MMA_DS_FULL))) break;
+                    BWD_TRACE(BEV_MMA_GOT_DS, tile_it);
                     tc_fence_after();
                     if (elect_one()) {
                         issue_acc(tmem + C::TM_DK, tmem + C::TM_DP, q_desc(st, false, C::PANEL_BYTES), t > 0);
@@ -578,14 +714,20 @@ __global__ void __launch_bounds__(512, 1)
                         }
                     }
                     __syncwarp();
+                    BWD_TRACE(BEV_MMA_ISSUED_DKDQ, tile_it);
                     dq_pending = 1u;
                     ++tile_it;
                     ++q_it;
                     // dP^T of the next tile, once dQ^T has been drained
                     if (more) {
+                        BWD_TRACE(BEV_MMA_WAIT_DQE, tile_it);
                         if (!(ok = warp_wait(B(ctl->dq_empty), (tile_it - 1) & 1u, ctl, p, SITE_BWD_MMA_DQ_EMPTY)))
                             break;
+                        BWD_TRACE(BEV_MMA_GOT_DQE, tile_it);
                         dq_pending = 0u;
+                        if (!(ok = warp_wait(B(ctl->do_full[q_it & 1u]), (q_it >> 1) & 1u, ctl, p,
+                                             SITE_BWD_MMA_DO_FULL)))
+                            break;
                         tc_fence_after();
                         if (elect_one()) {
                             issue_kq(dV0, q_desc(q_it & 1u, true, 16), tmem + C::TM_DP);
@@ -603,40 +745,67 @@ __global__ void __launch_bounds__(512, 1)
             __syncwarp();
         }
     } else if (warp >= 8) {
-        regs_dec<C::REGS_DRAIN>();
+        regs_inc<C::REGS_DRAIN>();  // above the launch budget of 128
         // ---------------------------------------------------------------- dQ drain + dK/dV epilogue
+        // Per tile: dQ^T (this thread: head-dim column dcol, 128 queries)
+        // comes out of tensor memory, which is released at once; it is then
+        // staged as fp32 [64 queries][128] rows in the tile's dO slot (free:
+        // dP^T and dV have read it) and added into the accumulator by the
+        // copy engine, 64 rows per reduce.  The slot is handed back to the
+        // producer once the reduces have read it.
         const int quad = warp & 3;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-        const int dcol = quad * 32 + lane;  // head-dim column of dQ^T this thread drains
-        uint32_t tile_it = 0, un_it = 0;
+        const int dcol = quad * 32 + lane;
+        const bool issuer = (warp == 8 && lane == 0);
+        uint32_t tile_it = 0, un_it = 0, q_it = 0, sync_ph = 0;
         bool ok = true;
-        for (int i = 0; i * static_cast<int>(gridDim.x) < n_rounds_end && ok; ++i) {
-            const int u = unit_at(i);
-            if (u >= p.num_units) continue;
+        // the four drain warps meet (bounded, like every other wait)
+        auto drain_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B(ctl->dr_sync));
+            const bool r = warp_wait(B(ctl->dr_sync), sync_ph, ctl, p, SITE_BWD_DRAIN_SYNC);
+            sync_ph ^= 1u;
+            return r;
+        };
+        for (uint32_t kq = 0; ok; ++kq) {
+            int u;
+            if (!(ok = next_unit(kq, u, ctl, p))) break;
+            if (u < 0) break;
             const Unit un = decode_unit<CAUSAL>(u, p);
             if (un.n == 0) continue;
             for (int t = 0; t < un.n && ok; ++t) {
+                BWD_TRACE(BEV_DR_WAIT, tile_it);
                 if (!(ok = warp_wait(B(ctl->dq_full), tile_it & 1u, ctl, p, SITE_BWD_DRAIN_DQ_FULL))) break;
+                BWD_TRACE(BEV_DR_GOT, tile_it);
                 ++tile_it;
                 tc_fence_after();
+                uint32_t v[128];
+                tmem_ld128_wait(tmem + lane_off + C::TM_DP, v);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(B(ctl->dq_empty));
+                BWD_TRACE(BEV_DR_RELEASED, tile_it);
+                const uint32_t st = q_it & 1u;
+                const uint32_t stage_buf = sQ + st * 2 * C::TILE_BYTES + C::TILE_BYTES;  // the dO slot
                 const int q0 = (un.t0 + t) * C::BM;
-                float *dst = p.dq_acc + (static_cast<size_t>(un.bh) * p.sq + q0) * C::D + dcol;
-                const int nq = min(C::BM, p.sq - q0);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t v[64];
-                    tmem_ld32_wait(tmem + lane_off + C::TM_DP + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(v));
-                    tmem_ld32_wait(tmem + lane_off + C::TM_DP + 64 * h + 32,
-                                   *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-                    if (h == 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(B(ctl->dq_empty));
-                    }
+                for (int h = 0; h < 2 && ok; ++h) {
+                    if (h == 1 && !(ok = drain_sync())) break;  // the first reduce has read the slot
 #pragma unroll
                     for (int c = 0; c < 64; ++c)
-                        if (64 * h + c < nq) atomicAdd(dst + static_cast<size_t>(64 * h + c) * C::D, __uint_as_float(v[c]));
+                        st_shared_f32(stage_buf + (c * C::D + dcol) * 4, __uint_as_float(v[64 * h + c]));
+                    fence_proxy_async_smem();
+                    if (!(ok = drain_sync())) break;
+                    if (issuer) {
+                        tma_reduce_add_3d(&tmdQacc, stage_buf, 0, q0 + 64 * h, un.bh);
+                        bulk_commit_group();
+                        bulk_wait_read_all();
+                    }
                 }
+                if (!ok) break;
+                if (issuer) mbar_arrive(B(ctl->do_empty[st]));
+                ++q_it;
+                BWD_TRACE(BEV_DR_DONE, tile_it);
             }
             if (!ok) break;
             // dK, dV of the unit: this thread's key row, D columns each
@@ -680,9 +849,10 @@ __global__ void __launch_bounds__(512, 1)
         const float sl2e = p.sl2e, scale = p.scale;
         uint32_t tile_it = 0, q_it = 0;
         bool ok = true;
-        for (int i = 0; i * static_cast<int>(gridDim.x) < n_rounds_end && ok; ++i) {
-            const int u = unit_at(i);
-            if (u >= p.num_units) continue;
+        for (uint32_t kq = 0; ok; ++kq) {
+            int u;
+            if (!(ok = next_unit(kq, u, ctl, p))) break;
+            if (u < 0) break;
             const Unit un = decode_unit<CAUSAL>(u, p);
             if (un.n == 0) continue;
             const int key = un.kb * C::BN + r;
@@ -691,7 +861,9 @@ __global__ void __launch_bounds__(512, 1)
                 const uint32_t st = q_it & 1u;
                 // the tile's LSE / D vectors arrive with Q and dO
                 if (!(ok = warp_wait(B(ctl->q_full[st]), (q_it >> 1) & 1u, ctl, p, SITE_BWD_SM_S_FULL))) break;
+                BWD_TRACE(BEV_SM_WAIT_S, tile_it);
                 if (!(ok = warp_wait(B(ctl->s_full), tile_it & 1u, ctl, p, SITE_BWD_SM_S_FULL))) break;
+                BWD_TRACE(BEV_SM_GOT_S, tile_it);
                 tc_fence_after();
                 const int q0 = (un.t0 + t) * C::BM + 64 * g;  // first query of this thread's columns
                 // columns c < lim are masked for this key row (key j sees query i iff i >= j - (sk - sq))
@@ -700,58 +872,63 @@ __global__ void __launch_bounds__(512, 1)
                 const bool masked = __any_sync(0xffffffffu, lim > 0);
                 const float *l2 = ld_smem + st * (C::LD_STAGE_BYTES / 4) + 64 * g;
                 const float *dsv = l2 + C::BM;
-                float pr[64];
+                // P^T of this thread's 64 columns, rounded to T, two per word: the
+                // dV product and dS both use these values.
+                uint32_t pk[32];
+                {
+                    uint32_t sr[64];
+                    tmem_ld64_wait(tS, sr);
 #pragma unroll
-                for (int ch = 0; ch < 2; ++ch) {
-                    uint32_t sr[32];
-                    tmem_ld32_wait(tS + 32 * ch, sr);
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int c = 0; c < 32; c += 4) {
-                        const float4 lv = *reinterpret_cast<const float4 *>(l2 + 32 * ch + c);
+                    for (int c = 0; c < 64; c += 4) {
+                        const float4 lv = *reinterpret_cast<const float4 *>(l2 + c);
                         const float lvv[4] = {lv.x, lv.y, lv.z, lv.w};
+                        float x[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            float x = ex2_approx(fmaf(__uint_as_float(sr[c + e]), sl2e, -lvv[e]));
-                            if (masked && (32 * ch + c + e) < lim) x = 0.f;
-                            pr[32 * ch + c + e] = x;
+                            x[e] = ex2_approx(fmaf(__uint_as_float(sr[c + e]), sl2e, -lvv[e]));
+                            if (masked && (c + e) < lim) x[e] = 0.f;
                         }
+                        pk[c / 2] = pack2<T>(x[0], x[1]);
+                        pk[c / 2 + 1] = pack2<T>(x[2], x[3]);
                     }
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) pk[c] = pack2<T>(pr[32 * ch + 2 * c], pr[32 * ch + 2 * c + 1]);
-                    tmem_st16(tS + 16 * ch, pk);
                 }
+                tmem_st16(tS, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+                tmem_st16(tS + 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(B(ctl->p_full));
+                BWD_TRACE(BEV_SM_P_DONE, tile_it);
                 // dS^T = scale * P^T (dP^T - D)
+                BWD_TRACE(BEV_SM_WAIT_DP, tile_it);
                 if (!(ok = warp_wait(B(ctl->dp_full), tile_it & 1u, ctl, p, SITE_BWD_SM_DP_FULL))) break;
+                BWD_TRACE(BEV_SM_GOT_DP, tile_it);
                 tc_fence_after();
+                {
+                    uint32_t dr[64];
+                    tmem_ld64_wait(tDP, dr);
+                    uint32_t dk[32];
 #pragma unroll
-                for (int ch = 0; ch < 2; ++ch) {
-                    uint32_t dr[32];
-                    tmem_ld32_wait(tDP + 32 * ch, dr);
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int c = 0; c < 32; c += 4) {
-                        const float4 dv4 = *reinterpret_cast<const float4 *>(dsv + 32 * ch + c);
+                    for (int c = 0; c < 64; c += 4) {
+                        const float4 dv4 = *reinterpret_cast<const float4 *>(dsv + c);
+                        const float2 p01 = unpack2<T>(pk[c / 2]), p23 = unpack2<T>(pk[c / 2 + 1]);
+                        const float pv[4] = {p01.x, p01.y, p23.x, p23.y};
                         const float dvv[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
                         float ds[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            ds[e] = scale * pr[32 * ch + c + e] * (__uint_as_float(dr[c + e]) - dvv[e]);
-                        pk[c / 2] = pack2<T>(ds[0], ds[1]);
-                        pk[c / 2 + 1] = pack2<T>(ds[2], ds[3]);
+                        for (int e = 0; e < 4; ++e) ds[e] = scale * pv[e] * (__uint_as_float(dr[c + e]) - dvv[e]);
+                        dk[c / 2] = pack2<T>(ds[0], ds[1]);
+                        dk[c / 2 + 1] = pack2<T>(ds[2], ds[3]);
                     }
-                    tmem_st16(tDP + 16 * ch, pk);
+                    tmem_st16(tDP, *reinterpret_cast<const uint32_t(*)[16]>(dk));
+                    tmem_st16(tDP + 16, *reinterpret_cast<const uint32_t(*)[16]>(dk + 16));
                     // shared copy for dQ^T: MN-major B, panel g (queries 64g..), row r,
-                    // 16-byte chunks 4*ch .. 4*ch+3 of the row, 128-byte swizzle
+                    // 16-byte chunks 0..7 of the row, 128-byte swizzle
 #pragma unroll
-                    for (int k8 = 0; k8 < 4; ++k8) {
-                        const uint32_t chunk = static_cast<uint32_t>((4 * ch + k8) ^ (r & 7));
-                        st_shared_v4(sDS + g * C::PANEL_BYTES + r * 128 + chunk * 16, pk[4 * k8], pk[4 * k8 + 1],
-                                     pk[4 * k8 + 2], pk[4 * k8 + 3]);
+                    for (int k8 = 0; k8 < 8; ++k8) {
+                        const uint32_t chunk = static_cast<uint32_t>(k8 ^ (r & 7));
+                        st_shared_v4(sDS + g * C::PANEL_BYTES + r * 128 + chunk * 16, dk[4 * k8], dk[4 * k8 + 1],
+                                     dk[4 * k8 + 2], dk[4 * k8 + 3]);
                     }
                 }
                 tmem_wait_st();
@@ -759,12 +936,14 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(B(ctl->ds_full));
+                BWD_TRACE(BEV_SM_DS_DONE, tile_it);
                 ++tile_it;
                 ++q_it;
             }
         }
     }
 
+    if (warp == 8 && lane == 0) bulk_wait_all();  // the dQ reduces have landed
     tc_fence_before();
     __syncthreads();
     if (warp == 12) {

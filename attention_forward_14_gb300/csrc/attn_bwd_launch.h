@@ -12,6 +12,7 @@ namespace bwd {
 
 struct BwdLaunchArgs {
     CUtensorMap q, k, v, dout;
+    CUtensorMap dq_acc;  // fp32 [bh][sq][128], box 128 x 64 rows, no swizzle (reduce-add target)
     BwdParams p;
     int grid;       // main kernel CTAs (persistent)
     int sm_count;

@@ -39,6 +39,10 @@ int cuda_fail(cudaError_t e, const char *what)
     return fail(ATTN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
+#ifdef ATTN_TRACE_ENABLE
+unsigned long long *g_trace_buf = nullptr;  // timeline builds only: where launches record
+#endif
+
 // Watchdog status word, one per device that loads this library.
 __device__ uint32_t g_watchdog[4];
 
@@ -132,6 +136,24 @@ int make_map_packed(CUtensorMap *map, const void *ptr, int dtype, int64_t tokens
                      const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (packed) failed (CUresult %d)", static_cast<int>(r));
+    return ATTN_OK;
+}
+
+// The backward's fp32 dQ accumulator [bh, sq, d] as 3-D [bh][sq][d] for
+// tile reduce-adds of 64 rows x d columns (row-major in shared memory, no
+// swizzle); rows past sq are clipped by the copy engine.
+int make_map_f32_rows(CUtensorMap *map, void *ptr, int64_t bh, int64_t s, int64_t d)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    int rc = get_encode(&enc);
+    if (rc != ATTN_OK) return rc;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(s), static_cast<cuuint64_t>(bh)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 4), static_cast<cuuint64_t>(s * d * 4)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 64, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (fp32 rows) failed (CUresult %d)", static_cast<int>(r));
     return ATTN_OK;
 }
 
@@ -259,9 +281,23 @@ constexpr uint64_t kDefaultTimeoutNs = 2000ull * 1000ull * 1000ull;  // 2 s per 
 
 int64_t bwd_sq_pad(int64_t sq) { return (sq + 127) / 128 * 128; }
 
+// fp32 dQ accumulator [bh, sq, d], LSE2 and D [bh, sq_pad] each, and 256
+// bytes for the scheduler's unit counter.
 int64_t bwd_workspace_bytes(int64_t bh, int64_t sq, int64_t d)
 {
-    return bh * sq * d * 4 + 2 * bh * bwd_sq_pad(sq) * 4;
+    return bh * sq * d * 4 + 2 * bh * bwd_sq_pad(sq) * 4 + 256;
+}
+
+// Heads per scheduling group of the backward: the group's fp32 dQ
+// accumulator, Q and dO (8 * sq * d bytes per head) fit in 64 MB, half of
+// L2, while its units run.
+int32_t bwd_group(int64_t bh, int64_t sq, int64_t d)
+{
+    const int64_t per_head = 8 * sq * d;
+    int64_t g = per_head > 0 ? (int64_t(64) << 20) / per_head : bh;
+    if (g < 1) g = 1;
+    if (g > bh) g = bh;
+    return static_cast<int32_t>(g);
 }
 
 int run_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse, void *dq,
@@ -312,6 +348,7 @@ int run_bwd(const void *q, const void *k, const void *v, const void *o, const vo
     if ((rc = make_map(&a.dout, dout, dtype, bh, sq, d)) != ATTN_OK) return rc;
     if ((rc = make_map(&a.k, k, dtype, bh, sk, d)) != ATTN_OK) return rc;
     if ((rc = make_map(&a.v, v, dtype, bh, sk, d)) != ATTN_OK) return rc;
+    if ((rc = make_map_f32_rows(&a.dq_acc, workspace, bh, sq, d)) != ATTN_OK) return rc;
     bwd::BwdParams &p = a.p;
     const int64_t sq_pad = bwd_sq_pad(sq);
     p.o = o;
@@ -320,6 +357,7 @@ int run_bwd(const void *q, const void *k, const void *v, const void *o, const vo
     p.dq_acc = static_cast<float *>(workspace);
     p.lse2 = p.dq_acc + bh * sq * d;
     p.dsum = p.lse2 + bh * sq_pad;
+    p.counter = reinterpret_cast<int32_t *>(p.dsum + bh * sq_pad);
     p.dq = dq;
     p.dk = dk;
     p.dv = dv;
@@ -330,6 +368,10 @@ int run_bwd(const void *q, const void *k, const void *v, const void *o, const vo
     p.sq_pad = static_cast<int32_t>(sq_pad);
     p.num_kblk = static_cast<int32_t>((sk + 127) / 128);
     p.num_units = static_cast<int32_t>(bh * p.num_kblk);
+    p.group = bwd_group(bh, sq, d);
+#ifdef ATTN_TRACE_ENABLE
+    p.trace = g_trace_buf;
+#endif
     p.sl2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     p.scale = scale;
     p.timeout_ns = kDefaultTimeoutNs;

@@ -250,6 +250,102 @@ def bench_varlen(args, w):
     print(json.dumps(line), flush=True)
 
 
+def bench_bwd(args, bw):
+    """Backward workload: one step = one attn_bwd call (prep, main and dQ
+    convert kernels) on the forward's outputs, inputs resident in HBM."""
+    import torch
+    import attention_forward_14_gb300 as af
+    from attention_forward_14_gb300 import workloads as W
+
+    if int(os.environ.get("WORLD_SIZE", "1")) != 1:
+        raise SystemExit("the backward workloads run on one GPU")
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = bw.w
+    q, k, v = W.inputs(w)
+    do = W.draw_grad(w.b, w.h, w.sq, w.d, w.dtype, bw.grad_seed)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = af.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.empty(af.bwd_workspace_bytes(w.b, w.h, w.sq, w.d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        af.attn_bwd(qd, kd, vd, o, dod, lse, causal=w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+                    stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    step_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    value = bw.flops() / (ms * 1e-3) / 1e12
+    achieved = bw.flops() / (step_ms * 1e-3) / 1e12
+
+    # end to end: H2D of q, k, v, o, dO, lse from pinned memory, the
+    # backward, D2H of dq, dk, dv, every step
+    hs = [t.cpu().pin_memory() for t in (qd, kd, vd, o, dod, lse)]
+    outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+    devs = (qd, kd, vd, o, dod, lse)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        for dst, src in zip(devs, hs):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in zip(outs, (dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    peaks = load_peaks()
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": bw.name, "pass": "backward", "b": w.b, "h": w.h, "sq": w.sq, "sk": w.sk, "d": w.d,
+                   "causal": w.causal, "qk_std": w.qk_std, "flops_per_step": bw.flops(),
+                   "flops_rule": "2.5 x forward (five products: S, dP, dV, dK, dQ)",
+                   "l2": "inputs larger than L2, no flush" if bw.bytes() > L2_BYTES else "inputs fit in L2"},
+        "pct_of_peak": 100.0 * value / peaks["bf16"],
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16"], "traffic": profiled_traffic(bw.name),
+                     "peak_kind": f"{peaks['source']} bf16 dense burst (cuBLAS)",
+                     "kernel": "attn_bwd_kernel (+ prep and dQ convert, timed together)",
+                     "algorithmic_bytes": bw.bytes()},
+        "e2e": {"value": bw.flops() / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hs),
+                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs), "ms_per_step": e2e_ms},
+        "gpu_launches": 3 * args.steps,
+        "clocks": sampler.summary(),
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        n = min(2048, w.sq, w.sk)
+        sub = [t[:1, :1, :n].double().numpy() for t in (q, k, v, do)]
+        t_start = time.perf_counter()
+        oracle.attn_bwd(*sub, w.causal, w.scale)
+        dt = time.perf_counter() - t_start
+        f = 2.5 * 4.0 * n * n * w.d * (0.5 if w.causal else 1.0)
+        line["cpu_baseline"] = {"value": f / dt / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(),
+                                "kind": "oracle", "sample": f"backward of the first {n} queries and keys of head 0 "
+                                f"(a self-contained block of the same problem), fp64", "seconds": dt}
+    print(json.dumps(line), flush=True)
+
+
 def _finish_fp8(args, w, world, rank, dist, dev, q, k, v, qd, kd, vd, o, lse, stream, t_all0, t_all1, total_ms,
                 launch_ms, sampler, step):
     """e4m3 line: roofline against the 8-bit tensor peak (measured bf16 peak
@@ -313,6 +409,10 @@ def main():
     name = args.workload or W.HEADLINE
     if name in W.VARLEN:
         return bench_varlen(args, W.VARLEN[name])
+    if name in W.BWD:
+        if args.impl == "reference":
+            raise SystemExit("the reference arm times the forward oracle only")
+        return bench_bwd(args, W.BWD[name])
     w = W.WORKLOADS[name]
 
     rank = int(os.environ.get("RANK", "0"))

@@ -234,9 +234,10 @@ int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v,
  *   d              : 128 only (ATTN_ERR_HEADDIM otherwise).
  *   workspace      : caller-owned device scratch, 16-byte aligned, of at
  *                    least attn_bwd_workspace_bytes(b, h, sq, d) bytes (an
- *                    fp32 dQ accumulator and two fp32 values per query
- *                    row); its contents on entry do not matter.  Calls on
- *                    different streams need different workspaces.
+ *                    fp32 dQ accumulator, two fp32 values per query row
+ *                    and a work counter); its contents on entry do not
+ *                    matter.  Calls on different streams need different
+ *                    workspaces.
  * Outputs dq, dk, dv are written in full (zeros where the gradient is zero,
  * e.g. dq of rows that see no key, or everything when sq or sk is 0).
  * Three kernels run on `stream`, asynchronously; the library allocates

@@ -10,8 +10,8 @@ The kernel computes, for key j and query i:
   P = exp2(s*scale*log2e - lse2)            |dP_hat - P| <= eps P
   D = dO_i . O_i with O rounded to the type   |dD| <= u a_i,  a_i = |dO_i|.|O_i|
   dP = dO_i . V_j in fp32                     |d dP| <= eps b_ij, b = |dO| |V|^T
-  dS = round(scale P (dP - D))
-     => |d dS| <= scale P (u a_i + eps (b_ij + |dP - D|)) + u |scale dS| + tiny
+  dS = round(scale round(P) (dP - D))        (P as rounded for dV, as in the kernel)
+     => |d dS| <= scale P (u a_i + eps (b_ij + |dP - D|)) + (2u + eps) |scale dS| + tiny
   dV = round(sum_i round(P) dO_i)             <= (u + eps) P^T |dO| + u |dV| + tiny
   dK = round(sum_i dS Q_i)                    <= E^T |Q| + eps |scale dS|^T |Q| + u |dK| + tiny
   dQ = round(sum_j dS K_j) (fp32 accumulator) <= E |K|   + eps |scale dS| |K|   + u |dQ| + tiny
@@ -57,7 +57,8 @@ def bounds(q, k, v, do, o, lse, dq_ref, dk_ref, dv_ref, causal, scale, dtype, ro
         dP = do[ri] @ v[cj].T
         dS = P * (dP - D[ri][:, None])
         B = np.abs(do[ri]) @ np.abs(v[cj]).T
-        E = scale * P * (u * a[ri][:, None] + EPS * (B + np.abs(dP - D[ri][:, None]))) + u * scale * np.abs(dS) + tiny
+        E = (scale * P * (u * a[ri][:, None] + EPS * (B + np.abs(dP - D[ri][:, None])))
+             + (2 * u + EPS) * scale * np.abs(dS) + tiny)
         return P, dS, E
 
     # dQ at the sampled rows: all keys

@@ -125,7 +125,8 @@ def test_bwd_rejects_bad_arguments(lib):
 
 def test_bwd_workspace_bytes(lib):
     # fp32 dQ accumulator + two fp32 values per query row padded to 128 rows
-    assert lib.attn_bwd_workspace_bytes(2, 3, 300, 128) == 6 * 300 * 128 * 4 + 2 * 6 * 384 * 4
-    assert lib.attn_bwd_workspace_bytes(1, 1, 0, 128) == 0
+    # + the scheduler's counter
+    assert lib.attn_bwd_workspace_bytes(2, 3, 300, 128) == 6 * 300 * 128 * 4 + 2 * 6 * 384 * 4 + 256
+    assert lib.attn_bwd_workspace_bytes(1, 1, 0, 128) == 256
     assert lib.attn_bwd_workspace_bytes(1, 1, 4, 64) == -3
     assert lib.attn_bwd_workspace_bytes(-1, 1, 4, 128) == -2

@@ -28,6 +28,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOPS on 1 GB300 (d=128, bf16, causal) and % of dense tensor peak"
+METRIC_BWD = "attention bwd TFLOPS on 1 GB300 (d=128, bf16, causal) and % of dense tensor peak"
 L2_BYTES = 129e6
 
 
@@ -59,27 +60,34 @@ def load_peaks():
     return dict(bf16=1900.0, bf16_sustained=1700.0, hbm=6800.0, source="fallback")
 
 
-def kernel_source_hash():
+# Device sources of each kernel family: the counters in profiles/ are tied
+# to these (host-side API code does not change what a kernel reads/writes).
+KERNEL_SOURCES = {
+    "attn_fwd_kernel": ["ptx.cuh", "attn_fwd_kernel.cuh", "launch.h", "inst_d64.cu", "inst_d128_noncausal.cu",
+                        "inst_d128_causal.cu", "inst_d128_fp8.cu"],
+    "attn_bwd_kernel": ["ptx.cuh", "attn_bwd_kernel.cuh", "attn_bwd_launch.h", "attn_bwd_inst.cu"],
+}
+
+
+def kernel_source_hash(kernel: str = "attn_fwd_kernel"):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_forward_14_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.startswith("attn_bwd"):  # backward sources do not change the forward kernel
-            continue
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, kernel: str = "attn_fwd_kernel"):
     """DRAM bytes per launch from the committed ncu summary of this workload,
     or None when no summary exists or the kernel sources changed since."""
-    p = os.path.join(ROOT, "profiles", f"attn_fwd_kernel_{workload}.md")
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(p):
         return None
     txt = open(p).read()
     m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
     m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(kernel):
         return None
     return float(m_bytes.group(1))
 
@@ -313,7 +321,7 @@ def bench_bwd(args, bw):
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
     peaks = load_peaks()
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": 1, "steps": args.steps,
+        "metric": METRIC_BWD, "value": value, "unit": "TFLOPS", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": bw.name, "pass": "backward", "b": w.b, "h": w.h, "sq": w.sq, "sk": w.sk, "d": w.d,
@@ -322,7 +330,7 @@ def bench_bwd(args, bw):
                    "l2": "inputs larger than L2, no flush" if bw.bytes() > L2_BYTES else "inputs fit in L2"},
         "pct_of_peak": 100.0 * value / peaks["bf16"],
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16"], "traffic": profiled_traffic(bw.name),
+                     "frac": achieved / peaks["bf16"], "traffic": profiled_traffic(bw.name, "attn_bwd_kernel"),
                      "peak_kind": f"{peaks['source']} bf16 dense burst (cuBLAS)",
                      "kernel": "attn_bwd_kernel (+ prep and dQ convert, timed together)",
                      "algorithmic_bytes": bw.bytes()},

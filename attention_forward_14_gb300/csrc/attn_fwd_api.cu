@@ -277,6 +277,51 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_
 
 constexpr uint64_t kDefaultTimeoutNs = 2000ull * 1000ull * 1000ull;  // 2 s per wait
 
+// ---------------------------------------------------------------- host-buffer pipeline
+//
+// attn_fwd_host splits a large problem into chunks of whole heads and
+// overlaps the host->device copy of chunk c+1 and the device->host copy of
+// chunk c-1 with the forward of chunk c: copies in on one internal stream,
+// the forwards on the caller's stream, copies out on a second internal
+// stream, ordered by events.  The streams and events are created once per
+// device; a mutex keeps one call's record/wait sequence together.
+
+constexpr int kPipeChunks = 4;
+constexpr int64_t kPipeMinBytes = int64_t(64) << 20;  // smaller problems: one chunk
+
+struct HostPipe {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t in[kPipeChunks] = {}, out[kPipeChunks] = {};
+    std::mutex mu;
+};
+HostPipe g_pipe[kMaxDevices];
+
+int host_pipe(HostPipe **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_CUDA, "device ordinal %d out of range", dev);
+    HostPipe &hp = g_pipe[dev];
+    std::call_once(hp.once, [&] {
+        cudaError_t r = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking);
+        if (r == cudaSuccess) r = cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking);
+        if (r == cudaSuccess) r = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming);
+        if (r == cudaSuccess) r = cudaEventCreateWithFlags(&hp.done, cudaEventDisableTiming);
+        for (int c = 0; c < kPipeChunks && r == cudaSuccess; ++c) {
+            r = cudaEventCreateWithFlags(&hp.in[c], cudaEventDisableTiming);
+            if (r == cudaSuccess) r = cudaEventCreateWithFlags(&hp.out[c], cudaEventDisableTiming);
+        }
+        hp.err = r;
+    });
+    if (hp.err != cudaSuccess) return cuda_fail(hp.err, "host pipeline streams");
+    *out = &hp;
+    return ATTN_OK;
+}
+
 // ---------------------------------------------------------------- backward
 
 int64_t bwd_sq_pad(int64_t sq) { return (sq + 127) / 128 * 128; }
@@ -420,26 +465,58 @@ int attn_fwd_host(const void *q_host, const void *k_host, const void *v_host, vo
     if (rc != ATTN_OK || nothing) return rc;
     if (!o_host || (sk > 0 && (!q_host || !k_host || !v_host)))
         return fail(ATTN_ERR_NULL, "a host buffer is NULL");
+    DeviceInfo *di = nullptr;
+    if ((rc = device_info(&di)) != ATTN_OK) return rc;
+    HostPipe *hp = nullptr;
+    if ((rc = host_pipe(&hp)) != ATTN_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const size_t qbytes = static_cast<size_t>(b * h * sq * d) * 2;
-    const size_t kvbytes = static_cast<size_t>(b * h * sk * d) * 2;
+    const int64_t bh = b * h;
+    const int64_t qrow = sq * d * 2, krow = sk * d * 2;  // bytes per head
+    const bool lse_out = lse_host && lse_dev;
+    const int64_t total = bh * (2 * qrow + 2 * krow);
+    const int chunks = (total < kPipeMinBytes || bh < 2) ? 1 : static_cast<int>(bh < kPipeChunks ? bh : kPipeChunks);
+    const int64_t per = (bh + chunks - 1) / chunks;
+    auto bytes_at = [](const void *p, int64_t off) { return static_cast<const char *>(p) + off; };
+    auto mbytes_at = [](void *p, int64_t off) { return static_cast<char *>(p) + off; };
+
+    std::lock_guard<std::mutex> lock(hp->mu);
     cudaError_t e;
-    if (sk > 0) {
-        if ((e = cudaMemcpyAsync(q_dev, q_host, qbytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
-            return cuda_fail(e, "copy q to device");
-        if ((e = cudaMemcpyAsync(k_dev, k_host, kvbytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
-            return cuda_fail(e, "copy k to device");
-        if ((e = cudaMemcpyAsync(v_dev, v_host, kvbytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
-            return cuda_fail(e, "copy v to device");
+    if ((e = cudaEventRecord(hp->start, st)) != cudaSuccess) return cuda_fail(e, "record start");
+    if ((e = cudaStreamWaitEvent(hp->h2d, hp->start, 0)) != cudaSuccess) return cuda_fail(e, "order copies in");
+    if ((e = cudaStreamWaitEvent(hp->d2h, hp->start, 0)) != cudaSuccess) return cuda_fail(e, "order copies out");
+    for (int c = 0; c < chunks; ++c) {
+        const int64_t h0 = c * per;
+        const int64_t nh = (h0 + per <= bh) ? per : bh - h0;
+        if (nh <= 0) break;
+        if (sk > 0) {
+            if ((e = cudaMemcpyAsync(mbytes_at(q_dev, h0 * qrow), bytes_at(q_host, h0 * qrow), nh * qrow,
+                                     cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess)
+                return cuda_fail(e, "copy q to device");
+            if ((e = cudaMemcpyAsync(mbytes_at(k_dev, h0 * krow), bytes_at(k_host, h0 * krow), nh * krow,
+                                     cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess)
+                return cuda_fail(e, "copy k to device");
+            if ((e = cudaMemcpyAsync(mbytes_at(v_dev, h0 * krow), bytes_at(v_host, h0 * krow), nh * krow,
+                                     cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess)
+                return cuda_fail(e, "copy v to device");
+        }
+        if ((e = cudaEventRecord(hp->in[c], hp->h2d)) != cudaSuccess) return cuda_fail(e, "record copy-in");
+        if ((e = cudaStreamWaitEvent(st, hp->in[c], 0)) != cudaSuccess) return cuda_fail(e, "wait copy-in");
+        // the chunk's heads seen as one batch of nh heads ([b, h] flatten to b*h)
+        rc = run(bytes_at(q_dev, h0 * qrow), bytes_at(k_dev, h0 * krow), bytes_at(v_dev, h0 * krow),
+                 mbytes_at(o_dev, h0 * qrow), lse_dev ? lse_dev + h0 * sq : nullptr, 1, nh, sq, sk, d, causal, scale,
+                 dtype, st, -1, kDefaultTimeoutNs);
+        if (rc != ATTN_OK) return rc;
+        if ((e = cudaEventRecord(hp->out[c], st)) != cudaSuccess) return cuda_fail(e, "record forward");
+        if ((e = cudaStreamWaitEvent(hp->d2h, hp->out[c], 0)) != cudaSuccess) return cuda_fail(e, "wait forward");
+        if ((e = cudaMemcpyAsync(mbytes_at(o_host, h0 * qrow), bytes_at(o_dev, h0 * qrow), nh * qrow,
+                                 cudaMemcpyDeviceToHost, hp->d2h)) != cudaSuccess)
+            return cuda_fail(e, "copy o to host");
+        if (lse_out && (e = cudaMemcpyAsync(lse_host + h0 * sq, lse_dev + h0 * sq, nh * sq * 4, cudaMemcpyDeviceToHost,
+                                            hp->d2h)) != cudaSuccess)
+            return cuda_fail(e, "copy lse to host");
     }
-    rc = run(q_dev, k_dev, v_dev, o_dev, lse_dev, b, h, sq, sk, d, causal, scale, dtype, st, -1, kDefaultTimeoutNs);
-    if (rc != ATTN_OK) return rc;
-    if ((e = cudaMemcpyAsync(o_host, o_dev, qbytes, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
-        return cuda_fail(e, "copy o to host");
-    if (lse_host && lse_dev &&
-        (e = cudaMemcpyAsync(lse_host, lse_dev, static_cast<size_t>(b * h * sq) * 4, cudaMemcpyDeviceToHost, st)) !=
-            cudaSuccess)
-        return cuda_fail(e, "copy lse to host");
+    if ((e = cudaEventRecord(hp->done, hp->d2h)) != cudaSuccess) return cuda_fail(e, "record done");
+    if ((e = cudaStreamWaitEvent(st, hp->done, 0)) != cudaSuccess) return cuda_fail(e, "wait done");
     return ATTN_OK;
 }
 

@@ -79,15 +79,20 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
              int causal, float scale, int dtype, void *stream);
 
 /*
- * attn_fwd_host: attn_fwd for inputs and outputs in HOST memory, with the
- * host<->device copies on `stream`: copies q_host/k_host/v_host into the
- * caller's device buffers q_dev/k_dev/v_dev, runs attn_fwd into o_dev/lse_dev,
- * then copies O (and LSE when both lse pointers are non-NULL) back into
- * o_host/lse_host.  All buffers are caller-owned with the layouts of
- * attn_fwd; host buffers should be page-locked for the copies to be
- * asynchronous.  The call returns once everything is enqueued; the host
- * outputs are valid after the stream is synchronised.  Same error codes as
- * attn_fwd (copy failures give ATTN_ERR_CUDA).
+ * attn_fwd_host: attn_fwd for inputs and outputs in HOST memory: copies
+ * q_host/k_host/v_host into the caller's device buffers q_dev/k_dev/v_dev,
+ * runs attn_fwd into o_dev/lse_dev, then copies O (and LSE when both lse
+ * pointers are non-NULL) back into o_host/lse_host.  All buffers are
+ * caller-owned with the layouts of attn_fwd; host buffers should be
+ * page-locked for the copies to be asynchronous.  Problems of 64 MB and more
+ * are cut into up to 4 chunks of whole heads, and the copies in of one chunk
+ * and out of another overlap the forward of a third: the copies run on two
+ * streams the library creates once per device, the forwards on `stream`,
+ * ordered by events so that the whole operation comes after earlier work on
+ * `stream` and later work on `stream` comes after it.  The call returns once
+ * everything is enqueued; the host outputs are valid after `stream` is
+ * synchronised.  Same error codes as attn_fwd (copy failures give
+ * ATTN_ERR_CUDA).
  */
 int attn_fwd_host(const void *q_host, const void *k_host, const void *v_host,
                   void *o_host, float *lse_host,

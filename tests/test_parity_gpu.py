@@ -132,6 +132,27 @@ def test_host_entry_point_matches_device_entry_point():
     assert torch.equal(oh, od.cpu()) and torch.equal(lh, ld.cpu())
 
 
+@pytest.mark.parametrize("h,s", [(8, 8192), (7, 10000)])
+def test_host_entry_point_pipelined_chunks(h, s):
+    """Problems of 64 MB and more run as up to 4 chunks of heads with the
+    copies overlapping the forward (h = 7: chunks of 2, 2, 2 and 1 heads);
+    every head's result is the device entry point's, bit for bit, on a
+    caller stream that is not the default one."""
+    import attention_forward_14_gb300 as af
+    q, k, v = _draw(1, h, s, s, 128, "bf16", seed=19 + h)
+    dev = torch.device("cuda", 0)
+    od, ld = af.attn_fwd(q.to(dev), k.to(dev), v.to(dev), causal=True)
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    oh = torch.full_like(qh, float("nan")).pin_memory()
+    lh = torch.full(q.shape[:3], float("nan"), dtype=torch.float32).pin_memory()
+    bufs = [torch.empty_like(t, device=dev) for t in (q, k, v, q)]
+    lbuf = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    st = torch.cuda.Stream(dev)
+    af.attn_fwd_host(qh, kh, vh, oh, lh, *bufs, lbuf, causal=True, stream=st)
+    st.synchronize()
+    assert torch.equal(oh, od.cpu()) and torch.equal(lh, ld.cpu())
+
+
 def test_watchdog_reports_instead_of_hanging():
     """One K/V load is withheld: every wait runs out after 50 ms, the kernel
     records where, frees its resources and returns; the context stays usable."""

@@ -132,13 +132,30 @@ enum : uint32_t {
     SITE_BWD_DRAIN_SYNC = 38,
 };
 
+// Sizes for head dim D (64 or 128).  Tiles are always 128 rows (keys or
+// queries) of 128-byte swizzle panels of 64 elements.
+template <int D_>
 struct Cfg {
-    static constexpr int D = 128;
+    static constexpr int D = D_;
     static constexpr int BN = 128;                  // keys per unit = TMEM lanes
     static constexpr int BM = 128;                  // queries per tile
     static constexpr int PANEL_BYTES = 128 * 128;   // 128 rows x 128 B (64 elements)
-    static constexpr int TILE_BYTES = 2 * PANEL_BYTES;  // [128 rows][128 elements] of 16 bits
+    static constexpr int NPANEL = D / 64;
+    static constexpr int TILE_BYTES = NPANEL * PANEL_BYTES;  // a Q, K, V or dO tile [128 rows][D]
+    static constexpr int DS_BYTES = 2 * PANEL_BYTES;          // dS^T [128 keys][128 queries]
+    // D = 128: dQ^T = K^T dS^T (lanes = head dim), staged in the tile's dO
+    // slot.  D = 64: dQ = dS K (lanes = queries: an M = 64 product would
+    // have another accumulator layout), staged in a buffer of its own.
+    static constexpr bool DQ_T = (D == 128);
+    static constexpr int STAGE_BYTES = DQ_T ? 0 : BM * D * 4;
     static constexpr int NSTAGE = 2;
+    // rows of dQ per reduce-add when D = 128 (the staged half-tile of 64
+    // rows is sent as 64 / RED_ROWS bulk reduces)
+#ifndef ATTN_BWD_RED_ROWS
+#define ATTN_BWD_RED_ROWS 64
+#endif
+    static constexpr int RED_ROWS = ATTN_BWD_RED_ROWS;
+    static_assert(64 % RED_ROWS == 0, "reduce rows");
     // shared memory (offsets from a 1024-byte aligned base)
     static constexpr int CTL_OFF = 0;               // barriers, TMEM address, abort flag
     static constexpr int LD_OFF = 1024;             // per stage: lse2[128], dsum[128]
@@ -147,18 +164,24 @@ struct Cfg {
     static constexpr int V_OFF = K_OFF + TILE_BYTES;
     static constexpr int Q_OFF = V_OFF + TILE_BYTES;  // stage s: Q at Q_OFF + s*2*TILE, dO after it
     static constexpr int DS_OFF = Q_OFF + NSTAGE * 2 * TILE_BYTES;
-    static constexpr int SMEM_BYTES = DS_OFF + TILE_BYTES;
+    static constexpr int ST_OFF = DS_OFF + DS_BYTES;  // dQ staging (D = 64)
+    static constexpr int SMEM_BYTES = ST_OFF + STAGE_BYTES;
     // tensor memory columns
-    static constexpr int TM_DV = 0, TM_DK = 128, TM_S = 256, TM_DP = 384;
+    static constexpr int TM_DV = 0, TM_DK = D, TM_S = 2 * D, TM_DP = 2 * D + 128;
     static constexpr int TMEM_COLS = 512;
     static constexpr int THREADS = 512;
-    // setmaxnreg budgets: 2 x 128 softmax threads, 128 drain threads (all
-    // 128 dQ^T columns of a row in registers), 128 others;
-    // (144 + 144 + 136 + 88) * 128 = 512 * 128 registers at launch.
-    static constexpr int REGS_SOFTMAX = 144, REGS_DRAIN = 136, REGS_OTHER = 88;
+    // setmaxnreg budgets: 2 x 128 softmax threads, 128 drain threads (a
+    // dQ row of the tile in registers: 128 values for D = 128, 64 for
+    // D = 64), 128 others; both splits add up to 512 * 128 registers, the
+    // launch's 128 per thread: (144 + 144 + 136 + 88) and (152 + 152 + 120 + 88).
+    static constexpr int REGS_SOFTMAX = D == 128 ? 144 : 152;
+    static constexpr int REGS_DRAIN = D == 128 ? 136 : 120;
+    static constexpr int REGS_OTHER = 88;
     static_assert(LD_OFF + NSTAGE * LD_STAGE_BYTES <= K_OFF, "control / LSE area");
-    static_assert(K_OFF % 1024 == 0 && Q_OFF % 1024 == 0 && DS_OFF % 1024 == 0, "swizzle atoms need 1 KiB alignment");
+    static_assert(K_OFF % 1024 == 0 && V_OFF % 1024 == 0 && Q_OFF % 1024 == 0 && DS_OFF % 1024 == 0 &&
+                      ST_OFF % 1024 == 0, "swizzle atoms need 1 KiB alignment");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(TM_DP + 128 <= TMEM_COLS, "tensor memory budget");
     static_assert(REGS_SOFTMAX * 2 + REGS_DRAIN + REGS_OTHER == 4 * 128, "register split");
 };
 
@@ -339,11 +362,12 @@ __device__ __forceinline__ Unit decode_unit(int u, const BwdParams &p)
     const int gsz = min(p.group, p.bh - h0);
     un.kb = r / gsz;
     un.bh = h0 + (r - un.kb * gsz);
-    const int n_tiles = (p.sq + Cfg::BM - 1) / Cfg::BM;
+    constexpr int BM = 128, BN = 128;  // query tile, key block (both sizes)
+    const int n_tiles = (p.sq + BM - 1) / BM;
     int t0 = 0;
     if (CAUSAL) {
-        const int first_q = un.kb * Cfg::BN - (p.sk - p.sq);  // smallest query that sees key 128*kb
-        t0 = first_q > 0 ? first_q / Cfg::BM : 0;
+        const int first_q = un.kb * BN - (p.sk - p.sq);  // smallest query that sees key 128*kb
+        t0 = first_q > 0 ? first_q / BM : 0;
     }
     un.t0 = min(t0, n_tiles);
     un.n = n_tiles - un.t0;
@@ -397,21 +421,22 @@ __device__ __forceinline__ float2 unpack2<__half>(uint32_t u)
 
 // ---------------------------------------------------------------- prep
 
-// One query row per 16 threads: D = sum_c dO[c] O[c] (fp32), the row's
+// One query row per D/8 threads: D = sum_c dO[c] O[c] (fp32), the row's
 // LSE in base 2, and a zeroed accumulator row.  Rows sq..sq_pad-1 get the
 // padding values (LSE2 = +inf, so that P = 0 there, and D = 0).
-template <typename T>
+template <typename T, int D>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p)
 {
-    constexpr int D = Cfg::D;
-    // rows is even (sq_pad is a multiple of 128) and the two rows of a warp
-    // are 2k and 2k+1, so both halves of a warp run the same iterations and
-    // the 16-wide shuffles below always have their whole warp.
+    constexpr int TPR = D / 8;  // threads per row, 8 elements each
+    // rows is a multiple of 128 (sq_pad is) and the rows of a warp are
+    // consecutive, so all of a warp's rows run the same iterations and the
+    // TPR-wide shuffles below always have their whole warp.
     const int64_t rows = static_cast<int64_t>(p.bh) * p.sq_pad;
-    const int sub = threadIdx.x & 15;
+    const int sub = threadIdx.x % TPR;
+    const int shift = (TPR == 16) ? 4 : 3;
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.counter = 0;
-    for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4; r < rows;
-         r += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 4) {
+    for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> shift; r < rows;
+         r += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> shift) {
         const int64_t head = r / p.sq_pad;
         const int i = static_cast<int>(r - head * p.sq_pad);
         float acc = 0.f;
@@ -431,7 +456,7 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p)
             z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, 16);
+        for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, TPR);
         if (sub == 0) {
             float l2 = INFINITY;
             if (i < p.sq) {
@@ -460,17 +485,18 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_convert_kernel(const float *a
 
 // ---------------------------------------------------------------- main kernel
 
-template <typename T, bool CAUSAL>
+template <typename T, bool CAUSAL, int D>
 __global__ void __launch_bounds__(512, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmdQacc, const BwdParams p)
 {
-    using C = Cfg;
+    using C = Cfg<D>;
     constexpr bool BF16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t IDESC_S = idesc(128, C::BM, BF16, false, false);   // S^T, dP^T: [keys x queries]
     constexpr uint32_t IDESC_ACC = idesc(128, C::D, BF16, false, true);   // dV, dK: A from TMEM, B MN-major
-    constexpr uint32_t IDESC_DQ = idesc(C::D, C::BM, BF16, true, true);   // dQ^T: both MN-major
+    // dQ^T = K^T dS^T [D x queries] (D = 128) or dQ = dS K [queries x D] (D = 64); both operands MN-major
+    constexpr uint32_t IDESC_DQ = C::DQ_T ? idesc(C::D, C::BM, BF16, true, true) : idesc(C::BM, C::D, BF16, true, true);
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base_addr = smem_addr(smem_raw);
@@ -490,6 +516,7 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t sV = base_addr + C::V_OFF;
     const uint32_t sQ = base_addr + C::Q_OFF;  // stage s: Q at sQ + s*2*TILE, dO at + TILE
     const uint32_t sDS = base_addr + C::DS_OFF;
+    const uint32_t sST = base_addr + C::ST_OFF;  // dQ staging (D = 64)
     const float *ld_smem = reinterpret_cast<const float *>(smem_raw + C::LD_OFF);
 
     auto B = [&](const uint64_t &bar) { return smem_addr(&bar); };
@@ -566,7 +593,7 @@ __global__ void __launch_bounds__(512, 1)
                 if (!ok) break;
                 if (elect_one()) {
                     mbar_arrive_expect_tx(B(ctl->kv_full), 2 * C::TILE_BYTES);
-                    for (int pn = 0; pn < 2; ++pn) {
+                    for (int pn = 0; pn < C::NPANEL; ++pn) {
                         tma_load_3d(sK + pn * C::PANEL_BYTES, &tmK, B(ctl->kv_full), pn * 64, un.kb * C::BN, un.bh, pol);
                         tma_load_3d(sV + pn * C::PANEL_BYTES, &tmV, B(ctl->kv_full), pn * 64, un.kb * C::BN, un.bh, pol);
                     }
@@ -584,7 +611,7 @@ __global__ void __launch_bounds__(512, 1)
                     if (elect_one()) {
                         const uint32_t bar = B(ctl->q_full[st]);
                         mbar_arrive_expect_tx(bar, C::TILE_BYTES + 2 * C::BM * 4);
-                        for (int pn = 0; pn < 2; ++pn)
+                        for (int pn = 0; pn < C::NPANEL; ++pn)
                             tma_load_3d(q_tile + pn * C::PANEL_BYTES, &tmQ, bar, pn * 64, q0, un.bh, pol);
                         const size_t row = static_cast<size_t>(un.bh) * p.sq_pad + q0;
                         bulk_load(sLD + st * C::LD_STAGE_BYTES, p.lse2 + row, C::BM * 4, bar);
@@ -598,7 +625,7 @@ __global__ void __launch_bounds__(512, 1)
                     if (elect_one()) {
                         const uint32_t bar = B(ctl->do_full[st]);
                         mbar_arrive_expect_tx(bar, C::TILE_BYTES);
-                        for (int pn = 0; pn < 2; ++pn)
+                        for (int pn = 0; pn < C::NPANEL; ++pn)
                             tma_load_3d(q_tile + C::TILE_BYTES + pn * C::PANEL_BYTES, &tmdO, bar, pn * 64, q0, un.bh,
                                         pol);
                     }
@@ -619,8 +646,8 @@ __global__ void __launch_bounds__(512, 1)
             bool ok = true;
             const uint32_t dK0 = desc_lo(sK, 16);              // K, K-major (A of S^T)
             const uint32_t dV0 = desc_lo(sV, 16);              // V, K-major (A of dP^T)
-            const uint32_t dKt0 = desc_lo(sK, C::PANEL_BYTES); // K^T, MN-major (A of dQ^T)
-            const uint32_t dDS0 = desc_lo(sDS, C::PANEL_BYTES);// dS^T, MN-major (B of dQ^T)
+            const uint32_t dKt0 = desc_lo(sK, C::PANEL_BYTES); // K MN-major: A of dQ^T (D = 128), B of dQ (D = 64)
+            const uint32_t dDS0 = desc_lo(sDS, C::PANEL_BYTES);// dS^T MN-major: B of dQ^T, A of dQ
             auto kmajor_step = [](int kk) { return static_cast<uint32_t>(((kk >> 2) * C::PANEL_BYTES + (kk & 3) * 32) >> 4); };
             // [keys x queries] = A(K or V) . B(Q or dO)^T over the head dim
             auto issue_kq = [&](uint32_t a0, uint32_t b0, uint32_t d) {
@@ -635,11 +662,16 @@ __global__ void __launch_bounds__(512, 1)
                     mma_ts(d, a_tm + 64 * (s >> 2) + 8 * (s & 3), b0 + ((s * 16 * 128) >> 4), IDESC_ACC,
                            (accumulate || s > 0) ? 1u : 0u);
             };
-            // dQ^T [D x queries] = K^T . dS^T over the unit's keys
+            // dQ^T [D x queries] = K^T . dS^T, or dQ [queries x D] = dS . K, over the unit's keys
             auto issue_dq = [&](uint32_t d) {
 #pragma unroll
-                for (int s = 0; s < C::BN / 16; ++s)
-                    mma_ss(d, dKt0 + ((s * 16 * 128) >> 4), dDS0 + ((s * 16 * 128) >> 4), IDESC_DQ, s > 0 ? 1u : 0u);
+                for (int s = 0; s < C::BN / 16; ++s) {
+                    const uint32_t kt = dKt0 + ((s * 16 * 128) >> 4), ds = dDS0 + ((s * 16 * 128) >> 4);
+                    if constexpr (C::DQ_T)
+                        mma_ss(d, kt, ds, IDESC_DQ, s > 0 ? 1u : 0u);
+                    else
+                        mma_ss(d, ds, kt, IDESC_DQ, s > 0 ? 1u : 0u);
+                }
             };
             auto q_desc = [&](uint32_t st, bool dout, uint32_t lbo) {
                 return desc_lo(sQ + st * 2 * C::TILE_BYTES + (dout ? C::TILE_BYTES : 0), lbo);
@@ -745,14 +777,22 @@ __global__ void __launch_bounds__(512, 1)
             __syncwarp();
         }
     } else if (warp >= 8) {
-        regs_inc<C::REGS_DRAIN>();  // above the launch budget of 128
+        if constexpr (C::REGS_DRAIN > 128)
+            regs_inc<C::REGS_DRAIN>();
+        else
+            regs_dec<C::REGS_DRAIN>();
         // ---------------------------------------------------------------- dQ drain + dK/dV epilogue
-        // Per tile: dQ^T (this thread: head-dim column dcol, 128 queries)
-        // comes out of tensor memory, which is released at once; it is then
-        // staged as fp32 [64 queries][128] rows in the tile's dO slot (free:
-        // dP^T and dV have read it) and added into the accumulator by the
-        // copy engine, 64 rows per reduce.  The slot is handed back to the
-        // producer once the reduces have read it.
+        // Per tile the dQ product comes out of tensor memory, which is
+        // released at once, is staged as fp32 rows in shared memory and is
+        // added into the accumulator by the copy engine (TMA reduce-add).
+        //   D = 128: dQ^T, this thread holds head-dim column dcol for the 128
+        //            queries; staged as [64 queries][128] in the tile's dO
+        //            slot (free: dP^T and dV have read it), two halves.
+        //   D = 64:  dQ, this thread holds query row dcol's 64 columns;
+        //            staged in a buffer of its own as two [128][32] boxes
+        //            with the 128-byte swizzle (conflict-free row writes).
+        // The dO slot goes back to the producer once the reduces have read
+        // the staging.
         const int quad = warp & 3;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const int dcol = quad * 32 + lane;
@@ -779,25 +819,54 @@ __global__ void __launch_bounds__(512, 1)
                 BWD_TRACE(BEV_DR_GOT, tile_it);
                 ++tile_it;
                 tc_fence_after();
-                uint32_t v[128];
-                tmem_ld128_wait(tmem + lane_off + C::TM_DP, v);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(B(ctl->dq_empty));
-                BWD_TRACE(BEV_DR_RELEASED, tile_it);
                 const uint32_t st = q_it & 1u;
-                const uint32_t stage_buf = sQ + st * 2 * C::TILE_BYTES + C::TILE_BYTES;  // the dO slot
                 const int q0 = (un.t0 + t) * C::BM;
+                if constexpr (C::DQ_T) {
+                    uint32_t v[128];
+                    tmem_ld128_wait(tmem + lane_off + C::TM_DP, v);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(B(ctl->dq_empty));
+                    BWD_TRACE(BEV_DR_RELEASED, tile_it);
+                    const uint32_t stage_buf = sQ + st * 2 * C::TILE_BYTES + C::TILE_BYTES;  // the dO slot
 #pragma unroll
-                for (int h = 0; h < 2 && ok; ++h) {
-                    if (h == 1 && !(ok = drain_sync())) break;  // the first reduce has read the slot
+                    for (int h = 0; h < 2 && ok; ++h) {
+                        if (h == 1 && !(ok = drain_sync())) break;  // the first reduce has read the slot
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        st_shared_f32(stage_buf + (c * C::D + dcol) * 4, __uint_as_float(v[64 * h + c]));
+                        for (int c = 0; c < 64; ++c)
+                            st_shared_f32(stage_buf + (c * C::D + dcol) * 4, __uint_as_float(v[64 * h + c]));
+                        fence_proxy_async_smem();
+                        if (!(ok = drain_sync())) break;
+                        if (issuer) {
+#pragma unroll
+                            for (int r0 = 0; r0 < 64; r0 += C::RED_ROWS)
+                                tma_reduce_add_3d(&tmdQacc, stage_buf + r0 * C::D * 4, 0, q0 + 64 * h + r0, un.bh);
+                            bulk_commit_group();
+                            bulk_wait_read_all();
+                        }
+                    }
+                } else {
+                    uint32_t v[64];
+                    tmem_ld64_wait(tmem + lane_off + C::TM_DP, v);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(B(ctl->dq_empty));
+                    BWD_TRACE(BEV_DR_RELEASED, tile_it);
+                    // the previous tile's reduces have read the staging
+                    if (!(ok = drain_sync())) break;
+#pragma unroll
+                    for (int box = 0; box < 2; ++box)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const uint32_t chunk = static_cast<uint32_t>(c ^ (dcol & 7));
+                            st_shared_v4(sST + box * (C::BM * 128) + dcol * 128 + chunk * 16, v[32 * box + 4 * c],
+                                         v[32 * box + 4 * c + 1], v[32 * box + 4 * c + 2], v[32 * box + 4 * c + 3]);
+                        }
                     fence_proxy_async_smem();
                     if (!(ok = drain_sync())) break;
                     if (issuer) {
-                        tma_reduce_add_3d(&tmdQacc, stage_buf, 0, q0 + 64 * h, un.bh);
+                        tma_reduce_add_3d(&tmdQacc, sST, 0, q0, un.bh);
+                        tma_reduce_add_3d(&tmdQacc, sST + C::BM * 128, 32, q0, un.bh);
                         bulk_commit_group();
                         bulk_wait_read_all();
                     }

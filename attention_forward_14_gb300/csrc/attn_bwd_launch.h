@@ -12,21 +12,28 @@ namespace bwd {
 
 struct BwdLaunchArgs {
     CUtensorMap q, k, v, dout;
-    CUtensorMap dq_acc;  // fp32 [bh][sq][128], box 128 x 64 rows, no swizzle (reduce-add target)
+    CUtensorMap dq_acc;  // fp32 [bh][sq][D] reduce-add target (box and swizzle per Cfg<D>)
     BwdParams p;
     int grid;       // main kernel CTAs (persistent)
     int sm_count;
     cudaStream_t stream;
 };
 
-// prep -> main -> dQ convert, all on a.stream.  T: __half or __nv_bfloat16.
-template <typename T, bool CAUSAL>
+// prep -> main -> dQ convert, all on a.stream.  T: __half or __nv_bfloat16;
+// D: head dim 64 or 128.
+template <typename T, bool CAUSAL, int D>
 cudaError_t launch_bwd(const BwdLaunchArgs &a);
 
-extern template cudaError_t launch_bwd<__half, false>(const BwdLaunchArgs &);
-extern template cudaError_t launch_bwd<__half, true>(const BwdLaunchArgs &);
-extern template cudaError_t launch_bwd<__nv_bfloat16, false>(const BwdLaunchArgs &);
-extern template cudaError_t launch_bwd<__nv_bfloat16, true>(const BwdLaunchArgs &);
+#define ATTN_BWD_EXTERN(T, C, D) extern template cudaError_t launch_bwd<T, C, D>(const BwdLaunchArgs &);
+ATTN_BWD_EXTERN(__half, false, 64)
+ATTN_BWD_EXTERN(__half, true, 64)
+ATTN_BWD_EXTERN(__nv_bfloat16, false, 64)
+ATTN_BWD_EXTERN(__nv_bfloat16, true, 64)
+ATTN_BWD_EXTERN(__half, false, 128)
+ATTN_BWD_EXTERN(__half, true, 128)
+ATTN_BWD_EXTERN(__nv_bfloat16, false, 128)
+ATTN_BWD_EXTERN(__nv_bfloat16, true, 128)
+#undef ATTN_BWD_EXTERN
 
 }  // namespace bwd
 }  // namespace attn

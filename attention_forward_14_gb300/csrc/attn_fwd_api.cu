@@ -139,9 +139,10 @@ int make_map_packed(CUtensorMap *map, const void *ptr, int dtype, int64_t tokens
     return ATTN_OK;
 }
 
-// The backward's fp32 dQ accumulator [bh, sq, d] as 3-D [bh][sq][d] for
-// tile reduce-adds of 64 rows x d columns (row-major in shared memory, no
-// swizzle); rows past sq are clipped by the copy engine.
+// The backward's fp32 dQ accumulator [bh, sq, d] as 3-D [bh][sq][d] for the
+// tile reduce-adds: d = 128, RED_ROWS rows x 128 columns, row-major in
+// shared memory (no swizzle); d = 64, 128 rows x 32 columns with the
+// 128-byte swizzle.  Rows past sq are clipped by the copy engine.
 int make_map_f32_rows(CUtensorMap *map, void *ptr, int64_t bh, int64_t s, int64_t d)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
@@ -149,10 +150,12 @@ int make_map_f32_rows(CUtensorMap *map, void *ptr, int64_t bh, int64_t s, int64_
     if (rc != ATTN_OK) return rc;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(s), static_cast<cuuint64_t>(bh)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 4), static_cast<cuuint64_t>(s * d * 4)};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 64, 1};
+    const bool wide = d == 128;
+    cuuint32_t box[3] = {wide ? 128u : 32u, wide ? static_cast<cuuint32_t>(bwd::Cfg<128>::RED_ROWS) : 128u, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     wide ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (fp32 rows) failed (CUresult %d)", static_cast<int>(r));
     return ATTN_OK;
 }
@@ -286,7 +289,7 @@ constexpr uint64_t kDefaultTimeoutNs = 2000ull * 1000ull * 1000ull;  // 2 s per 
 // stream, ordered by events.  The streams and events are created once per
 // device; a mutex keeps one call's record/wait sequence together.
 
-constexpr int kPipeChunks = 4;
+constexpr int kPipeChunks = 8;
 constexpr int64_t kPipeMinBytes = int64_t(64) << 20;  // smaller problems: one chunk
 
 struct HostPipe {
@@ -356,7 +359,7 @@ int run_bwd(const void *q, const void *k, const void *v, const void *o, const vo
         return fail(ATTN_ERR_SHAPE, "sequence length above 2^30: sq=%lld sk=%lld", (long long)sq, (long long)sk);
     if (b > 0 && h >= (int64_t(1) << 31) / b)
         return fail(ATTN_ERR_SHAPE, "b*h not below 2^31: b=%lld h=%lld", (long long)b, (long long)h);
-    if (d != 128) return fail(ATTN_ERR_HEADDIM, "backward: head dim %lld not supported (128)", (long long)d);
+    if (d != 64 && d != 128) return fail(ATTN_ERR_HEADDIM, "backward: head dim %lld not supported (64 or 128)", (long long)d);
     if (dtype != ATTN_FP16 && dtype != ATTN_BF16) return fail(ATTN_ERR_DTYPE, "dtype %d is not fp16 (0) or bf16 (1)", dtype);
     if (!std::isfinite(scale)) return fail(ATTN_ERR_SCALE, "scale is not finite");
     const int64_t bh = b * h;
@@ -423,10 +426,17 @@ int run_bwd(const void *q, const void *k, const void *v, const void *o, const vo
     a.grid = p.num_units < di->sm_count ? p.num_units : di->sm_count;
     a.sm_count = di->sm_count;
     a.stream = stream;
-    if (dtype == ATTN_BF16)
-        e = causal ? bwd::launch_bwd<__nv_bfloat16, true>(a) : bwd::launch_bwd<__nv_bfloat16, false>(a);
-    else
-        e = causal ? bwd::launch_bwd<__half, true>(a) : bwd::launch_bwd<__half, false>(a);
+    if (d == 128) {
+        if (dtype == ATTN_BF16)
+            e = causal ? bwd::launch_bwd<__nv_bfloat16, true, 128>(a) : bwd::launch_bwd<__nv_bfloat16, false, 128>(a);
+        else
+            e = causal ? bwd::launch_bwd<__half, true, 128>(a) : bwd::launch_bwd<__half, false, 128>(a);
+    } else {
+        if (dtype == ATTN_BF16)
+            e = causal ? bwd::launch_bwd<__nv_bfloat16, true, 64>(a) : bwd::launch_bwd<__nv_bfloat16, false, 64>(a);
+        else
+            e = causal ? bwd::launch_bwd<__half, true, 64>(a) : bwd::launch_bwd<__half, false, 64>(a);
+    }
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "backward launch");
 }
 
@@ -800,7 +810,7 @@ int64_t attn_bwd_workspace_bytes(int64_t b, int64_t h, int64_t sq, int64_t d)
     g_err.clear();
     if (b < 0 || h < 0 || sq < 0 || sq > kMaxSeq || (b > 0 && h >= (int64_t(1) << 31) / b))
         return fail(ATTN_ERR_SHAPE, "invalid backward workspace query");
-    if (d != 128) return fail(ATTN_ERR_HEADDIM, "backward: head dim %lld not supported (128)", (long long)d);
+    if (d != 64 && d != 128) return fail(ATTN_ERR_HEADDIM, "backward: head dim %lld not supported (64 or 128)", (long long)d);
     return bwd_workspace_bytes(b * h, sq, d);
 }
 

@@ -215,7 +215,7 @@ class BwdWorkload:
 
     def bytes(self) -> int:
         w = self.w
-        e = 2
+        e = 2  # 16-bit inputs and gradients
         # read q, k, v, o, dO, lse; write dq, dk, dv
         return (e * w.b * w.h * (3 * w.sq * w.d + 2 * w.sk * w.d) + 4 * w.b * w.h * w.sq
                 + e * w.b * w.h * (w.sq * w.d + 2 * w.sk * w.d))
@@ -224,4 +224,5 @@ class BwdWorkload:
 BWD = {bw.name: bw for bw in [
     BwdWorkload("causal_b1_h32_s16384_d128_bf16_qk3", 20260008),
     BwdWorkload("causal_b2_h32_s4096_d128_bf16", 20260009),
+    BwdWorkload("noncausal_b8_h16_s1000_d64_bf16", 20260010),
 ]}

@@ -85,7 +85,7 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
  * pointers are non-NULL) back into o_host/lse_host.  All buffers are
  * caller-owned with the layouts of attn_fwd; host buffers should be
  * page-locked for the copies to be asynchronous.  Problems of 64 MB and more
- * are cut into up to 4 chunks of whole heads, and the copies in of one chunk
+ * are cut into up to 8 chunks of whole heads, and the copies in of one chunk
  * and out of another overlap the forward of a third: the copies run on two
  * streams the library creates once per device, the forwards on `stream`,
  * ordered by events so that the whole operation comes after earlier work on
@@ -236,7 +236,7 @@ int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v,
  *   o, lse         : the forward's outputs for these q, k, v; D is computed
  *                    from o (so an o rounded to dtype carries that rounding
  *                    into D).
- *   d              : 128 only (ATTN_ERR_HEADDIM otherwise).
+ *   d              : 64 or 128 (ATTN_ERR_HEADDIM otherwise).
  *   workspace      : caller-owned device scratch, 16-byte aligned, of at
  *                    least attn_bwd_workspace_bytes(b, h, sq, d) bytes (an
  *                    fp32 dQ accumulator, two fp32 values per query row

@@ -111,7 +111,7 @@ def call_bwd(lib, b=1, h=1, sq=4, sk=4, d=128, causal=0, scale=0.1, dtype=1, ws=
 
 
 def test_bwd_rejects_bad_arguments(lib):
-    assert call_bwd(lib, d=64)[0] == -3
+    assert call_bwd(lib, d=96)[0] == -3
     assert call_bwd(lib, dtype=7)[0] == -4
     assert call_bwd(lib, b=-1)[0] == -2
     assert call_bwd(lib, sq=(1 << 30) + 1)[0] == -2
@@ -128,5 +128,6 @@ def test_bwd_workspace_bytes(lib):
     # + the scheduler's counter
     assert lib.attn_bwd_workspace_bytes(2, 3, 300, 128) == 6 * 300 * 128 * 4 + 2 * 6 * 384 * 4 + 256
     assert lib.attn_bwd_workspace_bytes(1, 1, 0, 128) == 256
-    assert lib.attn_bwd_workspace_bytes(1, 1, 4, 64) == -3
+    assert lib.attn_bwd_workspace_bytes(1, 1, 4, 96) == -3
+    assert lib.attn_bwd_workspace_bytes(1, 1, 128, 64) == 128 * 64 * 4 + 2 * 128 * 4 + 256
     assert lib.attn_bwd_workspace_bytes(-1, 1, 4, 128) == -2

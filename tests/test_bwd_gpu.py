@@ -20,9 +20,9 @@ pytestmark = pytest.mark.gpu
 DT = {"bf16": torch.bfloat16, "fp16": torch.float16}
 
 
-def _draw(b, h, sq, sk, dtype, seed, qk_std=1.0):
-    q, k, v = W.draw(b, h, sq, sk, 128, dtype, seed, qk_std)
-    do = W.draw_grad(b, h, sq, 128, dtype, seed + 1000)
+def _draw(b, h, sq, sk, dtype, seed, qk_std=1.0, d=128):
+    q, k, v = W.draw(b, h, sq, sk, d, dtype, seed, qk_std)
+    do = W.draw_grad(b, h, sq, d, dtype, seed + 1000)
     return q, k, v, do
 
 
@@ -63,24 +63,31 @@ def _check_all(q, k, v, do, causal, scale, dtype, what):
 
 
 SHAPES = [
-    # b, h, sq, sk, dtype, causal
-    (1, 2, 128, 128, "bf16", False),
-    (1, 2, 128, 128, "bf16", True),
-    (2, 3, 300, 300, "bf16", True),      # ragged tail, several key blocks
-    (1, 2, 257, 385, "fp16", False),     # sq != sk, ragged both
-    (1, 2, 385, 257, "fp16", True),      # sq > sk: rows that see no key
-    (1, 2, 257, 385, "bf16", True),      # sq < sk, bottom-right causal
-    (1, 1, 1, 1, "bf16", False),
-    (1, 1, 1, 200, "fp16", True),
-    (1, 2, 1000, 1000, "bf16", True),
-    (2, 2, 640, 640, "fp16", False),
+    # b, h, sq, sk, dtype, causal, d
+    (1, 2, 128, 128, "bf16", False, 128),
+    (1, 2, 128, 128, "bf16", True, 128),
+    (2, 3, 300, 300, "bf16", True, 128),      # ragged tail, several key blocks
+    (1, 2, 257, 385, "fp16", False, 128),     # sq != sk, ragged both
+    (1, 2, 385, 257, "fp16", True, 128),      # sq > sk: rows that see no key
+    (1, 2, 257, 385, "bf16", True, 128),      # sq < sk, bottom-right causal
+    (1, 1, 1, 1, "bf16", False, 128),
+    (1, 1, 1, 200, "fp16", True, 128),
+    (1, 2, 1000, 1000, "bf16", True, 128),
+    (2, 2, 640, 640, "fp16", False, 128),
+    # head dim 64: dQ = dS K with the queries on the lanes
+    (1, 2, 128, 128, "bf16", False, 64),
+    (2, 3, 300, 300, "bf16", True, 64),
+    (1, 2, 257, 385, "fp16", False, 64),
+    (1, 2, 385, 257, "fp16", True, 64),
+    (1, 1, 1, 200, "bf16", True, 64),
+    (2, 2, 1000, 1000, "bf16", False, 64),
 ]
 
 
-@pytest.mark.parametrize("b,h,sq,sk,dtype,causal", SHAPES)
-def test_bwd_matches_oracle(b, h, sq, sk, dtype, causal):
-    q, k, v, do = _draw(b, h, sq, sk, dtype, 31000 + sq + 7 * sk + int(causal))
-    _check_all(q, k, v, do, causal, 1.0 / math.sqrt(128), dtype, f"b{b} h{h} sq{sq} sk{sk} {dtype} c{int(causal)}")
+@pytest.mark.parametrize("b,h,sq,sk,dtype,causal,d", SHAPES)
+def test_bwd_matches_oracle(b, h, sq, sk, dtype, causal, d):
+    q, k, v, do = _draw(b, h, sq, sk, dtype, 31000 + sq + 7 * sk + int(causal) + d, d=d)
+    _check_all(q, k, v, do, causal, 1.0 / math.sqrt(d), dtype, f"b{b} h{h} sq{sq} sk{sk} {dtype} c{int(causal)} d{d}")
 
 
 @pytest.mark.parametrize("scale", [0.0, -0.07, 0.3])

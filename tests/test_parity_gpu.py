@@ -134,8 +134,8 @@ def test_host_entry_point_matches_device_entry_point():
 
 @pytest.mark.parametrize("h,s", [(8, 8192), (7, 10000)])
 def test_host_entry_point_pipelined_chunks(h, s):
-    """Problems of 64 MB and more run as up to 4 chunks of heads with the
-    copies overlapping the forward (h = 7: chunks of 2, 2, 2 and 1 heads);
+    """Problems of 64 MB and more run as up to 8 chunks of heads with the
+    copies overlapping the forward (h = 7: seven chunks of one head);
     every head's result is the device entry point's, bit for bit, on a
     caller stream that is not the default one."""
     import attention_forward_14_gb300 as af

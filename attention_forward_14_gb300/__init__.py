@@ -8,6 +8,7 @@ is no fallback path.
 from .binding import (  # noqa: F401
     AttnError,
     attn_bwd,
+    attn_bwd_varlen,
     attn_fwd,
     attn_fwd_fp8,
     attn_fwd_host,

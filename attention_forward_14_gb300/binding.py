@@ -23,7 +23,8 @@ ERRORS = {
 # Every function include/attn_fwd.h declares.
 EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_fwd_varlen", "attn_fwd_fp8", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
            "attn_fwd_splitkv_default_splits", "attn_fwd_splitkv_noalloc", "attn_last_error", "attn_fwd_status", "attn_fwd_status_clear",
-           "attn_fwd_watchdog_selftest", "attn_version", "attn_bwd", "attn_bwd_workspace_bytes"]
+           "attn_fwd_watchdog_selftest", "attn_version", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_varlen",
+           "attn_bwd_varlen_workspace_bytes"]
 
 
 class AttnError(RuntimeError):
@@ -75,6 +76,11 @@ def _bind(lib):
                              vp, i64, vp]
     lib.attn_bwd_workspace_bytes.restype = i64
     lib.attn_bwd_workspace_bytes.argtypes = [i64, i64, i64, i64]
+    lib.attn_bwd_varlen.restype = c_int
+    lib.attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64,
+                                    c_int, c_float, c_int, vp, i64, vp]
+    lib.attn_bwd_varlen_workspace_bytes.restype = i64
+    lib.attn_bwd_varlen_workspace_bytes.argtypes = [i64, i64, i64, i64, i64]
     return lib
 
 
@@ -350,5 +356,45 @@ def attn_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = 
                           dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), b, h, sq, sk, d, int(bool(causal)),
                           float(scale), _dtype_code(q), workspace.data_ptr(),
                           workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
+    _check(rc, lib)
+    return dq, dk, dv
+
+
+def attn_bwd_varlen(q, k, v, o, dout, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                    causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None, workspace=None,
+                    stream=None):
+    """Gradients (dq, dk, dv) of attn_fwd_varlen.  q, o, dout: [total_q, h, d];
+    k, v: [total_k, h, d] of one dtype; lse: fp32 [h, total_q];
+    cu_seqlens_q / _k: int32 CUDA tensors [batch + 1]."""
+    import torch
+    lib = load()
+    total_q, h, d = q.shape
+    total_k = k.shape[0]
+    batch = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != batch + 1 or tuple(k.shape) != (total_k, h, d) or tuple(v.shape) != (total_k, h, d) \
+            or o.shape != q.shape or dout.shape != q.shape or tuple(lse.shape) != (h, total_q):
+        raise AttnError(-2, "shape mismatch among q, k, v, o, dout, lse, cu_seqlens")
+    if scale is None:
+        scale = 1.0 / float(d) ** 0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        need = _check(int(lib.attn_bwd_varlen_workspace_bytes(batch, h, total_q, max_seqlen_q, d)), lib)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout), ("lse", lse), ("dq", dq), ("dk", dk),
+                    ("dv", dv), ("workspace", workspace), ("cu_seqlens_q", cu_seqlens_q),
+                    ("cu_seqlens_k", cu_seqlens_k)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise AttnError(-2, f"{name} must be a contiguous CUDA tensor")
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+        raise AttnError(-4, "cu_seqlens must be int32")
+    with torch.cuda.device(q.device):
+        rc = lib.attn_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                                 lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), cu_seqlens_q.data_ptr(),
+                                 cu_seqlens_k.data_ptr(), batch, h, total_q, total_k, int(max_seqlen_q),
+                                 int(max_seqlen_k), d, int(bool(causal)), float(scale), _dtype_code(q),
+                                 workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                 _stream_handle(stream, q.device))
     _check(rc, lib)
     return dq, dk, dv

@@ -1,5 +1,7 @@
 // Instances of the attention backward: {fp16, bf16} x {causal, not} x head
-// dim {64, 128}, and the launch sequence prep -> main -> dQ convert.
+// dim {64, 128} for the dense layout (ATTN_BWD_INST_VARLEN unset) or the
+// packed one (attn_bwd_inst_varlen.cu sets it), and the launch sequence
+// prep -> main -> dQ convert.
 #include <atomic>
 
 #include "attn_bwd_launch.h"
@@ -7,7 +9,7 @@
 namespace attn {
 namespace bwd {
 
-template <typename T, bool CAUSAL, int D>
+template <typename T, bool CAUSAL, int D, bool VARLEN>
 cudaError_t launch_bwd(const BwdLaunchArgs &a)
 {
     // The shared-memory opt-in is a per-device property of the function:
@@ -18,7 +20,7 @@ cudaError_t launch_bwd(const BwdLaunchArgs &a)
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(attr_set.load() & bit)) {
-        e = cudaFuncSetAttribute(attn_bwd_kernel<T, CAUSAL, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(attn_bwd_kernel<T, CAUSAL, D, VARLEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg<D>::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set.fetch_or(bit);
@@ -26,12 +28,14 @@ cudaError_t launch_bwd(const BwdLaunchArgs &a)
     const int64_t prep_rows = static_cast<int64_t>(a.p.bh) * a.p.sq_pad;
     int prep_blocks = static_cast<int>((prep_rows * (D / 8) + 255) / 256);
     if (prep_blocks > 8 * a.sm_count) prep_blocks = 8 * a.sm_count;
-    attn_bwd_prep_kernel<T, D><<<prep_blocks, 256, 0, a.stream>>>(a.p);
+    attn_bwd_prep_kernel<T, D, VARLEN><<<prep_blocks, 256, 0, a.stream>>>(a.p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    attn_bwd_kernel<T, CAUSAL, D><<<a.grid, Cfg<D>::THREADS, Cfg<D>::SMEM_BYTES, a.stream>>>(a.q, a.k, a.v, a.dout,
+    attn_bwd_kernel<T, CAUSAL, D, VARLEN><<<a.grid, Cfg<D>::THREADS, Cfg<D>::SMEM_BYTES, a.stream>>>(a.q, a.k, a.v, a.dout,
                                                                                               a.dq_acc, a.p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const int64_t n8 = static_cast<int64_t>(a.p.bh) * a.p.sq * D / 8;
+    // dQ rows: [bh, sq] dense, [total_q, heads] packed
+    const int64_t dq_rows = a.p.cu_q ? static_cast<int64_t>(a.p.total_q) * a.p.heads : static_cast<int64_t>(a.p.bh) * a.p.sq;
+    const int64_t n8 = dq_rows * D / 8;
     int cv_blocks = static_cast<int>((n8 + 255) / 256);
     if (cv_blocks > 8 * a.sm_count) cv_blocks = 8 * a.sm_count;
     if (cv_blocks < 1) cv_blocks = 1;
@@ -39,14 +43,20 @@ cudaError_t launch_bwd(const BwdLaunchArgs &a)
     return cudaGetLastError();
 }
 
-template cudaError_t launch_bwd<__half, false, 64>(const BwdLaunchArgs &);
-template cudaError_t launch_bwd<__half, true, 64>(const BwdLaunchArgs &);
-template cudaError_t launch_bwd<__nv_bfloat16, false, 64>(const BwdLaunchArgs &);
-template cudaError_t launch_bwd<__nv_bfloat16, true, 64>(const BwdLaunchArgs &);
-template cudaError_t launch_bwd<__half, false, 128>(const BwdLaunchArgs &);
-template cudaError_t launch_bwd<__half, true, 128>(const BwdLaunchArgs &);
-template cudaError_t launch_bwd<__nv_bfloat16, false, 128>(const BwdLaunchArgs &);
-template cudaError_t launch_bwd<__nv_bfloat16, true, 128>(const BwdLaunchArgs &);
+
+#ifndef ATTN_BWD_INST_VARLEN
+#define ATTN_BWD_INST_VARLEN false
+#endif
+#define ATTN_BWD_INST(T, C, D) template cudaError_t launch_bwd<T, C, D, ATTN_BWD_INST_VARLEN>(const BwdLaunchArgs &);
+ATTN_BWD_INST(__half, false, 64)
+ATTN_BWD_INST(__half, true, 64)
+ATTN_BWD_INST(__nv_bfloat16, false, 64)
+ATTN_BWD_INST(__nv_bfloat16, true, 64)
+ATTN_BWD_INST(__half, false, 128)
+ATTN_BWD_INST(__half, true, 128)
+ATTN_BWD_INST(__nv_bfloat16, false, 128)
+ATTN_BWD_INST(__nv_bfloat16, true, 128)
+#undef ATTN_BWD_INST
 
 }  // namespace bwd
 }  // namespace attn

@@ -75,6 +75,16 @@ struct BwdParams {
     int32_t num_units;     // bh * num_kblk
     int32_t group;         // heads per scheduling group (see decode_unit)
     int32_t *counter;      // next unit to hand out (zeroed by the prep kernel)
+    // Varlen (packed sequences): cu_q / cu_k are the batch+1 cumulative
+    // offsets (device int32).  Q, O, dO, dQ and the dQ accumulator are
+    // [total_q, heads, D]; K, V, dK, dV [total_k, heads, D]; LSE [heads,
+    // total_q].  bh is then batch * heads (sequence-major), sq / sk the
+    // maximum lengths, and lse2 / dsum are [bh, sq_pad] per sequence.
+    // nullptr: the dense [b, h, s, D] layout.
+    const int32_t *cu_q;
+    const int32_t *cu_k;
+    int32_t heads;
+    int32_t total_q, total_k;
     float sl2e;            // scale * log2(e)
     float scale;           // folded into dS
     uint64_t timeout_ns;
@@ -338,10 +348,15 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 // ---------------------------------------------------------------- schedule
 
 struct Unit {
-    int bh;   // head plane
-    int kb;   // key block (keys 128*kb ..)
-    int t0;   // first query tile that sees a key of the block
-    int n;    // number of query tiles
+    int bh;      // (sequence, head) index: rows of lse2 / dsum; dense: the head plane
+    int head;    // varlen: head index (a TMA coordinate of the packed maps)
+    int kb;      // key block (keys 128*kb ..)
+    int sq, sk;  // query / key length of the unit's sequence
+    int q_tok0;  // varlen: token of query 0 / key 0 of the sequence (else 0)
+    int k_tok0;
+    int t0;      // first query tile that sees a key of the block
+    int n;       // number of query tiles (0: no work for the MMAs)
+    bool zero;   // the block has keys but the sequence has no query: dK = dV = 0
 };
 
 // Units are handed out in order from a global counter (dynamic
@@ -351,7 +366,7 @@ struct Unit {
 // the host to stay in L2 while its units run, and the light blocks of the
 // last group fill the tail.  Key j sees query i iff j <= i + (sk - sq)
 // (bottom-right alignment, as in the forward).
-template <bool CAUSAL>
+template <bool CAUSAL, bool VARLEN>
 __device__ __forceinline__ Unit decode_unit(int u, const BwdParams &p)
 {
     Unit un;
@@ -362,15 +377,34 @@ __device__ __forceinline__ Unit decode_unit(int u, const BwdParams &p)
     const int gsz = min(p.group, p.bh - h0);
     un.kb = r / gsz;
     un.bh = h0 + (r - un.kb * gsz);
+    if constexpr (VARLEN) {
+        const int seq = un.bh / p.heads;
+        un.head = un.bh - seq * p.heads;
+        un.q_tok0 = p.cu_q[seq];
+        un.sq = p.cu_q[seq + 1] - un.q_tok0;
+        un.k_tok0 = p.cu_k[seq];
+        un.sk = p.cu_k[seq + 1] - un.k_tok0;
+        // offsets outside the packed tensors: treat as an empty sequence
+        if (un.q_tok0 < 0 || un.sq < 0 || un.q_tok0 + un.sq > p.total_q || un.k_tok0 < 0 || un.sk < 0 ||
+            un.k_tok0 + un.sk > p.total_k)
+            un.sq = un.sk = 0;
+    } else {
+        un.head = 0;
+        un.q_tok0 = un.k_tok0 = 0;
+        un.sq = p.sq;
+        un.sk = p.sk;
+    }
     constexpr int BM = 128, BN = 128;  // query tile, key block (both sizes)
-    const int n_tiles = (p.sq + BM - 1) / BM;
+    const bool has_keys = un.kb * BN < un.sk;
+    const int n_tiles = has_keys ? (un.sq + BM - 1) / BM : 0;
     int t0 = 0;
     if (CAUSAL) {
-        const int first_q = un.kb * BN - (p.sk - p.sq);  // smallest query that sees key 128*kb
+        const int first_q = un.kb * BN - (un.sk - un.sq);  // smallest query that sees key 128*kb
         t0 = first_q > 0 ? first_q / BM : 0;
     }
     un.t0 = min(t0, n_tiles);
     un.n = n_tiles - un.t0;
+    un.zero = has_keys && un.n == 0;
     return un;
 }
 
@@ -422,9 +456,10 @@ __device__ __forceinline__ float2 unpack2<__half>(uint32_t u)
 // ---------------------------------------------------------------- prep
 
 // One query row per D/8 threads: D = sum_c dO[c] O[c] (fp32), the row's
-// LSE in base 2, and a zeroed accumulator row.  Rows sq..sq_pad-1 get the
-// padding values (LSE2 = +inf, so that P = 0 there, and D = 0).
-template <typename T, int D>
+// LSE in base 2, and a zeroed accumulator row.  Rows past the sequence's
+// query count (up to sq_pad) get the padding values (LSE2 = +inf, so that
+// P = 0 there, and D = 0).
+template <typename T, int D, bool VARLEN>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p)
 {
     constexpr int TPR = D / 8;  // threads per row, 8 elements each
@@ -437,11 +472,27 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p)
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.counter = 0;
     for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> shift; r < rows;
          r += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> shift) {
-        const int64_t head = r / p.sq_pad;
-        const int i = static_cast<int>(r - head * p.sq_pad);
+        const int64_t bh = r / p.sq_pad;  // (sequence, head) when packed; the head plane when dense
+        const int i = static_cast<int>(r - bh * p.sq_pad);
+        // where query row i of this (sequence, head) lives
+        int sq = p.sq;
+        int64_t elem, lse_at;  // element offset of the row in O / dO / dQ, and its LSE index
+        if constexpr (VARLEN) {
+            const int seq = static_cast<int>(bh / p.heads);
+            const int head = static_cast<int>(bh - static_cast<int64_t>(seq) * p.heads);
+            const int tok0 = p.cu_q[seq];
+            sq = p.cu_q[seq + 1] - tok0;
+            if (tok0 < 0 || sq < 0 || tok0 + sq > p.total_q) sq = 0;  // as the main kernel: an empty sequence
+            elem = (static_cast<int64_t>(tok0 + i) * p.heads + head) * D;
+            lse_at = static_cast<int64_t>(head) * p.total_q + tok0 + i;
+        } else {
+            elem = (bh * p.sq + i) * D;
+            lse_at = bh * p.sq + i;
+        }
+        const bool valid = i < sq;
         float acc = 0.f;
-        if (i < p.sq) {
-            const int64_t off = (head * p.sq + i) * D + sub * 8;
+        if (valid) {
+            const int64_t off = elem + sub * 8;
             const uint4 a = *reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.o) + off);
             const uint4 b = *reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.dout) + off);
             const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
@@ -459,12 +510,12 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p)
         for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, TPR);
         if (sub == 0) {
             float l2 = INFINITY;
-            if (i < p.sq) {
-                const float l = p.lse[head * p.sq + i];
+            if (valid) {
+                const float l = p.lse[lse_at];
                 l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
             }
             p.lse2[r] = l2;
-            p.dsum[r] = (i < p.sq) ? acc : 0.f;
+            p.dsum[r] = valid ? acc : 0.f;
         }
     }
 }
@@ -485,7 +536,7 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_convert_kernel(const float *a
 
 // ---------------------------------------------------------------- main kernel
 
-template <typename T, bool CAUSAL, int D>
+template <typename T, bool CAUSAL, int D, bool VARLEN>
 __global__ void __launch_bounds__(512, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -587,15 +638,25 @@ __global__ void __launch_bounds__(512, 1)
                 }
                 u = __shfl_sync(0xffffffffu, u, 0);
                 if (u < 0) break;
-                const Unit un = decode_unit<CAUSAL>(u, p);
+                const Unit un = decode_unit<CAUSAL, VARLEN>(u, p);
                 if (un.n == 0) continue;
+                // TMA coordinates after the 64-column panel: dense maps are
+                // [bh][s][D] (row, plane = bh); packed maps are [token][head][D]
+                // (row = head, plane = token).
+                constexpr bool vl = VARLEN;
+                auto qrow = [&](int r) { return vl ? un.head : r; };
+                auto qplane = [&](int r) { return vl ? un.q_tok0 + r : un.bh; };
+                auto krow = [&](int r) { return vl ? un.head : r; };
+                auto kplane = [&](int r) { return vl ? un.k_tok0 + r : un.bh; };
                 ok = warp_wait(B(ctl->kv_empty), (un_it & 1u) ^ 1u, ctl, p, SITE_BWD_LOAD_KV_EMPTY);
                 if (!ok) break;
                 if (elect_one()) {
                     mbar_arrive_expect_tx(B(ctl->kv_full), 2 * C::TILE_BYTES);
                     for (int pn = 0; pn < C::NPANEL; ++pn) {
-                        tma_load_3d(sK + pn * C::PANEL_BYTES, &tmK, B(ctl->kv_full), pn * 64, un.kb * C::BN, un.bh, pol);
-                        tma_load_3d(sV + pn * C::PANEL_BYTES, &tmV, B(ctl->kv_full), pn * 64, un.kb * C::BN, un.bh, pol);
+                        tma_load_3d(sK + pn * C::PANEL_BYTES, &tmK, B(ctl->kv_full), pn * 64, krow(un.kb * C::BN),
+                                    kplane(un.kb * C::BN), pol);
+                        tma_load_3d(sV + pn * C::PANEL_BYTES, &tmV, B(ctl->kv_full), pn * 64, krow(un.kb * C::BN),
+                                    kplane(un.kb * C::BN), pol);
                     }
                 }
                 __syncwarp();
@@ -612,7 +673,7 @@ __global__ void __launch_bounds__(512, 1)
                         const uint32_t bar = B(ctl->q_full[st]);
                         mbar_arrive_expect_tx(bar, C::TILE_BYTES + 2 * C::BM * 4);
                         for (int pn = 0; pn < C::NPANEL; ++pn)
-                            tma_load_3d(q_tile + pn * C::PANEL_BYTES, &tmQ, bar, pn * 64, q0, un.bh, pol);
+                            tma_load_3d(q_tile + pn * C::PANEL_BYTES, &tmQ, bar, pn * 64, qrow(q0), qplane(q0), pol);
                         const size_t row = static_cast<size_t>(un.bh) * p.sq_pad + q0;
                         bulk_load(sLD + st * C::LD_STAGE_BYTES, p.lse2 + row, C::BM * 4, bar);
                         bulk_load(sLD + st * C::LD_STAGE_BYTES + C::BM * 4, p.dsum + row, C::BM * 4, bar);
@@ -626,8 +687,8 @@ __global__ void __launch_bounds__(512, 1)
                         const uint32_t bar = B(ctl->do_full[st]);
                         mbar_arrive_expect_tx(bar, C::TILE_BYTES);
                         for (int pn = 0; pn < C::NPANEL; ++pn)
-                            tma_load_3d(q_tile + C::TILE_BYTES + pn * C::PANEL_BYTES, &tmdO, bar, pn * 64, q0, un.bh,
-                                        pol);
+                            tma_load_3d(q_tile + C::TILE_BYTES + pn * C::PANEL_BYTES, &tmdO, bar, pn * 64, qrow(q0),
+                                        qplane(q0), pol);
                     }
                     __syncwarp();
                     ++q_it;
@@ -681,7 +742,7 @@ __global__ void __launch_bounds__(512, 1)
                 int u;
                 if (!(ok = next_unit(kq, u, ctl, p))) break;
                 if (u < 0) break;
-                const Unit un = decode_unit<CAUSAL>(u, p);
+                const Unit un = decode_unit<CAUSAL, VARLEN>(u, p);
                 if (un.n == 0) continue;
                 if (!(ok = warp_wait(B(ctl->kv_full), un_it & 1u, ctl, p, SITE_BWD_MMA_KV_FULL))) break;
                 if (!(ok = warp_wait(B(ctl->q_full[q_it & 1u]), (q_it >> 1) & 1u, ctl, p, SITE_BWD_MMA_Q_FULL))) break;
@@ -811,8 +872,27 @@ __global__ void __launch_bounds__(512, 1)
             int u;
             if (!(ok = next_unit(kq, u, ctl, p))) break;
             if (u < 0) break;
-            const Unit un = decode_unit<CAUSAL>(u, p);
-            if (un.n == 0) continue;
+            const Unit un = decode_unit<CAUSAL, VARLEN>(u, p);
+            constexpr bool vl = VARLEN;
+            auto key_offset = [&](int key) {  // element offset of key row `key` of the unit's sequence in dK / dV
+                return vl ? (static_cast<size_t>(un.k_tok0 + key) * p.heads + un.head) * C::D
+                          : (static_cast<size_t>(un.bh) * p.sk + key) * C::D;
+            };
+            if (un.n == 0) {
+                if (un.zero) {  // a sequence with keys but no query: its dK and dV are 0
+                    const int key = un.kb * C::BN + quad * 32 + lane;
+                    if (key < un.sk)
+#pragma unroll
+                        for (int which = 0; which < 2; ++which) {
+                            uint4 *out = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(which ? p.dk : p.dv) + key_offset(key));
+                            for (int c = 0; c < C::D / 8; ++c) out[c] = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                }
+                continue;
+            }
+            // reduce-add coordinates (dense [bh][sq][D]; packed [token][head][D])
+            auto rrow = [&](int r) { return vl ? un.head : r; };
+            auto rplane = [&](int r) { return vl ? un.q_tok0 + r : un.bh; };
             for (int t = 0; t < un.n && ok; ++t) {
                 BWD_TRACE(BEV_DR_WAIT, tile_it);
                 if (!(ok = warp_wait(B(ctl->dq_full), tile_it & 1u, ctl, p, SITE_BWD_DRAIN_DQ_FULL))) break;
@@ -840,7 +920,8 @@ __global__ void __launch_bounds__(512, 1)
                         if (issuer) {
 #pragma unroll
                             for (int r0 = 0; r0 < 64; r0 += C::RED_ROWS)
-                                tma_reduce_add_3d(&tmdQacc, stage_buf + r0 * C::D * 4, 0, q0 + 64 * h + r0, un.bh);
+                                tma_reduce_add_3d(&tmdQacc, stage_buf + r0 * C::D * 4, 0, rrow(q0 + 64 * h + r0),
+                                                  rplane(q0 + 64 * h + r0));
                             bulk_commit_group();
                             bulk_wait_read_all();
                         }
@@ -865,8 +946,8 @@ __global__ void __launch_bounds__(512, 1)
                     fence_proxy_async_smem();
                     if (!(ok = drain_sync())) break;
                     if (issuer) {
-                        tma_reduce_add_3d(&tmdQacc, sST, 0, q0, un.bh);
-                        tma_reduce_add_3d(&tmdQacc, sST + C::BM * 128, 32, q0, un.bh);
+                        tma_reduce_add_3d(&tmdQacc, sST, 0, rrow(q0), rplane(q0));
+                        tma_reduce_add_3d(&tmdQacc, sST + C::BM * 128, 32, rrow(q0), rplane(q0));
                         bulk_commit_group();
                         bulk_wait_read_all();
                     }
@@ -882,8 +963,8 @@ __global__ void __launch_bounds__(512, 1)
             ++un_it;
             tc_fence_after();
             const int key = un.kb * C::BN + quad * 32 + lane;
-            const bool valid = key < p.sk;
-            const size_t roff = (static_cast<size_t>(un.bh) * p.sk + (valid ? key : 0)) * C::D;
+            const bool valid = key < un.sk;
+            const size_t roff = key_offset(valid ? key : 0);
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
                 uint4 *out = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(which ? p.dk : p.dv) + roff);
@@ -922,10 +1003,12 @@ __global__ void __launch_bounds__(512, 1)
             int u;
             if (!(ok = next_unit(kq, u, ctl, p))) break;
             if (u < 0) break;
-            const Unit un = decode_unit<CAUSAL>(u, p);
+            const Unit un = decode_unit<CAUSAL, VARLEN>(u, p);
             if (un.n == 0) continue;
             const int key = un.kb * C::BN + r;
-            const bool row_ok = key < p.sk;
+            const int sk_ = VARLEN ? un.sk : p.sk, sq_ = VARLEN ? un.sq : p.sq;
+            const bool row_ok = key < sk_;
+            const int diag = key - (sk_ - sq_);  // the first query this key row sees
             for (int t = 0; t < un.n && ok; ++t) {
                 const uint32_t st = q_it & 1u;
                 // the tile's LSE / D vectors arrive with Q and dO
@@ -936,7 +1019,7 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_after();
                 const int q0 = (un.t0 + t) * C::BM + 64 * g;  // first query of this thread's columns
                 // columns c < lim are masked for this key row (key j sees query i iff i >= j - (sk - sq))
-                int lim = CAUSAL ? key - (p.sk - p.sq) - q0 : 0;
+                int lim = CAUSAL ? diag - q0 : 0;
                 if (!row_ok) lim = 64;
                 const bool masked = __any_sync(0xffffffffu, lim > 0);
                 const float *l2 = ld_smem + st * (C::LD_STAGE_BYTES / 4) + 64 * g;
@@ -976,28 +1059,37 @@ __global__ void __launch_bounds__(512, 1)
                 {
                     uint32_t dr[64];
                     tmem_ld64_wait(tDP, dr);
-                    uint32_t dk[32];
+                    // HALVES stores each half of 32 queries as soon as it is packed
+                    // (fewer live registers: the varlen instances need that)
+                    constexpr int HALVES = VARLEN ? 2 : 1;
+                    constexpr int W = 32 / HALVES;  // packed words per pass
 #pragma unroll
-                    for (int c = 0; c < 64; c += 4) {
-                        const float4 dv4 = *reinterpret_cast<const float4 *>(dsv + c);
-                        const float2 p01 = unpack2<T>(pk[c / 2]), p23 = unpack2<T>(pk[c / 2 + 1]);
-                        const float pv[4] = {p01.x, p01.y, p23.x, p23.y};
-                        const float dvv[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
-                        float ds[4];
+                    for (int hh = 0; hh < HALVES; ++hh) {
+                        uint32_t dk[W];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) ds[e] = scale * pv[e] * (__uint_as_float(dr[c + e]) - dvv[e]);
-                        dk[c / 2] = pack2<T>(ds[0], ds[1]);
-                        dk[c / 2 + 1] = pack2<T>(ds[2], ds[3]);
-                    }
-                    tmem_st16(tDP, *reinterpret_cast<const uint32_t(*)[16]>(dk));
-                    tmem_st16(tDP + 16, *reinterpret_cast<const uint32_t(*)[16]>(dk + 16));
-                    // shared copy for dQ^T: MN-major B, panel g (queries 64g..), row r,
-                    // 16-byte chunks 0..7 of the row, 128-byte swizzle
+                        for (int c = 0; c < 2 * W; c += 4) {
+                            const int cc = 2 * W * hh + c;
+                            const float4 dv4 = *reinterpret_cast<const float4 *>(dsv + cc);
+                            const float2 p01 = unpack2<T>(pk[cc / 2]), p23 = unpack2<T>(pk[cc / 2 + 1]);
+                            const float pv[4] = {p01.x, p01.y, p23.x, p23.y};
+                            const float dvv[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
+                            float ds[4];
 #pragma unroll
-                    for (int k8 = 0; k8 < 8; ++k8) {
-                        const uint32_t chunk = static_cast<uint32_t>(k8 ^ (r & 7));
-                        st_shared_v4(sDS + g * C::PANEL_BYTES + r * 128 + chunk * 16, dk[4 * k8], dk[4 * k8 + 1],
-                                     dk[4 * k8 + 2], dk[4 * k8 + 3]);
+                            for (int e = 0; e < 4; ++e) ds[e] = scale * pv[e] * (__uint_as_float(dr[cc + e]) - dvv[e]);
+                            dk[c / 2] = pack2<T>(ds[0], ds[1]);
+                            dk[c / 2 + 1] = pack2<T>(ds[2], ds[3]);
+                        }
+#pragma unroll
+                        for (int q16 = 0; q16 < W / 16; ++q16)
+                            tmem_st16(tDP + W * hh + 16 * q16, *reinterpret_cast<const uint32_t(*)[16]>(dk + 16 * q16));
+                        // shared copy for dQ: MN-major operand, panel g (queries 64g..),
+                        // row r, 16-byte chunks of the row, 128-byte swizzle
+#pragma unroll
+                        for (int k8 = 0; k8 < W / 4; ++k8) {
+                            const uint32_t chunk = static_cast<uint32_t>((W / 4 * hh + k8) ^ (r & 7));
+                            st_shared_v4(sDS + g * C::PANEL_BYTES + r * 128 + chunk * 16, dk[4 * k8], dk[4 * k8 + 1],
+                                         dk[4 * k8 + 2], dk[4 * k8 + 3]);
+                        }
                     }
                 }
                 tmem_wait_st();

@@ -20,19 +20,23 @@ struct BwdLaunchArgs {
 };
 
 // prep -> main -> dQ convert, all on a.stream.  T: __half or __nv_bfloat16;
-// D: head dim 64 or 128.
-template <typename T, bool CAUSAL, int D>
+// D: head dim 64 or 128; VARLEN: packed sequences (a.p.cu_q set).
+template <typename T, bool CAUSAL, int D, bool VARLEN>
 cudaError_t launch_bwd(const BwdLaunchArgs &a);
 
-#define ATTN_BWD_EXTERN(T, C, D) extern template cudaError_t launch_bwd<T, C, D>(const BwdLaunchArgs &);
-ATTN_BWD_EXTERN(__half, false, 64)
-ATTN_BWD_EXTERN(__half, true, 64)
-ATTN_BWD_EXTERN(__nv_bfloat16, false, 64)
-ATTN_BWD_EXTERN(__nv_bfloat16, true, 64)
-ATTN_BWD_EXTERN(__half, false, 128)
-ATTN_BWD_EXTERN(__half, true, 128)
-ATTN_BWD_EXTERN(__nv_bfloat16, false, 128)
-ATTN_BWD_EXTERN(__nv_bfloat16, true, 128)
+#define ATTN_BWD_EXTERN(T, C, D, V) extern template cudaError_t launch_bwd<T, C, D, V>(const BwdLaunchArgs &);
+#define ATTN_BWD_EXTERN_V(V)                      \
+    ATTN_BWD_EXTERN(__half, false, 64, V)         \
+    ATTN_BWD_EXTERN(__half, true, 64, V)          \
+    ATTN_BWD_EXTERN(__nv_bfloat16, false, 64, V)  \
+    ATTN_BWD_EXTERN(__nv_bfloat16, true, 64, V)   \
+    ATTN_BWD_EXTERN(__half, false, 128, V)        \
+    ATTN_BWD_EXTERN(__half, true, 128, V)         \
+    ATTN_BWD_EXTERN(__nv_bfloat16, false, 128, V) \
+    ATTN_BWD_EXTERN(__nv_bfloat16, true, 128, V)
+ATTN_BWD_EXTERN_V(false)
+ATTN_BWD_EXTERN_V(true)
+#undef ATTN_BWD_EXTERN_V
 #undef ATTN_BWD_EXTERN
 
 }  // namespace bwd

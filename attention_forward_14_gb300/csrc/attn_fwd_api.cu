@@ -160,6 +160,25 @@ int make_map_f32_rows(CUtensorMap *map, void *ptr, int64_t bh, int64_t s, int64_
     return ATTN_OK;
 }
 
+// The same for a packed [tokens, h, d] accumulator (varlen backward), as
+// 3-D [tokens][h][d] with boxes of one head.
+int make_map_f32_packed(CUtensorMap *map, void *ptr, int64_t tokens, int64_t h, int64_t d)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    int rc = get_encode(&enc);
+    if (rc != ATTN_OK) return rc;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h), static_cast<cuuint64_t>(tokens)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 4), static_cast<cuuint64_t>(h * d * 4)};
+    const bool wide = d == 128;
+    cuuint32_t box[3] = {wide ? 128u : 32u, 1, wide ? static_cast<cuuint32_t>(bwd::Cfg<128>::RED_ROWS) : 128u};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     wide ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (fp32 packed) failed (CUresult %d)", static_cast<int>(r));
+    return ATTN_OK;
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 constexpr int64_t kMaxSeq = int64_t(1) << 30;
@@ -348,6 +367,21 @@ int32_t bwd_group(int64_t bh, int64_t sq, int64_t d)
     return static_cast<int32_t>(g);
 }
 
+template <bool VARLEN>
+cudaError_t launch_bwd_any(const bwd::BwdLaunchArgs &a, int64_t d, int dtype, int causal)
+{
+    if (d == 128) {
+        if (dtype == ATTN_BF16)
+            return causal ? bwd::launch_bwd<__nv_bfloat16, true, 128, VARLEN>(a)
+                          : bwd::launch_bwd<__nv_bfloat16, false, 128, VARLEN>(a);
+        return causal ? bwd::launch_bwd<__half, true, 128, VARLEN>(a) : bwd::launch_bwd<__half, false, 128, VARLEN>(a);
+    }
+    if (dtype == ATTN_BF16)
+        return causal ? bwd::launch_bwd<__nv_bfloat16, true, 64, VARLEN>(a)
+                      : bwd::launch_bwd<__nv_bfloat16, false, 64, VARLEN>(a);
+    return causal ? bwd::launch_bwd<__half, true, 64, VARLEN>(a) : bwd::launch_bwd<__half, false, 64, VARLEN>(a);
+}
+
 int run_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse, void *dq,
             void *dk, void *dv, int64_t b, int64_t h, int64_t sq, int64_t sk, int64_t d, int causal, float scale,
             int dtype, void *workspace, int64_t workspace_bytes, cudaStream_t stream)
@@ -423,20 +457,109 @@ int run_bwd(const void *q, const void *k, const void *v, const void *o, const vo
     p.sl2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     p.scale = scale;
     p.timeout_ns = kDefaultTimeoutNs;
+    p.cu_q = p.cu_k = nullptr;
+    p.heads = static_cast<int32_t>(h);
+    p.total_q = static_cast<int32_t>(sq);
+    p.total_k = static_cast<int32_t>(sk);
     a.grid = p.num_units < di->sm_count ? p.num_units : di->sm_count;
     a.sm_count = di->sm_count;
     a.stream = stream;
-    if (d == 128) {
-        if (dtype == ATTN_BF16)
-            e = causal ? bwd::launch_bwd<__nv_bfloat16, true, 128>(a) : bwd::launch_bwd<__nv_bfloat16, false, 128>(a);
-        else
-            e = causal ? bwd::launch_bwd<__half, true, 128>(a) : bwd::launch_bwd<__half, false, 128>(a);
-    } else {
-        if (dtype == ATTN_BF16)
-            e = causal ? bwd::launch_bwd<__nv_bfloat16, true, 64>(a) : bwd::launch_bwd<__nv_bfloat16, false, 64>(a);
-        else
-            e = causal ? bwd::launch_bwd<__half, true, 64>(a) : bwd::launch_bwd<__half, false, 64>(a);
+    e = launch_bwd_any<false>(a, d, dtype, causal);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "backward launch");
+}
+
+// fp32 dQ accumulator [total_q, h, d], LSE2 and D [batch * h, sq_pad], the
+// scheduler's counter.
+int64_t bwd_varlen_workspace_bytes(int64_t batch, int64_t h, int64_t total_q, int64_t max_seqlen_q, int64_t d)
+{
+    return total_q * h * d * 4 + 2 * batch * h * bwd_sq_pad(max_seqlen_q) * 4 + 256;
+}
+
+int run_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse,
+                   void *dq, void *dk, void *dv, const int32_t *cu_q, const int32_t *cu_k, int64_t batch, int64_t h,
+                   int64_t total_q, int64_t total_k, int64_t max_q, int64_t max_k, int64_t d, int causal, float scale,
+                   int dtype, void *workspace, int64_t workspace_bytes, cudaStream_t stream)
+{
+    if (batch < 0 || h < 0 || total_q < 0 || total_k < 0 || max_q < 0 || max_k < 0)
+        return fail(ATTN_ERR_SHAPE, "negative varlen size");
+    if (total_q > INT32_MAX || total_k > INT32_MAX || max_q > total_q || max_k > total_k)
+        return fail(ATTN_ERR_SHAPE, "varlen totals above 2^31-1 or max lengths above the totals");
+    if (h > 0 && batch >= (int64_t(1) << 31) / h) return fail(ATTN_ERR_SHAPE, "batch*h not below 2^31");
+    if (d != 64 && d != 128) return fail(ATTN_ERR_HEADDIM, "backward: head dim %lld not supported (64 or 128)", (long long)d);
+    if (dtype != ATTN_FP16 && dtype != ATTN_BF16) return fail(ATTN_ERR_DTYPE, "dtype %d is not fp16 (0) or bf16 (1)", dtype);
+    if (!std::isfinite(scale)) return fail(ATTN_ERR_SCALE, "scale is not finite");
+    if (batch == 0 || h == 0) return ATTN_OK;
+    const bool rows = total_q > 0, keys = total_k > 0;
+    if ((rows && !dq) || (keys && (!dk || !dv))) return fail(ATTN_ERR_NULL, "dq, dk or dv is NULL");
+    if ((rows && !aligned(dq, 16)) || (keys && (!aligned(dk, 16) || !aligned(dv, 16))))
+        return fail(ATTN_ERR_ALIGN, "dq, dk and dv must be 16-byte aligned");
+    DeviceInfo *di = nullptr;
+    int rc = device_info(&di);
+    if (rc != ATTN_OK) return rc;
+    const size_t qbytes = static_cast<size_t>(total_q * h * d) * 2, kbytes = static_cast<size_t>(total_k * h * d) * 2;
+    cudaError_t e;
+    if (!rows || !keys || max_q == 0 || max_k == 0) {  // no query or no key anywhere: the gradients that exist are 0
+        if (rows && (e = cudaMemsetAsync(dq, 0, qbytes, stream)) != cudaSuccess) return cuda_fail(e, "zero dq");
+        if (keys && (e = cudaMemsetAsync(dk, 0, kbytes, stream)) != cudaSuccess) return cuda_fail(e, "zero dk");
+        if (keys && (e = cudaMemsetAsync(dv, 0, kbytes, stream)) != cudaSuccess) return cuda_fail(e, "zero dv");
+        return ATTN_OK;
     }
+    if (!q || !k || !v || !o || !dout || !lse) return fail(ATTN_ERR_NULL, "q, k, v, o, dout or lse is NULL");
+    if (!cu_q || !cu_k) return fail(ATTN_ERR_NULL, "cu_seqlens_q / cu_seqlens_k is NULL");
+    if (!aligned(cu_q, 4) || !aligned(cu_k, 4)) return fail(ATTN_ERR_ALIGN, "cu_seqlens must be 4-byte aligned");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16))
+        return fail(ATTN_ERR_ALIGN, "q, k, v, o and dout must be 16-byte aligned");
+    if (!aligned(lse, 4)) return fail(ATTN_ERR_ALIGN, "lse must be 4-byte aligned");
+    const int64_t bh = batch * h;
+    const int64_t num_kblk = (max_k + 127) / 128;
+    if (bh * num_kblk > INT32_MAX) return fail(ATTN_ERR_SHAPE, "too many work units");
+    const int64_t need = bwd_varlen_workspace_bytes(batch, h, total_q, max_q, d);
+    if (!workspace) return fail(ATTN_ERR_NULL, "workspace is NULL");
+    if (!aligned(workspace, 16)) return fail(ATTN_ERR_ALIGN, "workspace must be 16-byte aligned");
+    if (workspace_bytes < need)
+        return fail(ATTN_ERR_SHAPE, "workspace too small: %lld bytes, need %lld", (long long)workspace_bytes,
+                    (long long)need);
+    bwd::BwdLaunchArgs a;
+    if ((rc = make_map_packed(&a.q, q, dtype, total_q, h, d)) != ATTN_OK) return rc;
+    if ((rc = make_map_packed(&a.dout, dout, dtype, total_q, h, d)) != ATTN_OK) return rc;
+    if ((rc = make_map_packed(&a.k, k, dtype, total_k, h, d)) != ATTN_OK) return rc;
+    if ((rc = make_map_packed(&a.v, v, dtype, total_k, h, d)) != ATTN_OK) return rc;
+    if ((rc = make_map_f32_packed(&a.dq_acc, workspace, total_q, h, d)) != ATTN_OK) return rc;
+    bwd::BwdParams &p = a.p;
+    const int64_t sq_pad = bwd_sq_pad(max_q);
+    p.o = o;
+    p.dout = dout;
+    p.lse = lse;
+    p.dq_acc = static_cast<float *>(workspace);
+    p.lse2 = p.dq_acc + total_q * h * d;
+    p.dsum = p.lse2 + bh * sq_pad;
+    p.counter = reinterpret_cast<int32_t *>(p.dsum + bh * sq_pad);
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.status = di->status;
+    p.bh = static_cast<int32_t>(bh);
+    p.sq = static_cast<int32_t>(max_q);
+    p.sk = static_cast<int32_t>(max_k);
+    p.sq_pad = static_cast<int32_t>(sq_pad);
+    p.num_kblk = static_cast<int32_t>(num_kblk);
+    p.num_units = static_cast<int32_t>(bh * num_kblk);
+    p.group = bwd_group(bh, max_q, d);
+    p.cu_q = cu_q;
+    p.cu_k = cu_k;
+    p.heads = static_cast<int32_t>(h);
+    p.total_q = static_cast<int32_t>(total_q);
+    p.total_k = static_cast<int32_t>(total_k);
+#ifdef ATTN_TRACE_ENABLE
+    p.trace = g_trace_buf;
+#endif
+    p.sl2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    p.scale = scale;
+    p.timeout_ns = kDefaultTimeoutNs;
+    a.grid = p.num_units < di->sm_count ? p.num_units : di->sm_count;
+    a.sm_count = di->sm_count;
+    a.stream = stream;
+    e = launch_bwd_any<true>(a, d, dtype, causal);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "backward launch");
 }
 
@@ -803,6 +926,27 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const v
     g_err.clear();
     return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, b, h, sq, sk, d, causal, scale, dtype, workspace,
                    workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int attn_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse,
+                    void *dq, void *dk, void *dv, const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                    int64_t batch, int64_t h, int64_t total_q, int64_t total_k, int64_t max_seqlen_q,
+                    int64_t max_seqlen_k, int64_t d, int causal, float scale, int dtype, void *workspace,
+                    int64_t workspace_bytes, void *stream)
+{
+    g_err.clear();
+    return run_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, batch, h, total_q, total_k,
+                          max_seqlen_q, max_seqlen_k, d, causal, scale, dtype, workspace, workspace_bytes,
+                          static_cast<cudaStream_t>(stream));
+}
+
+int64_t attn_bwd_varlen_workspace_bytes(int64_t batch, int64_t h, int64_t total_q, int64_t max_seqlen_q, int64_t d)
+{
+    g_err.clear();
+    if (batch < 0 || h < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_q > total_q || total_q > INT32_MAX)
+        return fail(ATTN_ERR_SHAPE, "invalid varlen backward workspace query");
+    if (d != 64 && d != 128) return fail(ATTN_ERR_HEADDIM, "backward: head dim %lld not supported (64 or 128)", (long long)d);
+    return bwd_varlen_workspace_bytes(batch, h, total_q, max_seqlen_q, d);
 }
 
 int64_t attn_bwd_workspace_bytes(int64_t b, int64_t h, int64_t sq, int64_t d)

@@ -257,6 +257,37 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o,
 /* Bytes of workspace attn_bwd needs, or a negative ATTN_ERR_* code. */
 int64_t attn_bwd_workspace_bytes(int64_t b, int64_t h, int64_t sq, int64_t d);
 
+/*
+ * Variable-length (packed) backward: attn_bwd applied to each sequence of a
+ * packed batch ("05 · kernel 工程与四代演化" 6.1 lists varlen_bwd beside
+ * varlen_fwd), with the layouts of attn_fwd_varlen:
+ *   q, o, dout, dq : [total_q, h, d] of dtype, 16-byte aligned.
+ *   k, v, dk, dv   : [total_k, h, d] of dtype, 16-byte aligned.
+ *   lse            : fp32 [h, total_q], as written by attn_fwd_varlen.
+ *   cu_seqlens_q/k : device int32 [batch + 1] offsets, as for
+ *                    attn_fwd_varlen; max_seqlen_q/k bound the lengths.
+ *   workspace      : caller-owned device scratch, 16-byte aligned, of at
+ *                    least attn_bwd_varlen_workspace_bytes(batch, h,
+ *                    total_q, max_seqlen_q, d) bytes.
+ * The causal mask is bottom-right per sequence.  A sequence whose offsets
+ * fall outside the totals is skipped (its gradients are not written).  d is
+ * 64 or 128.  Same error codes and asynchrony as attn_bwd.
+ */
+int attn_bwd_varlen(const void *q, const void *k, const void *v,
+                    const void *o, const void *dout, const float *lse,
+                    void *dq, void *dk, void *dv,
+                    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                    int64_t batch, int64_t h, int64_t total_q,
+                    int64_t total_k, int64_t max_seqlen_q,
+                    int64_t max_seqlen_k, int64_t d, int causal, float scale,
+                    int dtype, void *workspace, int64_t workspace_bytes,
+                    void *stream);
+
+/* Bytes of workspace attn_bwd_varlen needs, or a negative ATTN_ERR_* code. */
+int64_t attn_bwd_varlen_workspace_bytes(int64_t batch, int64_t h,
+                                        int64_t total_q, int64_t max_seqlen_q,
+                                        int64_t d);
+
 /* Thread-local message describing the last non-OK return on this thread
  * ("" if none).  The pointer stays valid until the next call on the thread. */
 const char *attn_last_error(void);

@@ -67,6 +67,9 @@ def _bind(lib):
     lib.oracle_attn_bwd_dkv_cols_f64.argtypes = [dp, dp, dp, dp, i64, i64, i64, ctypes.c_int,
                                                  ctypes.c_double, ctypes.POINTER(ctypes.c_int64),
                                                  i64, dp, dp]
+    lib.oracle_attn_fwd_kvcache_f64.restype = ctypes.c_int
+    lib.oracle_attn_fwd_kvcache_f64.argtypes = [dp, dp, dp, dp, dp, ctypes.POINTER(ctypes.c_int64), dp, dp,
+                                                i64, i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_double]
     return lib
 
 
@@ -214,3 +217,40 @@ def attn_bwd_dkv_cols(q_head, k_head, v_head, do_head, cols, causal: bool, scale
     if rc != 0:
         raise RuntimeError(f"oracle_attn_bwd_dkv_cols_f64 failed: {rc}")
     return dk, dv
+
+
+def attn_fwd_kvcache(q, k_cache, v_cache, cache_len, k_new=None, v_new=None, causal: bool = False,
+                     scale: float = 1.0, lib=None):
+    """KV-cache forward: the new rows written into (copies of) the caches at
+    each batch element's length, then attention over the valid keys.
+
+    q: [b, h, sq, d]; k_cache/v_cache: [b, h, s_cache, d]; cache_len: [b]
+    ints; k_new/v_new: [b, h, s_new, d] or None.  Returns (o, lse, k_cache
+    after the write, v_cache after the write), all fp64.
+    """
+    lib = lib or _load()
+    q = _f64(q)
+    kc = np.array(k_cache, dtype=np.float64, copy=True, order="C")
+    vc = np.array(v_cache, dtype=np.float64, copy=True, order="C")
+    b, h, sq, d = q.shape
+    s_cache = kc.shape[2]
+    assert kc.shape == (b, h, s_cache, d) and vc.shape == kc.shape
+    lens = np.ascontiguousarray(np.asarray(cache_len, dtype=np.int64))
+    assert lens.shape == (b,)
+    if k_new is None:
+        kn = vn = None
+        s_new = 0
+    else:
+        kn, vn = _f64(k_new), _f64(v_new)
+        s_new = kn.shape[2]
+        assert kn.shape == (b, h, s_new, d) and vn.shape == kn.shape
+    o = np.zeros((b, h, sq, d), np.float64)
+    lse = np.zeros((b, h, sq), np.float64)
+    null = ctypes.POINTER(ctypes.c_double)()
+    rc = lib.oracle_attn_fwd_kvcache_f64(
+        _ptr(q), _ptr(kc), _ptr(vc), _ptr(kn) if kn is not None else null,
+        _ptr(vn) if vn is not None else null, lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+        _ptr(o), _ptr(lse), b, h, sq, s_cache, s_new, d, int(bool(causal)), float(scale))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_fwd_kvcache_f64 failed: {rc}")
+    return o, lse, kc, vc

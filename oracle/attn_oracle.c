@@ -34,7 +34,9 @@
  * and, for the backward pass (end of the file): the gradients dQ, dK, dV of
  * the forward by definition (oracle_attn_bwd_f64), the same for selected
  * query rows or keys of one head (for spot checks of large problems), and
- * the probabilities P themselves (used to size error bounds).
+ * the probabilities P themselves (used to size error bounds); and the
+ * KV-cache forward (oracle_attn_fwd_kvcache_f64): the cache write of new
+ * tokens followed by the definition over each batch element's valid keys.
  * Parity is pinned by the CPU tests (brute force, closed forms, invariants,
  * finite differences of the forward for the gradients); nothing here is
  * "parity unpinned".
@@ -534,4 +536,74 @@ int oracle_attn_bwd_dkv_cols_f64(const double *q_head, const double *k_head,
     free(l);
     free(D);
     return ORACLE_OK;
+}
+
+/*
+ * KV-cache forward.  "05 · kernel 工程与四代演化", section 6.1, names a
+ * fwd_kvcache entry point without defining it; the reading taken here:
+ *   1. for each batch element e, with L0 = cache_len[e] clamped to
+ *      [0, s_cache], row t of the new keys and values goes to position
+ *      L0 + t of the cache; rows that would fall at or past s_cache are
+ *      dropped;
+ *   2. every query row of e attends, by definition, to the first
+ *      L = min(L0 + s_new, s_cache) keys of e's cache (causal mask
+ *      bottom-right aligned to L, as for the plain forward with sk = L).
+ * k_cache, v_cache: [b, h, s_cache, d], updated in place; k_new, v_new:
+ * [b, h, s_new, d] (may be NULL when s_new == 0); cache_len: [b];
+ * q, o: [b, h, sq, d]; lse: [b, h, sq] (may be NULL).
+ */
+static int64_t clamp_len(int64_t len, int64_t cap)
+{
+    if (len < 0) return 0;
+    return len > cap ? cap : len;
+}
+
+int oracle_attn_fwd_kvcache_f64(const double *q, double *k_cache, double *v_cache,
+                                const double *k_new, const double *v_new,
+                                const int64_t *cache_len, double *o, double *lse,
+                                int64_t b, int64_t h, int64_t sq, int64_t s_cache,
+                                int64_t s_new, int64_t d, int causal, double scale)
+{
+    if (check_dims(b, h, sq, s_cache, d) != ORACLE_OK || s_new < 0) return ORACLE_ERR_ARG;
+    if (s_new > 0 && (!k_new || !v_new)) return ORACLE_ERR_ARG;
+    /* step 1: the new rows go into the cache after the valid ones */
+    for (int64_t e = 0; e < b; ++e) {
+        int64_t start = clamp_len(cache_len[e], s_cache);
+        for (int64_t head = 0; head < h; ++head) {
+            int64_t plane = e * h + head;
+            for (int64_t t = 0; t < s_new; ++t) {
+                int64_t pos = start + t;
+                if (pos >= s_cache) break; /* no room left in the cache */
+                memcpy(k_cache + (plane * s_cache + pos) * d, k_new + (plane * s_new + t) * d,
+                       sizeof(double) * (size_t)d);
+                memcpy(v_cache + (plane * s_cache + pos) * d, v_new + (plane * s_new + t) * d,
+                       sizeof(double) * (size_t)d);
+            }
+        }
+    }
+    /* step 2: attention over the valid prefix of each element's cache */
+    int64_t total = b * h * sq;
+    int err = ORACLE_OK;
+#pragma omp parallel
+    {
+        double *srow = (double *)malloc(sizeof(double) * (size_t)(s_cache > 0 ? s_cache : 1));
+        if (!srow) {
+#pragma omp atomic write
+            err = ORACLE_ERR_NOMEM;
+        } else {
+#pragma omp for schedule(dynamic, 16)
+            for (int64_t r = 0; r < total; ++r) {
+                int64_t plane = r / sq, i = r % sq;
+                int64_t e = plane / h;
+                int64_t valid = clamp_len(cache_len[e], s_cache) + s_new;
+                if (valid > s_cache) valid = s_cache;
+                double l_out;
+                row_by_definition(q + r * d, k_cache + plane * s_cache * d, v_cache + plane * s_cache * d,
+                                  i, sq, valid, d, causal, scale, srow, o + r * d, &l_out);
+                if (lse) lse[r] = l_out;
+            }
+            free(srow);
+        }
+    }
+    return err;
 }

@@ -482,6 +482,109 @@ def pin_bwd_empty(lib):
     return fails
 
 
+# ---------------------------------------------------------------- KV cache
+
+def _kvcache_textbook(q, kc, vc, lens, kn, vn, causal, scale):
+    """The KV-cache reading written out in plain Python: copy the new rows
+    in after each element's clamped length, then the textbook formula over
+    the element's first L keys (mask bottom-right aligned to L)."""
+    kc = np.array(kc, np.float64, copy=True)
+    vc = np.array(vc, np.float64, copy=True)
+    b, h, sq, d = q.shape
+    cap = kc.shape[2]
+    s_new = 0 if kn is None else kn.shape[2]
+    o = np.zeros((b, h, sq, d))
+    lse = np.zeros((b, h, sq))
+    for e in range(b):
+        l0 = min(max(int(lens[e]), 0), cap)
+        for t in range(s_new):
+            if l0 + t < cap:
+                kc[e, :, l0 + t] = kn[e, :, t]
+                vc[e, :, l0 + t] = vn[e, :, t]
+        n = min(l0 + s_new, cap)
+        oe, le = _textbook_mp(q[e:e + 1], kc[e:e + 1, :, :n], vc[e:e + 1, :, :n], causal, scale)
+        o[e], lse[e] = oe[0], le[0]
+    return o, lse, kc, vc
+
+
+def pin_kvcache_bruteforce(lib):
+    """Tiny KV-cache problems (lengths that fit, fill, overflow the cache,
+    negative, beyond capacity, rows that see no key) against the reading
+    written out in Python with 40-digit arithmetic."""
+    fails = []
+    cases = [  # (b, h, sq, cap, s_new, d, lens)
+        (3, 2, 2, 7, 2, 4, [0, 3, 6]),
+        (2, 1, 1, 5, 0, 3, [5, 2]),
+        (2, 2, 3, 6, 1, 2, [-4, 9]),
+        (1, 2, 4, 6, 1, 4, [1]),
+        (2, 1, 2, 4, 3, 2, [2, 0]),
+    ]
+    for t, (b, h, sq, cap, s_new, d, lens) in enumerate(cases):
+        r = _rng(4000 + t)
+        q = r.standard_normal((b, h, sq, d))
+        kc = r.standard_normal((b, h, cap, d))
+        vc = r.standard_normal((b, h, cap, d))
+        kn = r.standard_normal((b, h, s_new, d)) if s_new else None
+        vn = r.standard_normal((b, h, s_new, d)) if s_new else None
+        scale = 0.7 / math.sqrt(d)
+        for causal in (False, True):
+            want = _kvcache_textbook(q, kc, vc, lens, kn, vn, causal, scale)
+            got = oracle.attn_fwd_kvcache(q, kc, vc, lens, kn, vn, causal, scale, lib=lib)
+            for name, g, w in zip(("o", "lse", "k_cache", "v_cache"), got, want):
+                fails += _cmp(f"kvcache case{t} c{int(causal)} {name}", g, w)
+    return fails
+
+
+def pin_kvcache_unused_slots(lib):
+    """Cache slots past an element's valid length take no part: NaN there
+    leaves the result equal to the one with zeros there."""
+    fails = []
+    r = _rng(4100)
+    b, h, sq, cap, s_new, d = 3, 2, 3, 10, 2, 4
+    lens = [0, 4, 8]
+    q = r.standard_normal((b, h, sq, d))
+    kc = r.standard_normal((b, h, cap, d))
+    vc = r.standard_normal((b, h, cap, d))
+    kn = r.standard_normal((b, h, s_new, d))
+    vn = r.standard_normal((b, h, s_new, d))
+    kz, vz, kx, vx = kc.copy(), vc.copy(), kc.copy(), vc.copy()
+    for e, n in enumerate(lens):
+        kz[e, :, n:], vz[e, :, n:] = 0.0, 0.0
+        kx[e, :, n:], vx[e, :, n:] = np.nan, np.nan
+    for causal in (False, True):
+        oz, lz, _, _ = oracle.attn_fwd_kvcache(q, kz, vz, lens, kn, vn, causal, 0.5, lib=lib)
+        ox, lx, _, _ = oracle.attn_fwd_kvcache(q, kx, vx, lens, kn, vn, causal, 0.5, lib=lib)
+        fails += _cmp(f"kvcache-nan c{int(causal)} o", ox, oz, 0.0)
+        fails += _cmp(f"kvcache-nan c{int(causal)} lse", lx, lz, 0.0)
+    return fails
+
+
+def pin_kvcache_decode_matches_prefill(lib):
+    """Causal attention over a whole sequence, computed in one pass, equals
+    feeding the sequence through the cache in chunks (each chunk's queries,
+    keys and values appended, its rows attending to everything so far)."""
+    fails = []
+    r = _rng(4200)
+    b, h, s, d, cap = 2, 2, 10, 8, 13
+    q = r.standard_normal((b, h, s, d))
+    k = r.standard_normal((b, h, s, d))
+    v = r.standard_normal((b, h, s, d))
+    full_o, full_l = oracle.attn_fwd(q, k, v, True, 0.4, lib=lib)
+    kc = np.zeros((b, h, cap, d))
+    vc = np.zeros((b, h, cap, d))
+    a = 0
+    for c in (1, 1, 3, 2, 1, 2):
+        sl = slice(a, a + c)
+        o, l, kc, vc = oracle.attn_fwd_kvcache(q[:, :, sl], kc, vc, [a] * b, k[:, :, sl], v[:, :, sl], True,
+                                               0.4, lib=lib)
+        fails += _cmp(f"kvcache-decode rows {a}..{a + c} o", o, full_o[:, :, sl])
+        fails += _cmp(f"kvcache-decode rows {a}..{a + c} lse", l, full_l[:, :, sl])
+        a += c
+    fails += _cmp("kvcache-decode cache k", kc[:, :, :s], k, 0.0)
+    fails += _cmp("kvcache-decode cache tail", kc[:, :, s:], np.zeros((b, h, cap - s, d)), 0.0)
+    return fails
+
+
 ALL_PINS = [
     pin_worked_examples,
     pin_bruteforce,
@@ -500,4 +603,7 @@ ALL_PINS = [
     pin_bwd_identical_keys_and_zero_scale,
     pin_bwd_rows_cols_and_probs,
     pin_bwd_empty,
+    pin_kvcache_bruteforce,
+    pin_kvcache_unused_slots,
+    pin_kvcache_decode_matches_prefill,
 ]

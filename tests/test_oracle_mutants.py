@@ -41,6 +41,13 @@ MUTANTS = [
      "acc += prow[j] * dprow[j] * k_head[j * d + c];"),
     ("bwd_cols_scale_dropped", "dKj[c] += scale * ds * qi[c];", "dKj[c] += ds * qi[c];"),
     ("bwd_cols_mask_ignored", "if (j > last_visible_key(i, sq, sk, causal)) continue;", ""),
+    # KV cache
+    ("kv_append_at_zero", "int64_t pos = start + t;", "int64_t pos = t;"),
+    ("kv_new_not_attended", "int64_t valid = clamp_len(cache_len[e], s_cache) + s_new;",
+     "int64_t valid = clamp_len(cache_len[e], s_cache);"),
+    ("kv_batch_index_wrong", "int64_t e = plane / h;", "int64_t e = plane % b;"),
+    ("kv_write_stops_early", "if (pos >= s_cache) break; /* no room left in the cache */",
+     "if (pos >= s_cache - 1) break;"),
     ("bwd_probs_strict_mask", "int64_t n = 1 + last; /* visible keys 0..last */",
      "int64_t n = last; /* visible keys 0..last-1 */"),
 ]

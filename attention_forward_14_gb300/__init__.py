@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     attn_fwd,
     attn_fwd_fp8,
     attn_fwd_host,
+    attn_fwd_kvcache,
     attn_fwd_splitkv,
     attn_fwd_varlen,
     bwd_workspace_bytes,

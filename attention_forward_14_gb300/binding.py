@@ -24,7 +24,7 @@ ERRORS = {
 EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_fwd_varlen", "attn_fwd_fp8", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
            "attn_fwd_splitkv_default_splits", "attn_fwd_splitkv_noalloc", "attn_last_error", "attn_fwd_status", "attn_fwd_status_clear",
            "attn_fwd_watchdog_selftest", "attn_version", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_varlen",
-           "attn_bwd_varlen_workspace_bytes"]
+           "attn_bwd_varlen_workspace_bytes", "attn_fwd_kvcache"]
 
 
 class AttnError(RuntimeError):
@@ -60,6 +60,9 @@ def _bind(lib):
     lib.attn_fwd_splitkv_noalloc.restype = c_int
     lib.attn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_float, c_int,
                                              c_int, vp]
+    lib.attn_fwd_kvcache.restype = c_int
+    lib.attn_fwd_kvcache.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int, c_float,
+                                     c_int, c_int, vp, i64, vp]
     lib.attn_last_error.restype = ctypes.c_char_p
     lib.attn_last_error.argtypes = []
     lib.attn_fwd_status.restype = c_int
@@ -256,6 +259,62 @@ def attn_fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = None, 
     with torch.cuda.device(q.device):
         rc = lib.attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                                   b, h, sq, sk, d, int(bool(causal)), float(scale), _dtype_code(q), int(num_splits),
+                                  workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                  _stream_handle(stream, q.device))
+    _check(rc, lib)
+    return o, lse
+
+
+def attn_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, k_new=None, v_new=None, causal: bool = False,
+                     scale: float | None = None, num_splits: int | None = None, o=None, lse=None, workspace=None,
+                     stream=None):
+    """Attention of q [b, h, sq, d] against a KV cache [b, h, s_cache, d]
+    whose batch element i holds cache_seqlens[i] valid tokens (int32 CUDA
+    tensor [b]).  With k_new / v_new [b, h, s_new, d] the new rows are
+    first written into the cache at each element's length (the caches are
+    updated in place; cache_seqlens is not) and attended to as well.
+    ``num_splits`` defaults to the library's split-KV choice for s_cache.
+    Returns (o, lse)."""
+    import torch
+    lib = load()
+    b, h, sq, d = q.shape
+    s_cache = k_cache.shape[2]
+    if tuple(k_cache.shape) != (b, h, s_cache, d) or tuple(v_cache.shape) != (b, h, s_cache, d):
+        raise AttnError(-2, f"cache shapes {tuple(k_cache.shape)} / {tuple(v_cache.shape)} do not match q")
+    if (k_new is None) != (v_new is None):
+        raise AttnError(-1, "k_new and v_new must both be given or both be None")
+    s_new = 0 if k_new is None else k_new.shape[2]
+    if k_new is not None and (tuple(k_new.shape) != (b, h, s_new, d) or tuple(v_new.shape) != (b, h, s_new, d)):
+        raise AttnError(-2, "k_new / v_new must be [b, h, s_new, d]")
+    if cache_seqlens.dtype != torch.int32 or cache_seqlens.numel() != b:
+        raise AttnError(-4, "cache_seqlens must be an int32 tensor of b elements")
+    tensors = [("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("cache_seqlens", cache_seqlens)]
+    if k_new is not None:
+        tensors += [("k_new", k_new), ("v_new", v_new)]
+    for name, t in tensors:
+        if not t.is_cuda or not t.is_contiguous():
+            raise AttnError(-2, f"{name} must be a contiguous CUDA tensor")
+        if name != "cache_seqlens" and t.dtype != q.dtype:
+            raise AttnError(-4, f"{name} dtype differs from q")
+    if scale is None:
+        scale = 1.0 / float(d) ** 0.5
+    if num_splits is None:
+        with torch.cuda.device(q.device):
+            num_splits = splitkv_default_splits(b, h, sq, max(s_cache, 1), d, causal)
+        num_splits = max(1, min(num_splits, (s_cache + 127) // 128))
+    need = splitkv_workspace_bytes(b, h, sq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((b, h, sq), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd_kvcache(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                  k_new.data_ptr() if k_new is not None else None,
+                                  v_new.data_ptr() if v_new is not None else None,
+                                  cache_seqlens.data_ptr(), o.data_ptr(), lse.data_ptr(), b, h, sq, s_cache, s_new,
+                                  d, int(bool(causal)), float(scale), _dtype_code(q), int(num_splits),
                                   workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                   _stream_handle(stream, q.device))
     _check(rc, lib)

@@ -218,6 +218,13 @@ struct SplitArgs {
     float *lse_part = nullptr;
 };
 
+// KV cache: per batch element, the number of valid keys is
+// clamp(seqlens[b], 0, sk) + add, at most sk (sk is the cache capacity).
+struct CacheArgs {
+    const int32_t *seqlens = nullptr;
+    int32_t add = 0;
+};
+
 int64_t kv_tiles(int64_t sk) { return (sk + 127) / 128; }
 
 int64_t splitkv_bytes(int64_t bh, int64_t sq, int64_t d, int64_t splits)
@@ -227,7 +234,7 @@ int64_t splitkv_bytes(int64_t bh, int64_t sq, int64_t d, int64_t splits)
 
 int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_t b, int64_t h, int64_t sq, int64_t sk,
         int64_t d, int causal, float scale, int dtype, cudaStream_t stream, int withheld_load, uint64_t timeout_ns,
-        const SplitArgs &split = SplitArgs())
+        const SplitArgs &split = SplitArgs(), const CacheArgs &cache = CacheArgs())
 {
     bool nothing = false;
     int rc = validate(q, k, v, o, lse, b, h, sq, sk, d, scale, dtype, &nothing);
@@ -255,13 +262,14 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_
     p.sk = static_cast<int32_t>(sk);
     p.num_mblk = static_cast<int32_t>((sq + 255) / 256);
     p.num_splits = split.num_splits;
-    p.tiles_per_split = static_cast<int32_t>((kv_tiles(sk) + split.num_splits - 1) / split.num_splits);
     p.o_part = split.o_part;
     p.lse_part = split.lse_part;
     p.cu_q = p.cu_k = nullptr;
     p.heads = static_cast<int32_t>(h);
     p.total_q = static_cast<int32_t>(sq);
     p.total_k = static_cast<int32_t>(sk);
+    p.seqlens_k = cache.seqlens;
+    p.seqlens_add = cache.add;
     const int64_t units = bh * p.num_mblk * split.num_splits;
     if (units > INT32_MAX) return fail(ATTN_ERR_SHAPE, "too many work units (%lld)", (long long)units);
     p.num_units = static_cast<int32_t>(units);
@@ -672,13 +680,27 @@ int attn_fwd_splitkv_default_splits(int64_t b, int64_t h, int64_t sq, int64_t sk
     if (rc != ATTN_OK) return rc;
     const int64_t units = b * h * ((sq + 255) / 256);
     const int64_t tiles = kv_tiles(sk);
-    const int64_t target = 2 * static_cast<int64_t>(di->sm_count);  // two waves: the tail evens out
-    if (units <= 0 || tiles <= 1 || units >= target) return 1;
-    int64_t s = (target + units - 1) / units;
-    const int64_t cap = tiles / 2 > 1 ? tiles / 2 : 1;  // keep >= 2 tiles per split
-    if (s > cap) s = cap;
-    if (s > 1024) s = 1024;
-    return static_cast<int>(s < 1 ? 1 : s);
+    const int64_t sms = di->sm_count;
+    // Many query rows that already fill the GPU: splitting only adds the
+    // fp32 partials' traffic (a few hundred KB per unit).
+    if (units <= 0 || tiles <= 1 || (units >= sms && sq > 64)) return 1;
+    // Otherwise the split count whose units fill the persistent CTAs' waves
+    // best, less 1% per wave (each unit has a fixed start-up cost), with at
+    // least two key tiles per split.
+    int64_t cap = tiles / 2 > 1 ? tiles / 2 : 1;
+    if (cap > 1024) cap = 1024;
+    int64_t best = 1;
+    double best_score = -1.0;
+    for (int64_t s = 1; s <= cap; ++s) {
+        const int64_t u = units * s;
+        const int64_t waves = (u + sms - 1) / sms;
+        const double score = static_cast<double>(u) / static_cast<double>(waves * sms) - 0.01 * static_cast<double>(waves);
+        if (score > best_score + 1e-9) {
+            best_score = score;
+            best = s;
+        }
+    }
+    return static_cast<int>(best);
 }
 
 int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int64_t b, int64_t h,
@@ -742,6 +764,81 @@ int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *
                             static_cast<int64_t>(ATTN_NOALLOC_SCRATCH_BYTES), stream);
 }
 
+// Attention against a KV cache with a length per batch element, after
+// (optionally) writing the new tokens' keys and values into the cache at
+// each element's current length.  Split-KV as in attn_fwd_splitkv.
+int attn_fwd_kvcache(const void *q, void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                     const int32_t *cache_seqlens, void *o, float *lse, int64_t b, int64_t h, int64_t sq,
+                     int64_t s_cache, int64_t s_new, int64_t d, int causal, float scale, int dtype, int num_splits,
+                     void *workspace, int64_t workspace_bytes, void *stream)
+{
+    g_err.clear();
+    bool nothing = false;
+    int rc = validate(q, k_cache, v_cache, o, lse, b, h, sq, s_cache, d, scale, dtype, &nothing);
+    if (rc != ATTN_OK) return rc;
+    if (s_new < 0 || s_new > kMaxSeq) return fail(ATTN_ERR_SHAPE, "s_new %lld not in 0..2^30", (long long)s_new);
+    if ((k_new == nullptr) != (v_new == nullptr))
+        return fail(ATTN_ERR_NULL, "k_new and v_new must both be given or both be NULL");
+    if (s_new > 0 && k_new == nullptr) return fail(ATTN_ERR_NULL, "s_new is %lld but k_new / v_new are NULL", (long long)s_new);
+    if (num_splits < 1 || num_splits > 1024) return fail(ATTN_ERR_SHAPE, "num_splits %d not in 1..1024", num_splits);
+    const int64_t bh = b * h;
+    const bool append = bh * s_new > 0 && s_cache > 0;
+    if (bh == 0 || (nothing && !append)) return ATTN_OK;
+    if (cache_seqlens == nullptr) return fail(ATTN_ERR_NULL, "cache_seqlens is NULL");
+    if (!aligned(cache_seqlens, 4)) return fail(ATTN_ERR_ALIGN, "cache_seqlens must be 4-byte aligned");
+    const int64_t esz = 2;  // fp16 / bf16 (validate checked the dtype)
+    if (append) {
+        if (!k_cache || !v_cache) return fail(ATTN_ERR_NULL, "k_cache or v_cache is NULL");
+        if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+            return fail(ATTN_ERR_ALIGN, "k_new, v_new, k_cache and v_cache must be 16-byte aligned");
+        // the copy reads the new rows while it writes the cache: no overlap
+        const uintptr_t nb = static_cast<uintptr_t>(bh * s_new * d * esz);
+        const uintptr_t cb = static_cast<uintptr_t>(bh * s_cache * d * esz);
+        const void *news[2] = {k_new, v_new};
+        const void *caches[2] = {k_cache, v_cache};
+        for (const void *nw : news)
+            for (const void *ca : caches) {
+                const uintptr_t a0 = reinterpret_cast<uintptr_t>(nw), c0 = reinterpret_cast<uintptr_t>(ca);
+                if (a0 < c0 + cb && c0 < a0 + nb)
+                    return fail(ATTN_ERR_SHAPE, "k_new / v_new overlap k_cache / v_cache");
+            }
+    }
+    if (!nothing && s_cache > 0 && num_splits > kv_tiles(s_cache))
+        return fail(ATTN_ERR_SHAPE, "num_splits %d exceeds the %lld key tiles of 128", num_splits,
+                    (long long)kv_tiles(s_cache));
+    SplitArgs sa;
+    if (!nothing && s_cache > 0 && num_splits > 1) {
+        const int64_t need = splitkv_bytes(bh, sq, d, num_splits);
+        if (!workspace) return fail(ATTN_ERR_NULL, "split-KV workspace is NULL (%lld bytes needed)", (long long)need);
+        if (!aligned(workspace, 16)) return fail(ATTN_ERR_ALIGN, "split-KV workspace must be 16-byte aligned");
+        if (workspace_bytes < need)
+            return fail(ATTN_ERR_SHAPE, "split-KV workspace of %lld bytes is smaller than the %lld needed",
+                        (long long)workspace_bytes, (long long)need);
+        sa.num_splits = num_splits;
+        sa.o_part = static_cast<float *>(workspace);
+        sa.lse_part = sa.o_part + static_cast<int64_t>(num_splits) * bh * sq * d;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (append) {
+        DeviceInfo *di = nullptr;
+        rc = device_info(&di);
+        if (rc != ATTN_OK) return rc;
+        const cudaError_t e =
+            (dtype == ATTN_BF16)
+                ? launch_kvcache_append<__nv_bfloat16>(k_new, v_new, k_cache, v_cache, cache_seqlens, bh, h, s_new,
+                                                       s_cache, static_cast<int>(d), di->sm_count, st)
+                : launch_kvcache_append<__half>(k_new, v_new, k_cache, v_cache, cache_seqlens, bh, h, s_new, s_cache,
+                                                static_cast<int>(d), di->sm_count, st);
+        if (e != cudaSuccess) return cuda_fail(e, "launch (cache append)");
+    }
+    if (nothing) return ATTN_OK;
+    CacheArgs ca;
+    ca.seqlens = cache_seqlens;
+    ca.add = static_cast<int32_t>(s_new);
+    return run(q, k_cache, v_cache, o, lse, b, h, sq, s_cache, d, causal, scale, dtype, st, -1, kDefaultTimeoutNs, sa,
+               ca);
+}
+
 int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse, const int32_t *cu_seqlens_q,
                     const int32_t *cu_seqlens_k, int64_t batch, int64_t h, int64_t total_q, int64_t total_k,
                     int64_t max_seqlen_q, int64_t max_seqlen_k, int64_t d, int causal, float scale, int dtype,
@@ -783,7 +880,6 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float 
     p.sk = static_cast<int32_t>(max_seqlen_k);
     p.num_mblk = static_cast<int32_t>((max_seqlen_q + 255) / 256);
     p.num_splits = 1;
-    p.tiles_per_split = static_cast<int32_t>(kv_tiles(max_seqlen_k > 0 ? max_seqlen_k : 1));
     p.o_part = nullptr;
     p.lse_part = nullptr;
     p.cu_q = cu_seqlens_q;
@@ -850,7 +946,6 @@ int attn_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *ls
     p.sk = static_cast<int32_t>(sk);
     p.num_mblk = static_cast<int32_t>((sq + 255) / 256);
     p.num_splits = 1;
-    p.tiles_per_split = static_cast<int32_t>(kv_tiles(sk));
     p.o_part = nullptr;
     p.lse_part = nullptr;
     p.cu_q = p.cu_k = nullptr;

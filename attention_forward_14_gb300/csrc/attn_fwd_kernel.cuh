@@ -71,14 +71,13 @@ struct FwdParams {
     float o_scale;         // multiplier of O (e4m3: the V descale; else 1)
     uint64_t timeout_ns;   // bound of every wait
     int32_t withheld_load; // K/V load index never issued (watchdog self-test), -1 = none
-    // Split-KV: each (bh, row block) is cut into num_splits ranges of
-    // tiles_per_split K/V tiles.  With num_splits > 1 the kernel writes, per
+    // Split-KV: the K/V tiles each (bh, row block) sees are cut into
+    // num_splits near-equal ranges.  With num_splits > 1 the kernel writes, per
     // split, O normalised by its own rounded-P sum (fp32, o_part
     // [split][bh][sq][D]) and two natural log-sum-exps (lse_part
     // [split][bh][sq][2]: of the fp32 p, and of p as rounded); a combine
     // kernel merges the splits.  num_splits == 1: o / lse written directly.
     int32_t num_splits;
-    int32_t tiles_per_split;
     float *o_part;
     float *lse_part;
     // Varlen (packed sequences): cu_q / cu_k are the batch+1 cumulative
@@ -89,6 +88,11 @@ struct FwdParams {
     const int32_t *cu_k;
     int32_t heads;
     int32_t total_q, total_k;
+    // KV cache (dense layout): sk is the capacity of the cache and batch
+    // element b has min(clamp(seqlens_k[b], 0, sk) + seqlens_add, sk) valid
+    // keys (device int32 [b]; bh = b * heads).  nullptr: all sk keys.
+    const int32_t *seqlens_k = nullptr;
+    int32_t seqlens_add = 0;
 #ifdef ATTN_TRACE_ENABLE
     unsigned long long *trace;  // per-warp event records (timeline builds only)
 #endif
@@ -249,12 +253,19 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams &p)
         un.q_tok0 = un.k_tok0 = 0;
         un.sq = p.sq;
         un.sk = p.sk;
+        if (p.seqlens_k != nullptr) {
+            const int cached = min(max(p.seqlens_k[bh / p.heads], 0), p.sk);
+            un.sk = static_cast<int>(min(static_cast<long long>(cached) + p.seqlens_add, static_cast<long long>(p.sk)));
+        }
     }
     const int last = min(un.row0 + C::UNIT_ROWS - 1, un.sq - 1);
     const int kend = CAUSAL ? min(un.sk, last + 1 + (un.sk - un.sq)) : un.sk;
     const int n_all = (kend > 0 && un.row0 < un.sq) ? (kend + C::BN - 1) / C::BN : 0;
-    un.jb = un.split * p.tiles_per_split;
-    un.n = max(0, min(n_all, un.jb + p.tiles_per_split) - un.jb);
+    // the unit's own tile range, cut into num_splits near-equal parts (the
+    // splits of a row block share its work whatever its visible length)
+    const int per = (n_all + p.num_splits - 1) / p.num_splits;
+    un.jb = un.split * per;
+    un.n = max(0, min(n_all, un.jb + per) - un.jb);
     return un;
 }
 
@@ -271,6 +282,27 @@ __device__ __forceinline__ size_t lse_index(const FwdParams &p, const Unit &un, 
 {
     if (p.cu_q != nullptr) return static_cast<size_t>(un.bh) * p.total_q + un.q_tok0 + row;
     return static_cast<size_t>(un.bh) * p.sq + row;
+}
+
+// Zero rows [valid, BN) of the V tile at shared address `tile`, in every
+// panel (a row is 128 contiguous bytes of a panel whatever the swizzle).
+// Those are keys past the end of the unit's sequence that the tile copy
+// still brought in, from the unused part of a KV cache or from the next
+// packed sequence: their probabilities are zero, but a NaN or an infinity
+// stored there would reach O through 0 * x in the P.V product.  Called by
+// a whole warp; the proxy fence makes the stores visible to the MMA that
+// the elected lane issues after the following __syncwarp.
+template <int D, int EB>
+__device__ __forceinline__ void zero_v_tail_rows(uint32_t tile, int valid)
+{
+    using C = Cfg<D, EB>;
+    const int lane = threadIdx.x & 31;
+    const int chunks = (C::BN - valid) * 8;  // 16-byte chunks per panel
+    for (int pn = 0; pn < C::NPANEL; ++pn)
+        for (int c = lane; c < chunks; c += 32)
+            st_shared_v4(tile + pn * C::PANEL_BYTES + valid * 128 + c * 16, 0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    __syncwarp();
 }
 
 // The i-th work unit of this CTA.  Rounds of gridDim.x units are dealt out
@@ -673,6 +705,8 @@ __global__ void __launch_bounds__(384, 1)
         uint32_t kv_it = 0, q_it = 0;
         uint32_t p_ph0 = 0u, p_ph1 = 0u;
         bool ok = true;
+        // keys past a unit's end are in bounds of the V copy (not zero-filled)
+        const bool zero_tail = p.cu_k != nullptr || p.seqlens_k != nullptr;
         auto kv_wait = [&](uint32_t &slot) -> bool {
             slot = kv_it % C::NSLOT;
             ATTN_TRACE(EV_MMA_WAIT_KV, kv_it);
@@ -726,25 +760,33 @@ __global__ void __launch_bounds__(384, 1)
             ATTN_TRACE(EV_MMA_GOT_Q, u);
             if (!ok) break;
             ++q_it;
+            // Q tile 1 holds none of the unit's rows (short queries, as in
+            // decoding): its products are skipped, and its softmax group
+            // skips the unit too.  Its copy is still made (and released).
+            const bool two = un.row0 + C::BM < un.sq;
             uint32_t kslot;
             if (!(ok = kv_wait(kslot))) break;
             tc_fence_after();
             if (elect_one()) {
                 issue_qk(0, kslot);
                 tc_commit(B(ctl->s_full[0]));
-                issue_qk(1, kslot);
-                tc_commit(B(ctl->s_full[1]));
-                tc_commit(B(ctl->kv_empty[kslot]));
-                if (un.n == 1) {
-                    tc_commit(B(ctl->q_empty[0]));
-                    tc_commit(B(ctl->q_empty[1]));
+                if (two) {
+                    issue_qk(1, kslot);
+                    tc_commit(B(ctl->s_full[1]));
                 }
+                tc_commit(B(ctl->kv_empty[kslot]));
+                if (un.n == 1) tc_commit(B(ctl->q_empty[0]));
+                if (un.n == 1 || !two) tc_commit(B(ctl->q_empty[1]));
             }
             __syncwarp();
             for (int j = 0; j < un.n && ok; ++j) {
                 const bool more = j + 1 < un.n;
                 uint32_t vslot, nslot = 0;
                 if (!(ok = kv_wait(vslot))) break;
+                if (zero_tail) {
+                    const int valid = un.sk - (un.jb + j) * C::BN;  // > 0: the tile holds a visible key
+                    if (valid < C::BN) zero_v_tail_rows<D, E::BYTES>(sKV + vslot * C::TILE_BYTES, valid);
+                }
                 if (more && !(ok = kv_wait(nslot))) break;
                 // tile 0
                 ATTN_TRACE(EV_MMA_WAIT_P, 0);
@@ -758,14 +800,17 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_after();
                 if (elect_one()) {
                     issue_pv(0, vslot, true, 1);
+                    if (!two) tc_commit(B(ctl->kv_empty[vslot]));
                     if (!more) tc_commit(B(ctl->o_full[0]));
                     if (more) {
                         issue_qk(0, nslot);
                         tc_commit(B(ctl->s_full[0]));
+                        if (!two) tc_commit(B(ctl->kv_empty[nslot]));
                         if (j + 2 == un.n) tc_commit(B(ctl->q_empty[0]));
                     }
                 }
                 __syncwarp();
+                if (!two) continue;
                 // tile 1
                 ATTN_TRACE(EV_MMA_WAIT_P, 1);
                 if (!(ok = warp_wait(B(ctl->p_half[1]), p_ph1, ctl, p, SITE_MMA_P_FULL))) break;
@@ -818,6 +863,7 @@ __global__ void __launch_bounds__(384, 1)
                 store_row_zero<T>(p, un, row, D);
                 continue;
             }
+            if (t == 1 && un.row0 + C::BM >= un.sq) continue;  // no row here: the tile is not computed
             // keys visible to this row: [0, kend)
             const int kend = CAUSAL ? min(un.sk, row + 1 + (un.sk - un.sq)) : un.sk;
             // l: sum of p in fp32 (gives LSE); lr: sum of p as rounded for
@@ -1000,6 +1046,36 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
         for (int i = 0; i < PER_LANE; ++i) dst[i] = T(acc[i] * inv);
         if (lse && lane == 0) lse[r] = (mx == -INFINITY) ? -INFINITY : mx + logf(sum);
+    }
+}
+
+// KV-cache append: row t of k_new / v_new of head plane bh goes to position
+// clamp(seqlens[bh / h], 0, s_cache) + t of the same plane of the cache;
+// rows that would land at or past s_cache are not written.  One thread per
+// 16-byte chunk of K and of V.
+template <typename T>
+__global__ void attn_kvcache_append_kernel(const T *k_new, const T *v_new, T *k_cache, T *v_cache,
+                                           const int32_t *seqlens, int64_t bh, int64_t h, int64_t s_new,
+                                           int64_t s_cache, int d)
+{
+    const int cpr = d * static_cast<int>(sizeof(T)) / 16;  // chunks per row
+    const int64_t n = bh * s_new * cpr;
+    const uint4 *kn = reinterpret_cast<const uint4 *>(k_new);
+    const uint4 *vn = reinterpret_cast<const uint4 *>(v_new);
+    uint4 *kc = reinterpret_cast<uint4 *>(k_cache);
+    uint4 *vc = reinterpret_cast<uint4 *>(v_cache);
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t row = i / cpr;
+        const int c = static_cast<int>(i - row * cpr);
+        const int64_t plane = row / s_new;
+        const int64_t t = row - plane * s_new;
+        const int64_t start = min(max(static_cast<int64_t>(seqlens[plane / h]), int64_t(0)), s_cache);
+        const int64_t pos = start + t;
+        if (pos >= s_cache) continue;
+        const int64_t dst = (plane * s_cache + pos) * cpr + c;
+        kc[dst] = kn[i];
+        vc[dst] = vn[i];
     }
 }
 

@@ -51,6 +51,22 @@ cudaError_t launch_fill_empty(void *o, float *lse, int64_t rows, int d, cudaStre
     return cudaGetLastError();
 }
 
+template <typename T>
+cudaError_t launch_kvcache_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                                  const int32_t *seqlens, int64_t bh, int64_t h, int64_t s_new, int64_t s_cache, int d,
+                                  int sm_count, cudaStream_t stream)
+{
+    const int64_t n = bh * s_new * (d * static_cast<int64_t>(sizeof(T)) / 16);
+    int64_t blocks = (n + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    attn_kvcache_append_kernel<T><<<static_cast<int>(blocks), 256, 0, stream>>>(
+        static_cast<const T *>(k_new), static_cast<const T *>(v_new), static_cast<T *>(k_cache),
+        static_cast<T *>(v_cache), seqlens, bh, h, s_new, s_cache, d);
+    return cudaGetLastError();
+}
+
 template <typename T, int D>
 cudaError_t launch_splitkv_combine(const float *o_part, const float *lse_part, void *o, float *lse, int64_t rows,
                                    int num_splits, int sm_count, cudaStream_t stream)

@@ -161,6 +161,18 @@ __device__ __forceinline__ void tc_fence_after()
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// Make this thread's generic-proxy shared-memory writes visible to the
+// async proxy (the tensor cores reading an operand).
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 // Arrive (once) on `bar` when all previously issued tcgen05 async ops of this
 // thread have completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar)

@@ -226,3 +226,74 @@ BWD = {bw.name: bw for bw in [
     BwdWorkload("causal_b2_h32_s4096_d128_bf16", 20260009),
     BwdWorkload("noncausal_b8_h16_s1000_d64_bf16", 20260010),
 ]}
+
+
+# KV-cache decoding: b sequences whose cached lengths are seeded, uniform in
+# [lo, hi], in a cache of capacity `cap`; each step writes s_new new tokens
+# per sequence and their s_new queries attend (causally) to everything
+# cached.  The lengths do not advance between steps, so every step repeats
+# the same work.
+@dataclass(frozen=True)
+class KvcacheWorkload:
+    name: str
+    b: int
+    h: int
+    cap: int
+    lo: int
+    hi: int
+    s_new: int
+    d: int
+    dtype: str
+    seed: int
+    causal: bool = True
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def sq(self) -> int:
+        return self.s_new
+
+    def lengths(self):
+        """Cached tokens per sequence before the step."""
+        return varlen_lengths(self.b, self.lo, self.hi, self.seed)
+
+    def visible(self):
+        """Keys seen by each query row, summed (causal: row i of a sequence
+        with n = min(len + s_new, cap) keys sees min(n, n - s_new + i + 1))."""
+        tot = 0
+        for l0 in self.lengths():
+            n = min(max(l0, 0) + self.s_new, self.cap)
+            for i in range(self.sq):
+                tot += max(0, min(n, n - self.sq + i + 1)) if self.causal else n
+        return tot
+
+    def flops(self) -> float:
+        return 4.0 * self.h * self.d * self.visible()
+
+    def bytes(self) -> int:
+        """Algorithmic HBM bytes of one step: the valid K and V read once,
+        Q and the new K/V rows read, the new rows written into the cache,
+        O and the fp32 LSE written."""
+        e = 2
+        valid = sum(min(max(l0, 0) + self.s_new, self.cap) for l0 in self.lengths())
+        rows = self.b * self.h
+        return (e * self.h * self.d * 2 * valid + e * rows * self.sq * self.d + 2 * e * rows * self.s_new * self.d
+                + 2 * e * rows * self.s_new * self.d + e * rows * self.sq * self.d + 4 * rows * self.sq)
+
+
+KVCACHE = {kw.name: kw for kw in [
+    KvcacheWorkload("kvcache_decode_b8_h32_cap16384_len1to16383_d128_bf16", 8, 32, 16384, 1, 16383, 1, 128, "bf16",
+                    20260011),
+]}
+
+
+def kvcache_inputs(kw: KvcacheWorkload):
+    """CPU tensors q [b,h,s_new,d], k_cache/v_cache [b,h,cap,d] (every slot
+    drawn: the unused ones take no part), k_new/v_new [b,h,s_new,d] and the
+    int32 lengths [b]."""
+    q, kc, vc = draw(kw.b, kw.h, kw.sq, kw.cap, kw.d, kw.dtype, kw.seed)
+    _, kn, vn = draw(kw.b, kw.h, 1, kw.s_new, kw.d, kw.dtype, kw.seed + 1)
+    lens = torch.tensor(kw.lengths(), dtype=torch.int32)
+    return q, kc, vc, kn, vn, lens

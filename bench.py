@@ -258,6 +258,143 @@ def bench_varlen(args, w):
     print(json.dumps(line), flush=True)
 
 
+def cpu_baseline_kvcache(kw, q, kc, vc, kn, vn, lens, heads: int = 8):
+    """The fp64 KV-cache oracle, as it stands, on the host cores: all
+    sequences of the decode step, `heads` of their heads, the caches cut to
+    the longest valid length.  Returns (TFLOPS, description, cores, seconds)."""
+    import oracle
+
+    hs = slice(0, min(heads, kw.h))
+    need = min(kw.cap, max(min(max(int(x), 0), kw.cap) + kw.s_new for x in lens.tolist()))
+    args = [t[:, hs].double().numpy() for t in (q, kc[:, :, :need], vc[:, :, :need], kn, vn)]
+    t0 = time.perf_counter()
+    oracle.attn_fwd_kvcache(args[0], args[1], args[2], lens.tolist(), args[3], args[4], kw.causal, kw.scale)
+    dt = time.perf_counter() - t0
+    flops = kw.flops() * (hs.stop / kw.h)
+    desc = (f"heads 0..{hs.stop - 1} of all {kw.b} sequences of {kw.name} (cache write and attention, caches "
+            f"cut to {need} slots; {flops / 1e9:.2f} GFLOP counted as 4*d per visible key)")
+    return flops / dt / 1e12, desc, oracle.num_threads(), dt
+
+
+def bench_kvcache(args, kw):
+    """KV-cache decode workload: one step = one attn_fwd_kvcache call (the
+    cache write, the split-KV forward and the combine)."""
+    import torch
+    import attention_forward_14_gb300 as af
+    from attention_forward_14_gb300 import binding
+    from attention_forward_14_gb300 import workloads as W
+
+    q, kc, vc, kn, vn, lens = W.kvcache_inputs(kw)
+    if args.impl == "reference":
+        per = max(1.0, 120.0 / max(1, args.steps + args.warmup))
+        vals, times, desc, cores = [], [], "", None
+        for i in range(args.warmup + args.steps):
+            tf, desc, cores, dt = cpu_baseline_kvcache(kw, q, kc, vc, kn, vn, lens)
+            if i >= args.warmup:
+                vals.append(tf)
+                times.append(dt)
+        value = statistics.median(vals)
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": kw.name, "b": kw.b, "h": kw.h, "cap": kw.cap, "lengths": kw.lengths(),
+                       "s_new": kw.s_new, "d": kw.d, "causal": kw.causal},
+            "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    qd, kcd, vcd, knd, vnd, lensd = (t.to(dev) for t in (q, kc, vc, kn, vn, lens))
+    o = torch.empty_like(qd)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    splits = args.num_splits or binding.splitkv_default_splits(kw.b, kw.h, kw.sq, kw.cap, kw.d, kw.causal)
+    ws = torch.empty(max(16, binding.splitkv_workspace_bytes(kw.b, kw.h, kw.sq, kw.d, splits)), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        af.attn_fwd_kvcache(qd, kcd, vcd, lensd, knd, vnd, causal=kw.causal, scale=kw.scale, num_splits=splits,
+                            o=o, lse=lse, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    # end to end: per step the new tokens (q, k_new, v_new) and the lengths
+    # go host -> device from pinned memory, O and LSE come back; the cache is
+    # the resident state of the decoder and stays on the device.
+    qh, knh, vnh, lh = (t.pin_memory() for t in (q, kn, vn, lens))
+    oh = torch.empty_like(qh).pin_memory()
+    lseh = torch.empty(q.shape[:3], dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        for src, dst in ((qh, qd), (knh, knd), (vnh, vnd), (lh, lensd)):
+            dst.copy_(src, non_blocking=True)
+        step()
+        oh.copy_(o, non_blocking=True)
+        lseh.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    x1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = x0.elapsed_time(x1) / args.e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (qh, knh, vnh, lh))
+    d2h = oh.numel() * oh.element_size() + lseh.numel() * 4
+
+    peaks = load_peaks()
+    value = kw.flops() / (ms * 1e-3) / 1e12
+    achieved = kw.bytes() / (kern_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": kw.dtype,
+        "data": "synthetic",
+        "config": {"workload": kw.name, "b": kw.b, "h": kw.h, "cap": kw.cap, "lengths": kw.lengths(),
+                   "s_new": kw.s_new, "d": kw.d, "causal": kw.causal, "flops_per_step": kw.flops(),
+                   "l2": f"cache {2 * kc.numel() * 2 / 1e9:.1f} GB > L2, valid K/V {kw.bytes() / 1e9:.2f} GB/step, "
+                         "no flush"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm"], "traffic": profiled_traffic(kw.name),
+                     "peak_kind": f"{peaks['source']} HBM copy",
+                     "kernel": "attn_kvcache_append_kernel + attn_fwd_kernel + attn_splitkv_combine_kernel "
+                               "(one step)",
+                     "algorithmic_bytes": kw.bytes(), "num_splits": splits},
+        "e2e": {"value": kw.flops() / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * (2 + (1 if splits > 1 else 0)),
+        "clocks": sampler.summary(),
+    }
+    if not args.no_cpu_baseline:
+        tf, desc, cores, dt = cpu_baseline_kvcache(kw, q, kc, vc, kn, vn, lens)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": desc,
+                                "seconds": dt}
+    print(json.dumps(line), flush=True)
+
+
 def bench_bwd(args, bw):
     """Backward workload: one step = one attn_bwd call (prep, main and dQ
     convert kernels) on the forward's outputs, inputs resident in HBM."""
@@ -410,6 +547,7 @@ def main():
     ap.add_argument("--workload", default=None)
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-splits", type=int, default=0, help="KV-cache workloads: split count (0 = default)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -417,6 +555,8 @@ def main():
     name = args.workload or W.HEADLINE
     if name in W.VARLEN:
         return bench_varlen(args, W.VARLEN[name])
+    if name in W.KVCACHE:
+        return bench_kvcache(args, W.KVCACHE[name])
     if name in W.BWD:
         if args.impl == "reference":
             raise SystemExit("the reference arm times the forward oracle only")

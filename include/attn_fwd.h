@@ -104,9 +104,10 @@ int attn_fwd_host(const void *q_host, const void *k_host, const void *v_host,
 /*
  * Split-KV forward.  "05 · kernel 工程与四代演化" 2.1 lists split-KV kernels
  * beside the forward and backward ones.  The key range of every (b, h,
- * 256-row block) is cut into `num_splits` ranges of whole 128-key tiles,
- * processed by separate CTAs (this fills the GPU when b*h*ceil(sq/256) is
- * small, as in decoding).  Each range yields a partial softmax: O normalised
+ * 256-row block) -- the keys that block sees -- is cut into `num_splits`
+ * near-equal ranges of whole 128-key tiles, processed by separate CTAs
+ * (this fills the GPU when b*h*ceil(sq/256) is small, as in decoding).
+ * Each range yields a partial softmax: O normalised
  * by its own row sum plus the range's log-sum-exp.  A second kernel merges
  * the ranges with the rescale-and-add step of the online recurrence
  * (flash-attention-minimal forward_kernel: m_new = max, l_new = sum of
@@ -179,9 +180,11 @@ int attn_fwd_fp8(const void *q, const void *k, const void *v, void *o,
 int64_t attn_fwd_splitkv_workspace_bytes(int64_t b, int64_t h, int64_t sq,
                                          int64_t d, int num_splits);
 
-/* A split count that gives the current device at least two work units per
- * SM while keeping at least two key tiles per split (1 when the problem
- * already has that many units), or a negative ATTN_ERR_* code. */
+/* A split count for the current device: 1 when the problem has more than
+ * 64 query rows and at least one work unit per SM; otherwise the count
+ * whose units (b*h*ceil(sq/256)*splits) fill whole waves of the SMs best,
+ * less 1% per wave, keeping at least two key tiles per split.  A negative
+ * ATTN_ERR_* code for invalid sizes. */
 int attn_fwd_splitkv_default_splits(int64_t b, int64_t h, int64_t sq,
                                     int64_t sk, int64_t d, int causal);
 
@@ -216,6 +219,46 @@ int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v,
                              int64_t sq, int64_t sk, int64_t d, int causal,
                              float scale, int dtype, int num_splits,
                              void *stream);
+
+/*
+ * KV-cache forward (decoding).  "05 · kernel 工程与四代演化" 6.1 lists
+ * fwd_kvcache among the exported entry points without defining it; the
+ * reading here is the plainest one: attention of the new queries against a
+ * cache whose batch elements hold different numbers of valid tokens, after
+ * the new tokens' keys and values have been written into the cache.
+ *
+ *   q          : [b, h, sq, d] of dtype, contiguous, 16-byte aligned.
+ *   k_cache,
+ *   v_cache    : [b, h, s_cache, d] of dtype, contiguous, 16-byte aligned;
+ *                s_cache is the capacity.  Written when k_new is given.
+ *   k_new,
+ *   v_new      : [b, h, s_new, d] of dtype, contiguous, 16-byte aligned,
+ *                or both NULL (then s_new must be 0).  They must not
+ *                overlap the caches (ATTN_ERR_SHAPE).
+ *   cache_seqlens : device int32 [b], the number of valid cached tokens of
+ *                each batch element before this call (read, not updated).
+ *                Values are clamped to [0, s_cache].
+ * With L0 = clamp(cache_seqlens[b], 0, s_cache):
+ *   1. row t of k_new / v_new is written to position L0 + t of the cache;
+ *      rows that would land at or past s_cache are dropped;
+ *   2. batch element b attends to its first L = min(L0 + s_new, s_cache)
+ *      cached keys: attn_fwd on q[b] and k/v_cache[b, :, :L], with the
+ *      causal mask bottom-right aligned to L (query i sees keys
+ *      j <= i + L - sq), O = 0 and LSE = -inf for a row that sees no key.
+ * Cache slots at or past L are never read into the result (they may hold
+ * anything, NaN included).  num_splits, workspace and workspace_bytes are
+ * those of attn_fwd_splitkv with sk = s_cache (num_splits 1: no workspace).
+ * o, lse, d, causal, scale, dtype, stream as for attn_fwd.  Asynchronous;
+ * the cache write precedes the attention on `stream`.
+ * Returns ATTN_OK or a negative ATTN_ERR_* code.
+ */
+int attn_fwd_kvcache(const void *q, void *k_cache, void *v_cache,
+                     const void *k_new, const void *v_new,
+                     const int32_t *cache_seqlens, void *o, float *lse,
+                     int64_t b, int64_t h, int64_t sq, int64_t s_cache,
+                     int64_t s_new, int64_t d, int causal, float scale,
+                     int dtype, int num_splits, void *workspace,
+                     int64_t workspace_bytes, void *stream);
 
 /*
  * Backward pass: the gradients of attn_fwd.  "05 · kernel 工程与四代演化" 6.1

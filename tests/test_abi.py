@@ -131,3 +131,32 @@ def test_bwd_workspace_bytes(lib):
     assert lib.attn_bwd_workspace_bytes(1, 1, 4, 96) == -3
     assert lib.attn_bwd_workspace_bytes(1, 1, 128, 64) == 128 * 64 * 4 + 2 * 128 * 4 + 256
     assert lib.attn_bwd_workspace_bytes(-1, 1, 4, 128) == -2
+
+
+def call_kvcache(lib, kn=None, vn=None, seqlens=P, b=1, h=2, sq=1, cap=1000, s_new=0, d=128, splits=1,
+                 ws=None, ws_bytes=0, cache=P):
+    rc = lib.attn_fwd_kvcache(P, cache, cache, kn, vn, seqlens, P, None, b, h, sq, cap, s_new, d, 1, 0.1, 1,
+                              splits, ws, ws_bytes, None)
+    return rc, lib.attn_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(seqlens=None), -1),                       # no lengths
+    (dict(seqlens=P + 2), -6),                      # misaligned lengths
+    (dict(s_new=2), -1),                            # new rows announced, none given
+    (dict(kn=P + 1024, s_new=1), -1),               # k_new without v_new
+    (dict(s_new=-1), -2),
+    (dict(splits=0), -2), (dict(splits=9), -2),     # 1000 keys = 8 tiles of 128
+    (dict(splits=4), -1),                           # split-KV without a workspace
+    (dict(kn=P, vn=P, s_new=1), -2),                # new rows overlap the cache
+    (dict(kn=P + 8, vn=P + 8, s_new=1, cache=P + 2048), -6),  # misaligned new rows
+    (dict(d=96), -3),
+])
+def test_kvcache_argument_errors(lib, kw, code):
+    rc, msg = call_kvcache(lib, **kw)
+    assert rc == code, (rc, msg)
+
+
+def test_kvcache_nothing_to_do(lib):
+    assert call_kvcache(lib, b=0, seqlens=None)[0] == 0
+    assert call_kvcache(lib, h=0, seqlens=None)[0] == 0

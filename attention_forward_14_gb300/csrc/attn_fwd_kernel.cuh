@@ -705,8 +705,9 @@ __global__ void __launch_bounds__(384, 1)
         uint32_t kv_it = 0, q_it = 0;
         uint32_t p_ph0 = 0u, p_ph1 = 0u;
         bool ok = true;
-        // keys past a unit's end are in bounds of the V copy (not zero-filled)
-        const bool zero_tail = p.cu_k != nullptr || p.seqlens_k != nullptr;
+        // keys past a unit's end are in bounds of the V copy (not zero-filled);
+        // the 8-bit forward is dense only, where the copy engine zero-fills them
+        const bool zero_tail = !E::FP8 && (p.cu_k != nullptr || p.seqlens_k != nullptr);
         auto kv_wait = [&](uint32_t &slot) -> bool {
             slot = kv_it % C::NSLOT;
             ATTN_TRACE(EV_MMA_WAIT_KV, kv_it);

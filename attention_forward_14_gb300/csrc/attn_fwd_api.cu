@@ -2,6 +2,7 @@
 // include/attn_fwd.h): argument validation, TMA tensor maps, persistent grid
 // sizing, dispatch to the <head_dim, dtype, causal> instances, device
 // watchdog status.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -46,6 +47,13 @@ unsigned long long *g_trace_buf = nullptr;  // timeline builds only: where launc
 // Watchdog status word, one per device that loads this library.
 __device__ uint32_t g_watchdog[4];
 
+// Counter pairs of the forward's dynamic schedule.  Each launch that uses
+// one takes the next pair in turn; the kernel leaves it at zero when it
+// finishes, so a pair is ready again once its previous launch has ended
+// (launches more than kSchedSlots apart never overlap in practice).
+constexpr int kSchedSlots = 256;
+__device__ int32_t g_fwd_sched[2 * kSchedSlots];
+
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
@@ -54,6 +62,8 @@ struct DeviceInfo {
     int sm_count = 0;
     int cc_major = 0, cc_minor = 0;
     uint32_t *status = nullptr;
+    int32_t *sched = nullptr;
+    std::atomic<uint32_t> sched_next{0};
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -71,6 +81,8 @@ int device_info(DeviceInfo **out)
         if (r == cudaSuccess) r = cudaDeviceGetAttribute(&di.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
         if (r == cudaSuccess && di.cc_major == 10 && di.cc_minor == 3)
             r = cudaGetSymbolAddress(reinterpret_cast<void **>(&di.status), g_watchdog);
+        if (r == cudaSuccess && di.cc_major == 10 && di.cc_minor == 3)
+            r = cudaGetSymbolAddress(reinterpret_cast<void **>(&di.sched), g_fwd_sched);
         di.err = r;
     });
     if (di.err != cudaSuccess) return cuda_fail(di.err, "device query");
@@ -220,10 +232,18 @@ struct SplitArgs {
 
 // KV cache: per batch element, the number of valid keys is
 // clamp(seqlens[b], 0, sk) + add, at most sk (sk is the cache capacity).
+// Units of unequal work (per-element lengths) are handed out dynamically.
 struct CacheArgs {
     const int32_t *seqlens = nullptr;
     int32_t add = 0;
 };
+
+// The next counter pair of the dynamic schedule on this device.
+int32_t *sched_slot(DeviceInfo *di)
+{
+    const uint32_t s = di->sched_next.fetch_add(1, std::memory_order_relaxed) % kSchedSlots;
+    return di->sched + 2 * s;
+}
 
 int64_t kv_tiles(int64_t sk) { return (sk + 127) / 128; }
 
@@ -270,6 +290,7 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_
     p.total_k = static_cast<int32_t>(sk);
     p.seqlens_k = cache.seqlens;
     p.seqlens_add = cache.add;
+    p.sched = cache.seqlens != nullptr ? sched_slot(di) : nullptr;
     const int64_t units = bh * p.num_mblk * split.num_splits;
     if (units > INT32_MAX) return fail(ATTN_ERR_SHAPE, "too many work units (%lld)", (long long)units);
     p.num_units = static_cast<int32_t>(units);
@@ -884,6 +905,7 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float 
     p.lse_part = nullptr;
     p.cu_q = cu_seqlens_q;
     p.cu_k = cu_seqlens_k;
+    p.sched = sched_slot(di);  // sequences differ in length: hand units out dynamically
     p.heads = static_cast<int32_t>(h);
     p.total_q = static_cast<int32_t>(total_q);
     p.total_k = static_cast<int32_t>(total_k);

@@ -93,6 +93,10 @@ struct FwdParams {
     // keys (device int32 [b]; bh = b * heads).  nullptr: all sk keys.
     const int32_t *seqlens_k = nullptr;
     int32_t seqlens_add = 0;
+    // Dynamic schedule: {next unit to hand out, CTAs finished}, both zero on
+    // entry; the last CTA to finish sets them back to zero.  nullptr: every
+    // CTA takes a fixed share of the units (unit_at).
+    int32_t *sched = nullptr;
 #ifdef ATTN_TRACE_ENABLE
     unsigned long long *trace;  // per-warp event records (timeline builds only)
 #endif
@@ -135,6 +139,8 @@ enum : uint32_t {
     SITE_SOFTMAX_S_FULL = 6,
     SITE_SOFTMAX_O_FULL = 7,
     SITE_DRAIN = 8,
+    SITE_UNIT_FULL = 9,
+    SITE_UNIT_EMPTY = 10,
 };
 
 // Input element types: fp16, bf16 (16-bit, kind::f16 MMAs, P two per
@@ -205,10 +211,14 @@ struct Ctl {
     uint64_t kv_full[8], kv_empty[8];
     uint64_t s_full[2], p_half[2], p_full[2], o_full[2];
     uint64_t mma_done;
+    uint64_t unit_full[4], unit_empty[4];  // ring of claimed unit indices (dynamic schedule)
+    int32_t unit_idx[4];
     uint32_t tmem_base;
     uint32_t abort;
 };
 static_assert(sizeof(Ctl) <= 1024, "control block");
+constexpr int kUnitRing = 4;
+constexpr int kUnitReaders = 9;  // the MMA warp and the 8 softmax warps
 
 struct Unit {
     int bh;      // dense: b*h index of the head plane; varlen: head index
@@ -361,6 +371,50 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Ctl *ct
 {
     const bool w = bar_wait(bar, parity, ctl, p, site);
     return __all_sync(0xffffffffu, w);
+}
+
+// The i-th unit of this CTA, for a warp that consumes the schedule (the MMA
+// and softmax warps), called by the whole warp.  u = -1: no more units;
+// u = -2: a hole in the last round of the fixed deal (skip it).  With the
+// dynamic schedule the index comes from the ring the producer fills, and
+// lane 0 releases the slot.  Returns false when a wait gave up.
+__device__ __forceinline__ bool consumer_unit(uint32_t i, int &u, Ctl *ctl, const FwdParams &p)
+{
+    if (p.sched == nullptr) {
+        if (static_cast<long long>(i) * gridDim.x >= p.num_units) {
+            u = -1;
+        } else {
+            u = unit_at(static_cast<int>(i));
+            if (u >= p.num_units) u = -2;
+        }
+        return true;
+    }
+    const uint32_t slot = i % kUnitRing;
+    if (!warp_wait(smem_addr(&ctl->unit_full[slot]), (i / kUnitRing) & 1u, ctl, p, SITE_UNIT_FULL)) return false;
+    u = *reinterpret_cast<volatile int32_t *>(&ctl->unit_idx[slot]);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(smem_addr(&ctl->unit_empty[slot]));
+    return true;
+}
+
+// The same for the producer warp, which with the dynamic schedule claims
+// the next unit from the global counter (in order: the unit order is the
+// priority order) and publishes it in the ring.
+__device__ __forceinline__ bool producer_unit(uint32_t i, int &u, Ctl *ctl, const FwdParams &p)
+{
+    if (p.sched == nullptr) return consumer_unit(i, u, ctl, p);
+    const uint32_t slot = i % kUnitRing;
+    if (!warp_wait(smem_addr(&ctl->unit_empty[slot]), ((i / kUnitRing) & 1u) ^ 1u, ctl, p, SITE_UNIT_EMPTY))
+        return false;
+    int v = -1;
+    if ((threadIdx.x & 31) == 0) {
+        v = atomicAdd(p.sched, 1);
+        if (v >= p.num_units) v = -1;
+        ctl->unit_idx[slot] = v;
+        mbar_arrive(smem_addr(&ctl->unit_full[slot]));
+    }
+    u = __shfl_sync(0xffffffffu, v, 0);
+    return true;
 }
 
 template <typename T>
@@ -584,6 +638,10 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(B(ctl->kv_empty[s]), 1);
         }
         mbar_init(B(ctl->mma_done), 1);
+        for (int s = 0; s < kUnitRing; ++s) {
+            mbar_init(B(ctl->unit_full[s]), 1);
+            mbar_init(B(ctl->unit_empty[s]), kUnitReaders);
+        }
         ctl->abort = 0u;
         fence_barrier_init();
     }
@@ -616,9 +674,11 @@ __global__ void __launch_bounds__(384, 1)
         const uint64_t pol_kv = l2_evict_normal();
         uint32_t kv_it = 0, q_it = 0;
         bool ok = true;
-        for (int i = 0; i * static_cast<int>(gridDim.x) < p.num_units && ok; ++i) {
-            const int u = unit_at(i);
-            if (u >= p.num_units) continue;
+        for (uint32_t i = 0; ok; ++i) {
+            int u;
+            if (!(ok = producer_unit(i, u, ctl, p))) break;
+            if (u == -1) break;
+            if (u < 0) continue;
             const Unit un = decode_unit<D, CAUSAL>(u, p);
             if (un.n == 0) continue;
             // TMA coordinates (after the 64-column panel): dense maps are
@@ -750,9 +810,11 @@ __global__ void __launch_bounds__(384, 1)
                     mma_ts(d, a + kk * 8, b0 + bo, IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
             }
         };
-        for (int i = 0; i * static_cast<int>(gridDim.x) < p.num_units && ok; ++i) {
-            const int u = unit_at(i);
-            if (u >= p.num_units) continue;
+        for (uint32_t i = 0; ok; ++i) {
+            int u;
+            if (!(ok = consumer_unit(i, u, ctl, p))) break;
+            if (u == -1) break;
+            if (u < 0) continue;
             const Unit un = decode_unit<D, CAUSAL>(u, p);
             if (un.n == 0) continue;
             ATTN_TRACE(EV_MMA_WAIT_Q, u);
@@ -855,9 +917,11 @@ __global__ void __launch_bounds__(384, 1)
         const bool neg = sl2e < 0.f;  // the row maximum of scale*s is scale*min(s)
         uint32_t s_ph = 0u, o_ph = 0u;
         bool ok = true;
-        for (int i = 0; i * static_cast<int>(gridDim.x) < p.num_units && ok; ++i) {
-                const int u = unit_at(i);
-                if (u >= p.num_units) continue;
+        for (uint32_t i = 0; ok; ++i) {
+            int u;
+            if (!(ok = consumer_unit(i, u, ctl, p))) break;
+            if (u == -1) break;
+            if (u < 0) continue;
             const Unit un = decode_unit<D, CAUSAL>(u, p);
             const int row = un.row0 + t * C::BM + r_in_tile;
             if (un.n == 0) {
@@ -993,6 +1057,16 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 8) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+    // Dynamic schedule: every claim of this CTA has returned; the last CTA
+    // to get here leaves the counter pair at zero for the next launch.
+    if (p.sched != nullptr && threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+            p.sched[0] = 0;
+            p.sched[1] = 0;
+            __threadfence();
+        }
     }
 }
 

@@ -238,6 +238,17 @@ struct CacheArgs {
     int32_t add = 0;
 };
 
+// Head planes per group of the causal unit order: as many as keep the K and
+// V of the group's heads (sk keys of d elements) within 48 MB of L2.
+int32_t l2_group(int64_t bh, int64_t sk, int64_t d, int64_t elem_bytes)
+{
+    const int64_t per_head = 2 * sk * d * elem_bytes;
+    int64_t g = per_head > 0 ? (int64_t(48) << 20) / per_head : bh;
+    if (g < 1) g = 1;
+    if (g > bh) g = bh;
+    return static_cast<int32_t>(g);
+}
+
 // The next counter pair of the dynamic schedule on this device.
 int32_t *sched_slot(DeviceInfo *di)
 {
@@ -906,6 +917,7 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float 
     p.cu_q = cu_seqlens_q;
     p.cu_k = cu_seqlens_k;
     p.sched = sched_slot(di);  // sequences differ in length: hand units out dynamically
+    p.group = l2_group(bh, max_seqlen_k, d, 2);
     p.heads = static_cast<int32_t>(h);
     p.total_q = static_cast<int32_t>(total_q);
     p.total_k = static_cast<int32_t>(total_k);

@@ -97,6 +97,11 @@ struct FwdParams {
     // entry; the last CTA to finish sets them back to zero.  nullptr: every
     // CTA takes a fixed share of the units (unit_at).
     int32_t *sched = nullptr;
+    // Causal unit order: > 0 orders the units in groups of `group` head
+    // planes, heaviest row block first within each group, so that the K/V
+    // the units in flight stream stay in L2; 0 orders all heads heaviest
+    // first.
+    int32_t group = 0;
 #ifdef ATTN_TRACE_ENABLE
     unsigned long long *trace;  // per-warp event records (timeline builds only)
 #endif
@@ -239,7 +244,14 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams &p)
     un.split = u % p.num_splits;
     const int v = u / p.num_splits;  // (bh, row block) index
     int mblk, bh;
-    if (CAUSAL) {  // heaviest row blocks first
+    if (CAUSAL && p.group > 0) {  // head groups, heaviest row blocks first within each
+        const int per = p.group * p.num_mblk;
+        const int g = v / per;
+        const int r = v - g * per;
+        const int gsize = min(p.group, p.bh - g * p.group);
+        mblk = p.num_mblk - 1 - r / gsize;
+        bh = g * p.group + r % gsize;
+    } else if (CAUSAL) {  // heaviest row blocks first
         mblk = p.num_mblk - 1 - v / p.bh;
         bh = v % p.bh;
     } else {       // consecutive units share a head (K/V reuse in L2)

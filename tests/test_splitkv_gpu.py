@@ -95,3 +95,21 @@ def test_decode_workload_full(name):
     o, lse = _run(q, k, v, w.causal, w.scale, splits)
     o_ref, lse_ref = oracle.attn_fwd(q.double().numpy(), k.double().numpy(), v.double().numpy(), w.causal, w.scale)
     compare(o, lse, o_ref, lse_ref, w.dtype, name)
+
+
+def test_default_split_counts():
+    """The default fills whole waves of the SMs for short queries and does
+    not split problems with many query rows that already fill the GPU."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # many query rows, at least one unit per SM: no split
+    assert binding.splitkv_default_splits(1, 32, 2048, 16384, 128, True) == 1
+    # decode, b*h = 256 units: the count with the best wave fill
+    s = binding.splitkv_default_splits(8, 32, 1, 16384, 128)
+    units = 256 * s
+    fill = units / (sms * -(-units // sms))
+    assert s > 1 and fill > 0.9, (s, fill)
+    # one key tile: nothing to split
+    assert binding.splitkv_default_splits(4, 4, 1, 100, 64) == 1
+    # every split keeps at least two key tiles
+    s = binding.splitkv_default_splits(1, 1, 1, 1024, 128)
+    assert 1 <= s <= 4

@@ -92,3 +92,27 @@ def test_varlen_workload_full_size(name):
             o_ref, lse_ref = oracle.attn_fwd(qs[:, hh:hh + 1].double().numpy(), ks[:, hh:hh + 1].double().numpy(),
                                              vs[:, hh:hh + 1].double().numpy(), w.causal, w.scale)
             compare(o[a:b, hh][None, None], lse[hh, a:b][None, None], o_ref, lse_ref, w.dtype, f"seq {s} head {hh}")
+
+
+def test_varlen_repeated_launches_reuse_the_schedule_counters():
+    """Packed problems hand out work units through a device counter that each
+    launch takes from a rotating set of 256 and leaves at zero.  300 launches
+    of two alternating problems (so every counter is reused) must each give
+    the first result of their problem bit for bit."""
+    dev = torch.device("cuda", 0)
+    probs = []
+    for seed, lens in ((11, [700, 64, 1500]), (12, [300, 2049])):
+        q, k, v, cu_q, cu_k, _ = W.draw_varlen(lens, lens, 4, 128, "bf16", seed)
+        probs.append(((q.to(dev), k.to(dev), v.to(dev), cu_q.to(dev), cu_k.to(dev)), max(lens)))
+    ref = []
+    for (q, k, v, cq, ck), mx in probs:
+        o, lse = af.attn_fwd_varlen(q, k, v, cq, ck, mx, mx, causal=True)
+        ref.append((o.clone(), lse.clone()))
+    torch.cuda.synchronize()
+    outs = []
+    for i in range(300):
+        (q, k, v, cq, ck), mx = probs[i % 2]
+        outs.append(af.attn_fwd_varlen(q, k, v, cq, ck, mx, mx, causal=True))
+    torch.cuda.synchronize()
+    for i, (o, lse) in enumerate(outs):
+        assert torch.equal(o, ref[i % 2][0]) and torch.equal(lse, ref[i % 2][1]), f"launch {i} differs"

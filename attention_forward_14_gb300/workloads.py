@@ -297,3 +297,39 @@ def kvcache_inputs(kw: KvcacheWorkload):
     _, kn, vn = draw(kw.b, kw.h, 1, kw.s_new, kw.d, kw.dtype, kw.seed + 1)
     lens = torch.tensor(kw.lengths(), dtype=torch.int32)
     return q, kc, vc, kn, vn, lens
+
+
+# Backward of the packed workload: its q, k, v plus a seeded output gradient
+# dO ~ N(0, 1) [total, h, d]; one step is one attn_bwd_varlen call.
+@dataclass(frozen=True)
+class BwdVarlenWorkload:
+    fwd: str
+    grad_seed: int
+
+    @property
+    def w(self) -> VarlenWorkload:
+        return VARLEN[self.fwd]
+
+    @property
+    def name(self) -> str:
+        return "bwd_" + self.fwd
+
+    def flops(self) -> float:
+        return 2.5 * self.w.flops()
+
+    def bytes(self) -> int:
+        t = sum(self.w.lengths())
+        e = 2
+        # read q, k, v, o, dO and lse; write dq, dk, dv
+        return 8 * e * t * self.w.h * self.w.d + 4 * self.w.h * t
+
+
+BWD_VARLEN = {bw.name: bw for bw in [
+    BwdVarlenWorkload("varlen_16seq_512to8192_h32_d128_bf16_causal", 20260012),
+]}
+
+
+def bwd_varlen_grad(bw: BwdVarlenWorkload):
+    """The seeded dO [total, h, d] of the packed backward workload."""
+    t = sum(bw.w.lengths())
+    return draw_grad(1, t, bw.w.h, bw.w.d, bw.w.dtype, bw.grad_seed)[0]

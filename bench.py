@@ -491,6 +491,95 @@ def bench_bwd(args, bw):
     print(json.dumps(line), flush=True)
 
 
+def bench_bwd_varlen(args, bw):
+    """Packed backward workload: one step = one attn_bwd_varlen call (prep,
+    main and dQ convert kernels) on the packed forward's outputs."""
+    import torch
+    import attention_forward_14_gb300 as af
+    from attention_forward_14_gb300 import workloads as W
+
+    if int(os.environ.get("WORLD_SIZE", "1")) != 1:
+        raise SystemExit("the backward workloads run on one GPU")
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = bw.w
+    lens = w.lengths()
+    q, k, v, cu_q, cu_k, _ = W.varlen_inputs(w)
+    do = W.bwd_varlen_grad(bw)
+    qd, kd, vd, dod, cqd, ckd = (t.to(dev) for t in (q, k, v, do, cu_q, cu_k))
+    mx = max(lens)
+    o, lse = af.attn_fwd_varlen(qd, kd, vd, cqd, ckd, mx, mx, causal=w.causal, scale=w.scale)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    stream = torch.cuda.current_stream(dev)
+    from attention_forward_14_gb300 import binding
+    need = int(binding.load().attn_bwd_varlen_workspace_bytes(len(lens), w.h, q.shape[0], mx, w.d))
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+
+    def step():
+        af.attn_bwd_varlen(qd, kd, vd, o, dod, lse, cqd, ckd, mx, mx, causal=w.causal, scale=w.scale, dq=dq, dk=dk,
+                           dv=dv, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    step_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    value = bw.flops() / (ms * 1e-3) / 1e12
+    achieved = bw.flops() / (step_ms * 1e-3) / 1e12
+
+    # end to end: H2D of q, k, v, o, dO, lse and the offsets from pinned
+    # memory, the backward, D2H of dq, dk, dv, every step
+    devs = (qd, kd, vd, o, dod, lse, cqd, ckd)
+    hs = [t.cpu().pin_memory() for t in devs]
+    outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        for dst, src in zip(devs, hs):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in zip(outs, (dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    peaks = load_peaks()
+    line = {
+        "metric": METRIC_BWD, "value": value, "unit": "TFLOPS", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": bw.name, "pass": "backward", "sequences": w.n, "lengths": lens,
+                   "total_tokens": int(q.shape[0]), "h": w.h, "d": w.d, "causal": w.causal,
+                   "flops_per_step": bw.flops(), "flops_rule": "2.5 x forward (five products: S, dP, dV, dK, dQ)",
+                   "l2": "inputs larger than L2, no flush"},
+        "pct_of_peak": 100.0 * value / peaks["bf16"],
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16"], "traffic": profiled_traffic(bw.name, "attn_bwd_kernel"),
+                     "peak_kind": f"{peaks['source']} bf16 dense burst (cuBLAS)",
+                     "kernel": "attn_bwd_kernel (+ prep and dQ convert, timed together)",
+                     "algorithmic_bytes": bw.bytes()},
+        "e2e": {"value": bw.flops() / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hs),
+                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs), "ms_per_step": e2e_ms},
+        "gpu_launches": 3 * args.steps,
+        "clocks": sampler.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def _finish_fp8(args, w, world, rank, dist, dev, q, k, v, qd, kd, vd, o, lse, stream, t_all0, t_all1, total_ms,
                 launch_ms, sampler, step):
     """e4m3 line: roofline against the 8-bit tensor peak (measured bf16 peak
@@ -555,6 +644,10 @@ def main():
     name = args.workload or W.HEADLINE
     if name in W.VARLEN:
         return bench_varlen(args, W.VARLEN[name])
+    if name in W.BWD_VARLEN:
+        if args.impl == "reference":
+            raise SystemExit("the reference arm times the forward oracle only")
+        return bench_bwd_varlen(args, W.BWD_VARLEN[name])
     if name in W.KVCACHE:
         return bench_kvcache(args, W.KVCACHE[name])
     if name in W.BWD:

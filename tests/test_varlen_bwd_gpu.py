@@ -86,3 +86,55 @@ def test_varlen_bwd_matches_oracle_and_dense(lens_q, lens_k, h, d, dtype, causal
             assert torch.equal(ddv[0].cpu(), dv[c:e].transpose(0, 1)), f"seq{s}: dV differs from the dense backward"
             tol = 2.0 ** -7 * float(ddq.abs().max()) + 1e-6
             assert float((ddq[0].cpu().float() - dq[a:b].transpose(0, 1).float()).abs().max()) <= tol
+
+
+@pytest.mark.parametrize("name", list(W.BWD_VARLEN))
+def test_bwd_varlen_workload_sampled(name):
+    """The benchmarked packed backward at full size.  All planes run with the
+    GPU forward's O and LSE, except two sampled (sequence, head) planes (the
+    longest sequence and a seeded other one) that get the oracle's; on
+    those, sampled query rows of dQ and sampled keys of dK, dV are checked
+    against the oracle under the per-element bound."""
+    bw = W.BWD_VARLEN[name]
+    w = bw.w
+    lens = w.lengths()
+    q, k, v, cu_q, cu_k, dense = W.varlen_inputs(w)
+    do = W.bwd_varlen_grad(bw)
+    dev = torch.device("cuda", 0)
+    qd, kd, vd, dod, cqd, ckd = (t.to(dev) for t in (q, k, v, do, cu_q, cu_k))
+    mx = max(lens)
+    o, lse = af.attn_fwd_varlen(qd, kd, vd, cqd, ckd, mx, mx, causal=w.causal, scale=w.scale)
+    rng = np.random.default_rng(9)
+    longest = int(np.argmax(lens))
+    other = int(rng.integers(0, len(lens) - 1))
+    other = other + 1 if other >= longest else other
+    planes = [(longest, 0), (other, int(rng.integers(0, w.h)))]
+    ref = {}
+    for s, hi in planes:
+        a, L = int(cu_q[s]), lens[s]
+        qs, ks, vs = (t[0, hi].double().numpy() for t in dense[s])
+        dos = do[a:a + L, hi].double().numpy()
+        o_ref, lse_ref = oracle.attn_fwd(qs[None, None], ks[None, None], vs[None, None], w.causal, w.scale)
+        o[a:a + L, hi] = torch.from_numpy(o_ref[0, 0]).to(o.dtype).to(dev)
+        lse[hi, a:a + L] = torch.from_numpy(lse_ref[0, 0]).float().to(dev)
+        rows = np.unique(np.concatenate([[0, L - 1], rng.integers(0, L, 40)]))
+        cols = np.unique(np.concatenate([[0, L - 1], rng.integers(0, L, 40)]))
+        dq_r = oracle.attn_bwd_dq_rows(qs, ks, vs, dos, rows, w.causal, w.scale)
+        dk_r, dv_r = oracle.attn_bwd_dkv_cols(qs, ks, vs, dos, cols, w.causal, w.scale)
+        ref[(s, hi)] = (qs, ks, vs, dos, o_ref[0, 0], lse_ref[0, 0], rows, cols, dq_r, dk_r, dv_r)
+    dq, dk, dv = af.attn_bwd_varlen(qd, kd, vd, o, dod, lse, cqd, ckd, mx, mx, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    for (s, hi), (qs, ks, vs, dos, o_ref, lse_ref, rows, cols, dq_r, dk_r, dv_r) in ref.items():
+        a = int(cu_q[s])
+        bq, bk, bv = bounds(qs, ks, vs, dos, o_ref, lse_ref, dq_r, dk_r, dv_r, w.causal, w.scale, w.dtype,
+                            rows=rows, cols=cols)
+        ri = torch.as_tensor(a + rows, device=dev)
+        ci = torch.as_tensor(a + cols, device=dev)
+        got_q = dq[ri, hi].float().cpu().double().numpy()
+        got_k = dk[ci, hi].float().cpu().double().numpy()
+        got_v = dv[ci, hi].float().cpu().double().numpy()
+        res = [check(f"{name} {nm} (seq {s}, head {hi})", g, r, bd)
+               for nm, g, r, bd in (("dq", got_q, dq_r, bq), ("dk", got_k, dk_r, bk), ("dv", got_v, dv_r, bv))]
+        print(name, (s, hi), [(round(x, 3), f"{y:.2e}") for x, y in res])
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t).all()

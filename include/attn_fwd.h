@@ -149,6 +149,10 @@ int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o,
  * The causal mask is bottom-right per sequence.  A sequence whose offsets
  * fall outside the totals is skipped (its outputs are not written).  Same
  * error codes as attn_fwd.
+ * Work units of unequal size are handed out through one of 256 device
+ * counters that launches of this entry point and of attn_fwd_kvcache take in
+ * turn (each launch leaves its counter at zero when it ends), so at most 256
+ * such launches may be in flight on one device at a time.
  */
 int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o,
                     float *lse, const int32_t *cu_seqlens_q,
@@ -249,7 +253,9 @@ int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v,
  * anything, NaN included).  num_splits, workspace and workspace_bytes are
  * those of attn_fwd_splitkv with sk = s_cache (num_splits 1: no workspace).
  * o, lse, d, causal, scale, dtype, stream as for attn_fwd.  Asynchronous;
- * the cache write precedes the attention on `stream`.
+ * the cache write precedes the attention on `stream`.  The schedule
+ * counters of attn_fwd_varlen are used here too (same limit of 256 launches
+ * in flight per device).
  * Returns ATTN_OK or a negative ATTN_ERR_* code.
  */
 int attn_fwd_kvcache(const void *q, void *k_cache, void *v_cache,

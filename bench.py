@@ -768,6 +768,9 @@ def main():
                        if in_bytes > L2_BYTES else "inputs fit in L2 (no flush)"},
             "pct_of_peak": 100.0 * value / world / peaks["bf16"],
             "pct_of_sustained_peak": 100.0 * value / world / peaks["bf16_sustained"],
+            # algorithmic bytes / launch time: the figure that matters below the ridge (small problems)
+            "algorithmic_gbs": w.bytes() / (kern_ms * 1e-3) / 1e9,
+            "pct_of_hbm": 100.0 * w.bytes() / (kern_ms * 1e-3) / 1e9 / peaks["hbm"],
             "roofline": ({"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
                           "frac": achieved / peaks["bf16"], "traffic": profiled_traffic(w.name),
                           "peak_kind": f"{peaks['source']} bf16 dense burst (cuBLAS)",
@@ -787,7 +790,8 @@ def main():
         if not args.no_cpu_baseline and world == 1:
             tf, desc, cores, dt = cpu_baseline(w, q, k, v)
             line["cpu_baseline"] = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
-                                    "sample": desc, "seconds": dt}
+                                    "sample": desc, "seconds": dt,
+                                    "extrapolated_full_seconds": w.flops() / (tf * 1e12)}
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()

@@ -287,6 +287,27 @@ __host__ __device__ constexpr uint32_t idesc(int M, int N, bool bf16, bool a_mn,
            ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Zero rows [valid, 128) of a shared-memory tile of NPANEL panels of 128
+// rows x 128 bytes (a row is 128 contiguous bytes of a panel whatever the
+// swizzle).  Packed sequences: a tile that runs past a sequence's end holds
+// the next sequence's tokens, which every product must see as zeros (their
+// probabilities are zero, but 0 * x with x non-finite would not be).  Called
+// by a whole warp; the proxy fence makes the stores visible to the tensor
+// cores, which the elected lane drives after the closing __syncwarp.
+template <int NPANEL>
+__device__ __forceinline__ void zero_rows_from(uint32_t tile, int valid)
+{
+    if (valid >= 128) return;
+    const int lane = threadIdx.x & 31;
+    const int first = valid > 0 ? valid : 0;
+    const int chunks = (128 - first) * 8;  // 16-byte chunks per panel
+    for (int pn = 0; pn < NPANEL; ++pn)
+        for (int c = lane; c < chunks; c += 32)
+            st_shared_v4(tile + pn * 16384 + first * 128 + c * 16, 0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    __syncwarp();
+}
+
 // ---------------------------------------------------------------- waits
 
 // Forced inline: the callers run under different setmaxnreg budgets.
@@ -733,7 +754,13 @@ __global__ void __launch_bounds__(512, 1)
                 const Unit un = decode_unit<CAUSAL, VARLEN>(u, p);
                 if (un.n == 0) continue;
                 if (!(ok = warp_wait(B(ctl->kv_full), un_it & 1u, ctl, p, SITE_BWD_MMA_KV_FULL))) break;
+                if constexpr (VARLEN) {  // keys past the sequence's end
+                    zero_rows_from<C::NPANEL>(sK, un.sk - un.kb * C::BN);
+                    zero_rows_from<C::NPANEL>(sV, un.sk - un.kb * C::BN);
+                }
                 if (!(ok = warp_wait(B(ctl->q_full[q_it & 1u]), (q_it >> 1) & 1u, ctl, p, SITE_BWD_MMA_Q_FULL))) break;
+                if constexpr (VARLEN)  // queries past the sequence's end
+                    zero_rows_from<C::NPANEL>(sQ + (q_it & 1u) * 2 * C::TILE_BYTES, un.sq - un.t0 * C::BM);
                 tc_fence_after();
                 if (elect_one()) {
                     issue_kq(dK0, q_desc(q_it & 1u, false, 16), tmem + C::TM_S);
@@ -745,6 +772,8 @@ __global__ void __launch_bounds__(512, 1)
                     dq_pending = 0u;
                 }
                 if (!(ok = warp_wait(B(ctl->do_full[q_it & 1u]), (q_it >> 1) & 1u, ctl, p, SITE_BWD_MMA_DO_FULL))) break;
+                if constexpr (VARLEN)
+                    zero_rows_from<C::NPANEL>(sQ + (q_it & 1u) * 2 * C::TILE_BYTES + C::TILE_BYTES, un.sq - un.t0 * C::BM);
                 tc_fence_after();
                 if (elect_one()) {
                     issue_kq(dV0, q_desc(q_it & 1u, true, 16), tmem + C::TM_DP);
@@ -772,6 +801,9 @@ __global__ void __launch_bounds__(512, 1)
                                              SITE_BWD_MMA_Q_FULL)))
                             break;
                         BWD_TRACE(BEV_MMA_GOT_Q, tile_it);
+                        if constexpr (VARLEN)
+                            zero_rows_from<C::NPANEL>(sQ + ((q_it + 1) & 1u) * 2 * C::TILE_BYTES,
+                                                      un.sq - (un.t0 + t + 1) * C::BM);
                         tc_fence_after();
                         if (elect_one()) {
                             issue_kq(dK0, q_desc((q_it + 1) & 1u, false, 16), tmem + C::TM_S);
@@ -809,6 +841,9 @@ __global__ void __launch_bounds__(512, 1)
                         if (!(ok = warp_wait(B(ctl->do_full[q_it & 1u]), (q_it >> 1) & 1u, ctl, p,
                                              SITE_BWD_MMA_DO_FULL)))
                             break;
+                        if constexpr (VARLEN)
+                            zero_rows_from<C::NPANEL>(sQ + (q_it & 1u) * 2 * C::TILE_BYTES + C::TILE_BYTES,
+                                                      un.sq - (un.t0 + t + 1) * C::BM);
                         tc_fence_after();
                         if (elect_one()) {
                             issue_kq(dV0, q_desc(q_it & 1u, true, 16), tmem + C::TM_DP);

@@ -138,3 +138,42 @@ def test_bwd_varlen_workload_sampled(name):
         print(name, (s, hi), [(round(x, 3), f"{y:.2e}") for x, y in res])
     for t in (dq, dk, dv):
         assert torch.isfinite(t).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [128, 64])
+def test_varlen_nonfinite_neighbour_does_not_leak(causal, d):
+    """Tiles that cross a sequence's end read the next sequence's tokens.
+    With every input of the second sequence set to NaN, the first
+    sequence's forward outputs and gradients must be those of a clean run
+    (O, LSE, dK, dV bit for bit; dQ up to the order of its fp32 sums)."""
+    lens = [300, 200]
+    h = 2
+    q, k, v, cu_q, cu_k, _ = W.draw_varlen(lens, lens, h, d, "bf16", 4242 + d)
+    g = torch.Generator().manual_seed(4343)
+    do = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+    dev = torch.device("cuda", 0)
+    cq, ck = cu_q.to(dev), cu_k.to(dev)
+    n0 = lens[0]
+
+    def run(poison):
+        qd, kd, vd, dod = (t.clone().to(dev) for t in (q, k, v, do))
+        if poison:
+            for t in (qd, kd, vd, dod):
+                t[n0:] = float("nan")
+        o, lse = af.attn_fwd_varlen(qd, kd, vd, cq, ck, max(lens), max(lens), causal=causal)
+        if poison:
+            o[n0:] = float("nan")
+            lse[:, n0:] = float("nan")
+        dq, dk, dv = af.attn_bwd_varlen(qd, kd, vd, o, dod, lse, cq, ck, max(lens), max(lens), causal=causal)
+        torch.cuda.synchronize()
+        return [t[:n0].cpu() for t in (o, dq, dk, dv)] + [lse[:, :n0].cpu()]
+
+    clean = run(False)
+    dirty = run(True)
+    for name, a, b in zip(("o", "dq", "dk", "dv", "lse"), clean, dirty):
+        assert torch.isfinite(b).all(), f"{name}: non-finite values leaked into the first sequence"
+        if name == "dq":
+            assert torch.allclose(a.float(), b.float(), rtol=1e-2, atol=1e-3), name
+        else:
+            assert torch.equal(a, b), f"{name} differs from the clean run"

@@ -38,7 +38,7 @@ def run_gpu(q, k, v, causal, scale, with_lse=True):
 
 
 def compare(o, lse, o_ref, lse_ref, dtype: str, what: str = ""):
-    """Assert the benchmark spec's bounds; returns the error figures."""
+    """Assert the tolerances above (O max-abs and rel-L2, LSE max-abs); returns the error figures."""
     tol = TOL[dtype]
     assert o.shape == o_ref.shape, (o.shape, o_ref.shape)
     assert np.isfinite(o).all(), f"{what}: non-finite O ({np.isnan(o).sum()} NaN)"

@@ -24,6 +24,8 @@ CASES = [
     (3, 4, 1, 3000, 0, 64, "fp16", False, 4, (3000, 129, 1)),          # no new rows
     (2, 2, 5, 1000, 5, 128, "fp16", True, 3, (100, 997)),              # last rows dropped (full)
     (2, 2, 300, 700, 300, 128, "bf16", True, 1, (0, 400)),             # chunked prefill into a cache
+    (2, 2, 300, 700, 300, 128, "bf16", True, 3, (0, 400)),             # the same, split-KV
+    (2, 4, 40, 2000, 40, 64, "fp16", True, 5, (1960, 700)),            # speculative-decode-sized chunk, d = 64
     (2, 2, 64, 500, 0, 64, "bf16", True, 2, (10, -5)),                 # rows with no key, negative length
     (1, 2, 8, 256, 2, 128, "bf16", False, 2, (1000,)),                 # length beyond capacity: clamped
     (2, 3, 2, 130, 1, 64, "fp16", True, 2, (127, 128)),                # tail tiles of one key

@@ -116,3 +116,29 @@ def test_varlen_repeated_launches_reuse_the_schedule_counters():
     torch.cuda.synchronize()
     for i, (o, lse) in enumerate(outs):
         assert torch.equal(o, ref[i % 2][0]) and torch.equal(lse, ref[i % 2][1]), f"launch {i} differs"
+
+
+def test_varlen_concurrent_streams():
+    """Packed forwards in flight on two streams at once take different
+    schedule counters: each gives the result it gives alone."""
+    dev = torch.device("cuda", 0)
+    probs = []
+    for seed, lens in ((21, [900, 333, 1200]), (22, [64, 2000, 17])):
+        q, k, v, cu_q, cu_k, _ = W.draw_varlen(lens, lens, 8, 128, "bf16", seed)
+        probs.append(((q.to(dev), k.to(dev), v.to(dev), cu_q.to(dev), cu_k.to(dev)), max(lens)))
+    ref = []
+    for (q, k, v, cq, ck), mx in probs:
+        o, lse = af.attn_fwd_varlen(q, k, v, cq, ck, mx, mx, causal=True)
+        ref.append((o.clone(), lse.clone()))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    outs = [[], []]
+    for _ in range(20):
+        for i, st in enumerate(streams):
+            (q, k, v, cq, ck), mx = probs[i]
+            with torch.cuda.stream(st):
+                outs[i].append(af.attn_fwd_varlen(q, k, v, cq, ck, mx, mx, causal=True, stream=st))
+    torch.cuda.synchronize()
+    for i in range(2):
+        for n, (o, lse) in enumerate(outs[i]):
+            assert torch.equal(o, ref[i][0]) and torch.equal(lse, ref[i][1]), f"stream {i} launch {n} differs"

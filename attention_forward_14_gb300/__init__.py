@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     attn_fwd_fp8,
     attn_fwd_host,
     attn_fwd_kvcache,
+    attn_fwd_kvcache_paged,
     attn_fwd_splitkv,
     attn_fwd_varlen,
     bwd_workspace_bytes,

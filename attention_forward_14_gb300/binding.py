@@ -24,7 +24,7 @@ ERRORS = {
 EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_fwd_varlen", "attn_fwd_fp8", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
            "attn_fwd_splitkv_default_splits", "attn_fwd_splitkv_noalloc", "attn_last_error", "attn_fwd_status", "attn_fwd_status_clear",
            "attn_fwd_watchdog_selftest", "attn_version", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_varlen",
-           "attn_bwd_varlen_workspace_bytes", "attn_fwd_kvcache"]
+           "attn_bwd_varlen_workspace_bytes", "attn_fwd_kvcache", "attn_fwd_kvcache_paged"]
 
 
 class AttnError(RuntimeError):
@@ -63,6 +63,9 @@ def _bind(lib):
     lib.attn_fwd_kvcache.restype = c_int
     lib.attn_fwd_kvcache.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int, c_float,
                                      c_int, c_int, vp, i64, vp]
+    lib.attn_fwd_kvcache_paged.restype = c_int
+    lib.attn_fwd_kvcache_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64,
+                                           i64, c_int, c_float, c_int, c_int, vp, i64, vp]
     lib.attn_last_error.restype = ctypes.c_char_p
     lib.attn_last_error.argtypes = []
     lib.attn_fwd_status.restype = c_int
@@ -317,6 +320,63 @@ def attn_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, k_new=None, v_new=None,
                                   d, int(bool(causal)), float(scale), _dtype_code(q), int(num_splits),
                                   workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                   _stream_handle(stream, q.device))
+    _check(rc, lib)
+    return o, lse
+
+
+def attn_fwd_kvcache_paged(q, k_pool, v_pool, cache_seqlens, block_table, k_new=None, v_new=None,
+                           causal: bool = False, scale: float | None = None, num_splits: int | None = None, o=None,
+                           lse=None, workspace=None, stream=None):
+    """attn_fwd_kvcache over a paged cache: k_pool / v_pool [num_pages,
+    page_size, h, d], block_table int32 [b, pages_per_seq] (CUDA tensors).
+    Returns (o, lse)."""
+    import torch
+    lib = load()
+    b, h, sq, d = q.shape
+    num_pages, page_size = k_pool.shape[0], k_pool.shape[1]
+    if tuple(k_pool.shape) != (num_pages, page_size, h, d) or tuple(v_pool.shape) != tuple(k_pool.shape):
+        raise AttnError(-2, f"pool shapes {tuple(k_pool.shape)} / {tuple(v_pool.shape)} do not match q")
+    if block_table.dim() != 2 or block_table.shape[0] != b or block_table.dtype != torch.int32:
+        raise AttnError(-2, "block_table must be int32 [b, pages_per_seq]")
+    pages_per_seq = block_table.shape[1]
+    if (k_new is None) != (v_new is None):
+        raise AttnError(-1, "k_new and v_new must both be given or both be None")
+    s_new = 0 if k_new is None else k_new.shape[2]
+    if k_new is not None and (tuple(k_new.shape) != (b, h, s_new, d) or tuple(v_new.shape) != (b, h, s_new, d)):
+        raise AttnError(-2, "k_new / v_new must be [b, h, s_new, d]")
+    if cache_seqlens.dtype != torch.int32 or cache_seqlens.numel() != b:
+        raise AttnError(-4, "cache_seqlens must be an int32 tensor of b elements")
+    tensors = [("q", q), ("k_pool", k_pool), ("v_pool", v_pool), ("cache_seqlens", cache_seqlens),
+               ("block_table", block_table)]
+    if k_new is not None:
+        tensors += [("k_new", k_new), ("v_new", v_new)]
+    for name, t in tensors:
+        if not t.is_cuda or not t.is_contiguous():
+            raise AttnError(-2, f"{name} must be a contiguous CUDA tensor")
+        if name not in ("cache_seqlens", "block_table") and t.dtype != q.dtype:
+            raise AttnError(-4, f"{name} dtype differs from q")
+    if scale is None:
+        scale = 1.0 / float(d) ** 0.5
+    cap = pages_per_seq * page_size
+    if num_splits is None:
+        with torch.cuda.device(q.device):
+            num_splits = splitkv_default_splits(b, h, sq, max(cap, 1), d, causal)
+        num_splits = max(1, min(num_splits, (cap + 127) // 128))
+    need = splitkv_workspace_bytes(b, h, sq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((b, h, sq), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd_kvcache_paged(q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
+                                        k_new.data_ptr() if k_new is not None else None,
+                                        v_new.data_ptr() if v_new is not None else None,
+                                        cache_seqlens.data_ptr(), block_table.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                        b, h, sq, num_pages, page_size, pages_per_seq, s_new, d, int(bool(causal)),
+                                        float(scale), _dtype_code(q), int(num_splits), workspace.data_ptr(),
+                                        workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
     _check(rc, lib)
     return o, lse
 

@@ -236,6 +236,10 @@ struct SplitArgs {
 struct CacheArgs {
     const int32_t *seqlens = nullptr;
     int32_t add = 0;
+    // paged: K and V are pools [num_pages][page_size][h][d]; the capacity
+    // (the sk of run) is pages_per_seq * page_size
+    const int32_t *block_table = nullptr;
+    int64_t pages_per_seq = 0, page_size = 0, num_pages = 0;
 };
 
 // Head planes per group of the causal unit order: as many as keep the K and
@@ -282,8 +286,14 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_
     }
     LaunchArgs a;
     if ((rc = make_map(&a.q, q, dtype, bh, sq, d)) != ATTN_OK) return rc;
-    if ((rc = make_map(&a.k, k, dtype, bh, sk, d)) != ATTN_OK) return rc;
-    if ((rc = make_map(&a.v, v, dtype, bh, sk, d)) != ATTN_OK) return rc;
+    if (cache.block_table != nullptr) {
+        const int64_t pool = cache.num_pages * cache.page_size;
+        if ((rc = make_map_packed(&a.k, k, dtype, pool, h, d)) != ATTN_OK) return rc;
+        if ((rc = make_map_packed(&a.v, v, dtype, pool, h, d)) != ATTN_OK) return rc;
+    } else {
+        if ((rc = make_map(&a.k, k, dtype, bh, sk, d)) != ATTN_OK) return rc;
+        if ((rc = make_map(&a.v, v, dtype, bh, sk, d)) != ATTN_OK) return rc;
+    }
     FwdParams &p = a.p;
     p.o = o;
     p.lse = lse;
@@ -301,6 +311,10 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_
     p.total_k = static_cast<int32_t>(sk);
     p.seqlens_k = cache.seqlens;
     p.seqlens_add = cache.add;
+    p.block_table = cache.block_table;
+    p.pages_per_seq = static_cast<int32_t>(cache.pages_per_seq);
+    p.page_size = static_cast<int32_t>(cache.page_size);
+    p.num_pages = static_cast<int32_t>(cache.num_pages);
     p.sched = cache.seqlens != nullptr ? sched_slot(di) : nullptr;
     const int64_t units = bh * p.num_mblk * split.num_splits;
     if (units > INT32_MAX) return fail(ATTN_ERR_SHAPE, "too many work units (%lld)", (long long)units);
@@ -798,13 +812,18 @@ int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *
 
 // Attention against a KV cache with a length per batch element, after
 // (optionally) writing the new tokens' keys and values into the cache at
-// each element's current length.  Split-KV as in attn_fwd_splitkv.
-int attn_fwd_kvcache(const void *q, void *k_cache, void *v_cache, const void *k_new, const void *v_new,
-                     const int32_t *cache_seqlens, void *o, float *lse, int64_t b, int64_t h, int64_t sq,
-                     int64_t s_cache, int64_t s_new, int64_t d, int causal, float scale, int dtype, int num_splits,
-                     void *workspace, int64_t workspace_bytes, void *stream)
+// each element's current length.  Split-KV as in attn_fwd_splitkv.  With
+// `paged`, the caches are page pools addressed through a block table.
+struct PagedArgs {
+    const int32_t *block_table;
+    int64_t num_pages, page_size, pages_per_seq;
+};
+
+static int kvcache_impl(const void *q, void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                        const int32_t *cache_seqlens, void *o, float *lse, int64_t b, int64_t h, int64_t sq,
+                        int64_t s_cache, int64_t s_new, int64_t d, int causal, float scale, int dtype, int num_splits,
+                        void *workspace, int64_t workspace_bytes, void *stream, const PagedArgs *paged)
 {
-    g_err.clear();
     bool nothing = false;
     int rc = validate(q, k_cache, v_cache, o, lse, b, h, sq, s_cache, d, scale, dtype, &nothing);
     if (rc != ATTN_OK) return rc;
@@ -818,6 +837,10 @@ int attn_fwd_kvcache(const void *q, void *k_cache, void *v_cache, const void *k_
     if (bh == 0 || (nothing && !append)) return ATTN_OK;
     if (cache_seqlens == nullptr) return fail(ATTN_ERR_NULL, "cache_seqlens is NULL");
     if (!aligned(cache_seqlens, 4)) return fail(ATTN_ERR_ALIGN, "cache_seqlens must be 4-byte aligned");
+    if (paged) {
+        if (paged->block_table == nullptr) return fail(ATTN_ERR_NULL, "block_table is NULL");
+        if (!aligned(paged->block_table, 4)) return fail(ATTN_ERR_ALIGN, "block_table must be 4-byte aligned");
+    }
     const int64_t esz = 2;  // fp16 / bf16 (validate checked the dtype)
     if (append) {
         if (!k_cache || !v_cache) return fail(ATTN_ERR_NULL, "k_cache or v_cache is NULL");
@@ -825,7 +848,8 @@ int attn_fwd_kvcache(const void *q, void *k_cache, void *v_cache, const void *k_
             return fail(ATTN_ERR_ALIGN, "k_new, v_new, k_cache and v_cache must be 16-byte aligned");
         // the copy reads the new rows while it writes the cache: no overlap
         const uintptr_t nb = static_cast<uintptr_t>(bh * s_new * d * esz);
-        const uintptr_t cb = static_cast<uintptr_t>(bh * s_cache * d * esz);
+        const uintptr_t cb = static_cast<uintptr_t>(paged ? paged->num_pages * paged->page_size * h * d * esz
+                                                          : bh * s_cache * d * esz);
         const void *news[2] = {k_new, v_new};
         const void *caches[2] = {k_cache, v_cache};
         for (const void *nw : news)
@@ -855,20 +879,66 @@ int attn_fwd_kvcache(const void *q, void *k_cache, void *v_cache, const void *k_
         DeviceInfo *di = nullptr;
         rc = device_info(&di);
         if (rc != ATTN_OK) return rc;
-        const cudaError_t e =
-            (dtype == ATTN_BF16)
-                ? launch_kvcache_append<__nv_bfloat16>(k_new, v_new, k_cache, v_cache, cache_seqlens, bh, h, s_new,
-                                                       s_cache, static_cast<int>(d), di->sm_count, st)
-                : launch_kvcache_append<__half>(k_new, v_new, k_cache, v_cache, cache_seqlens, bh, h, s_new, s_cache,
-                                                static_cast<int>(d), di->sm_count, st);
+        const int dd = static_cast<int>(d);
+        cudaError_t e;
+        if (paged)
+            e = (dtype == ATTN_BF16)
+                    ? launch_kvcache_append_paged<__nv_bfloat16>(k_new, v_new, k_cache, v_cache, cache_seqlens,
+                                                                 paged->block_table, bh, h, s_new, paged->pages_per_seq,
+                                                                 paged->page_size, paged->num_pages, dd, di->sm_count, st)
+                    : launch_kvcache_append_paged<__half>(k_new, v_new, k_cache, v_cache, cache_seqlens,
+                                                          paged->block_table, bh, h, s_new, paged->pages_per_seq,
+                                                          paged->page_size, paged->num_pages, dd, di->sm_count, st);
+        else
+            e = (dtype == ATTN_BF16) ? launch_kvcache_append<__nv_bfloat16>(k_new, v_new, k_cache, v_cache, cache_seqlens,
+                                                                             bh, h, s_new, s_cache, dd, di->sm_count, st)
+                                     : launch_kvcache_append<__half>(k_new, v_new, k_cache, v_cache, cache_seqlens, bh, h,
+                                                                     s_new, s_cache, dd, di->sm_count, st);
         if (e != cudaSuccess) return cuda_fail(e, "launch (cache append)");
     }
     if (nothing) return ATTN_OK;
     CacheArgs ca;
     ca.seqlens = cache_seqlens;
     ca.add = static_cast<int32_t>(s_new);
+    if (paged) {
+        ca.block_table = paged->block_table;
+        ca.pages_per_seq = paged->pages_per_seq;
+        ca.page_size = paged->page_size;
+        ca.num_pages = paged->num_pages;
+    }
     return run(q, k_cache, v_cache, o, lse, b, h, sq, s_cache, d, causal, scale, dtype, st, -1, kDefaultTimeoutNs, sa,
                ca);
+}
+
+int attn_fwd_kvcache(const void *q, void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                     const int32_t *cache_seqlens, void *o, float *lse, int64_t b, int64_t h, int64_t sq,
+                     int64_t s_cache, int64_t s_new, int64_t d, int causal, float scale, int dtype, int num_splits,
+                     void *workspace, int64_t workspace_bytes, void *stream)
+{
+    g_err.clear();
+    return kvcache_impl(q, k_cache, v_cache, k_new, v_new, cache_seqlens, o, lse, b, h, sq, s_cache, s_new, d, causal,
+                        scale, dtype, num_splits, workspace, workspace_bytes, stream, nullptr);
+}
+
+// The KV-cache forward over a paged cache (see the header).
+int attn_fwd_kvcache_paged(const void *q, void *k_pool, void *v_pool, const void *k_new, const void *v_new,
+                           const int32_t *cache_seqlens, const int32_t *block_table, void *o, float *lse, int64_t b,
+                           int64_t h, int64_t sq, int64_t num_pages, int64_t page_size, int64_t pages_per_seq,
+                           int64_t s_new, int64_t d, int causal, float scale, int dtype, int num_splits,
+                           void *workspace, int64_t workspace_bytes, void *stream)
+{
+    g_err.clear();
+    if (page_size < 128 || page_size % 128 != 0)
+        return fail(ATTN_ERR_SHAPE, "page_size %lld is not a positive multiple of 128", (long long)page_size);
+    if (num_pages < 1 || pages_per_seq < 1)
+        return fail(ATTN_ERR_SHAPE, "num_pages and pages_per_seq must be at least 1");
+    if (num_pages > INT32_MAX / page_size)
+        return fail(ATTN_ERR_SHAPE, "the pool holds more than 2^31-1 tokens");
+    if (pages_per_seq > kMaxSeq / page_size)
+        return fail(ATTN_ERR_SHAPE, "pages_per_seq * page_size above 2^30");
+    const PagedArgs pg{block_table, num_pages, page_size, pages_per_seq};
+    return kvcache_impl(q, k_pool, v_pool, k_new, v_new, cache_seqlens, o, lse, b, h, sq, pages_per_seq * page_size,
+                        s_new, d, causal, scale, dtype, num_splits, workspace, workspace_bytes, stream, &pg);
 }
 
 int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse, const int32_t *cu_seqlens_q,

@@ -93,6 +93,15 @@ struct FwdParams {
     // keys (device int32 [b]; bh = b * heads).  nullptr: all sk keys.
     const int32_t *seqlens_k = nullptr;
     int32_t seqlens_add = 0;
+    // Paged KV cache: K and V are a pool of pages [num_pages][page_size]
+    // [heads][D] (read through packed maps, like varlen), and logical key r
+    // of batch element b lives in page block_table[b * pages_per_seq +
+    // r / page_size], row r % page_size.  page_size is a multiple of the
+    // 128-key tile, so no tile straddles two pages.  nullptr: not paged.
+    const int32_t *block_table = nullptr;
+    int32_t pages_per_seq = 0;
+    int32_t page_size = 0;
+    int32_t num_pages = 0;
     // Dynamic schedule: {next unit to hand out, CTAs finished}, both zero on
     // entry; the last CTA to finish sets them back to zero.  nullptr: every
     // CTA takes a fixed share of the units (unit_at).
@@ -697,10 +706,20 @@ __global__ void __launch_bounds__(384, 1)
             // [bh][s][D] (row, plane = bh); varlen maps are [token][head][D]
             // (row = head, plane = token).
             const bool vl = p.cu_q != nullptr;
+            const bool paged = p.block_table != nullptr;
             auto row_coord = [&](int r) { return vl ? un.bh : r; };
             auto plane_coord = [&](int r) { return vl ? un.q_tok0 + r : un.bh; };
-            auto krow_coord = [&](int r) { return vl ? un.bh : r; };
-            auto kplane_coord = [&](int r) { return vl ? un.k_tok0 + r : un.bh; };
+            auto krow_coord = [&](int r) { return vl ? un.bh : (paged ? un.bh % p.heads : r); };
+            auto kplane_coord = [&](int r) {
+                if (vl) return un.k_tok0 + r;
+                if (!paged) return un.bh;
+                // the pool token of logical key r; a page index outside the
+                // pool gives a coordinate past its end (the copy reads zeros)
+                const long long pg = p.block_table[static_cast<long long>(un.bh / p.heads) * p.pages_per_seq +
+                                                   r / p.page_size];
+                if (pg < 0 || pg >= p.num_pages) return static_cast<int>(static_cast<long long>(p.num_pages) * p.page_size);
+                return static_cast<int>(pg * p.page_size + r % p.page_size);
+            };
             for (int t = 0; t < C::QT && ok; ++t) {
                 ok = warp_wait(B(ctl->q_empty[t]), (q_it & 1u) ^ 1u, ctl, p, SITE_LOAD_Q_EMPTY);
                 if (!ok) break;
@@ -1163,6 +1182,41 @@ __global__ void attn_kvcache_append_kernel(const T *k_new, const T *v_new, T *k_
         const int64_t dst = (plane * s_cache + pos) * cpr + c;
         kc[dst] = kn[i];
         vc[dst] = vn[i];
+    }
+}
+
+// The same for a paged cache: logical position pos of batch element e is
+// row pos % page_size of page block_table[e * pages_per_seq + pos /
+// page_size] of the pool [num_pages][page_size][h][d]; positions at or past
+// pages_per_seq * page_size, and pages outside the pool, are not written.
+template <typename T>
+__global__ void attn_kvcache_append_paged_kernel(const T *k_new, const T *v_new, T *k_pool, T *v_pool,
+                                                 const int32_t *seqlens, const int32_t *block_table, int64_t bh,
+                                                 int64_t h, int64_t s_new, int64_t pages_per_seq, int64_t page_size,
+                                                 int64_t num_pages, int d)
+{
+    const int cpr = d * static_cast<int>(sizeof(T)) / 16;  // chunks per row
+    const int64_t n = bh * s_new * cpr;
+    const int64_t cap = pages_per_seq * page_size;
+    const uint4 *kn = reinterpret_cast<const uint4 *>(k_new);
+    const uint4 *vn = reinterpret_cast<const uint4 *>(v_new);
+    uint4 *kp = reinterpret_cast<uint4 *>(k_pool);
+    uint4 *vp = reinterpret_cast<uint4 *>(v_pool);
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t row = i / cpr;
+        const int c = static_cast<int>(i - row * cpr);
+        const int64_t plane = row / s_new;
+        const int64_t t = row - plane * s_new;
+        const int64_t e = plane / h, head = plane - e * h;
+        const int64_t pos = min(max(static_cast<int64_t>(seqlens[e]), int64_t(0)), cap) + t;
+        if (pos >= cap) continue;
+        const int64_t page = block_table[e * pages_per_seq + pos / page_size];
+        if (page < 0 || page >= num_pages) continue;
+        const int64_t token = page * page_size + pos % page_size;
+        const int64_t dst = (token * h + head) * cpr + c;
+        kp[dst] = kn[i];
+        vp[dst] = vn[i];
     }
 }
 

@@ -67,6 +67,23 @@ cudaError_t launch_kvcache_append(const void *k_new, const void *v_new, void *k_
     return cudaGetLastError();
 }
 
+template <typename T>
+cudaError_t launch_kvcache_append_paged(const void *k_new, const void *v_new, void *k_pool, void *v_pool,
+                                        const int32_t *seqlens, const int32_t *block_table, int64_t bh, int64_t h,
+                                        int64_t s_new, int64_t pages_per_seq, int64_t page_size, int64_t num_pages,
+                                        int d, int sm_count, cudaStream_t stream)
+{
+    const int64_t n = bh * s_new * (d * static_cast<int64_t>(sizeof(T)) / 16);
+    int64_t blocks = (n + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    attn_kvcache_append_paged_kernel<T><<<static_cast<int>(blocks), 256, 0, stream>>>(
+        static_cast<const T *>(k_new), static_cast<const T *>(v_new), static_cast<T *>(k_pool),
+        static_cast<T *>(v_pool), seqlens, block_table, bh, h, s_new, pages_per_seq, page_size, num_pages, d);
+    return cudaGetLastError();
+}
+
 template <typename T, int D>
 cudaError_t launch_splitkv_combine(const float *o_part, const float *lse_part, void *o, float *lse, int64_t rows,
                                    int num_splits, int sm_count, cudaStream_t stream)

@@ -246,6 +246,7 @@ class KvcacheWorkload:
     dtype: str
     seed: int
     causal: bool = True
+    page_size: int = 0  # > 0: a paged cache of pages of this many keys (capacity / page_size per sequence)
 
     @property
     def scale(self) -> float:
@@ -286,6 +287,9 @@ class KvcacheWorkload:
 KVCACHE = {kw.name: kw for kw in [
     KvcacheWorkload("kvcache_decode_b8_h32_cap16384_len1to16383_d128_bf16", 8, 32, 16384, 1, 16383, 1, 128, "bf16",
                     20260011),
+    # the same decoding step over a paged cache: 256-key pages, shuffled in the pool
+    KvcacheWorkload("kvcache_paged_decode_b8_h32_page256_len1to16383_d128_bf16", 8, 32, 16384, 1, 16383, 1, 128,
+                    "bf16", 20260011, page_size=256),
 ]}
 
 
@@ -297,6 +301,25 @@ def kvcache_inputs(kw: KvcacheWorkload):
     _, kn, vn = draw(kw.b, kw.h, 1, kw.s_new, kw.d, kw.dtype, kw.seed + 1)
     lens = torch.tensor(kw.lengths(), dtype=torch.int32)
     return q, kc, vc, kn, vn, lens
+
+
+def kvcache_paged_inputs(kw: KvcacheWorkload):
+    """The dense workload's caches cut into pages of kw.page_size keys,
+    placed in the pool [b * pages, page_size, h, d] in a seeded random order;
+    returns (q, k_pool, v_pool, k_new, v_new, lengths, block_table)."""
+    q, kc, vc, kn, vn, lens = kvcache_inputs(kw)
+    pages = kw.cap // kw.page_size
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(kw.seed) + 7)
+    table = torch.randperm(kw.b * pages, generator=g).reshape(kw.b, pages).to(torch.int32)
+
+    def pool(c):  # [b, h, cap, d] -> pages [b*pages, page_size, h, d] at their table slots
+        out = torch.empty((kw.b * pages, kw.page_size, kw.h, kw.d), dtype=c.dtype)
+        paged = c.reshape(kw.b, kw.h, pages, kw.page_size, kw.d).permute(0, 2, 3, 1, 4)
+        out[table.reshape(-1).long()] = paged.reshape(kw.b * pages, kw.page_size, kw.h, kw.d)
+        return out
+
+    return q, pool(kc), pool(vc), kn, vn, lens, table
 
 
 # Backward of the packed workload: its q, k, v plus a seeded output gradient

@@ -285,6 +285,9 @@ def bench_kvcache(args, kw):
     from attention_forward_14_gb300 import workloads as W
 
     q, kc, vc, kn, vn, lens = W.kvcache_inputs(kw)
+    table = None
+    if kw.page_size:
+        _, kc_pool, vc_pool, _, _, _, table = W.kvcache_paged_inputs(kw)
     if args.impl == "reference":
         per = max(1.0, 120.0 / max(1, args.steps + args.warmup))
         vals, times, desc, cores = [], [], "", None
@@ -307,7 +310,11 @@ def bench_kvcache(args, kw):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    qd, kcd, vcd, knd, vnd, lensd = (t.to(dev) for t in (q, kc, vc, kn, vn, lens))
+    if kw.page_size:  # the device holds the pools; the dense caches serve the CPU leg only
+        kcd, vcd, tabd = kc_pool.to(dev), vc_pool.to(dev), table.to(dev)
+        qd, knd, vnd, lensd = (t.to(dev) for t in (q, kn, vn, lens))
+    else:
+        qd, kcd, vcd, knd, vnd, lensd = (t.to(dev) for t in (q, kc, vc, kn, vn, lens))
     o = torch.empty_like(qd)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -316,8 +323,12 @@ def bench_kvcache(args, kw):
                      device=dev)
 
     def step():
-        af.attn_fwd_kvcache(qd, kcd, vcd, lensd, knd, vnd, causal=kw.causal, scale=kw.scale, num_splits=splits,
-                            o=o, lse=lse, workspace=ws, stream=stream)
+        if kw.page_size:
+            af.attn_fwd_kvcache_paged(qd, kcd, vcd, lensd, tabd, knd, vnd, causal=kw.causal, scale=kw.scale,
+                                      num_splits=splits, o=o, lse=lse, workspace=ws, stream=stream)
+        else:
+            af.attn_fwd_kvcache(qd, kcd, vcd, lensd, knd, vnd, causal=kw.causal, scale=kw.scale, num_splits=splits,
+                                o=o, lse=lse, workspace=ws, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -375,6 +386,7 @@ def bench_kvcache(args, kw):
         "data": "synthetic",
         "config": {"workload": kw.name, "b": kw.b, "h": kw.h, "cap": kw.cap, "lengths": kw.lengths(),
                    "s_new": kw.s_new, "d": kw.d, "causal": kw.causal, "flops_per_step": kw.flops(),
+                   "page_size": kw.page_size or None,
                    "l2": f"cache {2 * kc.numel() * 2 / 1e9:.1f} GB > L2, valid K/V {kw.bytes() / 1e9:.2f} GB/step, "
                          "no flush"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",

@@ -267,6 +267,40 @@ int attn_fwd_kvcache(const void *q, void *k_cache, void *v_cache,
                      int64_t workspace_bytes, void *stream);
 
 /*
+ * attn_fwd_kvcache over a paged cache: the same operation, with each batch
+ * element's cache made of fixed-size pages of a shared pool, as a decoder
+ * that allocates its cache page by page keeps it.
+ *
+ *   k_pool,
+ *   v_pool     : [num_pages, page_size, h, d] of dtype (token-major within a
+ *                page, heads inside), 16-byte aligned; written when k_new is
+ *                given.
+ *   block_table: device int32 [b, pages_per_seq]: logical page p of batch
+ *                element b is pool page block_table[b * pages_per_seq + p].
+ *                Pages of different elements must be distinct; a page index
+ *                outside [0, num_pages) reads as zeros and is not written.
+ *   page_size  : a positive multiple of 128 (a key tile never straddles two
+ *                pages).  The capacity of each element is
+ *                pages_per_seq * page_size (at most 2^30), the pool at most
+ *                2^31-1 tokens.
+ * Logical key r of element b is row r % page_size of page
+ * block_table[b, r / page_size]; everything else (q, k_new, v_new,
+ * cache_seqlens, the write, the lengths, the mask, num_splits with
+ * sk = pages_per_seq * page_size, o, lse) is as for attn_fwd_kvcache.
+ * Returns ATTN_OK or a negative ATTN_ERR_* code.
+ */
+int attn_fwd_kvcache_paged(const void *q, void *k_pool, void *v_pool,
+                           const void *k_new, const void *v_new,
+                           const int32_t *cache_seqlens,
+                           const int32_t *block_table, void *o, float *lse,
+                           int64_t b, int64_t h, int64_t sq,
+                           int64_t num_pages, int64_t page_size,
+                           int64_t pages_per_seq, int64_t s_new, int64_t d,
+                           int causal, float scale, int dtype, int num_splits,
+                           void *workspace, int64_t workspace_bytes,
+                           void *stream);
+
+/*
  * Backward pass: the gradients of attn_fwd.  "05 · kernel 工程与四代演化" 6.1
  * lists bwd among the exported entry points (and chapter 04 of that series
  * as its implementation, which is not among the pages); the operation is the

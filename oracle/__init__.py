@@ -254,3 +254,29 @@ def attn_fwd_kvcache(q, k_cache, v_cache, cache_len, k_new=None, v_new=None, cau
     if rc != 0:
         raise RuntimeError(f"oracle_attn_fwd_kvcache_f64 failed: {rc}")
     return o, lse, kc, vc
+
+
+def attn_fwd_kvcache_paged(q, k_pool, v_pool, block_table, cache_len, k_new=None, v_new=None, causal: bool = False,
+                           scale: float = 1.0, lib=None):
+    """The KV-cache forward over a paged cache.  A paged cache is a
+    re-indexing of a dense one: batch element e's logical cache is the
+    concatenation of the pool pages block_table[e, 0..P) ([num_pages,
+    page_size, h, d], token-major within a page).  The logical caches are
+    gathered, ``attn_fwd_kvcache`` runs on them, and the written rows go
+    back to their pages.  Pages of different elements must be distinct.
+    Returns (o, lse, k_pool after the write, v_pool after the write)."""
+    kp = np.array(k_pool, dtype=np.float64, copy=True)
+    vp = np.array(v_pool, dtype=np.float64, copy=True)
+    table = np.asarray(block_table, dtype=np.int64)
+    b, h, sq, d = np.shape(q)
+    num_pages, page_size = kp.shape[0], kp.shape[1]
+    pages = table.shape[1]
+    assert kp.shape == (num_pages, page_size, h, d) and vp.shape == kp.shape and table.shape == (b, pages)
+
+    def logical(pool):  # [b, P, page_size, h, d] -> [b, h, P * page_size, d]
+        return pool[table].reshape(b, pages * page_size, h, d).transpose(0, 2, 1, 3)
+
+    o, lse, kc, vc = attn_fwd_kvcache(q, logical(kp), logical(vp), cache_len, k_new, v_new, causal, scale, lib=lib)
+    kp[table] = kc.transpose(0, 2, 1, 3).reshape(b, pages, page_size, h, d)
+    vp[table] = vc.transpose(0, 2, 1, 3).reshape(b, pages, page_size, h, d)
+    return o, lse, kp, vp

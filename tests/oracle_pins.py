@@ -585,6 +585,47 @@ def pin_kvcache_decode_matches_prefill(lib):
     return fails
 
 
+def pin_kvcache_paged(lib):
+    """A paged cache is a re-indexing: the paged oracle with pages in order
+    equals the dense KV-cache oracle on the same logical caches; shuffling
+    the pool's pages (and the table with them) changes nothing; and each new
+    row lands in page table[e, pos // page_size], row pos % page_size, read
+    here directly from the pool."""
+    fails = []
+    r = _rng(4300)
+    b, h, sq, d, ps, pages, s_new = 2, 2, 3, 4, 4, 3, 2
+    lens = [5, 10]
+    q = r.standard_normal((b, h, sq, d))
+    kn = r.standard_normal((b, h, s_new, d))
+    vn = r.standard_normal((b, h, s_new, d))
+    num_pages = b * pages + 1
+    kp = r.standard_normal((num_pages, ps, h, d))
+    vp = r.standard_normal((num_pages, ps, h, d))
+    table = np.arange(b * pages).reshape(b, pages)
+    dense_k = kp[table].reshape(b, pages * ps, h, d).transpose(0, 2, 1, 3)
+    dense_v = vp[table].reshape(b, pages * ps, h, d).transpose(0, 2, 1, 3)
+    for causal in (False, True):
+        o, l, kp2, vp2 = oracle.attn_fwd_kvcache_paged(q, kp, vp, table, lens, kn, vn, causal, 0.6, lib=lib)
+        od, ld, kc, _ = oracle.attn_fwd_kvcache(q, dense_k, dense_v, lens, kn, vn, causal, 0.6, lib=lib)
+        fails += _cmp(f"paged-identity c{int(causal)} o", o, od, 0.0)
+        fails += _cmp(f"paged-identity c{int(causal)} lse", l, ld, 0.0)
+        for e in range(b):
+            for t in range(s_new):
+                pos = lens[e] + t
+                if pos >= pages * ps:
+                    continue
+                page, row = table[e, pos // ps], pos % ps
+                fails += _cmp(f"paged write e{e} t{t}", kp2[page, row], kn[e, :, t], 0.0)
+        perm = r.permutation(num_pages)   # pool page i moves to slot perm[i]
+        kq = np.empty_like(kp)
+        vq = np.empty_like(vp)
+        kq[perm], vq[perm] = kp, vp
+        o2, l2, _, _ = oracle.attn_fwd_kvcache_paged(q, kq, vq, perm[table], lens, kn, vn, causal, 0.6, lib=lib)
+        fails += _cmp(f"paged-shuffled c{int(causal)} o", o2, o, 0.0)
+        fails += _cmp(f"paged-shuffled c{int(causal)} lse", l2, l, 0.0)
+    return fails
+
+
 ALL_PINS = [
     pin_worked_examples,
     pin_bruteforce,
@@ -606,4 +647,5 @@ ALL_PINS = [
     pin_kvcache_bruteforce,
     pin_kvcache_unused_slots,
     pin_kvcache_decode_matches_prefill,
+    pin_kvcache_paged,
 ]

@@ -160,3 +160,20 @@ def test_kvcache_argument_errors(lib, kw, code):
 def test_kvcache_nothing_to_do(lib):
     assert call_kvcache(lib, b=0, seqlens=None)[0] == 0
     assert call_kvcache(lib, h=0, seqlens=None)[0] == 0
+
+
+def call_paged(lib, table=P, page_size=256, num_pages=8, pps=2, seqlens=P):
+    rc = lib.attn_fwd_kvcache_paged(P, P, P, None, None, seqlens, table, P, None, 1, 2, 1, num_pages, page_size, pps,
+                                    0, 128, 1, 0.1, 1, 1, None, 0, None)
+    return rc, lib.attn_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(page_size=100), -2), (dict(page_size=0), -2), (dict(page_size=192), -2),
+    (dict(num_pages=0), -2), (dict(pps=0), -2),
+    (dict(num_pages=1 << 24, page_size=1 << 8), -2),   # pool above 2^31-1 tokens
+    (dict(table=None), -1), (dict(table=P + 2), -6),
+])
+def test_kvcache_paged_argument_errors(lib, kw, code):
+    rc, msg = call_paged(lib, **kw)
+    assert rc == code, (rc, msg)

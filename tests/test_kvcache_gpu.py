@@ -133,3 +133,85 @@ def test_kvcache_argument_errors():
     with pytest.raises(binding.AttnError) as e:  # more splits than key tiles
         af.attn_fwd_kvcache(q, kc, kc.clone(), seqlens, num_splits=3)
     assert e.value.code == -2
+
+
+PAGED_CASES = [
+    # b, h, sq, page_size, pages_per_seq, s_new, d, dtype, causal, splits, cache lengths
+    (3, 4, 1, 128, 12, 1, 128, "bf16", True, 1, (1535, 300, 0)),     # decode; one element fills its pages
+    (3, 4, 1, 256, 6, 1, 128, "bf16", True, 4, (1000, 17, 1400)),    # split-KV, 256-key pages
+    (2, 2, 33, 128, 5, 33, 64, "fp16", True, 3, (100, 600)),          # a chunk of new tokens, d = 64
+    (2, 3, 4, 384, 2, 0, 128, "fp16", False, 2, (700, 5)),           # no new rows, 3-tile pages
+]
+
+
+def _paged_case(case):
+    b, h, sq, ps, pps, s_new, d, dt, causal, splits, lens = case
+    seed = zlib.crc32(repr(case).encode())
+    num_pages = b * pps + 3  # three pages no element uses
+    q, _, _ = W.draw(b, h, sq, 1, d, dt, seed=seed)
+    _, kp, vp = W.draw(1, num_pages * ps, 1, h, d, dt, seed=seed + 1)  # [1, num_pages*ps, h, d] as pool rows
+    kp = kp.reshape(num_pages, ps, h, d).contiguous()
+    vp = vp.reshape(num_pages, ps, h, d).contiguous()
+    if s_new:
+        _, kn, vn = W.draw(b, h, 1, s_new, d, dt, seed=seed + 2)
+    else:
+        kn = vn = None
+    g = torch.Generator().manual_seed(seed + 3)
+    table = torch.randperm(num_pages, generator=g)[: b * pps].reshape(b, pps).to(torch.int32)
+    used = set(table.flatten().tolist())
+    for pg in range(num_pages):  # pages no element uses: NaN
+        if pg not in used:
+            kp[pg] = float("nan")
+            vp[pg] = float("nan")
+    for e, n in enumerate(lens):  # rows past each element's length: NaN
+        start = min(max(n, 0), ps * pps)
+        for p in range(pps):
+            lo = max(start - p * ps, 0)
+            if lo < ps:
+                kp[int(table[e, p]), lo:] = float("nan")
+                vp[int(table[e, p]), lo:] = float("nan")
+    return q, kp, vp, kn, vn, table
+
+
+@pytest.mark.parametrize("case", PAGED_CASES, ids=lambda c: "_".join(map(str, c[:10])))
+def test_kvcache_paged_matches_oracle(case):
+    b, h, sq, ps, pps, s_new, d, dt, causal, splits, lens = case
+    q, kp, vp, kn, vn, table = _paged_case(case)
+    scale = 1 / math.sqrt(d)
+    dev = torch.device("cuda", 0)
+    kpd, vpd = kp.to(dev), vp.to(dev)
+    o, lse = af.attn_fwd_kvcache_paged(q.to(dev), kpd, vpd, torch.tensor(lens, dtype=torch.int32, device=dev),
+                                       table.to(dev), kn.to(dev) if kn is not None else None,
+                                       vn.to(dev) if vn is not None else None, causal=causal, scale=scale,
+                                       num_splits=splits)
+    torch.cuda.synchronize()
+    o_ref, lse_ref, kp_ref, vp_ref = oracle.attn_fwd_kvcache_paged(_np(q), _np(kp), _np(vp), table.numpy(),
+                                                                   list(lens), _np(kn), _np(vn), causal, scale)
+    compare(o.float().cpu().double().numpy(), lse.cpu().double().numpy(), o_ref, lse_ref, dt, f"paged {case}")
+    assert np.array_equal(kpd.float().cpu().double().numpy(), kp_ref, equal_nan=True), "k pool after the write"
+    assert np.array_equal(vpd.float().cpu().double().numpy(), vp_ref, equal_nan=True), "v pool after the write"
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_kvcache_paged_equals_dense_cache(splits):
+    """The same logical caches, once dense and once as shuffled 256-key
+    pages: bit for bit the same outputs."""
+    dev = torch.device("cuda", 0)
+    b, h, d, ps, pps = 2, 4, 128, 256, 4
+    cap = ps * pps
+    q, kc, vc = W.draw(b, h, 2, cap, d, "bf16", seed=777)
+    lens = torch.tensor([900, 333], dtype=torch.int32, device=dev)
+    g = torch.Generator().manual_seed(778)
+    table = torch.randperm(b * pps, generator=g).reshape(b, pps).to(torch.int32)
+    kp = torch.empty((b * pps, ps, h, d), dtype=torch.bfloat16)
+    vp = torch.empty_like(kp)
+    for e in range(b):
+        for p in range(pps):
+            kp[table[e, p]] = kc[e, :, p * ps:(p + 1) * ps].transpose(0, 1)
+            vp[table[e, p]] = vc[e, :, p * ps:(p + 1) * ps].transpose(0, 1)
+    for causal in (False, True):
+        o1, l1 = af.attn_fwd_kvcache(q.to(dev), kc.to(dev), vc.to(dev), lens, causal=causal, num_splits=splits)
+        o2, l2 = af.attn_fwd_kvcache_paged(q.to(dev), kp.to(dev), vp.to(dev), lens, table.to(dev), causal=causal,
+                                           num_splits=splits)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)

@@ -23,6 +23,7 @@ ERRORS = {
 # Every function include/attn_fwd.h declares.
 EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_fwd_varlen", "attn_fwd_fp8", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
            "attn_fwd_splitkv_default_splits", "attn_fwd_splitkv_noalloc", "attn_last_error", "attn_fwd_status", "attn_fwd_status_clear",
+           "attn_fwd_debug_status", "attn_fwd_sched_pin_slot",
            "attn_fwd_watchdog_selftest", "attn_version", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_varlen",
            "attn_bwd_varlen_workspace_bytes", "attn_fwd_kvcache", "attn_fwd_kvcache_paged"]
 
@@ -72,6 +73,10 @@ def _bind(lib):
     lib.attn_fwd_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.attn_fwd_status_clear.restype = c_int
     lib.attn_fwd_status_clear.argtypes = []
+    lib.attn_fwd_debug_status.restype = c_int
+    lib.attn_fwd_debug_status.argtypes = []
+    lib.attn_fwd_sched_pin_slot.restype = c_int
+    lib.attn_fwd_sched_pin_slot.argtypes = [c_int]
     lib.attn_fwd_watchdog_selftest.restype = c_int
     lib.attn_fwd_watchdog_selftest.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_float,
                                                c_int, c_int, c_int, vp]

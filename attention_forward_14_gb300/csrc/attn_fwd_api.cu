@@ -17,6 +17,7 @@
 #include "attn_bwd_launch.h"
 #include "attn_fwd.h"
 #include "launch.h"
+#include "sched_ticket.h"
 
 namespace {
 
@@ -47,12 +48,14 @@ unsigned long long *g_trace_buf = nullptr;  // timeline builds only: where launc
 // Watchdog status word, one per device that loads this library.
 __device__ uint32_t g_watchdog[4];
 
-// Counter pairs of the forward's dynamic schedule.  Each launch that uses
-// one takes the next pair in turn; the kernel leaves it at zero when it
-// finishes, so a pair is ready again once its previous launch has ended
-// (launches more than kSchedSlots apart never overlap in practice).
-constexpr int kSchedSlots = 256;
-__device__ int32_t g_fwd_sched[2 * kSchedSlots];
+// Counter slots of the forward's dynamic schedule.  Each launch that uses
+// one takes the next slot in turn, tagged with its own generation number
+// (sched_ticket.h); the kernel leaves the slot at zero when it finishes, so a
+// slot is ready again once its previous launch has ended.  A launch that
+// finds its slot still held by another generation (more than kSchedSlots
+// such launches in flight) reports STATUS_SCHED_COLLISION instead of sharing
+// the counters.
+__device__ int32_t g_fwd_sched[kSchedWords * kSchedSlots];
 
 constexpr int kMaxDevices = 64;
 
@@ -63,7 +66,8 @@ struct DeviceInfo {
     int cc_major = 0, cc_minor = 0;
     uint32_t *status = nullptr;
     int32_t *sched = nullptr;
-    std::atomic<uint32_t> sched_next{0};
+    std::atomic<uint64_t> sched_next{0};
+    std::atomic<int> sched_pinned{-1};  // testing hook: every launch on this slot
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -195,8 +199,9 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 constexpr int64_t kMaxSeq = int64_t(1) << 30;
 
-int validate(const void *q, const void *k, const void *v, const void *o, const float *lse, int64_t b, int64_t h,
-             int64_t sq, int64_t sk, int64_t d, float scale, int dtype, bool *nothing)
+// The size, head-dim, dtype and scale checks of every forward entry point
+// (no pointer is looked at).
+int validate_sizes(int64_t b, int64_t h, int64_t sq, int64_t sk, int64_t d, float scale, int dtype)
 {
     if (b < 0 || h < 0 || sq < 0 || sk < 0)
         return fail(ATTN_ERR_SHAPE, "negative size: b=%lld h=%lld sq=%lld sk=%lld", (long long)b, (long long)h,
@@ -208,6 +213,14 @@ int validate(const void *q, const void *k, const void *v, const void *o, const f
     if (d != 64 && d != 128) return fail(ATTN_ERR_HEADDIM, "head dim %lld not supported (64 or 128)", (long long)d);
     if (dtype != ATTN_FP16 && dtype != ATTN_BF16) return fail(ATTN_ERR_DTYPE, "dtype %d is not fp16 (0) or bf16 (1)", dtype);
     if (!std::isfinite(scale)) return fail(ATTN_ERR_SCALE, "scale is not finite");
+    return ATTN_OK;
+}
+
+int validate(const void *q, const void *k, const void *v, const void *o, const float *lse, int64_t b, int64_t h,
+             int64_t sq, int64_t sk, int64_t d, float scale, int dtype, bool *nothing)
+{
+    const int rc = validate_sizes(b, h, sq, sk, d, scale, dtype);
+    if (rc != ATTN_OK) return rc;
     *nothing = (b * h * sq == 0);
     if (*nothing) return ATTN_OK;
     if (!o) return fail(ATTN_ERR_NULL, "o is NULL");
@@ -253,11 +266,14 @@ int32_t l2_group(int64_t bh, int64_t sk, int64_t d, int64_t elem_bytes)
     return static_cast<int32_t>(g);
 }
 
-// The next counter pair of the dynamic schedule on this device.
-int32_t *sched_slot(DeviceInfo *di)
+// The next counter slot of the dynamic schedule on this device, and the
+// generation that tags this launch in it.
+int32_t *sched_slot(DeviceInfo *di, uint32_t *gen)
 {
-    const uint32_t s = di->sched_next.fetch_add(1, std::memory_order_relaxed) % kSchedSlots;
-    return di->sched + 2 * s;
+    const SchedTicket t = sched_ticket(di->sched_next.fetch_add(1, std::memory_order_relaxed),
+                                       di->sched_pinned.load(std::memory_order_relaxed));
+    *gen = t.gen;
+    return di->sched + kSchedWords * t.slot;
 }
 
 int64_t kv_tiles(int64_t sk) { return (sk + 127) / 128; }
@@ -315,7 +331,7 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_
     p.pages_per_seq = static_cast<int32_t>(cache.pages_per_seq);
     p.page_size = static_cast<int32_t>(cache.page_size);
     p.num_pages = static_cast<int32_t>(cache.num_pages);
-    p.sched = cache.seqlens != nullptr ? sched_slot(di) : nullptr;
+    p.sched = cache.seqlens != nullptr ? sched_slot(di, &p.sched_gen) : nullptr;
     const int64_t units = bh * p.num_mblk * split.num_splits;
     if (units > INT32_MAX) return fail(ATTN_ERR_SHAPE, "too many work units (%lld)", (long long)units);
     p.num_units = static_cast<int32_t>(units);
@@ -786,15 +802,22 @@ int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *
                              void *stream)
 {
     g_err.clear();
-    // Host-side size check first: the partials must fit the fixed scratch.
-    if (b < 0 || h < 0 || sq < 0 || (d != 64 && d != 128) || num_splits < 1 || num_splits > 1024)
-        return fail(ATTN_ERR_SHAPE, "attn_fwd_splitkv_noalloc: invalid sizes or split count");
-    const int64_t need = (num_splits == 1) ? 0 : splitkv_bytes(b * h, sq, d, num_splits);
-    if (need > static_cast<int64_t>(ATTN_NOALLOC_SCRATCH_BYTES))
+    // The checks of attn_fwd_splitkv that need no pointer come first (the
+    // same codes for the same mistakes: a bad head dim is ATTN_ERR_HEADDIM);
+    // they bound b*h below 2^31 and sq by 2^30, so the scratch size is
+    // computed without overflow (in double, then compared).
+    int rc = validate_sizes(b, h, sq, sk, d, scale, dtype);
+    if (rc != ATTN_OK) return rc;
+    if (num_splits < 1 || num_splits > 1024) return fail(ATTN_ERR_SHAPE, "num_splits %d not in 1..1024", num_splits);
+    const double need = (num_splits == 1 || sk == 0)
+                            ? 0.0
+                            : static_cast<double>(num_splits) * static_cast<double>(b * h) * static_cast<double>(sq) *
+                                  static_cast<double>(d + 2) * 4.0;
+    if (need > static_cast<double>(ATTN_NOALLOC_SCRATCH_BYTES))
         return fail(ATTN_ERR_SHAPE,
-                    "attn_fwd_splitkv_noalloc: %d splits of b=%lld h=%lld sq=%lld d=%lld need %lld bytes of scratch, "
+                    "attn_fwd_splitkv_noalloc: %d splits of b=%lld h=%lld sq=%lld d=%lld need %.0f bytes of scratch, "
                     "more than its fixed %lld; use fewer splits, or attn_fwd_splitkv with a workspace",
-                    num_splits, (long long)b, (long long)h, (long long)sq, (long long)d, (long long)need,
+                    num_splits, (long long)b, (long long)h, (long long)sq, (long long)d, need,
                     (long long)ATTN_NOALLOC_SCRATCH_BYTES);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -986,7 +1009,7 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float 
     p.lse_part = nullptr;
     p.cu_q = cu_seqlens_q;
     p.cu_k = cu_seqlens_k;
-    p.sched = sched_slot(di);  // sequences differ in length: hand units out dynamically
+    p.sched = sched_slot(di, &p.sched_gen);  // sequences differ in length: hand units out dynamically
     p.group = l2_group(bh, max_seqlen_k, d, 2);
     p.heads = static_cast<int32_t>(h);
     p.total_q = static_cast<int32_t>(total_q);
@@ -1096,9 +1119,25 @@ int attn_fwd_status_clear(void)
     DeviceInfo *di = nullptr;
     int rc = device_info(&di);
     if (rc != ATTN_OK) return rc;
-    cudaError_t e = cudaMemset(di->status, 0, 4 * sizeof(uint32_t));
+    // after the device is idle, so that no launch holds a schedule slot
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemset(di->status, 0, 4 * sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMemset(di->sched, 0, sizeof(int32_t) * kSchedWords * kSchedSlots);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "clear watchdog status");
+}
+
+int attn_fwd_debug_status(void) { return attn_fwd_status(nullptr); }
+
+int attn_fwd_sched_pin_slot(int slot)
+{
+    g_err.clear();
+    if (slot < -1 || slot >= kSchedSlots) return fail(ATTN_ERR_SHAPE, "slot %d not in -1..%d", slot, kSchedSlots - 1);
+    DeviceInfo *di = nullptr;
+    int rc = device_info(&di);
+    if (rc != ATTN_OK) return rc;
+    di->sched_pinned.store(slot, std::memory_order_relaxed);
+    return ATTN_OK;
 }
 
 int attn_fwd_watchdog_selftest(const void *q, const void *k, const void *v, void *o, float *lse, int64_t b, int64_t h,

@@ -102,10 +102,15 @@ struct FwdParams {
     int32_t pages_per_seq = 0;
     int32_t page_size = 0;
     int32_t num_pages = 0;
-    // Dynamic schedule: {next unit to hand out, CTAs finished}, both zero on
-    // entry; the last CTA to finish sets them back to zero.  nullptr: every
-    // CTA takes a fixed share of the units (unit_at).
+    // Dynamic schedule: one slot of kSchedWords words {next unit to hand
+    // out, CTAs finished, owner generation, unused}, all zero when the slot is
+    // free.  Each CTA first claims the slot for this launch's generation
+    // `sched_gen` (owner 0 -> gen); a CTA that finds another generation there
+    // records a collision in the status word and takes no unit.  The last
+    // CTA to finish sets the slot back to zero.  nullptr: every CTA takes a
+    // fixed share of the units (unit_at).
     int32_t *sched = nullptr;
+    uint32_t sched_gen = 0;
     // Causal unit order: > 0 orders the units in groups of `group` head
     // planes, heaviest row block first within each group, so that the K/V
     // the units in flight stream stay in L2; 0 orders all heads heaviest
@@ -141,6 +146,7 @@ enum : uint32_t {
     EV_SM_EPI_WAIT, EV_SM_EPI_GOT, EV_SM_EPI_DONE,
     EV_MMA_WAIT_Q = 20, EV_MMA_GOT_Q, EV_MMA_WAIT_KV, EV_MMA_GOT_KV, EV_MMA_WAIT_P, EV_MMA_GOT_P, EV_MMA_ISSUED,
     EV_LD_WAIT = 40, EV_LD_GOT,
+    EV_K_ENTRY = 60, EV_K_READY, EV_K_EXIT,
 };
 
 // Watchdog sites (recorded in status[3]).
@@ -155,6 +161,14 @@ enum : uint32_t {
     SITE_DRAIN = 8,
     SITE_UNIT_FULL = 9,
     SITE_UNIT_EMPTY = 10,
+    SITE_SCHED_SLOT = 11,
+};
+
+// Status codes (status[0]): a wait that ran out, and a dynamic-schedule
+// slot that another launch still held.
+enum : uint32_t {
+    STATUS_TIMEOUT = 1,
+    STATUS_SCHED_COLLISION = 2,
 };
 
 // Input element types: fp16, bf16 (16-bit, kind::f16 MMAs, P two per
@@ -229,6 +243,7 @@ struct Ctl {
     int32_t unit_idx[4];
     uint32_t tmem_base;
     uint32_t abort;
+    uint32_t collided;  // the schedule slot belongs to another launch: take no unit
 };
 static_assert(sizeof(Ctl) <= 1024, "control block");
 constexpr int kUnitRing = 4;
@@ -349,6 +364,18 @@ __device__ __forceinline__ int unit_at(int i)
     return i * g + c;
 }
 
+// The first failure of a launch (or of earlier launches, until the status is
+// cleared) is kept: {code, block, warp, site}.
+__device__ __forceinline__ void record_status(uint32_t *status, uint32_t code, uint32_t site)
+{
+    if (atomicCAS(&status[0], 0u, code) == 0u) {
+        status[1] = blockIdx.x;
+        status[2] = threadIdx.x >> 5;
+        status[3] = site;
+        __threadfence();
+    }
+}
+
 static __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl *ctl, const FwdParams &p,
                                               uint32_t site)
 {
@@ -360,12 +387,7 @@ static __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, 
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > p.timeout_ns) {
             *abort_flag = 1u;
-            if (atomicCAS(&p.status[0], 0u, 1u) == 0u) {
-                p.status[1] = blockIdx.x;
-                p.status[2] = threadIdx.x >> 5;
-                p.status[3] = site;
-                __threadfence();
-            }
+            record_status(p.status, STATUS_TIMEOUT, site);
             return false;
         }
     }
@@ -429,7 +451,7 @@ __device__ __forceinline__ bool producer_unit(uint32_t i, int &u, Ctl *ctl, cons
         return false;
     int v = -1;
     if ((threadIdx.x & 31) == 0) {
-        v = atomicAdd(p.sched, 1);
+        v = ctl->collided ? -1 : atomicAdd(p.sched, 1);
         if (v >= p.num_units) v = -1;
         ctl->unit_idx[slot] = v;
         mbar_arrive(smem_addr(&ctl->unit_full[slot]));
@@ -644,6 +666,7 @@ __global__ void __launch_bounds__(384, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     ATTN_TRACE_DECL
+    ATTN_TRACE(EV_K_ENTRY, 0);
 
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
@@ -664,6 +687,17 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(B(ctl->unit_empty[s]), kUnitReaders);
         }
         ctl->abort = 0u;
+        ctl->collided = 0u;
+        if (p.sched != nullptr) {
+            // take the schedule slot for this launch, or find it held by
+            // another one (more launches in flight than there are slots)
+            const uint32_t prev = atomicCAS(reinterpret_cast<unsigned int *>(p.sched + 2), 0u, p.sched_gen);
+            if (prev != 0u && prev != p.sched_gen) {
+                ctl->collided = 1u;
+                record_status(p.status, STATUS_SCHED_COLLISION, SITE_SCHED_SLOT);
+            }
+            __threadfence();
+        }
         fence_barrier_init();
     }
     if (warp == 8) {
@@ -679,6 +713,7 @@ __global__ void __launch_bounds__(384, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
+    ATTN_TRACE(EV_K_READY, 0);
 
     if (warp >= 8) {
       // Warpgroup 2: the setmaxnreg and all of this warpgroup's work sit in
@@ -1083,6 +1118,7 @@ __global__ void __launch_bounds__(384, 1)
         }
     }
 
+    ATTN_TRACE(EV_K_EXIT, 0);
     tc_fence_before();
     __syncthreads();
     if (warp == 8) {
@@ -1090,13 +1126,17 @@ __global__ void __launch_bounds__(384, 1)
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
     // Dynamic schedule: every claim of this CTA has returned; the last CTA
-    // to get here leaves the counter pair at zero for the next launch.
-    if (p.sched != nullptr && threadIdx.x == 0) {
+    // to get here leaves the slot free (zero) for the next launch, clearing
+    // the owner last.  A CTA that found the slot held by another launch never
+    // touched its counters and is not counted; the slot then stays held by
+    // this launch until attn_fwd_status_clear (the collision was reported).
+    if (p.sched != nullptr && threadIdx.x == 0 && !ctl->collided) {
         __threadfence();
         if (atomicAdd(p.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
             p.sched[0] = 0;
             p.sched[1] = 0;
             __threadfence();
+            atomicExch(reinterpret_cast<unsigned int *>(p.sched + 2), 0u);
         }
     }
 }

@@ -34,6 +34,19 @@
  * attn_last_error().  Argument errors are detected before anything is
  * enqueued.  Precision: fp32 accumulation and statistics; P is rounded to
  * `dtype` before the P.V product; O is rounded to nearest-even into `dtype`.
+ *
+ * Argument types: sizes are int64_t (so that b*h*s*d products of large
+ * problems are formed without overflow on either side of the call) and
+ * `stream` is a void* holding a cudaStream_t, so that this header needs no
+ * CUDA header.  The device watchdog word is read with attn_fwd_status (all
+ * four words) or attn_fwd_debug_status (the code only).
+ *
+ * Device state: the library keeps, per device, a status word, the counter
+ * slots of the dynamic schedule and a scratch array (attn_fwd_splitkv_noalloc),
+ * whose device addresses it looks up on the first call on that device and
+ * keeps for the life of the process.  cudaDeviceReset, or anything else that
+ * destroys the device's primary context, invalidates them: the library must
+ * not be used on that device afterwards.
  */
 #ifndef ATTN_FWD_H
 #define ATTN_FWD_H
@@ -150,9 +163,16 @@ int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o,
  * fall outside the totals is skipped (its outputs are not written).  Same
  * error codes as attn_fwd.
  * Work units of unequal size are handed out through one of 256 device
- * counters that launches of this entry point and of attn_fwd_kvcache take in
- * turn (each launch leaves its counter at zero when it ends), so at most 256
- * such launches may be in flight on one device at a time.
+ * counter slots that launches of this entry point and of attn_fwd_kvcache
+ * take in turn, each launch tagged with its own generation number (each
+ * launch leaves its slot free when it ends), so at most 256 such launches may
+ * be in flight on one device at a time.  A launch that finds its slot still
+ * held by another launch does not share its counters: the CTAs that find it
+ * so take no work and record ATTN_STATUS_SCHED_COLLISION in the status word
+ * (attn_fwd_status); the outputs of that launch are then not to be trusted,
+ * and the slot stays held until attn_fwd_status_clear.  A CUDA graph that
+ * holds such a launch must not be replayed concurrently with itself (both
+ * replays carry the same generation).
  */
 int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o,
                     float *lse, const int32_t *cu_seqlens_q,
@@ -205,17 +225,22 @@ int attn_fwd_splitkv_default_splits(int64_t b, int64_t h, int64_t sq,
  * and outputs, with the layouts and semantics of attn_fwd.  It allocates
  * nothing.
  *
- *   num_splits : as for attn_fwd_splitkv.  Sizes whose partials need more
- *                than ATTN_NOALLOC_SCRATCH_BYTES (see
- *                attn_fwd_splitkv_workspace_bytes) are rejected with
- *                ATTN_ERR_SHAPE and a message saying how much they need.
+ *   num_splits : 1..min(1024, ceil(sk / 128)), as for attn_fwd_splitkv.
+ *                With num_splits == 1 or sk == 0 the scratch is not
+ *                touched, and such calls do not race with others.  Sizes
+ *                whose partials need more than ATTN_NOALLOC_SCRATCH_BYTES
+ *                (see attn_fwd_splitkv_workspace_bytes) are rejected with
+ *                ATTN_ERR_SHAPE and a message saying how much they need;
+ *                other argument errors give the codes of attn_fwd_splitkv.
  *
  * The first call on each device looks up the array's device address on that
- * device.  All calls on a
- * device share the one array, and it keeps the last call's contents (nothing
- * in it needs to start at zero: each call writes what it reads).  Calls that
- * overlap on the GPU -- on different streams, or from different host threads
- * -- race on the array; serialise them.
+ * device (make that first call before any stream capture); the address is
+ * kept for the life of the process, so a device reset invalidates it (see
+ * "Device state" above).  All calls on a device share the one array, and it
+ * keeps the last call's contents (nothing in it needs to start at zero: each
+ * call writes what it reads).  Calls that overlap on the GPU -- on different
+ * streams, or from different host threads -- race on the array; serialise
+ * them.
  */
 #define ATTN_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v,
@@ -379,13 +404,32 @@ const char *attn_last_error(void);
  * Device watchdog.  Every wait inside the kernels is bounded; a wait that
  * runs out records a nonzero code in a per-device status word and the kernel
  * winds down (waits for its own copies and MMAs, frees tensor memory) and
- * returns instead of hanging.  attn_fwd_status synchronises the current
- * device, copies the status into out[0..3] = {code, block, warp, site} (out
- * may be NULL) and returns code (0 = no timeout, <0 = CUDA error while
- * reading).  attn_fwd_status_clear zeroes it.
+ * returns instead of hanging.  The first failure is kept until cleared:
+ *   code ATTN_STATUS_TIMEOUT (1)         a wait ran out;
+ *   code ATTN_STATUS_SCHED_COLLISION (2) a launch found its schedule slot
+ *                                        held by another (attn_fwd_varlen).
+ * attn_fwd_status synchronises the current device, copies the status into
+ * out[0..3] = {code, block, warp, site} (out may be NULL) and returns code
+ * (0 = nothing recorded, <0 = CUDA error while reading).
+ * attn_fwd_status_clear synchronises the device, then zeroes the status word
+ * and frees every schedule slot; call it with no forward in flight on the
+ * device (from any thread).
+ * attn_fwd_debug_status is attn_fwd_status(NULL): the code alone.
  */
+#define ATTN_STATUS_TIMEOUT 1
+#define ATTN_STATUS_SCHED_COLLISION 2
 int attn_fwd_status(uint32_t *out);
 int attn_fwd_status_clear(void);
+int attn_fwd_debug_status(void);
+
+/*
+ * Testing hook: make every later launch of the dynamic schedule on the
+ * current device take counter slot `slot` (0..255) instead of the next one
+ * in turn; -1 restores the turn.  It exists so that a test can put two
+ * launches on one slot and check that the collision is reported.  Returns
+ * ATTN_OK or ATTN_ERR_SHAPE for a slot outside -1..255.
+ */
+int attn_fwd_sched_pin_slot(int slot);
 
 /*
  * attn_fwd_watchdog_selftest: launches the forward on tiny caller-provided

@@ -177,3 +177,29 @@ def call_paged(lib, table=P, page_size=256, num_pages=8, pps=2, seqlens=P):
 def test_kvcache_paged_argument_errors(lib, kw, code):
     rc, msg = call_paged(lib, **kw)
     assert rc == code, (rc, msg)
+
+
+def test_noalloc_rejects_bad_head_dim_like_the_other_entry_points(lib):
+    """A bad head dim is ATTN_ERR_HEADDIM from the no-alloc entry point too
+    (its scratch-size check comes after the checks it shares with
+    attn_fwd_splitkv), and absurd sizes are rejected without overflow."""
+    rc = lib.attn_fwd_splitkv_noalloc(P, P, P, P, None, 1, 2, 3, 1000, 96, 0, 0.1, 1, 2, None)
+    assert rc == -3, lib.attn_last_error()
+    rc = lib.attn_fwd_splitkv_noalloc(P, P, P, P, None, 1 << 15, (1 << 16) - 1, 1 << 30, 1 << 30, 128, 0, 0.1, 1,
+                                      1024, None)
+    assert rc == -2 and "scratch" in lib.attn_last_error().decode()
+    rc = lib.attn_fwd_splitkv_noalloc(P, P, P, P, None, 1, 2, 3, 1000, 128, 0, 0.1, 1, 0, None)
+    assert rc == -2
+
+
+def test_debug_status_and_slot_hook_without_device(lib):
+    """attn_fwd_debug_status (the watchdog code alone) and the schedule-slot
+    testing hook exist; without a GPU they return an error, not a crash, and
+    the hook rejects slots outside -1..255 before looking for a device."""
+    import torch
+    assert lib.attn_fwd_sched_pin_slot(256) == -2
+    assert lib.attn_fwd_sched_pin_slot(-2) == -2
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lib.attn_fwd_debug_status() in (-7, -8)
+    assert lib.attn_fwd_sched_pin_slot(3) in (-7, -8)

@@ -42,14 +42,17 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_splitkv_on_two_calls_in_a_row():
-    """Two consecutive calls (different inputs, so the second cannot pass on
-    what the first left in the shared scratch) agree with attn_fwd_splitkv
-    given its own workspace, within the bf16 tolerances of the parity tests
-    (O max-abs 2e-2 and rel-L2 1e-2, LSE 1e-3)."""
+def test_noalloc_matches_oracle_and_splitkv_on_two_calls_in_a_row():
+    """Two consecutive calls (different inputs, one of them causal, so the
+    second cannot pass on what the first left in the shared scratch) are
+    checked element by element against the fp64 oracle on the same seeded
+    inputs, within the bf16 tolerances of the parity tests (O max-abs 2e-2
+    and rel-L2 1e-2, LSE 1e-3); they are also compared with
+    attn_fwd_splitkv given its own workspace."""
     import torch
     from parity import compare
     import attention_forward_14_gb300 as af
+    import oracle
 
     lib = binding.load()
     dev = torch.device("cuda", 0)
@@ -57,13 +60,18 @@ def test_noalloc_matches_splitkv_on_two_calls_in_a_row():
     assert binding.splitkv_workspace_bytes(b, h, sq, d, splits) <= 16 * 1024 * 1024
     scale = 1.0 / math.sqrt(d)
     for call, (seed, causal) in enumerate(((101, False), (202, True))):
-        q, k, v = (t.to(dev) for t in W.draw(b, h, sq, sk, d, "bf16", seed))
+        qc, kc, vc = W.draw(b, h, sq, sk, d, "bf16", seed)
+        q, k, v = (t.to(dev) for t in (qc, kc, vc))
         o = torch.full_like(q, float("nan"))
         lse = torch.full((b, h, sq), float("nan"), dtype=torch.float32, device=dev)
         rc = _noalloc(lib, q, k, v, o, lse, causal, scale, splits)
         assert rc == 0, lib.attn_last_error().decode()
-        o_ref, lse_ref = af.attn_fwd_splitkv(q, k, v, causal=causal, scale=scale, num_splits=splits)
         torch.cuda.synchronize()
-        compare(o.float().cpu().double().numpy(), lse.cpu().double().numpy(),
-                o_ref.float().cpu().double().numpy(), lse_ref.cpu().double().numpy(), "bf16",
-                f"no-alloc call {call + 1}")
+        got_o, got_lse = o.float().cpu().double().numpy(), lse.cpu().double().numpy()
+        o_ref, lse_ref = oracle.attn_fwd(qc.double().numpy(), kc.double().numpy(), vc.double().numpy(), causal,
+                                         scale)
+        compare(got_o, got_lse, o_ref, lse_ref, "bf16", f"no-alloc call {call + 1} against the oracle")
+        o_sk, lse_sk = af.attn_fwd_splitkv(q, k, v, causal=causal, scale=scale, num_splits=splits)
+        torch.cuda.synchronize()
+        compare(got_o, got_lse, o_sk.float().cpu().double().numpy(), lse_sk.cpu().double().numpy(), "bf16",
+                f"no-alloc call {call + 1} against attn_fwd_splitkv")

@@ -175,8 +175,8 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, 
 
 def attn_fwd_fp8(q, k, v, causal: bool = False, scale: float | None = None, descale_q: float = 1.0,
                  descale_k: float = 1.0, descale_v: float = 1.0, o=None, lse=None, stream=None):
-    """e4m3 inputs [b, h, s, 128] (torch.float8_e4m3fn CUDA tensors) with
-    per-tensor descales; returns (o bf16 [b, h, sq, 128], lse fp32)."""
+    """e4m3 inputs [b, h, s, d], d = 64 or 128 (torch.float8_e4m3fn CUDA tensors) with
+    per-tensor descales; returns (o bf16 [b, h, sq, d], lse fp32)."""
     import torch
     lib = load()
     b, h, sq, d = q.shape

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libattn_fwd.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["attn_fwd_api.cu", "inst_d64.cu", "inst_d128_noncausal.cu", "inst_d128_causal.cu", "inst_d128_fp8.cu",
+SOURCES = ["attn_fwd_api.cu", "inst_d64.cu", "inst_d128_noncausal.cu", "inst_d128_causal.cu", "inst_fp8.cu",
            "attn_bwd_inst.cu", "attn_bwd_inst_varlen.cu"]
 
 

@@ -116,22 +116,27 @@ int get_encode(PFN_cuTensorMapEncodeTiled_v12000 *fn)
 }
 
 // 3-D view [bh, s, d] of a contiguous [b, h, s, d] tensor; box = 128 rows x
-// 64 elements (one 128-byte swizzle panel), so rows past s of each head are
-// zero-filled by the copy engine rather than read from the next head.
-int make_map(CUtensorMap *map, const void *ptr, int dtype, int64_t bh, int64_t s, int64_t d, int elem_bytes = 2)
+// one 128-byte swizzle panel (64 16-bit or 128 8-bit elements), so rows past
+// s of each head are zero-filled by the copy engine rather than read from the
+// next head.  Rows shorter than 128 bytes (8-bit, d = 64) are one 64-byte
+// panel with the 64-byte swizzle.
+int make_map(CUtensorMap *map, const void *ptr, int dtype, int64_t bh, int64_t s, int64_t d, int elem_bytes = 2,
+             int box_rows = 128)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     int rc = get_encode(&enc);
     if (rc != ATTN_OK) return rc;
+    const int64_t row_bytes = d * elem_bytes < 128 ? d * elem_bytes : 128;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(s), static_cast<cuuint64_t>(bh)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * elem_bytes), static_cast<cuuint64_t>(s * d * elem_bytes)};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), 128, 1};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(row_bytes / elem_bytes), static_cast<cuuint32_t>(box_rows), 1};
     cuuint32_t estr[3] = {1, 1, 1};
     const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                    : dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUresult r = enc(map, dt, 3, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
     return ATTN_OK;
 }
@@ -139,14 +144,15 @@ int make_map(CUtensorMap *map, const void *ptr, int dtype, int64_t bh, int64_t s
 // Packed [tokens, h, d] tensor seen as 3-D [tokens][h][d]: box = 64
 // elements x 1 head x 128 tokens, the same 128-row x 128-byte shared-memory
 // image as the dense map.  Rows past the last token are zero-filled.
-int make_map_packed(CUtensorMap *map, const void *ptr, int dtype, int64_t tokens, int64_t h, int64_t d)
+int make_map_packed(CUtensorMap *map, const void *ptr, int dtype, int64_t tokens, int64_t h, int64_t d,
+                    int box_rows = 128)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     int rc = get_encode(&enc);
     if (rc != ATTN_OK) return rc;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h), static_cast<cuuint64_t>(tokens)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2), static_cast<cuuint64_t>(h * d * 2)};
-    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                      const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -302,6 +308,7 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_
     }
     LaunchArgs a;
     if ((rc = make_map(&a.q, q, dtype, bh, sq, d)) != ATTN_OK) return rc;
+    if ((rc = make_map(&a.o, o, dtype, bh, sq, d, 2, 32)) != ATTN_OK) return rc;  // stores of 32 rows
     if (cache.block_table != nullptr) {
         const int64_t pool = cache.num_pages * cache.page_size;
         if ((rc = make_map_packed(&a.k, k, dtype, pool, h, d)) != ATTN_OK) return rc;
@@ -994,6 +1001,7 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float 
     if ((rc = make_map_packed(&a.q, q, dtype, total_q, h, d)) != ATTN_OK) return rc;
     if ((rc = make_map_packed(&a.k, k, dtype, total_k, h, d)) != ATTN_OK) return rc;
     if ((rc = make_map_packed(&a.v, v, dtype, total_k, h, d)) != ATTN_OK) return rc;
+    if ((rc = make_map_packed(&a.o, o, dtype, total_q, h, d, 32)) != ATTN_OK) return rc;  // stores of 32 rows
     FwdParams &p = a.p;
     p.o = o;
     p.lse = lse;
@@ -1040,7 +1048,8 @@ int attn_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *ls
                  void *stream)
 {
     g_err.clear();
-    if (d != 128) return fail(ATTN_ERR_HEADDIM, "the e4m3 forward supports head dim 128 only (got %lld)", (long long)d);
+    if (d != 64 && d != 128)
+        return fail(ATTN_ERR_HEADDIM, "the e4m3 forward supports head dims 64 and 128 (got %lld)", (long long)d);
     if (!std::isfinite(descale_q) || !std::isfinite(descale_k) || !std::isfinite(descale_v))
         return fail(ATTN_ERR_SCALE, "descale factors must be finite");
     const double sqk = static_cast<double>(scale) * descale_q * descale_k;
@@ -1064,6 +1073,7 @@ int attn_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *ls
     if ((rc = make_map(&a.q, q, ATTN_BF16, bh, sq, d, 1)) != ATTN_OK) return rc;
     if ((rc = make_map(&a.k, k, ATTN_BF16, bh, sk, d, 1)) != ATTN_OK) return rc;
     if ((rc = make_map(&a.v, v, ATTN_BF16, bh, sk, d, 1)) != ATTN_OK) return rc;
+    if ((rc = make_map(&a.o, o, ATTN_BF16, bh, sq, d, 2, 32)) != ATTN_OK) return rc;  // bf16 output, 32-row stores
     FwdParams &p = a.p;
     p.o = o;
     p.lse = lse;
@@ -1091,7 +1101,10 @@ int attn_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *ls
 #endif
     a.grid = static_cast<int>(units < di->sm_count ? units : di->sm_count);
     a.stream = st;
-    e = causal ? launch_fwd<128, __nv_fp8_e4m3, true>(a) : launch_fwd<128, __nv_fp8_e4m3, false>(a);
+    if (d == 64)
+        e = causal ? launch_fwd<64, __nv_fp8_e4m3, true>(a) : launch_fwd<64, __nv_fp8_e4m3, false>(a);
+    else
+        e = causal ? launch_fwd<128, __nv_fp8_e4m3, true>(a) : launch_fwd<128, __nv_fp8_e4m3, false>(a);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch (e4m3)");
     return ATTN_OK;
 }

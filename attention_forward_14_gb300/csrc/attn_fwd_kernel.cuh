@@ -16,6 +16,10 @@
 //               handed to the softmax groups: 216 per softmax thread, 72
 //               for the others; 256*216 + 128*72 = 384*168 at launch,
 //               and 216 + 216 + 72 = 3*168 on each SM sub-partition)
+// Epilogue: each softmax warp writes its 32 finished rows (O / row sum,
+// rounded) into its own 4 KiB shared-memory slice, 64 columns at a time,
+// and its lane 0 has the copy engine store the slice to global memory
+// (whole 128-byte rows instead of one 16-byte piece of 32 rows per store).
 // A work unit is (batch*head, 256-row block).  Per unit the producer loads
 // the two Q tiles once and streams K_j, V_j tiles (128 keys each) through an
 // NSLOT-deep shared-memory ring.  The MMA thread computes S_t = Q_t K_j^T
@@ -147,6 +151,7 @@ enum : uint32_t {
     EV_MMA_WAIT_Q = 20, EV_MMA_GOT_Q, EV_MMA_WAIT_KV, EV_MMA_GOT_KV, EV_MMA_WAIT_P, EV_MMA_GOT_P, EV_MMA_ISSUED,
     EV_LD_WAIT = 40, EV_LD_GOT,
     EV_K_ENTRY = 60, EV_K_READY, EV_K_EXIT,
+    EV_SM_EPI_WRITTEN = 81,
 };
 
 // Watchdog sites (recorded in status[3]).
@@ -212,25 +217,49 @@ struct Cfg {
     static constexpr int QT = 2;                   // Q tiles per unit
     static constexpr int UNIT_ROWS = BM * QT;      // 256
     static constexpr int BN = 128;                 // keys per K/V tile
-    static constexpr int PANEL_ELEMS = 128 / EB;   // one 128-byte swizzle panel
-    static constexpr int NPANEL = D * EB / 128;
-    static constexpr int PANEL_BYTES = 128 * 128;  // 128 rows x 128 B
+    // A panel is 128 rows of ROW_BYTES with the swizzle of that width: 128
+    // bytes, or 64 bytes when a whole row is shorter (8-bit, head dim 64).
+    static constexpr int ROW_BYTES = (D * EB < 128) ? D * EB : 128;
+    static constexpr int PANEL_ELEMS = ROW_BYTES / EB;
+    static constexpr int NPANEL = D * EB / ROW_BYTES;
+    static constexpr int PANEL_BYTES = 128 * ROW_BYTES;
     static constexpr int TILE_BYTES = NPANEL * PANEL_BYTES;  // one Q, K or V tile
-    static constexpr int NSLOT = (TILE_BYTES == 2 * PANEL_BYTES) ? 5 : 8;
+    static constexpr int NSLOT = (TILE_BYTES == 2 * PANEL_BYTES) ? 4 : 8;
+    static constexpr uint32_t DESC_HI = ROW_BYTES == 128 ? kDescHi : kDescHi64;
     static constexpr int QK_STEPS = D * EB / 32;   // 32-byte k-steps of S = Q K^T
+    static constexpr int KSTEPS_PER_ROW = ROW_BYTES / 32;
     static constexpr int PV_KEYS = 32 / EB;        // keys per k-step of O += P V
     static constexpr int PV_STEPS = BN / PV_KEYS;
     static constexpr int CTL_BYTES = 1024;
     static constexpr int Q_OFF = CTL_BYTES;
     static constexpr int KV_OFF = Q_OFF + QT * TILE_BYTES;
-    static constexpr int SMEM_BYTES = KV_OFF + NSLOT * TILE_BYTES + 1024;  // +1 KiB for alignment
+    // O staging: a 32-row x 128-byte slice (64 columns of the 16-bit
+    // output) per softmax warp, written by the warp and stored to global
+    // memory by the copy engine, O_NPANEL times per tile.
+    static constexpr int O_PANEL_COLS = 64;
+    static constexpr int O_NPANEL = D / O_PANEL_COLS;
+    static constexpr int OST_WARP_BYTES = 32 * 128;
+    static constexpr int OST_BYTES = 4 * OST_WARP_BYTES;  // per softmax group
+    static constexpr int OST_OFF = KV_OFF + NSLOT * TILE_BYTES;
+    // Head dim 64, 16-bit: tensor memory has room for the row sums of P as
+    // rounded, so the tensor core computes them and the softmax does not.
+    // The P.V product is N = 64 + 16 wide: its B operand is V's 64 columns
+    // followed by a block of ones (16 rows x 128 bytes of shared memory,
+    // reached through the descriptor's leading byte offset), so columns
+    // 64..79 of the accumulator hold the rounded row sums, rescaled with O.
+    static constexpr bool LR_MMA = (D == 64 && EB == 2);
+    static constexpr int PV_N = LR_MMA ? D + 16 : D;
+    static constexpr int TMEM_O_STRIDE = LR_MMA ? 128 : D;  // O_t (and its row sums) at TMEM_O + t*stride
+    static constexpr int ONES_OFF = OST_OFF + QT * OST_BYTES;
+    static constexpr int ONES_BYTES = LR_MMA ? 2048 : 0;
+    static constexpr int SMEM_BYTES = ONES_OFF + ONES_BYTES + 1024;  // +1 KiB for alignment
     static constexpr int TMEM_COLS = 512;
     static constexpr int TMEM_S = 0;               // S_t at column t*BN (P_t aliases it)
-    static constexpr int TMEM_O = QT * BN;         // O_t at TMEM_O + t*D
+    static constexpr int TMEM_O = QT * BN;         // O_t at TMEM_O + t*TMEM_O_STRIDE
     static constexpr int THREADS = 384;
     static constexpr int REGS_SOFTMAX = 216;
     static constexpr int REGS_OTHER = 72;
-    static_assert(TMEM_O + QT * D <= TMEM_COLS, "tensor memory budget");
+    static_assert(TMEM_O + QT * TMEM_O_STRIDE <= TMEM_COLS && PV_N <= TMEM_O_STRIDE, "tensor memory budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
@@ -343,10 +372,10 @@ __device__ __forceinline__ void zero_v_tail_rows(uint32_t tile, int valid)
 {
     using C = Cfg<D, EB>;
     const int lane = threadIdx.x & 31;
-    const int chunks = (C::BN - valid) * 8;  // 16-byte chunks per panel
+    const int chunks = (C::BN - valid) * (C::ROW_BYTES / 16);  // 16-byte chunks per panel
     for (int pn = 0; pn < C::NPANEL; ++pn)
         for (int c = lane; c < chunks; c += 32)
-            st_shared_v4(tile + pn * C::PANEL_BYTES + valid * 128 + c * 16, 0u, 0u, 0u, 0u);
+            st_shared_v4(tile + pn * C::PANEL_BYTES + valid * C::ROW_BYTES + c * 16, 0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
     __syncwarp();
 }
@@ -545,9 +574,10 @@ __device__ __forceinline__ void rescale_rows(uint32_t tO, float alpha)
 // two per 32-bit column) is stored into the first 64 tensor-memory columns
 // at tS.  The first half (keys 0..63) is stored and announced on `half_bar`
 // as soon as it is ready, so the P.V product can start on it while the
-// second half is computed.  Returns {sum of p, sum of p as rounded}.  The
+// second half is computed.  Returns {sum of p, sum of p as rounded}; the
+// second is 0 when LR is false (the tensor core sums the rounded P).  The
 // caller waits for the second store (tmem_wait_st) and announces it.
-template <typename T, bool MASKED>
+template <typename T, bool MASKED, bool LR = true>
 __device__ __forceinline__ float2 exp_store_tile(const uint32_t (&sr)[128], int lim, float sl2e, float m_use, uint32_t tS,
                                                  uint32_t half_bar)
 {
@@ -573,7 +603,7 @@ __device__ __forceinline__ float2 exp_store_tile(const uint32_t (&sr)[128], int 
             const float p1 = ex2_approx(x.y);
             l4[c & 3] = __fadd2_rn(l4[c & 3], make_float2(p0, p1));
             const uint32_t pk = pack2<T>(p0, p1);
-            lr4[c & 3] = add_halves<T>(pk, lr4[c & 3]);
+            if constexpr (LR) lr4[c & 3] = add_halves<T>(pk, lr4[c & 3]);
             if (c < 32)
                 pa[c] = pk;
             else
@@ -641,17 +671,30 @@ __device__ __forceinline__ void store_row_zero(const FwdParams &p, const Unit &u
     if (p.lse) p.lse[lse_index(p, un, row)] = -INFINITY;
 }
 
+// Whether the 32 rows of a warp starting at row r0 go through the warp's
+// staging slice and the copy engine (rows past the end of a dense tensor are
+// dropped by the copy engine).  Not for split partials (fp32, written row by
+// row), not for rows that all lie past the sequence, and not for packed rows
+// that run past their sequence, whose last rows belong to the next one.
+template <typename C>
+__device__ __forceinline__ bool o_staged(const FwdParams &p, const Unit &un, int r0)
+{
+    if (p.num_splits > 1 || r0 >= un.sq) return false;
+    return p.cu_q == nullptr || r0 + 32 <= un.sq;
+}
+
 template <int D, typename T, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const FwdParams p)
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const FwdParams p)
 {
     using E = Elem<T>;
     using C = Cfg<D, E::BYTES>;
     using TO = typename E::Out;
     // format code 1 = bf16 in kind::f16; 0 = f16, or e4m3 in kind::f8f6f4
     constexpr uint32_t IDESC_QK = idesc_f16(128, C::BN, E::BF16, false);
-    constexpr uint32_t IDESC_PV = idesc_f16(128, D, E::BF16, true);
+    constexpr uint32_t IDESC_PV = idesc_f16(128, C::PV_N, E::BF16, true);
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -660,6 +703,7 @@ __global__ void __launch_bounds__(384, 1)
     Ctl *ctl = reinterpret_cast<Ctl *>(smem);
     const uint32_t sQ = base_addr + C::Q_OFF;    // Q tile t at sQ + t*TILE_BYTES
     const uint32_t sKV = base_addr + C::KV_OFF;  // slot s at sKV + s*TILE_BYTES
+    const uint32_t sOst = base_addr + C::OST_OFF;  // O staging panel of group t at sOst + t*OST_BYTES
 
     auto B = [&](const uint64_t &bar) { return smem_addr(&bar); };
 
@@ -704,10 +748,18 @@ __global__ void __launch_bounds__(384, 1)
         tmem_alloc(smem_addr(&ctl->tmem_base), C::TMEM_COLS);
         tmem_relinquish();
     }
+    if constexpr (C::LR_MMA) {
+        if (threadIdx.x < C::ONES_BYTES / 16) {  // the block of ones (1.0 in T, two per word)
+            const uint32_t one2 = E::BF16 ? 0x3F803F80u : 0x3C003C00u;
+            st_shared_v4(base_addr + C::ONES_OFF + threadIdx.x * 16, one2, one2, one2, one2);
+            fence_proxy_async_smem();
+        }
+    }
     if (warp == 9 && lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmO);
     }
     tc_fence_before();
     __syncthreads();
@@ -848,15 +900,17 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t dq0 = desc_lo(sQ, 16);
         const uint32_t dk0 = desc_lo(sKV, 16);
         const uint32_t dv0 = desc_lo(sKV, C::PANEL_BYTES);
+        const uint32_t ones_addr = base_addr + C::ONES_OFF;
         auto issue_qk = [&](int t, uint32_t kslot) {
             const uint32_t a0 = dq0 + ((t * C::TILE_BYTES) >> 4);
             const uint32_t b0 = dk0 + ((kslot * C::TILE_BYTES) >> 4);
             const uint32_t d = tmem + C::TMEM_S + t * C::BN;
 #pragma unroll
             for (int kk = 0; kk < C::QK_STEPS; ++kk) {  // 32 bytes of the head dim per step
-                const uint32_t off = ((kk / 4) * C::PANEL_BYTES + (kk % 4) * 32) >> 4;
+                const uint32_t off =
+                    ((kk / C::KSTEPS_PER_ROW) * C::PANEL_BYTES + (kk % C::KSTEPS_PER_ROW) * 32) >> 4;
                 if constexpr (E::FP8)
-                    mma_ss_f8(d, a0 + off, b0 + off, IDESC_QK, kk > 0 ? 1u : 0u);
+                    mma_ss_f8(d, a0 + off, b0 + off, IDESC_QK, kk > 0 ? 1u : 0u, C::DESC_HI);
                 else
                     mma_ss(d, a0 + off, b0 + off, IDESC_QK, kk > 0 ? 1u : 0u);
             }
@@ -865,14 +919,18 @@ __global__ void __launch_bounds__(384, 1)
         auto issue_pv = [&](int t, uint32_t vslot, bool accumulate, int half) {
             const uint32_t b0 = dv0 + ((vslot * C::TILE_BYTES) >> 4);
             const uint32_t a = tmem + C::TMEM_S + t * C::BN;  // P_t, 32 bits of keys per column
-            const uint32_t d = tmem + C::TMEM_O + t * D;
+            const uint32_t d = tmem + C::TMEM_O + t * C::TMEM_O_STRIDE;
 #pragma unroll
             for (int k2 = 0; k2 < C::PV_STEPS / 2; ++k2) {
                 const int kk = half * (C::PV_STEPS / 2) + k2;
-                const uint32_t bo = (kk * C::PV_KEYS * 128) >> 4;  // PV_KEYS rows of 128 B
+                const uint32_t bo = (kk * C::PV_KEYS * C::ROW_BYTES) >> 4;  // PV_KEYS rows
                 if constexpr (E::FP8)
-                    mma_ts_f8(d, a + kk * 8, b0 + bo, IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
-                else
+                    mma_ts_f8(d, a + kk * 8, b0 + bo, IDESC_PV, (accumulate || kk > 0) ? 1u : 0u, C::DESC_HI);
+                else if constexpr (C::LR_MMA) {
+                    // [V | ones]: the ones block is the second 64-column atom along N
+                    const uint32_t vaddr = sKV + vslot * C::TILE_BYTES + kk * C::PV_KEYS * C::ROW_BYTES;
+                    mma_ts(d, a + kk * 8, desc_lo(vaddr, ones_addr - vaddr), IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+                } else
                     mma_ts(d, a + kk * 8, b0 + bo, IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
             }
         };
@@ -978,10 +1036,11 @@ __global__ void __launch_bounds__(384, 1)
         const int r_in_tile = quad * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS = tmem + lane_off + C::TMEM_S + t * C::BN;
-        const uint32_t tO = tmem + lane_off + C::TMEM_O + t * D;
+        const uint32_t tO = tmem + lane_off + C::TMEM_O + t * C::TMEM_O_STRIDE;
         const float sl2e = p.sl2e;
         const bool neg = sl2e < 0.f;  // the row maximum of scale*s is scale*min(s)
         uint32_t s_ph = 0u, o_ph = 0u;
+        uint32_t epi_n = 0u;  // O panels this group has staged so far
         bool ok = true;
         for (uint32_t i = 0; ok; ++i) {
             int u;
@@ -1030,6 +1089,8 @@ __global__ void __launch_bounds__(384, 1)
                     if (__any_sync(0xffffffffu, need)) {
                         const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m - m_new);
                         rescale_rows<D>(tO, alpha);
+                        if constexpr (C::LR_MMA)  // the rounded row sum, column D of the accumulator
+                            tmem_st1(tO + D, __float_as_uint(__uint_as_float(tmem_ld1_wait(tO + D)) * alpha));
                         l *= alpha;
                         lr *= alpha;
                         m = m_new;
@@ -1042,9 +1103,9 @@ __global__ void __launch_bounds__(384, 1)
                 const float m_use = ((m == -INFINITY) ? 0.f : m) - E::SHIFT;  // exp reference
                 float2 sums;  // {sum of p, sum of p as rounded}
                 if (masked)
-                    sums = exp_store_tile<T, true>(sr, lim, sl2e, m_use, tS, B(ctl->p_half[t]));
+                    sums = exp_store_tile<T, true, !C::LR_MMA>(sr, lim, sl2e, m_use, tS, B(ctl->p_half[t]));
                 else
-                    sums = exp_store_tile<T, false>(sr, lim, sl2e, m_use, tS, B(ctl->p_half[t]));
+                    sums = exp_store_tile<T, false, !C::LR_MMA>(sr, lim, sl2e, m_use, tS, B(ctl->p_half[t]));
                 l += sums.x;
                 lr += sums.y;
                 ATTN_TRACE(EV_SM_EXP, j);
@@ -1063,6 +1124,7 @@ __global__ void __launch_bounds__(384, 1)
                 ATTN_TRACE(EV_SM_EPI_GOT, u);
                 o_ph ^= 1u;
                 tc_fence_after();
+                if constexpr (C::LR_MMA) lr = __uint_as_float(tmem_ld1_wait(tO + D));
                 const float inv_l = (lr > 0.f) ? p.o_scale / lr : 0.f;
                 const float m_ref = m - E::SHIFT;  // reference of l and lr
                 const bool valid = row < un.sq;
@@ -1091,22 +1153,75 @@ __global__ void __launch_bounds__(384, 1)
                     tc_fence_before();
                     continue;
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<TO *>(p.o) + o_row_offset(p, un, valid ? row : 0, D));
+                const int tile_row0 = un.row0 + t * C::BM;
+                // The copy engine stores whole 128-row panels and drops rows
+                // past the end of the tensor; in the packed layout those rows
+                // belong to the next sequence, so a packed tile that runs past
+                // its sequence is stored row by row instead.
+                if (o_staged<C>(p, un, tile_row0 + quad * 32)) {
+                    // This warp's 32 rows go through its staging slice, 64
+                    // columns at a time; lane 0 has the copy engine store the
+                    // slice and, before the slice is written again, waits
+                    // until the copy engine has read it.
+                    const uint32_t slice = sOst + warp * C::OST_WARP_BYTES;
+                    const uint32_t my_row = slice + static_cast<uint32_t>(lane) * 128u;
+                    const uint32_t swz = static_cast<uint32_t>(lane & 7);
 #pragma unroll
-                for (int ch = 0; ch < D / 32; ++ch) {
-                    uint32_t orr[32];
-                    tmem_ld32_wait(tO + ch * 32, orr);
-                    uint32_t pk[16];
+                    for (int pn = 0; pn < C::O_NPANEL; ++pn) {
+                        if (lane == 0 && epi_n > 0) bulk_wait_read_all();
+                        __syncwarp();
+                        // this row's 64 columns, 16-bit, in the 128-byte swizzle
+                        // of the output map: 16-byte chunk c at c ^ (row % 8)
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const float2 v = __fmul2_rn(make_float2(__uint_as_float(orr[2 * c]), __uint_as_float(orr[2 * c + 1])),
-                                                    make_float2(inv_l, inv_l));
-                        pk[c] = pack2<TO>(v.x, v.y);
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t orr[32];
+                            tmem_ld32_wait(tO + pn * 64 + half * 32, orr);
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) {
+                                const float2 v = __fmul2_rn(
+                                    make_float2(__uint_as_float(orr[2 * c]), __uint_as_float(orr[2 * c + 1])),
+                                    make_float2(inv_l, inv_l));
+                                pk[c] = pack2<TO>(v.x, v.y);
+                            }
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const uint32_t chunk = static_cast<uint32_t>(half * 4 + k);
+                                st_shared_v4(my_row + ((chunk ^ swz) << 4), pk[4 * k], pk[4 * k + 1], pk[4 * k + 2],
+                                             pk[4 * k + 3]);
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const int r0 = tile_row0 + quad * 32;
+                            const bool vl = p.cu_q != nullptr;
+                            tma_store_3d(&tmO, slice, pn * C::O_PANEL_COLS, vl ? un.bh : r0, vl ? un.q_tok0 + r0 : un.bh);
+                            bulk_commit_group();
+                        }
+                        ATTN_TRACE(EV_SM_EPI_WRITTEN, pn);
+                        ++epi_n;
                     }
-                    if (valid) {
+                } else {
+                    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<TO *>(p.o) +
+                                                           o_row_offset(p, un, valid ? row : 0, D));
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            dst[ch * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                    for (int ch = 0; ch < D / 32; ++ch) {
+                        uint32_t orr[32];
+                        tmem_ld32_wait(tO + ch * 32, orr);
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const float2 v = __fmul2_rn(
+                                make_float2(__uint_as_float(orr[2 * c]), __uint_as_float(orr[2 * c + 1])),
+                                make_float2(inv_l, inv_l));
+                            pk[c] = pack2<TO>(v.x, v.y);
+                        }
+                        if (valid) {
+#pragma unroll
+                            for (int v4 = 0; v4 < 4; ++v4)
+                                dst[ch * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                        }
                     }
                 }
                 if (valid && p.lse)
@@ -1116,6 +1231,9 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_before();
             }
         }
+        // this warp's O stores complete before the CTA's shared memory goes
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     ATTN_TRACE(EV_K_EXIT, 0);

@@ -13,7 +13,7 @@
 namespace attn {
 
 struct LaunchArgs {
-    CUtensorMap q, k, v;
+    CUtensorMap q, k, v, o;
     FwdParams p;
     int grid;
     cudaStream_t stream;
@@ -36,7 +36,7 @@ cudaError_t launch_fwd(const LaunchArgs &a)
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < kMaxDev) ready[dev].store(1, std::memory_order_release);
     }
-    kern<<<a.grid, Cfg<D, Elem<T>::BYTES>::THREADS, smem, a.stream>>>(a.q, a.k, a.v, a.p);
+    kern<<<a.grid, Cfg<D, Elem<T>::BYTES>::THREADS, smem, a.stream>>>(a.q, a.k, a.v, a.o, a.p);
     return cudaGetLastError();
 }
 
@@ -110,5 +110,7 @@ ATTN_DECLARE_INSTANCE(128, __nv_bfloat16, false)
 ATTN_DECLARE_INSTANCE(128, __nv_bfloat16, true)
 ATTN_DECLARE_INSTANCE(128, __nv_fp8_e4m3, false)
 ATTN_DECLARE_INSTANCE(128, __nv_fp8_e4m3, true)
+ATTN_DECLARE_INSTANCE(64, __nv_fp8_e4m3, false)
+ATTN_DECLARE_INSTANCE(64, __nv_fp8_e4m3, true)
 
 }  // namespace attn

@@ -82,6 +82,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread may sleep (issuing nothing)
+// for up to `ns` nanoseconds, waking as soon as the phase completes.  For
+// waiters that are not on the critical path.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)
@@ -99,6 +115,33 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
         : "memory");
+}
+
+// 3-D tiled store shared -> global, tracked in this thread's bulk async-group
+// (elements outside the tensor's extents are not written).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int32_t c0, int32_t c1, int32_t c2)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// This thread's committed bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// This thread's committed bulk stores have completed (global writes done).
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // Bring a tile into L2 ahead of its load (no shared-memory destination).
@@ -187,6 +230,9 @@ __device__ __forceinline__ void tc_commit(uint32_t bar)
 // (bits 32-45), descriptor version 1 (bit 46), 128-byte swizzle = 2 (bits
 // 61-63) -- is the same for every operand here.
 constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+// The same for operands with 64-byte rows (8-bit elements, head dim 64):
+// stride byte offset 512 B >> 4, 64-byte swizzle = 4.
+constexpr uint32_t kDescHi64 = (512u >> 4) | (1u << 14) | (4u << 29);
 
 __host__ __device__ constexpr uint32_t desc_lo(uint32_t saddr, uint32_t lbo_bytes)
 {
@@ -220,9 +266,10 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_
         : "memory");
 }
 
-// The same two products with 8-bit (e4m3 / e5m2) operands: kind::f8f6f4.
+// The same two products with 8-bit (e4m3 / e5m2) operands: kind::f8f6f4;
+// `desc_hi` is the high word of the shared-memory descriptors.
 __device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
-                                          uint32_t accumulate)
+                                          uint32_t accumulate, uint32_t desc_hi = kDescHi)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
@@ -230,19 +277,19 @@ __device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint32_t a_lo, uint32
         "mov.b64 db, {%2, %5};\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi)
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(desc_hi)
         : "memory");
 }
 
 __device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
-                                          uint32_t accumulate)
+                                          uint32_t accumulate, uint32_t desc_hi = kDescHi)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
         "mov.b64 db, {%2, %5};\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi)
+        "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(desc_hi)
         : "memory");
 }
 
@@ -295,6 +342,23 @@ __device__ __forceinline__ void tmem_ld128_wait(uint32_t taddr, uint32_t (&r)[12
 
 #define ATTN_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), \
                    "r"(r[i + 4]), "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
+
+// One 32-bit column of this thread's lane.
+__device__ __forceinline__ uint32_t tmem_ld1_wait(uint32_t taddr)
+{
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\t"
+                 "tcgen05.wait::ld.sync.aligned;"
+                 : "=r"(r)
+                 : "r"(taddr)
+                 : "memory");
+    return r;
+}
+
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
 
 // Store 32 columns of 32-bit to this thread's lane (asynchronous; pair with
 // tmem_wait_st before signalling a consumer).

@@ -69,6 +69,8 @@ WORKLOADS = {
         Workload("causal_b1_h32_s16384_d128_bf16_qk3", 1, 32, 16384, 16384, 128, "bf16", True, 3.0, 20260004),
         # the long causal problem with 8-bit (e4m3) inputs
         Workload("causal_b1_h32_s16384_d128_e4m3", 1, 32, 16384, 16384, 128, "e4m3", True, 1.0, 20260007),
+        # the ragged head-dim-64 problem with 8-bit (e4m3) inputs
+        Workload("noncausal_b8_h16_s1000_d64_e4m3", 8, 16, 1000, 1000, 64, "e4m3", False, 1.0, 20260013),
         # decode step: one query row per (batch, head) against a 16k-key cache
         Workload("decode_b8_h32_q1_s16384_d128_bf16", 8, 32, 1, 16384, 128, "bf16", False, 1.0, 20260005,
                  splitkv=True),

@@ -64,7 +64,7 @@ def load_peaks():
 # to these (host-side API code does not change what a kernel reads/writes).
 KERNEL_SOURCES = {
     "attn_fwd_kernel": ["ptx.cuh", "attn_fwd_kernel.cuh", "launch.h", "inst_d64.cu", "inst_d128_noncausal.cu",
-                        "inst_d128_causal.cu", "inst_d128_fp8.cu"],
+                        "inst_d128_causal.cu", "inst_fp8.cu"],
     "attn_bwd_kernel": ["ptx.cuh", "attn_bwd_kernel.cuh", "attn_bwd_launch.h", "attn_bwd_inst.cu"],
 }
 

@@ -191,7 +191,8 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o,
  *   O = softmax(scale * descale_q * descale_k * q.k^T [+ causal]) (descale_v * v)
  * Both products run on the 8-bit tensor cores; P is rounded to e4m3 (its
  * reference sits 8 below the row maximum, so P <= 2^8.5 < 448) and O is
- * written as bf16 [b, h, sq, d]; LSE as for attn_fwd.  d must be 128.
+ * written as bf16 [b, h, sq, d]; LSE as for attn_fwd.  d must be 64 or 128
+ * (64: the 64-byte rows are read with the 64-byte swizzle).
  * Returns ATTN_OK or a negative ATTN_ERR_* code.
  */
 int attn_fwd_fp8(const void *q, const void *k, const void *v, void *o,

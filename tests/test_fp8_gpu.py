@@ -9,9 +9,13 @@ weights still sum to one and, to first order,
 which is bounded per element by 2^-4 * max_j |v_j - O_i| over the keys the
 row sees (the bound is reached only when few keys share the weight, e.g.
 near the causal diagonal).  The check is that bound (+ 1/8 for the second
-order term) plus bf16 output rounding, per element; in addition the
-incoherent average must stay small: rel-L2 <= 5e-2.  LSE uses the unrounded
-fp32 sum: 1e-3."""
+order term) plus bf16 output rounding, per element.  In addition, the
+incoherent average: a round-to-nearest error spread evenly over half an ulp
+of a 3-bit mantissa has an RMS of 2^-4 / sqrt(3) relative, which bounds the
+RMS of the deviation term relative to the spread of V, so rel-L2 must stay
+below 2^-4 / sqrt(3) * (1 + 1/8) = 4.06e-2 (measured 1.6-2.5%).  LSE uses the
+unrounded fp32 sum: 1e-3.  Head dims 64 (64-byte rows, 64-byte swizzle) and
+128."""
 import math
 import zlib
 
@@ -25,7 +29,7 @@ import oracle
 
 pytestmark = pytest.mark.gpu
 
-REL_L2 = 5e-2
+REL_L2 = 2.0 ** -4 / math.sqrt(3.0) * (1 + 2.0 ** -3)
 
 
 def _row_bound(o_ref, v, causal, sq, sk):
@@ -51,8 +55,7 @@ def _fp8_inputs(b, h, sq, sk, d, seed, qk_std=1.0):
     return (t.float().to(torch.float8_e4m3fn) for t in (q, k, v))
 
 
-def _check(b, h, sq, sk, causal, seed, dq=1.0, dk=1.0, dv=1.0, qk_std=1.0, what=""):
-    d = 128
+def _check(b, h, sq, sk, causal, seed, dq=1.0, dk=1.0, dv=1.0, qk_std=1.0, what="", d=128):
     q8, k8, v8 = _fp8_inputs(b, h, sq, sk, d, seed, qk_std)
     dev = torch.device("cuda", 0)
     scale = 1 / math.sqrt(d)
@@ -82,31 +85,44 @@ def _check(b, h, sq, sk, causal, seed, dq=1.0, dk=1.0, dv=1.0, qk_std=1.0, what=
 @pytest.mark.parametrize("shape", [(1, 2, 256, 256), (2, 3, 300, 300), (1, 2, 1, 1000), (1, 1, 513, 100),
                                    (1, 2, 1024, 1024)], ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8_matches_oracle(shape, causal):
+@pytest.mark.parametrize("d", [128, 64])
+def test_fp8_matches_oracle(shape, causal, d):
     b, h, sq, sk = shape
-    _check(b, h, sq, sk, causal, seed=zlib.crc32(repr((shape, causal)).encode()), what=f"{shape} c{causal}")
+    _check(b, h, sq, sk, causal, seed=zlib.crc32(repr((shape, causal, d)).encode()), what=f"{shape} c{causal} d{d}",
+           d=d)
 
 
-def test_fp8_descales():
-    _check(1, 2, 300, 500, True, seed=4, dq=0.5, dk=2.0, dv=0.25, what="descales")
+@pytest.mark.parametrize("d", [128, 64])
+def test_fp8_descales(d):
+    _check(1, 2, 300, 500, True, seed=4, dq=0.5, dk=2.0, dv=0.25, what=f"descales d{d}", d=d)
 
 
-def test_fp8_large_logits():
+@pytest.mark.parametrize("d", [128, 64])
+def test_fp8_large_logits(d):
     """Q, K ~ N(0, 4) before the e4m3 rounding: sharper softmax rows."""
-    _check(1, 2, 512, 2048, True, seed=8, qk_std=2.0, what="qk2")
+    _check(1, 2, 512, 2048, True, seed=8, qk_std=2.0, what=f"qk2 d{d}", d=d)
 
 
 def test_fp8_rejects_other_head_dims():
     dev = torch.device("cuda", 0)
-    x = torch.zeros(1, 1, 4, 64, device=dev).to(torch.float8_e4m3fn)
+    x = torch.zeros(1, 1, 4, 96, device=dev).to(torch.float8_e4m3fn)
     with pytest.raises(af.AttnError):
         af.attn_fwd_fp8(x, x, x)
 
 
+def _check_block(o, lse, o_ref, lse_ref, v_rows_bound, what):
+    err = np.abs(o - o_ref)
+    bound = v_rows_bound + 2.0 ** -8 * np.abs(o_ref) + 1e-6
+    assert float((err / bound).max()) <= 1.0, what
+    assert float(np.linalg.norm(o - o_ref) / np.linalg.norm(o_ref)) <= REL_L2, what
+    assert float(np.abs(lse - lse_ref).max()) <= 1e-3, what
+
+
 @pytest.mark.parametrize("name", W.FP8)
 def test_fp8_workload_sampled(name):
-    """The benchmarked e4m3 problem at full size; two whole heads and sampled
-    rows of two more against the oracle under the same bound."""
+    """The benchmarked e4m3 problems at full size: two whole heads, and 64
+    seeded query rows of each of two more heads, against the oracle under
+    the same bounds."""
     w = W.WORKLOADS[name]
     q8, k8, v8 = W.inputs(w)
     dev = torch.device("cuda", 0)
@@ -116,12 +132,17 @@ def test_fp8_workload_sampled(name):
     lse = lse.cpu().double().numpy()
     assert np.isfinite(o).all()
     qf, kf, vf = (t.float().double().numpy() for t in (q8, k8, v8))
-    for bi, hi in W.sample_heads(w, n=2):
+    pairs = W.sample_heads(w, n=4)
+    for bi, hi in pairs[:2]:
         o_ref, lse_ref = oracle.attn_fwd(qf[bi:bi + 1, hi:hi + 1], kf[bi:bi + 1, hi:hi + 1], vf[bi:bi + 1, hi:hi + 1],
                                          w.causal, w.scale)
-        oo = o[bi:bi + 1, hi:hi + 1]
-        err = np.abs(oo - o_ref)
-        bound = _row_bound(o_ref, vf[bi:bi + 1, hi:hi + 1], w.causal, w.sq, w.sk) + 2.0 ** -8 * np.abs(o_ref) + 1e-6
-        assert float((err / bound).max()) <= 1.0
-        assert float(np.linalg.norm(oo - o_ref) / np.linalg.norm(o_ref)) <= REL_L2
-        assert float(np.abs(lse[bi:bi + 1, hi:hi + 1] - lse_ref).max()) <= 1e-3
+        bound = _row_bound(o_ref, vf[bi:bi + 1, hi:hi + 1], w.causal, w.sq, w.sk)
+        _check_block(o[bi:bi + 1, hi:hi + 1], lse[bi:bi + 1, hi:hi + 1], o_ref, lse_ref, bound, f"head ({bi},{hi})")
+    rng = np.random.default_rng(w.seed)
+    rows = np.sort(rng.choice(w.sq, size=min(64, w.sq), replace=False))
+    for bi, hi in pairs[2:]:
+        o_ref, lse_ref = oracle.attn_head_rows(qf[bi, hi], kf[bi, hi], vf[bi, hi], rows, w.causal, w.scale)
+        full = np.zeros((1, 1, w.sq, w.d))
+        full[0, 0, rows] = o_ref
+        bound = _row_bound(full, vf[bi:bi + 1, hi:hi + 1], w.causal, w.sq, w.sk)[0, 0, rows]
+        _check_block(o[bi, hi][rows], lse[bi, hi][rows], o_ref, lse_ref, bound, f"rows of head ({bi},{hi})")

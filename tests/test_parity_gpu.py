@@ -163,7 +163,9 @@ def test_watchdog_reports_instead_of_hanging():
     code = binding.watchdog_selftest(q, k, v, o, lse, False, 0.1, withheld_load=1, timeout_ms=50)
     assert code != 0
     st = binding.status()
-    assert st[0] != 0 and 1 <= st[3] <= 8
+    # code 1 (a wait ran out) at one of the kernel's wait sites: loads,
+    # MMA operands, S / P / O hand-offs, the unit ring, the O staging panel
+    assert st[0] == 1 and 1 <= st[3] <= 13
     binding.status_clear()
     assert binding.status()[0] == 0
     # the GPU still computes correctly afterwards

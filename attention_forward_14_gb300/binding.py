@@ -12,6 +12,7 @@ import threading
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(HERE, "libattn_fwd.so")
+CHECKED_LIB_PATH = os.path.join(HERE, "libattn_fwd_checked.so")  # every computed index bounds-checked
 _lib = None
 _lock = threading.Lock()
 
@@ -19,11 +20,12 @@ FP16, BF16 = 0, 1
 ERRORS = {
     0: "ATTN_OK", -1: "ATTN_ERR_NULL", -2: "ATTN_ERR_SHAPE", -3: "ATTN_ERR_HEADDIM", -4: "ATTN_ERR_DTYPE",
     -5: "ATTN_ERR_SCALE", -6: "ATTN_ERR_ALIGN", -7: "ATTN_ERR_ARCH", -8: "ATTN_ERR_CUDA", -9: "ATTN_ERR_WATCHDOG",
+    -10: "ATTN_ERR_BUILD",
 }
 # Every function include/attn_fwd.h declares.
 EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_fwd_varlen", "attn_fwd_fp8", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
            "attn_fwd_splitkv_default_splits", "attn_fwd_splitkv_noalloc", "attn_last_error", "attn_fwd_status", "attn_fwd_status_clear",
-           "attn_fwd_debug_status", "attn_fwd_sched_pin_slot",
+           "attn_fwd_debug_status", "attn_fwd_sched_pin_slot", "attn_fwd_bounds_selftest",
            "attn_fwd_watchdog_selftest", "attn_version", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_varlen",
            "attn_bwd_varlen_workspace_bytes", "attn_fwd_kvcache", "attn_fwd_kvcache_paged"]
 
@@ -77,6 +79,8 @@ def _bind(lib):
     lib.attn_fwd_debug_status.argtypes = []
     lib.attn_fwd_sched_pin_slot.restype = c_int
     lib.attn_fwd_sched_pin_slot.argtypes = [c_int]
+    lib.attn_fwd_bounds_selftest.restype = c_int
+    lib.attn_fwd_bounds_selftest.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_float, c_int, vp]
     lib.attn_fwd_watchdog_selftest.restype = c_int
     lib.attn_fwd_watchdog_selftest.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_float,
                                                c_int, c_int, c_int, vp]
@@ -98,6 +102,8 @@ def _bind(lib):
 def load(path: str | None = None):
     """Load (once) and bind the C ABI.  Raises if the library is absent."""
     global _lib
+    if path is None and _lib is not None:  # the common case: no lock
+        return _lib
     with _lock:
         if _lib is not None and path is None:
             return _lib
@@ -129,6 +135,25 @@ def _stream_handle(stream, device):
     import torch
     s = stream if stream is not None else torch.cuda.current_stream(device)
     return ctypes.c_void_p(s.cuda_stream)
+
+
+class _OnDevice:
+    """Make `device` current for the call (the library works on the current
+    device); does nothing when it already is."""
+    __slots__ = ("ctx",)
+
+    def __init__(self, device):
+        import torch
+        idx = device.index if device.index is not None else torch.cuda.current_device()
+        self.ctx = None if idx == torch.cuda.current_device() else torch.cuda.device(idx)
+
+    def __enter__(self):
+        if self.ctx is not None:
+            self.ctx.__enter__()
+
+    def __exit__(self, *exc):
+        if self.ctx is not None:
+            self.ctx.__exit__(*exc)
 
 
 def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None,
@@ -164,7 +189,7 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, 
         raise AttnError(-2, "o must be a contiguous tensor shaped and typed like q")
     if lse is not None and (tuple(lse.shape) != (b, h, sq) or lse.dtype != torch.float32 or not lse.is_contiguous()):
         raise AttnError(-2, "lse must be contiguous fp32 [b, h, sq]")
-    with torch.cuda.device(q.device):
+    with _OnDevice(q.device):
         rc = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                           lse.data_ptr() if lse is not None else None,
                           b, h, sq, sk, d, int(bool(causal)), float(scale), _dtype_code(q),

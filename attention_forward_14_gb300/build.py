@@ -1,7 +1,12 @@
-"""Build libattn_fwd.so (sm_103a) in-tree with nvcc.
+"""Build libattn_fwd.so (sm_103a) in-tree with nvcc, and its checked variant.
 
 Each translation unit under csrc/ is compiled in parallel, then linked into
-``attention_forward_14_gb300/libattn_fwd.so``.  Usage:
+``attention_forward_14_gb300/libattn_fwd.so``.  The checked variant,
+``libattn_fwd_checked.so``, compiles the forward's translation units again
+with ATTN_CHECKED=1 (every computed copy coordinate, output offset, decoded
+unit and on-chip address is compared with its bounds; a violation is
+recorded in the status word and the CTA winds down) and links them with the
+same backward objects.  Usage:
 ``python -m attention_forward_14_gb300.build [--force] [-v]``.
 """
 from __future__ import annotations
@@ -18,9 +23,12 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libattn_fwd.so")
+LIB_CHECKED = os.path.join(HERE, "libattn_fwd_checked.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["attn_fwd_api.cu", "inst_d64.cu", "inst_d128_noncausal.cu", "inst_d128_causal.cu", "inst_fp8.cu",
            "attn_bwd_inst.cu", "attn_bwd_inst_varlen.cu"]
+# the translation units that hold the forward kernel (compiled again, checked)
+FWD_SOURCES = ["attn_fwd_api.cu", "inst_d64.cu", "inst_d128_noncausal.cu", "inst_d128_causal.cu", "inst_fp8.cu"]
 
 
 def nvcc() -> str:
@@ -44,9 +52,13 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, checked: bool = True) -> str:
+    """Build the library (and, with ``checked``, its checked variant) when a
+    source is newer than it; returns the library's path."""
     deps = _deps()
-    if not force and not _stale(LIB, deps):
+    want = [(LIB, False)] + ([(LIB_CHECKED, True)] if checked else [])
+    todo = [(lib, chk) for lib, chk in want if force or _stale(lib, deps)]
+    if not todo:
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
@@ -55,24 +67,31 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if verbose:
         flags += ["-Xptxas", "-v"]
 
-    def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = [cc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
+    def obj_path(src, chk):
+        return os.path.join(BUILD, os.path.splitext(src)[0] + ("_checked.o" if chk else ".o"))
+
+    def compile_one(job):
+        src, chk = job
+        obj = obj_path(src, chk)
+        cmd = [cc, *flags, *(["-DATTN_CHECKED=1"] if chk else []), "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+            raise RuntimeError(f"nvcc failed for {src}{' (checked)' if chk else ''}:\n{r.stdout}\n{r.stderr}")
         if verbose:
             sys.stderr.write(r.stdout + r.stderr)
         return obj
 
-    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    jobs = [(src, False) for src in SOURCES]  # the checked library reuses the backward objects
+    jobs += [(src, True) for src in FWD_SOURCES if any(chk for _, chk in todo)]
+    with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        list(ex.map(compile_one, jobs))
+    for lib, chk in todo:
+        objs = [obj_path(src, chk and src in FWD_SOURCES) for src in SOURCES]
+        tmp = lib + f".tmp{os.getpid()}"
+        r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, lib)
     return LIB
 
 

@@ -13,17 +13,14 @@ template <typename T, bool CAUSAL, int D, bool VARLEN>
 cudaError_t launch_bwd(const BwdLaunchArgs &a)
 {
     // The shared-memory opt-in is a per-device property of the function:
-    // set it once per device.
-    static std::atomic<unsigned long long> attr_set{0ull};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(attr_set.load() & bit)) {
+    // set it once per device (the flag belongs to the calling library).
+    cudaError_t e;
+    std::atomic<int> &ready = a.attr_ready[bwd_instance_id<T, CAUSAL, D, VARLEN>()];
+    if (ready.load(std::memory_order_acquire) == 0) {
         e = cudaFuncSetAttribute(attn_bwd_kernel<T, CAUSAL, D, VARLEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg<D>::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        attr_set.fetch_or(bit);
+        ready.store(1, std::memory_order_release);
     }
     const int64_t prep_rows = static_cast<int64_t>(a.p.bh) * a.p.sq_pad;
     int prep_blocks = static_cast<int>((prep_rows * (D / 8) + 255) / 256);

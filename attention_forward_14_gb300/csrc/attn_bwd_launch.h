@@ -2,6 +2,9 @@
 // attn_bwd_inst.cu), called by the C ABI in attn_fwd_api.cu.
 #pragma once
 
+#include <atomic>
+#include <type_traits>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -17,7 +20,20 @@ struct BwdLaunchArgs {
     int grid;       // main kernel CTAs (persistent)
     int sm_count;
     cudaStream_t stream;
+    // The calling library's flag, for the current device, of whether each
+    // instance's shared-memory opt-in is set (indexed by bwd_instance_id; see
+    // LaunchArgs::attr_ready for why it is not a static of the launcher).
+    std::atomic<int> *attr_ready;
 };
+
+constexpr int kBwdInstances = 16;  // {fp16, bf16} x {causal, not} x head dim {64, 128} x {dense, packed}
+
+template <typename T, bool CAUSAL, int D, bool VARLEN>
+constexpr int bwd_instance_id()
+{
+    return (((std::is_same<T, __nv_bfloat16>::value ? 1 : 0) * 2 + (CAUSAL ? 1 : 0)) * 2 + (D == 64 ? 0 : 1)) * 2 +
+           (VARLEN ? 1 : 0);
+}
 
 // prep -> main -> dQ convert, all on a.stream.  T: __half or __nv_bfloat16;
 // D: head dim 64 or 128; VARLEN: packed sequences (a.p.cu_q set).

@@ -68,6 +68,8 @@ struct DeviceInfo {
     int32_t *sched = nullptr;
     std::atomic<uint64_t> sched_next{0};
     std::atomic<int> sched_pinned{-1};  // testing hook: every launch on this slot
+    std::atomic<int> fwd_attr[kFwdInstances] = {};  // shared-memory opt-in set, per kernel instance
+    std::atomic<int> bwd_attr[bwd::kBwdInstances] = {};
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -115,6 +117,57 @@ int get_encode(PFN_cuTensorMapEncodeTiled_v12000 *fn)
     return ATTN_OK;
 }
 
+// cuTensorMapEncodeTiled (rank 3, no interleave, unit element strides, 256-B
+// L2 promotion, no OOB fill) through a small per-thread cache keyed by every
+// other argument.  A map is a pure function of those arguments (the address
+// and the shape), so a cached map is exactly the one the encoder would
+// produce again; calls that reuse their buffers skip the encode.
+struct MapKey {
+    const void *ptr;
+    int dt, swizzle;
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3];
+};
+struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+    bool used;
+};
+constexpr int kMapCache = 16;
+thread_local MapEntry t_maps[kMapCache];
+thread_local int t_map_next = 0;
+
+int encode_map(CUtensorMap *map, CUtensorMapDataType dt, const void *ptr, const cuuint64_t (&dims)[3],
+               const cuuint64_t (&strides)[2], const cuuint32_t (&box)[3], CUtensorMapSwizzle swizzle, const char *what)
+{
+    MapKey key;
+    memset(&key, 0, sizeof(key));  // padding too: keys are compared bytewise
+    key.ptr = ptr;
+    key.dt = static_cast<int>(dt);
+    key.swizzle = static_cast<int>(swizzle);
+    memcpy(key.dims, dims, sizeof(key.dims));
+    memcpy(key.strides, strides, sizeof(key.strides));
+    memcpy(key.box, box, sizeof(key.box));
+    for (const MapEntry &e : t_maps)
+        if (e.used && memcmp(&e.key, &key, sizeof(key)) == 0) {
+            *map = e.map;
+            return ATTN_OK;
+        }
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    const int rc = get_encode(&enc);
+    if (rc != ATTN_OK) return rc;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(map, dt, 3, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (%s) failed (CUresult %d)", what, static_cast<int>(r));
+    MapEntry &slot = t_maps[t_map_next];
+    t_map_next = (t_map_next + 1) % kMapCache;
+    slot.key = key;
+    slot.map = *map;
+    slot.used = true;
+    return ATTN_OK;
+}
+
 // 3-D view [bh, s, d] of a contiguous [b, h, s, d] tensor; box = 128 rows x
 // one 128-byte swizzle panel (64 16-bit or 128 8-bit elements), so rows past
 // s of each head are zero-filled by the copy engine rather than read from the
@@ -123,22 +176,15 @@ int get_encode(PFN_cuTensorMapEncodeTiled_v12000 *fn)
 int make_map(CUtensorMap *map, const void *ptr, int dtype, int64_t bh, int64_t s, int64_t d, int elem_bytes = 2,
              int box_rows = 128)
 {
-    PFN_cuTensorMapEncodeTiled_v12000 enc;
-    int rc = get_encode(&enc);
-    if (rc != ATTN_OK) return rc;
     const int64_t row_bytes = d * elem_bytes < 128 ? d * elem_bytes : 128;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(s), static_cast<cuuint64_t>(bh)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * elem_bytes), static_cast<cuuint64_t>(s * d * elem_bytes)};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(row_bytes / elem_bytes), static_cast<cuuint32_t>(box_rows), 1};
-    cuuint32_t estr[3] = {1, 1, 1};
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(s), static_cast<cuuint64_t>(bh)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * elem_bytes), static_cast<cuuint64_t>(s * d * elem_bytes)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(row_bytes / elem_bytes), static_cast<cuuint32_t>(box_rows), 1};
     const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                    : dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUresult r = enc(map, dt, 3, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
-    return ATTN_OK;
+    return encode_map(map, dt, ptr, dims, strides, box,
+                      row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, "dense");
 }
 
 // Packed [tokens, h, d] tensor seen as 3-D [tokens][h][d]: box = 64
@@ -147,18 +193,11 @@ int make_map(CUtensorMap *map, const void *ptr, int dtype, int64_t bh, int64_t s
 int make_map_packed(CUtensorMap *map, const void *ptr, int dtype, int64_t tokens, int64_t h, int64_t d,
                     int box_rows = 128)
 {
-    PFN_cuTensorMapEncodeTiled_v12000 enc;
-    int rc = get_encode(&enc);
-    if (rc != ATTN_OK) return rc;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h), static_cast<cuuint64_t>(tokens)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2), static_cast<cuuint64_t>(h * d * 2)};
-    cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                     const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (packed) failed (CUresult %d)", static_cast<int>(r));
-    return ATTN_OK;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h), static_cast<cuuint64_t>(tokens)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2), static_cast<cuuint64_t>(h * d * 2)};
+    const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+    return encode_map(map, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ptr,
+                      dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "packed");
 }
 
 // The backward's fp32 dQ accumulator [bh, sq, d] as 3-D [bh][sq][d] for the
@@ -167,38 +206,24 @@ int make_map_packed(CUtensorMap *map, const void *ptr, int dtype, int64_t tokens
 // 128-byte swizzle.  Rows past sq are clipped by the copy engine.
 int make_map_f32_rows(CUtensorMap *map, void *ptr, int64_t bh, int64_t s, int64_t d)
 {
-    PFN_cuTensorMapEncodeTiled_v12000 enc;
-    int rc = get_encode(&enc);
-    if (rc != ATTN_OK) return rc;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(s), static_cast<cuuint64_t>(bh)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 4), static_cast<cuuint64_t>(s * d * 4)};
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(s), static_cast<cuuint64_t>(bh)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 4), static_cast<cuuint64_t>(s * d * 4)};
     const bool wide = d == 128;
-    cuuint32_t box[3] = {wide ? 128u : 32u, wide ? static_cast<cuuint32_t>(bwd::Cfg<128>::RED_ROWS) : 128u, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     wide ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (fp32 rows) failed (CUresult %d)", static_cast<int>(r));
-    return ATTN_OK;
+    const cuuint32_t box[3] = {wide ? 128u : 32u, wide ? static_cast<cuuint32_t>(bwd::Cfg<128>::RED_ROWS) : 128u, 1};
+    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ptr, dims, strides, box,
+                      wide ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, "fp32 rows");
 }
 
 // The same for a packed [tokens, h, d] accumulator (varlen backward), as
 // 3-D [tokens][h][d] with boxes of one head.
 int make_map_f32_packed(CUtensorMap *map, void *ptr, int64_t tokens, int64_t h, int64_t d)
 {
-    PFN_cuTensorMapEncodeTiled_v12000 enc;
-    int rc = get_encode(&enc);
-    if (rc != ATTN_OK) return rc;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h), static_cast<cuuint64_t>(tokens)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 4), static_cast<cuuint64_t>(h * d * 4)};
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h), static_cast<cuuint64_t>(tokens)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 4), static_cast<cuuint64_t>(h * d * 4)};
     const bool wide = d == 128;
-    cuuint32_t box[3] = {wide ? 128u : 32u, 1, wide ? static_cast<cuuint32_t>(bwd::Cfg<128>::RED_ROWS) : 128u};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     wide ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (fp32 packed) failed (CUresult %d)", static_cast<int>(r));
-    return ATTN_OK;
+    const cuuint32_t box[3] = {wide ? 128u : 32u, 1, wide ? static_cast<cuuint32_t>(bwd::Cfg<128>::RED_ROWS) : 128u};
+    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ptr, dims, strides, box,
+                      wide ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, "fp32 packed");
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -291,7 +316,7 @@ int64_t splitkv_bytes(int64_t bh, int64_t sq, int64_t d, int64_t splits)
 
 int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_t b, int64_t h, int64_t sq, int64_t sk,
         int64_t d, int causal, float scale, int dtype, cudaStream_t stream, int withheld_load, uint64_t timeout_ns,
-        const SplitArgs &split = SplitArgs(), const CacheArgs &cache = CacheArgs())
+        const SplitArgs &split = SplitArgs(), const CacheArgs &cache = CacheArgs(), int extra_units = 0)
 {
     bool nothing = false;
     int rc = validate(q, k, v, o, lse, b, h, sq, sk, d, scale, dtype, &nothing);
@@ -341,7 +366,7 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_
     p.sched = cache.seqlens != nullptr ? sched_slot(di, &p.sched_gen) : nullptr;
     const int64_t units = bh * p.num_mblk * split.num_splits;
     if (units > INT32_MAX) return fail(ATTN_ERR_SHAPE, "too many work units (%lld)", (long long)units);
-    p.num_units = static_cast<int32_t>(units);
+    p.num_units = static_cast<int32_t>(units + extra_units);  // extra units: the bounds self-test only
     p.sl2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     p.o_scale = 1.f;
     p.timeout_ns = timeout_ns;
@@ -349,8 +374,9 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int64_
 #ifdef ATTN_TRACE_ENABLE
     p.trace = g_trace_buf;
 #endif
-    a.grid = static_cast<int>(units < di->sm_count ? units : di->sm_count);
+    a.grid = static_cast<int>(p.num_units < di->sm_count ? p.num_units : di->sm_count);
     a.stream = stream;
+    a.attr_ready = di->fwd_attr;
     const bool c = causal != 0;
     if (d == 64)
         e = (dtype == ATTN_BF16) ? dispatch_causal<64, __nv_bfloat16>(a, c) : dispatch_causal<64, __half>(a, c);
@@ -541,6 +567,7 @@ int run_bwd(const void *q, const void *k, const void *v, const void *o, const vo
     a.grid = p.num_units < di->sm_count ? p.num_units : di->sm_count;
     a.sm_count = di->sm_count;
     a.stream = stream;
+    a.attr_ready = di->bwd_attr;
     e = launch_bwd_any<false>(a, d, dtype, causal);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "backward launch");
 }
@@ -636,6 +663,7 @@ int run_bwd_varlen(const void *q, const void *k, const void *v, const void *o, c
     a.grid = p.num_units < di->sm_count ? p.num_units : di->sm_count;
     a.sm_count = di->sm_count;
     a.stream = stream;
+    a.attr_ready = di->bwd_attr;
     e = launch_bwd_any<true>(a, d, dtype, causal);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "backward launch");
 }
@@ -1034,6 +1062,7 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float 
 #endif
     a.grid = static_cast<int>(units < di->sm_count ? units : di->sm_count);
     a.stream = st;
+    a.attr_ready = di->fwd_attr;
     const bool c = causal != 0;
     if (d == 64)
         e = (dtype == ATTN_BF16) ? dispatch_causal<64, __nv_bfloat16>(a, c) : dispatch_causal<64, __half>(a, c);
@@ -1101,6 +1130,7 @@ int attn_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *ls
 #endif
     a.grid = static_cast<int>(units < di->sm_count ? units : di->sm_count);
     a.stream = st;
+    a.attr_ready = di->fwd_attr;
     if (d == 64)
         e = causal ? launch_fwd<64, __nv_fp8_e4m3, true>(a) : launch_fwd<64, __nv_fp8_e4m3, false>(a);
     else
@@ -1168,6 +1198,28 @@ int attn_fwd_watchdog_selftest(const void *q, const void *k, const void *v, void
              static_cast<uint64_t>(timeout_ms) * 1000000ull);
     if (rc != ATTN_OK) return rc;
     return attn_fwd_status(nullptr);
+}
+
+int attn_fwd_bounds_selftest(const void *q, const void *k, const void *v, void *o, float *lse, int64_t b, int64_t h,
+                             int64_t sq, int64_t sk, int64_t d, float scale, int dtype, void *stream)
+{
+    g_err.clear();
+#if ATTN_CHECKED
+    if (b < 0 || h < 0 || sq < 1 || sk < 1 || b * h * sq > 4096 || sk > 1024)
+        return fail(ATTN_ERR_SHAPE, "self-test wants a tiny problem with rows and keys");
+    int rc = attn_fwd_status_clear();
+    if (rc != ATTN_OK) return rc;
+    // one unit past the end of a dense, unsplit problem: the decoded head
+    // plane is out of range, which the checks catch before any access
+    rc = run(q, k, v, o, lse, b, h, sq, sk, d, 0, scale, dtype, static_cast<cudaStream_t>(stream), -1,
+             kDefaultTimeoutNs, SplitArgs(), CacheArgs(), 1);
+    if (rc != ATTN_OK) return rc;
+    return attn_fwd_status(nullptr);
+#else
+    (void)q, (void)k, (void)v, (void)o, (void)lse, (void)b, (void)h, (void)sq, (void)sk, (void)d, (void)scale;
+    (void)dtype, (void)stream;
+    return fail(ATTN_ERR_BUILD, "attn_fwd_bounds_selftest needs the checked build (libattn_fwd_checked.so)");
+#endif
 }
 
 int attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse, void *dq,

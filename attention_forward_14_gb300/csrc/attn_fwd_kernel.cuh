@@ -55,6 +55,13 @@
 
 namespace attn {
 
+// Checked build: with ATTN_CHECKED=1 every computed load/store coordinate,
+// global output offset, decoded unit, tensor-memory base and shared-memory
+// window is compared with its bounds (see in_bounds).  Off by default.
+#ifndef ATTN_CHECKED
+#define ATTN_CHECKED 0
+#endif
+
 // Build options of the producer (see the producer warp).
 #ifndef ATTN_KV_PREFETCH
 #define ATTN_KV_PREFETCH 0
@@ -152,6 +159,7 @@ enum : uint32_t {
     EV_LD_WAIT = 40, EV_LD_GOT,
     EV_K_ENTRY = 60, EV_K_READY, EV_K_EXIT,
     EV_SM_EPI_WRITTEN = 81,
+    EV_REGS = 90, EV_UNIT, EV_DECODED, EV_Q_ISSUED,
 };
 
 // Watchdog sites (recorded in status[3]).
@@ -174,6 +182,19 @@ enum : uint32_t {
 enum : uint32_t {
     STATUS_TIMEOUT = 1,
     STATUS_SCHED_COLLISION = 2,
+    STATUS_BOUNDS = 3,  // checked builds: a computed index outside its bounds
+};
+
+// Bounds-check sites of the checked build (recorded in status[3]).
+enum : uint32_t {
+    SITE_CHK_SMEM = 20,     // dynamic shared memory window too small for the layout
+    SITE_CHK_TMEM = 21,     // tensor-memory allocation not the expected 512 columns at lane 0
+    SITE_CHK_UNIT = 22,     // decoded unit outside the problem
+    SITE_CHK_Q_LOAD = 23,   // Q copy coordinates
+    SITE_CHK_KV_LOAD = 24,  // K/V copy coordinates (page lookup included)
+    SITE_CHK_O_TILE = 25,   // O copy-engine store coordinates
+    SITE_CHK_O_ROW = 26,    // O / LSE row written by a thread
+    SITE_CHK_O_PART = 27,   // split partial row
 };
 
 // Input element types: fp16, bf16 (16-bit, kind::f16 MMAs, P two per
@@ -359,6 +380,32 @@ __device__ __forceinline__ size_t lse_index(const FwdParams &p, const Unit &un, 
     return static_cast<size_t>(un.bh) * p.sq + row;
 }
 
+// Rows of O (and entries of LSE) in either layout.
+__device__ __forceinline__ size_t o_rows_total(const FwdParams &p)
+{
+    return p.cu_q != nullptr ? static_cast<size_t>(p.total_q) * p.heads : static_cast<size_t>(p.bh) * p.sq;
+}
+
+// A decoded unit lies inside the problem: its head plane (head, when
+// packed), its rows and its key tiles lie within the tensors the maps and
+// the output pointers describe.
+__device__ __forceinline__ bool unit_in_bounds(int u, const Unit &un, const FwdParams &p, int unit_rows, int bn)
+{
+    if (u < 0 || u >= p.num_units || un.row0 < 0 || un.jb < 0 || un.n < 0 || un.split < 0 || un.split >= p.num_splits)
+        return false;
+    if (un.row0 >= p.num_mblk * unit_rows) return false;
+    // (an empty split range may start past the last key tile: it reads nothing)
+    const long long key_cap = (static_cast<long long>(p.sk) + bn - 1) / bn * bn;
+    if (un.n > 0 && static_cast<long long>(un.jb + un.n) * bn > key_cap) return false;
+    if (p.cu_q != nullptr) {
+        if (un.bh >= p.heads || un.q_tok0 < 0 || un.k_tok0 < 0 || un.q_tok0 + un.sq > p.total_q ||
+            un.k_tok0 + un.sk > p.total_k || un.sq > p.sq || un.sk > p.sk)
+            return false;
+        return un.n == 0 || (un.jb + un.n - 1) * bn < un.sk;
+    }
+    return un.bh < p.bh && un.sq == p.sq && un.sk >= 0 && un.sk <= p.sk;
+}
+
 // Zero rows [valid, BN) of the V tile at shared address `tile`, in every
 // panel (a row is 128 contiguous bytes of a panel whatever the swizzle).
 // Those are keys past the end of the unit's sequence that the tile copy
@@ -404,6 +451,24 @@ __device__ __forceinline__ void record_status(uint32_t *status, uint32_t code, u
         __threadfence();
     }
 }
+
+// Checked builds: `ok` false records STATUS_BOUNDS at `site` and raises the
+// CTA's abort flag, so that the other warps wind down as after a wait that
+// ran out; the caller skips the access.  Normal builds: always true (the
+// condition is not evaluated).
+#if ATTN_CHECKED
+#define ATTN_IN_BOUNDS(cond, site) in_bounds((cond), ctl, p, (site))
+__device__ __forceinline__ bool in_bounds(bool ok, Ctl *ctl, const FwdParams &p, uint32_t site)
+{
+    if (!ok) {
+        *reinterpret_cast<volatile uint32_t *>(&ctl->abort) = 1u;
+        record_status(p.status, STATUS_BOUNDS, site);
+    }
+    return ok;
+}
+#else
+#define ATTN_IN_BOUNDS(cond, site) true
+#endif
 
 static __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl *ctl, const FwdParams &p,
                                               uint32_t site)
@@ -766,11 +831,24 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     ATTN_TRACE(EV_K_READY, 0);
+#if ATTN_CHECKED
+    {
+        uint32_t dsmem;
+        asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dsmem));
+        const bool window = (base_addr - raw_addr) + C::SMEM_BYTES - 1024u <= dsmem;
+        const bool tcols = (tmem >> 16) == 0u && (tmem & 0xFFFFu) + C::TMEM_COLS <= 512u;
+        const bool setup_ok = (threadIdx.x != 0) || (ATTN_IN_BOUNDS(window, SITE_CHK_SMEM) &&
+                                                     ATTN_IN_BOUNDS(tcols, SITE_CHK_TMEM));
+        // every thread takes the same decision: no role starts on a bad layout
+        if (!__syncthreads_and(setup_ok ? 1 : 0)) goto wind_down;
+    }
+#endif
 
     if (warp >= 8) {
       // Warpgroup 2: the setmaxnreg and all of this warpgroup's work sit in
       // one warpgroup-uniform branch, so the compiler knows the budget.
       regs_dec<C::REGS_OTHER>();
+      ATTN_TRACE(EV_REGS, 0);
       if (warp == 9) {
         // ------------------------------------------------------------ producer
         // The whole warp walks the schedule, so counters and addresses are
@@ -787,7 +865,17 @@ __global__ void __launch_bounds__(384, 1)
             if (!(ok = producer_unit(i, u, ctl, p))) break;
             if (u == -1) break;
             if (u < 0) continue;
+            ATTN_TRACE(EV_UNIT, u);
+            if (!ATTN_IN_BOUNDS(u < p.num_units, SITE_CHK_UNIT)) {  // before decode reads any offset
+                ok = false;
+                break;
+            }
             const Unit un = decode_unit<D, CAUSAL>(u, p);
+            ATTN_TRACE(EV_DECODED, u);
+            if (!ATTN_IN_BOUNDS(unit_in_bounds(u, un, p, C::UNIT_ROWS, C::BN), SITE_CHK_UNIT)) {
+                ok = false;
+                break;
+            }
             if (un.n == 0) continue;
             // TMA coordinates (after the 64-column panel): dense maps are
             // [bh][s][D] (row, plane = bh); varlen maps are [token][head][D]
@@ -810,6 +898,17 @@ __global__ void __launch_bounds__(384, 1)
             for (int t = 0; t < C::QT && ok; ++t) {
                 ok = warp_wait(B(ctl->q_empty[t]), (q_it & 1u) ^ 1u, ctl, p, SITE_LOAD_Q_EMPTY);
                 if (!ok) break;
+                {
+                    // the tile starts inside the unit's padded rows (a tile
+                    // wholly past the end reads zeros, as the copy engine fills)
+                    const int qr = un.row0 + t * C::BM;
+                    if (!ATTN_IN_BOUNDS(qr < p.num_mblk * C::UNIT_ROWS && (vl ? un.q_tok0 + qr < p.total_q + C::UNIT_ROWS
+                                                                             : un.bh < p.bh),
+                                        SITE_CHK_Q_LOAD)) {
+                        ok = false;
+                        break;
+                    }
+                }
                 if (elect_one()) {
                     mbar_arrive_expect_tx(B(ctl->q_full[t]), C::TILE_BYTES);
                     for (int pn = 0; pn < C::NPANEL; ++pn)
@@ -821,6 +920,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             if (!ok) break;
             ++q_it;
+            ATTN_TRACE(EV_Q_ISSUED, u);
             if (ATTN_KV_PREFETCH > 0 && elect_one()) {
                 for (int jj = 0; jj < ATTN_KV_PREFETCH && jj < un.n; ++jj)
                     for (int pn = 0; pn < C::NPANEL; ++pn) {
@@ -848,6 +948,25 @@ __global__ void __launch_bounds__(384, 1)
                                    SITE_LOAD_KV_EMPTY);
                     ATTN_TRACE(EV_LD_GOT, kv_it);
                     if (!ok) break;
+#if ATTN_CHECKED
+                    {
+                        // the tile starts at a visible key of a plane (token, page) of the map
+                        const int kr = (un.jb + j) * C::BN;
+                        const int kp = kplane_coord(kr), kh = krow_coord(kr);
+                        bool in = kr < (p.sk + C::BN - 1) / C::BN * C::BN && kr >= 0;
+                        if (vl)
+                            in = in && kp >= 0 && kp < p.total_k && kh < p.heads;
+                        else if (paged)
+                            in = in && kp >= 0 && static_cast<long long>(kp) <= static_cast<long long>(p.num_pages) * p.page_size &&
+                                 kh < p.heads;
+                        else
+                            in = in && kp < p.bh;
+                        if (!ATTN_IN_BOUNDS(in, SITE_CHK_KV_LOAD)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+#endif
                     if (static_cast<int32_t>(kv_it) != p.withheld_load && elect_one()) {
                         mbar_arrive_expect_tx(B(ctl->kv_full[slot]), C::TILE_BYTES);
                         const CUtensorMap *m = which ? &tmV : &tmK;
@@ -939,7 +1058,17 @@ __global__ void __launch_bounds__(384, 1)
             if (!(ok = consumer_unit(i, u, ctl, p))) break;
             if (u == -1) break;
             if (u < 0) continue;
+            ATTN_TRACE(EV_UNIT, u);
+            if (!ATTN_IN_BOUNDS(u < p.num_units, SITE_CHK_UNIT)) {  // before decode reads any offset
+                ok = false;
+                break;
+            }
             const Unit un = decode_unit<D, CAUSAL>(u, p);
+            ATTN_TRACE(EV_DECODED, u);
+            if (!ATTN_IN_BOUNDS(unit_in_bounds(u, un, p, C::UNIT_ROWS, C::BN), SITE_CHK_UNIT)) {
+                ok = false;
+                break;
+            }
             if (un.n == 0) continue;
             ATTN_TRACE(EV_MMA_WAIT_Q, u);
             for (int t = 0; t < C::QT && ok; ++t)
@@ -1030,6 +1159,7 @@ __global__ void __launch_bounds__(384, 1)
       }
     } else {
         regs_inc<C::REGS_SOFTMAX>();
+        ATTN_TRACE(EV_REGS, 0);
         // ------------------------------------------------------------ softmax groups
         const int t = warp >> 2;      // Q tile of this group
         const int quad = warp & 3;    // TMEM lane quadrant this warp may access
@@ -1047,10 +1177,23 @@ __global__ void __launch_bounds__(384, 1)
             if (!(ok = consumer_unit(i, u, ctl, p))) break;
             if (u == -1) break;
             if (u < 0) continue;
+            ATTN_TRACE(EV_UNIT, u);
+            if (!ATTN_IN_BOUNDS(u < p.num_units, SITE_CHK_UNIT)) {  // before decode reads any offset
+                ok = false;
+                break;
+            }
             const Unit un = decode_unit<D, CAUSAL>(u, p);
+            ATTN_TRACE(EV_DECODED, u);
+            if (!ATTN_IN_BOUNDS(unit_in_bounds(u, un, p, C::UNIT_ROWS, C::BN), SITE_CHK_UNIT)) {
+                ok = false;
+                break;
+            }
             const int row = un.row0 + t * C::BM + r_in_tile;
             if (un.n == 0) {
-                store_row_zero<T>(p, un, row, D);
+                const bool in = row >= un.sq || (p.num_splits > 1 ? un.split < p.num_splits
+                                                                  : o_row_offset(p, un, row, D) / D < o_rows_total(p));
+                if (__all_sync(0xffffffffu, ATTN_IN_BOUNDS(in, SITE_CHK_O_ROW)))
+                    store_row_zero<T>(p, un, row, D);
                 continue;
             }
             if (t == 1 && un.row0 + C::BM >= un.sq) continue;  // no row here: the tile is not computed
@@ -1131,6 +1274,11 @@ __global__ void __launch_bounds__(384, 1)
                 if (p.num_splits > 1) {
                     // split partial: O / lr in fp32, both log-sum-exps
                     const size_t r = (static_cast<size_t>(un.split) * p.bh + un.bh) * p.sq + (valid ? row : 0);
+                    if (!__all_sync(0xffffffffu, ATTN_IN_BOUNDS(r < static_cast<size_t>(p.num_splits) * p.bh * p.sq,
+                                                                 SITE_CHK_O_PART))) {
+                        ok = false;
+                        break;
+                    }
                     float4 *dstf = reinterpret_cast<float4 *>(p.o_part + r * D);
 #pragma unroll
                     for (int ch = 0; ch < D / 32; ++ch) {
@@ -1172,37 +1320,44 @@ __global__ void __launch_bounds__(384, 1)
                         __syncwarp();
                         // this row's 64 columns, 16-bit, in the 128-byte swizzle
                         // of the output map: 16-byte chunk c at c ^ (row % 8)
+                        uint32_t orr[64];
+                        tmem_ld64_wait(tO + pn * 64, orr);
 #pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            uint32_t orr[32];
-                            tmem_ld32_wait(tO + pn * 64 + half * 32, orr);
-                            uint32_t pk[16];
+                        for (int chunk = 0; chunk < 8; ++chunk) {
+                            uint32_t pk[4];
 #pragma unroll
-                            for (int c = 0; c < 16; ++c) {
+                            for (int c = 0; c < 4; ++c) {
+                                const int col = chunk * 8 + 2 * c;
                                 const float2 v = __fmul2_rn(
-                                    make_float2(__uint_as_float(orr[2 * c]), __uint_as_float(orr[2 * c + 1])),
+                                    make_float2(__uint_as_float(orr[col]), __uint_as_float(orr[col + 1])),
                                     make_float2(inv_l, inv_l));
                                 pk[c] = pack2<TO>(v.x, v.y);
                             }
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const uint32_t chunk = static_cast<uint32_t>(half * 4 + k);
-                                st_shared_v4(my_row + ((chunk ^ swz) << 4), pk[4 * k], pk[4 * k + 1], pk[4 * k + 2],
-                                             pk[4 * k + 3]);
-                            }
+                            st_shared_v4(my_row + ((static_cast<uint32_t>(chunk) ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
                             const int r0 = tile_row0 + quad * 32;
                             const bool vl = p.cu_q != nullptr;
-                            tma_store_3d(&tmO, slice, pn * C::O_PANEL_COLS, vl ? un.bh : r0, vl ? un.q_tok0 + r0 : un.bh);
-                            bulk_commit_group();
+                            if (ATTN_IN_BOUNDS(r0 >= 0 && r0 < un.sq && (vl ? un.q_tok0 + r0 + 32 <= p.total_q && un.bh < p.heads
+                                                                          : un.bh < p.bh),
+                                               SITE_CHK_O_TILE)) {
+                                tma_store_3d(&tmO, slice, pn * C::O_PANEL_COLS, vl ? un.bh : r0,
+                                             vl ? un.q_tok0 + r0 : un.bh);
+                                bulk_commit_group();
+                            }
                         }
                         ATTN_TRACE(EV_SM_EPI_WRITTEN, pn);
                         ++epi_n;
                     }
                 } else {
+                    if (!__all_sync(0xffffffffu,
+                                    ATTN_IN_BOUNDS(!valid || o_row_offset(p, un, row, D) / D < o_rows_total(p),
+                                                   SITE_CHK_O_ROW))) {
+                        ok = false;
+                        break;
+                    }
                     uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<TO *>(p.o) +
                                                            o_row_offset(p, un, valid ? row : 0, D));
 #pragma unroll
@@ -1224,7 +1379,7 @@ __global__ void __launch_bounds__(384, 1)
                         }
                     }
                 }
-                if (valid && p.lse)
+                if (valid && p.lse && ATTN_IN_BOUNDS(lse_index(p, un, row) < o_rows_total(p), SITE_CHK_O_ROW))
                     p.lse[lse_index(p, un, row)] =
                         (l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
                 ATTN_TRACE(EV_SM_EPI_DONE, u);
@@ -1236,6 +1391,9 @@ __global__ void __launch_bounds__(384, 1)
         __syncwarp();
     }
 
+#if ATTN_CHECKED
+wind_down:
+#endif
     ATTN_TRACE(EV_K_EXIT, 0);
     tc_fence_before();
     __syncthreads();

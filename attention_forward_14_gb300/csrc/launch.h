@@ -17,7 +17,22 @@ struct LaunchArgs {
     FwdParams p;
     int grid;
     cudaStream_t stream;
+    // The calling library's flags, for the current device, of whether each
+    // instance's dynamic shared-memory opt-in is set (indexed by
+    // fwd_instance_id).  They belong to the library that launches: a
+    // function-local static here would be one object for the whole process
+    // (a unique symbol), shared with any other library built from these
+    // sources (the checked build), whose kernels are other functions.
+    std::atomic<int> *attr_ready;
 };
+
+constexpr int kFwdInstances = 12;  // head dim {64, 128} x {fp16, bf16, e4m3} x {causal, not}
+
+template <int D, typename T, bool CAUSAL>
+constexpr int fwd_instance_id()
+{
+    return ((D == 64 ? 0 : 1) * 3 + (Elem<T>::FP8 ? 2 : (Elem<T>::BF16 ? 1 : 0))) * 2 + (CAUSAL ? 1 : 0);
+}
 
 // The dynamic shared-memory opt-in is a per-device attribute of each
 // instance: set it the first time an instance runs on a device.
@@ -25,16 +40,12 @@ template <int D, typename T, bool CAUSAL>
 cudaError_t launch_fwd(const LaunchArgs &a)
 {
     constexpr int smem = Cfg<D, Elem<T>::BYTES>::SMEM_BYTES;
-    constexpr int kMaxDev = 64;
-    static std::atomic<int> ready[kMaxDev];
     auto kern = attn_fwd_kernel<D, T, CAUSAL>;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDev || ready[dev].load(std::memory_order_acquire) == 0) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    std::atomic<int> &ready = a.attr_ready[fwd_instance_id<D, T, CAUSAL>()];
+    if (ready.load(std::memory_order_acquire) == 0) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < kMaxDev) ready[dev].store(1, std::memory_order_release);
+        ready.store(1, std::memory_order_release);
     }
     kern<<<a.grid, Cfg<D, Elem<T>::BYTES>::THREADS, smem, a.stream>>>(a.q, a.k, a.v, a.o, a.p);
     return cudaGetLastError();

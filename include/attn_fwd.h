@@ -69,7 +69,8 @@ enum {
     ATTN_ERR_ALIGN = -6,   /* q/k/v/o not 16-byte aligned, lse not 4-byte     */
     ATTN_ERR_ARCH = -7,    /* current device is not compute capability 10.3   */
     ATTN_ERR_CUDA = -8,    /* a CUDA runtime/driver call failed                */
-    ATTN_ERR_WATCHDOG = -9 /* a device-side wait gave up (see attn_fwd_status) */
+    ATTN_ERR_WATCHDOG = -9, /* a device-side wait gave up (see attn_fwd_status) */
+    ATTN_ERR_BUILD = -10    /* the entry point needs the checked build          */
 };
 
 /*
@@ -408,7 +409,9 @@ const char *attn_last_error(void);
  * returns instead of hanging.  The first failure is kept until cleared:
  *   code ATTN_STATUS_TIMEOUT (1)         a wait ran out;
  *   code ATTN_STATUS_SCHED_COLLISION (2) a launch found its schedule slot
- *                                        held by another (attn_fwd_varlen).
+ *                                        held by another (attn_fwd_varlen);
+ *   code ATTN_STATUS_BOUNDS (3)          checked build only: a computed index
+ *                                        was outside its bounds (see below).
  * attn_fwd_status synchronises the current device, copies the status into
  * out[0..3] = {code, block, warp, site} (out may be NULL) and returns code
  * (0 = nothing recorded, <0 = CUDA error while reading).
@@ -419,6 +422,7 @@ const char *attn_last_error(void);
  */
 #define ATTN_STATUS_TIMEOUT 1
 #define ATTN_STATUS_SCHED_COLLISION 2
+#define ATTN_STATUS_BOUNDS 3
 int attn_fwd_status(uint32_t *out);
 int attn_fwd_status_clear(void);
 int attn_fwd_debug_status(void);
@@ -445,6 +449,28 @@ int attn_fwd_watchdog_selftest(const void *q, const void *k, const void *v,
                                int64_t sq, int64_t sk, int64_t d, int causal,
                                float scale, int dtype, int withheld_load,
                                int timeout_ms, void *stream);
+
+/*
+ * Checked build.  libattn_fwd_checked.so exports this same interface from
+ * the same sources compiled with every computed index of the forward kernel
+ * checked: copy coordinates of Q, K, V (page lookups included) and of the O
+ * stores, thread-written O, LSE and split-partial offsets, the decoded work
+ * units, the tensor-memory allocation and the shared-memory window.  An index
+ * outside its bounds is not used: the kernel records {ATTN_STATUS_BOUNDS,
+ * block, warp, site} in the status word and the CTA winds down as after a
+ * wait that ran out.  It stands in for a memory checker, which is not
+ * available on every machine, and is slower than the normal build.
+ *
+ * attn_fwd_bounds_selftest runs attn_fwd on tiny caller buffers (contract of
+ * attn_fwd, no mask, b*h*sq <= 4096, 1 <= sk <= 1024) with one work unit past
+ * the end of the problem, whose head plane is out of range, synchronises and
+ * returns the recorded status code (expected ATTN_STATUS_BOUNDS).  The
+ * normal build returns ATTN_ERR_BUILD.
+ */
+int attn_fwd_bounds_selftest(const void *q, const void *k, const void *v,
+                             void *o, float *lse, int64_t b, int64_t h,
+                             int64_t sq, int64_t sk, int64_t d, float scale,
+                             int dtype, void *stream);
 
 /* Library version string. */
 const char *attn_version(void);

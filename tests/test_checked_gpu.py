@@ -1,0 +1,107 @@
+"""The checked build (libattn_fwd_checked.so: the same sources with every
+computed index of the forward compared with its bounds -- copy coordinates,
+page lookups, thread-written O / LSE / split-partial offsets, decoded units,
+the tensor-memory allocation and the shared-memory window) runs the
+small-shape parity suite, the split-KV, packed, KV-cache, paged and e4m3
+cases, each against the fp64 oracle as in their own test files, with the
+status word read after every case: no check may fire on valid inputs.  Its
+self-test puts one unit past the end of a problem and checks that the
+bounds violation is reported instead of used.  Nothing here faults: an index
+that fails its check is not used."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from attention_forward_14_gb300 import binding
+from attention_forward_14_gb300 import workloads as W
+
+import test_fp8_gpu as F8
+import test_kvcache_gpu as KV
+import test_parity_gpu as P
+import test_splitkv_gpu as SK
+import test_varlen_gpu as VL
+
+pytestmark = pytest.mark.gpu
+
+BOUNDS, SITE_CHK_UNIT = 3, 22
+
+
+@pytest.fixture(scope="module", autouse=True)
+def checked_library():
+    """Route the binding through the checked build for this module."""
+    from attention_forward_14_gb300.build import build
+    build()
+    saved = binding.load()
+    checked = binding.load(binding.CHECKED_LIB_PATH)
+    binding._lib = checked
+    binding.status_clear()
+    try:
+        yield checked
+    finally:
+        binding._lib = saved
+
+
+def _clean(what):
+    code = binding.status()
+    assert code[0] == 0, f"{what}: status {code}"
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", P.SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_checked_small_shapes(shape, causal, dtype, d):
+    P.test_small_shapes(shape, causal, dtype, d)
+    _clean(f"small {shape} c{causal} {dtype} d{d}")
+
+
+@pytest.mark.parametrize("case", SK.CASES, ids=lambda c: "_".join(map(str, c)))
+def test_checked_splitkv(case):
+    SK.test_splitkv_matches_oracle(case)
+    _clean(f"splitkv {case}")
+
+
+@pytest.mark.parametrize("case", VL.CASES, ids=lambda c: f"{len(c[0])}seq_h{c[2]}_d{c[3]}_{c[4]}_c{int(c[5])}")
+def test_checked_varlen(case):
+    VL.test_varlen_matches_oracle(case)
+    _clean(f"varlen {case}")
+
+
+@pytest.mark.parametrize("case", KV.CASES, ids=lambda c: "_".join(map(str, c[:9])))
+def test_checked_kvcache(case):
+    KV.test_kvcache_matches_oracle(case)
+    _clean(f"kvcache {case}")
+
+
+@pytest.mark.parametrize("case", KV.PAGED_CASES, ids=lambda c: "_".join(map(str, c[:10])))
+def test_checked_kvcache_paged(case):
+    KV.test_kvcache_paged_matches_oracle(case)
+    _clean(f"paged {case}")
+
+
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("causal", [False, True])
+def test_checked_fp8(causal, d):
+    F8._check(2, 3, 300, 300, causal, seed=17 + d, what=f"checked e4m3 c{causal} d{d}", d=d)
+    _clean(f"e4m3 c{causal} d{d}")
+
+
+def test_checked_bounds_selftest_reports_instead_of_using():
+    """One unit past the end of a 1-head problem: its head plane is out of
+    range; every warp role finds that before touching memory, the status says
+    where, and the next call on the same context is correct and clean."""
+    dev = torch.device("cuda", 0)
+    q, k, v = (t.to(dev) for t in W.draw(1, 1, 256, 256, 64, "bf16", seed=5))
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 1, 256, device=dev)
+    lib = binding.load()
+    rc = lib.attn_fwd_bounds_selftest(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), 1, 1, 256,
+                                      256, 64, 0.125, 1, None)
+    assert rc == BOUNDS, (rc, lib.attn_last_error())
+    st = binding.status()
+    assert st[0] == BOUNDS and st[3] == SITE_CHK_UNIT
+    binding.status_clear()
+    P.check_full(*W.draw(1, 2, 300, 300, 64, "bf16", seed=6), False, 0.125, "after the bounds self-test")
+    _clean("after the bounds self-test")

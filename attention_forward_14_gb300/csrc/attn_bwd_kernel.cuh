@@ -117,7 +117,7 @@ enum : uint32_t {
     BEV_MMA_WAIT_P = 1, BEV_MMA_GOT_P, BEV_MMA_WAIT_DS, BEV_MMA_GOT_DS, BEV_MMA_WAIT_DQE, BEV_MMA_GOT_DQE,
     BEV_MMA_WAIT_Q, BEV_MMA_GOT_Q, BEV_MMA_ISSUED_DV, BEV_MMA_ISSUED_S, BEV_MMA_ISSUED_DKDQ, BEV_MMA_ISSUED_DP,
     BEV_SM_WAIT_S = 20, BEV_SM_GOT_S, BEV_SM_P_DONE, BEV_SM_WAIT_DP, BEV_SM_GOT_DP, BEV_SM_DS_DONE,
-    BEV_DR_WAIT = 40, BEV_DR_GOT, BEV_DR_RELEASED, BEV_DR_DONE,
+    BEV_DR_WAIT = 40, BEV_DR_GOT, BEV_DR_RELEASED, BEV_DR_DONE, BEV_DR_DKV_WAIT, BEV_DR_DKV_GOT, BEV_DR_DKV_DONE,
     BEV_LD_WAIT = 60, BEV_LD_GOT,
 };
 
@@ -982,7 +982,9 @@ __global__ void __launch_bounds__(512, 1)
             }
             if (!ok) break;
             // dK, dV of the unit: this thread's key row, D columns each
+            BWD_TRACE(BEV_DR_DKV_WAIT, un_it);
             if (!(ok = warp_wait(B(ctl->dkv_full), un_it & 1u, ctl, p, SITE_BWD_DRAIN_DKV_FULL))) break;
+            BWD_TRACE(BEV_DR_DKV_GOT, un_it);
             ++un_it;
             tc_fence_after();
             const int key = un.kb * C::BN + quad * 32 + lane;
@@ -1009,6 +1011,7 @@ __global__ void __launch_bounds__(512, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(B(ctl->dkv_empty));
+            BWD_TRACE(BEV_DR_DKV_DONE, un_it);
         }
     } else {
         regs_inc<C::REGS_SOFTMAX>();

@@ -635,6 +635,18 @@ __device__ __forceinline__ void rescale_rows(uint32_t tO, float alpha)
     }
 }
 
+// This warp's tensor-memory stores are complete: every lane waits for its
+// own and orders them before the warp barrier, and one lane arrives on
+// `bar` for the warp (the P hand-off barriers count warps, not threads: 32
+// arrivals on one shared-memory word per warp cost more than the barrier).
+__device__ __forceinline__ void warp_announce_tmem(uint32_t bar)
+{
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // p = 2^(s*sl2e - m_use) for the 128 columns of this row; P (rounded to T,
 // two per 32-bit column) is stored into the first 64 tensor-memory columns
 // at tS.  The first half (keys 0..63) is stored and announced on `half_bar`
@@ -675,9 +687,7 @@ __device__ __forceinline__ float2 exp_store_tile(const uint32_t (&sr)[128], int 
                 pb[c - 32] = pk;
             if (c == 31) {
                 tmem_st32(tS, pa);
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(half_bar);
+                warp_announce_tmem(half_bar);
             }
         }
         tmem_st32(tS + 32, pb);
@@ -707,9 +717,7 @@ __device__ __forceinline__ float2 exp_store_tile(const uint32_t (&sr)[128], int 
                 pb[c - 16] = pk;
             if (c == 15) {
                 tmem_st16(tS, pa);
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(half_bar);
+                warp_announce_tmem(half_bar);
             }
         }
         tmem_st16(tS + 16, pb);
@@ -782,8 +790,8 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(B(ctl->q_full[t]), 1);
             mbar_init(B(ctl->q_empty[t]), 1);
             mbar_init(B(ctl->s_full[t]), 1);
-            mbar_init(B(ctl->p_half[t]), 128);
-            mbar_init(B(ctl->p_full[t]), 128);
+            mbar_init(B(ctl->p_half[t]), 4);  // one arrival per softmax warp
+            mbar_init(B(ctl->p_full[t]), 4);
             mbar_init(B(ctl->o_full[t]), 1);
         }
         for (int s = 0; s < C::NSLOT; ++s) {
@@ -1252,9 +1260,7 @@ __global__ void __launch_bounds__(384, 1)
                 l += sums.x;
                 lr += sums.y;
                 ATTN_TRACE(EV_SM_EXP, j);
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(B(ctl->p_full[t]));
+                warp_announce_tmem(B(ctl->p_full[t]));
                 ATTN_TRACE(EV_SM_ARRIVE, j);
             }
             if (!ok) break;

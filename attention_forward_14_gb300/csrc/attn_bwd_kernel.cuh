@@ -10,10 +10,9 @@
 //   dS = P * (dP - D),   dQ = scale dS K,   dK = scale dS^T Q
 //
 // Three launches on the caller's stream:
-//   attn_bwd_prep_kernel    -D per query row, -LSE * log2(e) per row (-inf
-//                           for padding and rows that see no key; both
-//                           negated for the softmax's packed arithmetic), and
-//                           a zeroed fp32 dQ accumulator;
+//   attn_bwd_prep_kernel    D per query row, LSE * log2(e) per row (+inf for
+//                           padding and rows that see no key), and a zeroed
+//                           fp32 dQ accumulator;
 //   attn_bwd_kernel         one persistent CTA per SM; a work unit is one
 //                           block of 128 keys of one head.  K and V stay in
 //                           shared memory while the unit streams 128-query
@@ -65,8 +64,8 @@ struct BwdParams {
     const void *o;         // forward output [bh, sq, D] of T   (prep)
     const void *dout;      // dO [bh, sq, D] of T                (prep)
     const float *lse;      // forward LSE [bh, sq] (natural log)  (prep)
-    float *lse2;           // [bh, sq_pad]: -LSE * log2(e); -inf for padding / no key
-    float *dsum;           // [bh, sq_pad]: -D = -rowsum(dO * O); 0 for padding
+    float *lse2;           // [bh, sq_pad]: LSE * log2(e); +inf for padding / no key
+    float *dsum;           // [bh, sq_pad]: D = rowsum(dO * O); 0 for padding
     float *dq_acc;         // [bh, sq, D] fp32 accumulator of dQ
     void *dq;              // [bh, sq, D] of T                   (convert)
     void *dk, *dv;         // [bh, sk, D] of T
@@ -169,7 +168,7 @@ struct Cfg {
     static_assert(64 % RED_ROWS == 0, "reduce rows");
     // shared memory (offsets from a 1024-byte aligned base)
     static constexpr int CTL_OFF = 0;               // barriers, TMEM address, abort flag
-    static constexpr int LD_OFF = 1024;             // per stage: -LSE2[128], -D[128]
+    static constexpr int LD_OFF = 1024;             // per stage: lse2[128], dsum[128]
     static constexpr int LD_STAGE_BYTES = 1024;
     static constexpr int K_OFF = 3072;
     static constexpr int V_OFF = K_OFF + TILE_BYTES;
@@ -465,10 +464,10 @@ __device__ __forceinline__ float2 unpack2<__half>(uint32_t u)
 
 // ---------------------------------------------------------------- prep
 
-// One query row per D/8 threads: -D = -sum_c dO[c] O[c] (fp32), minus the
-// row's LSE in base 2, and a zeroed accumulator row.  Rows past the
-// sequence's query count (up to sq_pad) get the padding values (-LSE2 =
-// -inf, so that P = 0 there, and D = 0).
+// One query row per D/8 threads: D = sum_c dO[c] O[c] (fp32), the row's
+// LSE in base 2, and a zeroed accumulator row.  Rows past the sequence's
+// query count (up to sq_pad) get the padding values (LSE2 = +inf, so that
+// P = 0 there, and D = 0).
 template <typename T, int D, bool VARLEN>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p)
 {
@@ -519,15 +518,13 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p)
 #pragma unroll
         for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, TPR);
         if (sub == 0) {
-            // stored negated, so that the softmax adds them in packed
-            // (two-wide) fused multiply-adds: x = s * scale * log2(e) - LSE2
-            float nl2 = -INFINITY;
+            float l2 = INFINITY;
             if (valid) {
                 const float l = p.lse[lse_at];
-                nl2 = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
+                l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
             }
-            p.lse2[r] = nl2;
-            p.dsum[r] = valid ? -acc : 0.f;
+            p.lse2[r] = l2;
+            p.dsum[r] = valid ? acc : 0.f;
         }
     }
 }
@@ -1026,7 +1023,6 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t tS = tmem + lane_off + C::TM_S + 64 * g;
         const uint32_t tDP = tmem + lane_off + C::TM_DP + 64 * g;
         const float sl2e = p.sl2e, scale = p.scale;
-        const float2 scale2 = make_float2(scale, scale);
         uint32_t tile_it = 0, q_it = 0;
         bool ok = true;
         for (uint32_t kq = 0; ok; ++kq) {
@@ -1052,9 +1048,8 @@ __global__ void __launch_bounds__(512, 1)
                 int lim = CAUSAL ? diag - q0 : 0;
                 if (!row_ok) lim = 64;
                 const bool masked = __any_sync(0xffffffffu, lim > 0);
-                const float *l2 = ld_smem + st * (C::LD_STAGE_BYTES / 4) + 64 * g;  // -LSE2 of the columns
-                const float *dsv = l2 + C::BM;                                     // -D of the columns
-                const float2 sl2e2 = make_float2(sl2e, sl2e);
+                const float *l2 = ld_smem + st * (C::LD_STAGE_BYTES / 4) + 64 * g;
+                const float *dsv = l2 + C::BM;
                 // P^T of this thread's 64 columns, rounded to T, two per word: the
                 // dV product and dS both use these values.
                 uint32_t pk[32];
@@ -1064,14 +1059,13 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                     for (int c = 0; c < 64; c += 4) {
                         const float4 lv = *reinterpret_cast<const float4 *>(l2 + c);
-                        const float2 a = __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
-                                                    sl2e2, make_float2(lv.x, lv.y));
-                        const float2 b = __ffma2_rn(make_float2(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])),
-                                                    sl2e2, make_float2(lv.z, lv.w));
-                        float x[4] = {ex2_approx(a.x), ex2_approx(a.y), ex2_approx(b.x), ex2_approx(b.y)};
+                        const float lvv[4] = {lv.x, lv.y, lv.z, lv.w};
+                        float x[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
+                        for (int e = 0; e < 4; ++e) {
+                            x[e] = ex2_approx(fmaf(__uint_as_float(sr[c + e]), sl2e, -lvv[e]));
                             if (masked && (c + e) < lim) x[e] = 0.f;
+                        }
                         pk[c / 2] = pack2<T>(x[0], x[1]);
                         pk[c / 2 + 1] = pack2<T>(x[2], x[3]);
                     }
@@ -1101,17 +1095,15 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                         for (int c = 0; c < 2 * W; c += 4) {
                             const int cc = 2 * W * hh + c;
-                            const float4 nd4 = *reinterpret_cast<const float4 *>(dsv + cc);
-                            // (dP - D) * (scale * P), two at a time
-                            const float2 sp01 = __fmul2_rn(unpack2<T>(pk[cc / 2]), scale2);
-                            const float2 sp23 = __fmul2_rn(unpack2<T>(pk[cc / 2 + 1]), scale2);
-                            const float2 t01 = __fadd2_rn(make_float2(__uint_as_float(dr[cc]), __uint_as_float(dr[cc + 1])),
-                                                          make_float2(nd4.x, nd4.y));
-                            const float2 t23 = __fadd2_rn(make_float2(__uint_as_float(dr[cc + 2]), __uint_as_float(dr[cc + 3])),
-                                                          make_float2(nd4.z, nd4.w));
-                            const float2 ds01 = __fmul2_rn(t01, sp01), ds23 = __fmul2_rn(t23, sp23);
-                            dk[c / 2] = pack2<T>(ds01.x, ds01.y);
-                            dk[c / 2 + 1] = pack2<T>(ds23.x, ds23.y);
+                            const float4 dv4 = *reinterpret_cast<const float4 *>(dsv + cc);
+                            const float2 p01 = unpack2<T>(pk[cc / 2]), p23 = unpack2<T>(pk[cc / 2 + 1]);
+                            const float pv[4] = {p01.x, p01.y, p23.x, p23.y};
+                            const float dvv[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
+                            float ds[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) ds[e] = scale * pv[e] * (__uint_as_float(dr[cc + e]) - dvv[e]);
+                            dk[c / 2] = pack2<T>(ds[0], ds[1]);
+                            dk[c / 2 + 1] = pack2<T>(ds[2], ds[3]);
                         }
 #pragma unroll
                         for (int q16 = 0; q16 < W / 16; ++q16)

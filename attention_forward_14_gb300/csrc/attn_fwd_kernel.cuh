@@ -132,6 +132,17 @@ struct FwdParams {
 #endif
 };
 
+// Timeline event codes (see the hooks below).
+enum : uint32_t {
+    EV_SM_WAIT_S = 1, EV_SM_GOT_S, EV_SM_LD, EV_SM_MAX, EV_SM_RESCALE, EV_SM_EXP, EV_SM_ARRIVE,
+    EV_SM_EPI_WAIT, EV_SM_EPI_GOT, EV_SM_EPI_DONE,
+    EV_MMA_WAIT_Q = 20, EV_MMA_GOT_Q, EV_MMA_WAIT_KV, EV_MMA_GOT_KV, EV_MMA_WAIT_P, EV_MMA_GOT_P, EV_MMA_ISSUED,
+    EV_LD_WAIT = 40, EV_LD_GOT,
+    EV_K_ENTRY = 60, EV_K_READY, EV_K_EXIT,
+    EV_SM_EPI_WRITTEN = 81,
+    EV_REGS = 90, EV_UNIT, EV_DECODED, EV_Q_ISSUED,
+};
+
 // Pipeline timeline hooks.  Compiled out unless ATTN_TRACE_ENABLE is defined
 // (a separate diagnostic build that records {clock, event, arg} per warp).
 #ifdef ATTN_TRACE_ENABLE
@@ -140,6 +151,14 @@ struct FwdParams {
 __device__ __forceinline__ void attn_trace_record(const FwdParams &p, uint32_t &n, uint32_t ev, uint32_t arg)
 {
     constexpr uint32_t kCtas = 4, kWarps = 12, kEvents = 16384;
+#ifdef ATTN_TRACE_SPARSE
+    // sparse timelines: only the events that bound a softmax tile, the MMA
+    // warp's waits and the producer's slot waits, so that the hooks disturb
+    // the pipeline less
+    if (ev != EV_SM_GOT_S && ev != EV_SM_EXP && ev != EV_SM_ARRIVE && ev != EV_LD_WAIT && ev != EV_LD_GOT &&
+        (ev < EV_MMA_WAIT_KV || ev > EV_MMA_GOT_P))
+        return;
+#endif
     if (p.trace == nullptr || blockIdx.x >= kCtas || (threadIdx.x & 31) != 0 || n >= kEvents) return;
     const uint32_t w = threadIdx.x >> 5;
     unsigned long long *rec = p.trace + 2ull * ((blockIdx.x * kWarps + w) * kEvents + n);
@@ -152,15 +171,6 @@ __device__ __forceinline__ void attn_trace_record(const FwdParams &p, uint32_t &
 #define ATTN_TRACE(ev, arg) ((void)0)
 #endif
 
-enum : uint32_t {
-    EV_SM_WAIT_S = 1, EV_SM_GOT_S, EV_SM_LD, EV_SM_MAX, EV_SM_RESCALE, EV_SM_EXP, EV_SM_ARRIVE,
-    EV_SM_EPI_WAIT, EV_SM_EPI_GOT, EV_SM_EPI_DONE,
-    EV_MMA_WAIT_Q = 20, EV_MMA_GOT_Q, EV_MMA_WAIT_KV, EV_MMA_GOT_KV, EV_MMA_WAIT_P, EV_MMA_GOT_P, EV_MMA_ISSUED,
-    EV_LD_WAIT = 40, EV_LD_GOT,
-    EV_K_ENTRY = 60, EV_K_READY, EV_K_EXIT,
-    EV_SM_EPI_WRITTEN = 81,
-    EV_REGS = 90, EV_UNIT, EV_DECODED, EV_Q_ISSUED,
-};
 
 // Watchdog sites (recorded in status[3]).
 enum : uint32_t {

@@ -144,10 +144,11 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def cpu_baseline(w, q, k, v, target_s: float = 12.0):
+def cpu_baseline(w, q, k, v, target_s: float = 12.0, want_rows: bool = False):
     """The fp64 oracle, as it stands, on the host cores: a bounded sample of
     query rows of the first head, sized to ~target_s seconds.  Returns
-    (TFLOPS, description, cores, seconds)."""
+    (TFLOPS, description, cores, seconds), and with want_rows also the
+    sampled rows and the oracle's O and LSE for them."""
     import numpy as np
     import oracle
 
@@ -159,9 +160,11 @@ def cpu_baseline(w, q, k, v, target_s: float = 12.0):
             return np.full(len(rows), w.sk, dtype=np.float64)
         return np.clip(np.asarray(rows) + 1 + (w.sk - w.sq), 0, w.sk).astype(np.float64)
 
+    last = {}
+
     def run(rows):
         t0 = time.perf_counter()
-        oracle.attn_head_rows(qh, kh, vh, rows, w.causal, w.scale)
+        last["o"], last["lse"] = oracle.attn_head_rows(qh, kh, vh, rows, w.causal, w.scale)
         return time.perf_counter() - t0
 
     rng = np.random.default_rng(w.seed)
@@ -175,6 +178,8 @@ def cpu_baseline(w, q, k, v, target_s: float = 12.0):
     flops = 4.0 * w.d * visible(rows).sum()
     desc = (f"{n} seeded query rows of head (0,0) of {w.name}, each against all its visible keys "
             f"({flops / 1e9:.1f} GFLOP counted as 4*d per visible key)")
+    if want_rows:
+        return flops / dt / 1e12, desc, cores, dt, (rows, last["o"], last["lse"])
     return flops / dt / 1e12, desc, cores, dt
 
 
@@ -815,10 +820,23 @@ def main():
             "clocks": sampler.summary(),
         }
         if not args.no_cpu_baseline and world == 1:
-            tf, desc, cores, dt = cpu_baseline(w, q, k, v)
+            tf, desc, cores, dt, (rows, o_ref, lse_ref) = cpu_baseline(w, q, k, v, want_rows=True)
             line["cpu_baseline"] = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
                                     "sample": desc, "seconds": dt,
                                     "extrapolated_full_seconds": w.flops() / (tf * 1e12)}
+            # the same rows of the kernel's last output, against the oracle's
+            import numpy as np
+            idx = torch.as_tensor(rows, dtype=torch.long, device=dev)
+            o_k = o[0, 0].index_select(0, idx).double().cpu().numpy()
+            l_k = lse[0, 0].index_select(0, idx).double().cpu().numpy()
+            fin = np.isfinite(lse_ref)
+            line["accuracy"] = {
+                "rows": int(len(rows)), "head": "(0, 0)", "against": "fp64 oracle (the cpu_baseline sample)",
+                "o_max_abs": float(np.abs(o_k - o_ref).max()),
+                "o_rel_l2": float(np.linalg.norm(o_k - o_ref) / max(np.linalg.norm(o_ref), 1e-300)),
+                "lse_max_abs": float(np.abs(l_k[fin] - lse_ref[fin]).max()) if fin.any() else 0.0,
+                "finite": bool(np.isfinite(o_k).all() and np.isfinite(l_k[fin]).all()),
+            }
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()

@@ -98,6 +98,26 @@ def draw(b, h, sq, sk, d, dtype, seed, qk_std=1.0, v_std=1.0):
     return q.to(tdt), k.to(tdt), v.to(tdt)
 
 
+def randn_device(shape, dtype, seed, device, std=1.0, chunk=1 << 26):
+    """Seeded N(0, std^2) values of ``shape``, drawn on ``device`` in fp32
+    ``chunk`` elements at a time (so a tensor of several GiB needs no
+    full-size fp32 copy) and rounded to ``dtype``.  The values depend on the
+    seed, the shape and the device type only.  For problems too large to draw
+    on the host; the tests copy the parts they check back to the host."""
+    tdt = DTYPES[dtype] if isinstance(dtype, str) else dtype
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    out = torch.empty(shape, dtype=tdt, device=device)
+    flat = out.view(-1)
+    for a in range(0, flat.numel(), chunk):
+        n = min(chunk, flat.numel() - a)
+        t = torch.randn(n, generator=g, dtype=torch.float32, device=device)
+        if std != 1.0:
+            t.mul_(std)
+        flat[a:a + n].copy_(t)
+    return out
+
+
 def draw_grad(b, h, sq, d, dtype, seed):
     """Seeded output gradient dO [b, h, sq, d] ~ N(0, 1) as a CPU tensor."""
     tdt = DTYPES[dtype] if isinstance(dtype, str) else dtype

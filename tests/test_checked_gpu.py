@@ -19,6 +19,7 @@ from attention_forward_14_gb300 import workloads as W
 
 import test_fp8_gpu as F8
 import test_kvcache_gpu as KV
+import test_max_size_gpu as MS
 import test_parity_gpu as P
 import test_splitkv_gpu as SK
 import test_varlen_gpu as VL
@@ -86,6 +87,16 @@ def test_checked_kvcache_paged(case):
 def test_checked_fp8(causal, d):
     F8._check(2, 3, 300, 300, causal, seed=17 + d, what=f"checked e4m3 c{causal} d{d}", d=d)
     _clean(f"e4m3 c{causal} d{d}")
+
+
+@pytest.mark.parametrize("which", ["dense", "varlen"])
+def test_checked_past_2_32_elements(which):
+    """The forwards of the >2^32-element problems: every computed offset of
+    the larger tensors within its bounds (and the boundary heads correct)."""
+    out = MS.dense_forward() if which == "dense" else MS.varlen_forward()
+    _clean(f"{which} forward past 2^32 elements")
+    del out
+    torch.cuda.empty_cache()
 
 
 def test_checked_bounds_selftest_reports_instead_of_using():

@@ -158,6 +158,7 @@ struct Cfg {
     // have another accumulator layout), staged in a buffer of its own.
     static constexpr bool DQ_T = (D == 128);
     static constexpr int STAGE_BYTES = DQ_T ? 0 : BM * D * 4;
+    // stages of the Q / dO ring (a third at D = 64, where it fits, was slower)
     static constexpr int NSTAGE = 2;
     // rows of dQ per reduce-add when D = 128 (the staged half-tile of 64
     // rows is sent as 64 / RED_ROWS bulk reduces)
@@ -170,14 +171,17 @@ struct Cfg {
     static constexpr int CTL_OFF = 0;               // barriers, TMEM address, abort flag
     static constexpr int LD_OFF = 1024;             // per stage: lse2[128], dsum[128]
     static constexpr int LD_STAGE_BYTES = 1024;
-    static constexpr int K_OFF = 3072;
+    static constexpr int K_OFF = LD_OFF + NSTAGE * LD_STAGE_BYTES;
     static constexpr int V_OFF = K_OFF + TILE_BYTES;
     static constexpr int Q_OFF = V_OFF + TILE_BYTES;  // stage s: Q at Q_OFF + s*2*TILE, dO after it
     static constexpr int DS_OFF = Q_OFF + NSTAGE * 2 * TILE_BYTES;
     static constexpr int ST_OFF = DS_OFF + DS_BYTES;  // dQ staging (D = 64)
     static constexpr int SMEM_BYTES = ST_OFF + STAGE_BYTES;
-    // tensor memory columns
+    // tensor memory columns.  D = 128 fills all 512, and dQ^T reuses the
+    // dP^T / dS^T columns; D = 64 gives dQ 64 columns of its own, so that
+    // the next tile's dP^T need not wait for dQ to leave tensor memory.
     static constexpr int TM_DV = 0, TM_DK = D, TM_S = 2 * D, TM_DP = 2 * D + 128;
+    static constexpr int TM_DQ = DQ_T ? TM_DP : TM_DP + 128;
     static constexpr int TMEM_COLS = 512;
     static constexpr int THREADS = 512;
     // setmaxnreg budgets: 2 x 128 softmax threads, 128 drain threads (a
@@ -191,14 +195,15 @@ struct Cfg {
     static_assert(K_OFF % 1024 == 0 && V_OFF % 1024 == 0 && Q_OFF % 1024 == 0 && DS_OFF % 1024 == 0 &&
                       ST_OFF % 1024 == 0, "swizzle atoms need 1 KiB alignment");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-    static_assert(TM_DP + 128 <= TMEM_COLS, "tensor memory budget");
+    static_assert(NSTAGE == 2, "stage barriers in Ctl");
+    static_assert(TM_DP + 128 <= TMEM_COLS && TM_DQ + (DQ_T ? BM : D) <= TMEM_COLS, "tensor memory budget");
     static_assert(REGS_SOFTMAX * 2 + REGS_DRAIN + REGS_OTHER == 4 * 128, "register split");
 };
 
 struct Ctl {
     uint64_t kv_full, kv_empty;
     uint64_t q_full[2], q_empty[2];    // Q and the LSE / D vectors of a stage
-    uint64_t do_full[2], do_empty[2];  // dO of a stage (its slot also stages dQ)
+    uint64_t do_full[2], do_empty[2];  // dO of a stage (its slot also stages dQ when D = 128)
     uint64_t s_full, dp_full, p_full, ds_full;
     uint64_t dq_full, dq_empty;
     uint64_t dkv_full, dkv_empty;
@@ -587,7 +592,7 @@ __global__ void __launch_bounds__(512, 1)
     if (threadIdx.x == 0) {
         mbar_init(B(ctl->kv_full), 1);
         mbar_init(B(ctl->kv_empty), 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < C::NSTAGE; ++s) {
             mbar_init(B(ctl->q_full[s]), 1);
             mbar_init(B(ctl->q_empty[s]), 1);
             mbar_init(B(ctl->do_full[s]), 1);
@@ -671,9 +676,9 @@ __global__ void __launch_bounds__(512, 1)
                 __syncwarp();
                 ++un_it;
                 for (int t = 0; t < un.n && ok; ++t) {
-                    const uint32_t st = q_it & 1u;
+                    const uint32_t st = q_it % C::NSTAGE;
                     BWD_TRACE(BEV_LD_WAIT, q_it);
-                    ok = warp_wait(B(ctl->q_empty[st]), ((q_it >> 1) & 1u) ^ 1u, ctl, p, SITE_BWD_LOAD_Q_EMPTY);
+                    ok = warp_wait(B(ctl->q_empty[st]), ((q_it / C::NSTAGE) & 1u) ^ 1u, ctl, p, SITE_BWD_LOAD_Q_EMPTY);
                     BWD_TRACE(BEV_LD_GOT, q_it);
                     if (!ok) break;
                     const int q0 = (un.t0 + t) * C::BM;
@@ -688,9 +693,9 @@ __global__ void __launch_bounds__(512, 1)
                         bulk_load(sLD + st * C::LD_STAGE_BYTES + C::BM * 4, p.dsum + row, C::BM * 4, bar);
                     }
                     __syncwarp();
-                    // dO's slot is also where the previous user of the stage
-                    // staged its dQ: wait for that to be read out
-                    ok = warp_wait(B(ctl->do_empty[st]), ((q_it >> 1) & 1u) ^ 1u, ctl, p, SITE_BWD_LOAD_DO_EMPTY);
+                    // D = 128: dO's slot is also where the previous user of the
+                    // stage staged its dQ: wait for that to be read out
+                    ok = warp_wait(B(ctl->do_empty[st]), ((q_it / C::NSTAGE) & 1u) ^ 1u, ctl, p, SITE_BWD_LOAD_DO_EMPTY);
                     if (!ok) break;
                     if (elect_one()) {
                         const uint32_t bar = B(ctl->do_full[st]);
@@ -705,9 +710,9 @@ __global__ void __launch_bounds__(512, 1)
             }
             // Wind-down: let the last copies land before the CTA exits.
             if (un_it > 0) drain_wait(B(ctl->kv_full), (un_it - 1) & 1u, p.timeout_ns);
-            for (uint32_t k = (q_it > 2 ? q_it - 2 : 0u); k < q_it; ++k) {
-                drain_wait(B(ctl->q_full[k & 1u]), (k >> 1) & 1u, p.timeout_ns);
-                drain_wait(B(ctl->do_full[k & 1u]), (k >> 1) & 1u, p.timeout_ns);
+            for (uint32_t k = (q_it > C::NSTAGE ? q_it - C::NSTAGE : 0u); k < q_it; ++k) {
+                drain_wait(B(ctl->q_full[k % C::NSTAGE]), (k / C::NSTAGE) & 1u, p.timeout_ns);
+                drain_wait(B(ctl->do_full[k % C::NSTAGE]), (k / C::NSTAGE) & 1u, p.timeout_ns);
             }
             __syncwarp();
         } else if (warp == 12) {
@@ -758,30 +763,30 @@ __global__ void __launch_bounds__(512, 1)
                     zero_rows_from<C::NPANEL>(sK, un.sk - un.kb * C::BN);
                     zero_rows_from<C::NPANEL>(sV, un.sk - un.kb * C::BN);
                 }
-                if (!(ok = warp_wait(B(ctl->q_full[q_it & 1u]), (q_it >> 1) & 1u, ctl, p, SITE_BWD_MMA_Q_FULL))) break;
+                if (!(ok = warp_wait(B(ctl->q_full[q_it % C::NSTAGE]), (q_it / C::NSTAGE) & 1u, ctl, p, SITE_BWD_MMA_Q_FULL))) break;
                 if constexpr (VARLEN)  // queries past the sequence's end
-                    zero_rows_from<C::NPANEL>(sQ + (q_it & 1u) * 2 * C::TILE_BYTES, un.sq - un.t0 * C::BM);
+                    zero_rows_from<C::NPANEL>(sQ + (q_it % C::NSTAGE) * 2 * C::TILE_BYTES, un.sq - un.t0 * C::BM);
                 tc_fence_after();
                 if (elect_one()) {
-                    issue_kq(dK0, q_desc(q_it & 1u, false, 16), tmem + C::TM_S);
+                    issue_kq(dK0, q_desc(q_it % C::NSTAGE, false, 16), tmem + C::TM_S);
                     tc_commit(B(ctl->s_full));
                 }
                 __syncwarp();
-                if (dq_pending) {  // the previous unit's last dQ^T still occupies the dP^T columns
+                if (C::DQ_T && dq_pending) {  // the previous unit's last dQ^T still occupies the dP^T columns
                     if (!(ok = warp_wait(B(ctl->dq_empty), (tile_it - 1) & 1u, ctl, p, SITE_BWD_MMA_DQ_EMPTY))) break;
                     dq_pending = 0u;
                 }
-                if (!(ok = warp_wait(B(ctl->do_full[q_it & 1u]), (q_it >> 1) & 1u, ctl, p, SITE_BWD_MMA_DO_FULL))) break;
+                if (!(ok = warp_wait(B(ctl->do_full[q_it % C::NSTAGE]), (q_it / C::NSTAGE) & 1u, ctl, p, SITE_BWD_MMA_DO_FULL))) break;
                 if constexpr (VARLEN)
-                    zero_rows_from<C::NPANEL>(sQ + (q_it & 1u) * 2 * C::TILE_BYTES + C::TILE_BYTES, un.sq - un.t0 * C::BM);
+                    zero_rows_from<C::NPANEL>(sQ + (q_it % C::NSTAGE) * 2 * C::TILE_BYTES + C::TILE_BYTES, un.sq - un.t0 * C::BM);
                 tc_fence_after();
                 if (elect_one()) {
-                    issue_kq(dV0, q_desc(q_it & 1u, true, 16), tmem + C::TM_DP);
+                    issue_kq(dV0, q_desc(q_it % C::NSTAGE, true, 16), tmem + C::TM_DP);
                     tc_commit(B(ctl->dp_full));
                 }
                 __syncwarp();
                 for (int t = 0; t < un.n && ok; ++t) {
-                    const uint32_t st = q_it & 1u;
+                    const uint32_t st = q_it % C::NSTAGE;
                     // dV += P^T dO
                     BWD_TRACE(BEV_MMA_WAIT_P, tile_it);
                     if (!(ok = warp_wait(B(ctl->p_full), tile_it & 1u, ctl, p, SITE_BWD_MMA_P_FULL))) break;
@@ -790,23 +795,28 @@ __global__ void __launch_bounds__(512, 1)
                         !(ok = warp_wait(B(ctl->dkv_empty), (un_it - 1) & 1u, ctl, p, SITE_BWD_MMA_DKV_EMPTY)))
                         break;
                     tc_fence_after();
-                    if (elect_one()) issue_acc(tmem + C::TM_DV, tmem + C::TM_S, q_desc(st, true, C::PANEL_BYTES), t > 0);
+                    if (elect_one()) {
+                        issue_acc(tmem + C::TM_DV, tmem + C::TM_S, q_desc(st, true, C::PANEL_BYTES), t > 0);
+                        // D = 64: dV is the last reader of the tile's dO (its dQ is
+                        // staged elsewhere), so the slot goes back from here
+                        if constexpr (!C::DQ_T) tc_commit(B(ctl->do_empty[st]));
+                    }
                     __syncwarp();
                     BWD_TRACE(BEV_MMA_ISSUED_DV, tile_it);
                     // S^T of the next tile (its P^T columns were just consumed, in order)
                     const bool more = t + 1 < un.n;
                     if (more) {
                         BWD_TRACE(BEV_MMA_WAIT_Q, tile_it);
-                        if (!(ok = warp_wait(B(ctl->q_full[(q_it + 1) & 1u]), ((q_it + 1) >> 1) & 1u, ctl, p,
+                        if (!(ok = warp_wait(B(ctl->q_full[(q_it + 1) % C::NSTAGE]), ((q_it + 1) / C::NSTAGE) & 1u, ctl, p,
                                              SITE_BWD_MMA_Q_FULL)))
                             break;
                         BWD_TRACE(BEV_MMA_GOT_Q, tile_it);
                         if constexpr (VARLEN)
-                            zero_rows_from<C::NPANEL>(sQ + ((q_it + 1) & 1u) * 2 * C::TILE_BYTES,
+                            zero_rows_from<C::NPANEL>(sQ + ((q_it + 1) % C::NSTAGE) * 2 * C::TILE_BYTES,
                                                       un.sq - (un.t0 + t + 1) * C::BM);
                         tc_fence_after();
                         if (elect_one()) {
-                            issue_kq(dK0, q_desc((q_it + 1) & 1u, false, 16), tmem + C::TM_S);
+                            issue_kq(dK0, q_desc((q_it + 1) % C::NSTAGE, false, 16), tmem + C::TM_S);
                             tc_commit(B(ctl->s_full));
                         }
                         __syncwarp();
@@ -815,10 +825,15 @@ __global__ void __launch_bounds__(512, 1)
                     BWD_TRACE(BEV_MMA_WAIT_DS, tile_it);
                     if (!(ok = warp_wait(B(ctl->ds_full), tile_it & 1u, ctl, p, SITE_BWD_MMA_DS_FULL))) break;
                     BWD_TRACE(BEV_MMA_GOT_DS, tile_it);
+                    if (!C::DQ_T && dq_pending) {  // D = 64: the previous dQ has left its columns
+                        if (!(ok = warp_wait(B(ctl->dq_empty), (tile_it - 1) & 1u, ctl, p, SITE_BWD_MMA_DQ_EMPTY)))
+                            break;
+                        dq_pending = 0u;
+                    }
                     tc_fence_after();
                     if (elect_one()) {
                         issue_acc(tmem + C::TM_DK, tmem + C::TM_DP, q_desc(st, false, C::PANEL_BYTES), t > 0);
-                        issue_dq(tmem + C::TM_DP);
+                        issue_dq(tmem + C::TM_DQ);
                         tc_commit(B(ctl->dq_full));
                         tc_commit(B(ctl->q_empty[st]));
                         if (!more) {
@@ -831,22 +846,24 @@ __global__ void __launch_bounds__(512, 1)
                     dq_pending = 1u;
                     ++tile_it;
                     ++q_it;
-                    // dP^T of the next tile, once dQ^T has been drained
+                    // dP^T of the next tile (D = 128: once dQ^T has been drained)
                     if (more) {
-                        BWD_TRACE(BEV_MMA_WAIT_DQE, tile_it);
-                        if (!(ok = warp_wait(B(ctl->dq_empty), (tile_it - 1) & 1u, ctl, p, SITE_BWD_MMA_DQ_EMPTY)))
-                            break;
-                        BWD_TRACE(BEV_MMA_GOT_DQE, tile_it);
-                        dq_pending = 0u;
-                        if (!(ok = warp_wait(B(ctl->do_full[q_it & 1u]), (q_it >> 1) & 1u, ctl, p,
+                        if constexpr (C::DQ_T) {
+                            BWD_TRACE(BEV_MMA_WAIT_DQE, tile_it);
+                            if (!(ok = warp_wait(B(ctl->dq_empty), (tile_it - 1) & 1u, ctl, p, SITE_BWD_MMA_DQ_EMPTY)))
+                                break;
+                            BWD_TRACE(BEV_MMA_GOT_DQE, tile_it);
+                            dq_pending = 0u;
+                        }
+                        if (!(ok = warp_wait(B(ctl->do_full[q_it % C::NSTAGE]), (q_it / C::NSTAGE) & 1u, ctl, p,
                                              SITE_BWD_MMA_DO_FULL)))
                             break;
                         if constexpr (VARLEN)
-                            zero_rows_from<C::NPANEL>(sQ + (q_it & 1u) * 2 * C::TILE_BYTES + C::TILE_BYTES,
+                            zero_rows_from<C::NPANEL>(sQ + (q_it % C::NSTAGE) * 2 * C::TILE_BYTES + C::TILE_BYTES,
                                                       un.sq - (un.t0 + t + 1) * C::BM);
                         tc_fence_after();
                         if (elect_one()) {
-                            issue_kq(dV0, q_desc(q_it & 1u, true, 16), tmem + C::TM_DP);
+                            issue_kq(dV0, q_desc(q_it % C::NSTAGE, true, 16), tmem + C::TM_DP);
                             tc_commit(B(ctl->dp_full));
                         }
                         __syncwarp();
@@ -875,8 +892,8 @@ __global__ void __launch_bounds__(512, 1)
         //   D = 64:  dQ, this thread holds query row dcol's 64 columns;
         //            staged in a buffer of its own as two [128][32] boxes
         //            with the 128-byte swizzle (conflict-free row writes).
-        // The dO slot goes back to the producer once the reduces have read
-        // the staging.
+        // D = 128: the dO slot goes back to the producer once the reduces
+        // have read the staging (D = 64: the MMA warp returns it after dV).
         const int quad = warp & 3;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const int dcol = quad * 32 + lane;
@@ -922,7 +939,7 @@ __global__ void __launch_bounds__(512, 1)
                 BWD_TRACE(BEV_DR_GOT, tile_it);
                 ++tile_it;
                 tc_fence_after();
-                const uint32_t st = q_it & 1u;
+                const uint32_t st = q_it % C::NSTAGE;
                 const int q0 = (un.t0 + t) * C::BM;
                 if constexpr (C::DQ_T) {
                     uint32_t v[128];
@@ -951,7 +968,7 @@ __global__ void __launch_bounds__(512, 1)
                     }
                 } else {
                     uint32_t v[64];
-                    tmem_ld64_wait(tmem + lane_off + C::TM_DP, v);
+                    tmem_ld64_wait(tmem + lane_off + C::TM_DQ, v);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(B(ctl->dq_empty));
@@ -976,7 +993,7 @@ __global__ void __launch_bounds__(512, 1)
                     }
                 }
                 if (!ok) break;
-                if (issuer) mbar_arrive(B(ctl->do_empty[st]));
+                if (C::DQ_T && issuer) mbar_arrive(B(ctl->do_empty[st]));  // the staging in the dO slot is read
                 ++q_it;
                 BWD_TRACE(BEV_DR_DONE, tile_it);
             }
@@ -1036,9 +1053,9 @@ __global__ void __launch_bounds__(512, 1)
             const bool row_ok = key < sk_;
             const int diag = key - (sk_ - sq_);  // the first query this key row sees
             for (int t = 0; t < un.n && ok; ++t) {
-                const uint32_t st = q_it & 1u;
+                const uint32_t st = q_it % C::NSTAGE;
                 // the tile's LSE / D vectors arrive with Q and dO
-                if (!(ok = warp_wait(B(ctl->q_full[st]), (q_it >> 1) & 1u, ctl, p, SITE_BWD_SM_S_FULL))) break;
+                if (!(ok = warp_wait(B(ctl->q_full[st]), (q_it / C::NSTAGE) & 1u, ctl, p, SITE_BWD_SM_S_FULL))) break;
                 BWD_TRACE(BEV_SM_WAIT_S, tile_it);
                 if (!(ok = warp_wait(B(ctl->s_full), tile_it & 1u, ctl, p, SITE_BWD_SM_S_FULL))) break;
                 BWD_TRACE(BEV_SM_GOT_S, tile_it);

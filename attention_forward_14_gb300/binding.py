@@ -25,7 +25,7 @@ ERRORS = {
 # Every function include/attn_fwd.h declares.
 EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_fwd_varlen", "attn_fwd_fp8", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
            "attn_fwd_splitkv_default_splits", "attn_fwd_splitkv_noalloc", "attn_last_error", "attn_fwd_status", "attn_fwd_status_clear",
-           "attn_fwd_debug_status", "attn_fwd_sched_pin_slot", "attn_fwd_bounds_selftest",
+           "attn_fwd_debug_status", "attn_fwd_sched_pin_slot", "attn_fwd_bounds_selftest", "attn_bwd_bounds_selftest",
            "attn_fwd_watchdog_selftest", "attn_version", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_varlen",
            "attn_bwd_varlen_workspace_bytes", "attn_fwd_kvcache", "attn_fwd_kvcache_paged"]
 
@@ -81,6 +81,9 @@ def _bind(lib):
     lib.attn_fwd_sched_pin_slot.argtypes = [c_int]
     lib.attn_fwd_bounds_selftest.restype = c_int
     lib.attn_fwd_bounds_selftest.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_float, c_int, vp]
+    lib.attn_bwd_bounds_selftest.restype = c_int
+    lib.attn_bwd_bounds_selftest.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_float,
+                                             c_int, vp, i64, vp]
     lib.attn_fwd_watchdog_selftest.restype = c_int
     lib.attn_fwd_watchdog_selftest.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_float,
                                                c_int, c_int, c_int, vp]

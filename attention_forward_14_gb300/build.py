@@ -2,11 +2,11 @@
 
 Each translation unit under csrc/ is compiled in parallel, then linked into
 ``attention_forward_14_gb300/libattn_fwd.so``.  The checked variant,
-``libattn_fwd_checked.so``, compiles the forward's translation units again
-with ATTN_CHECKED=1 (every computed copy coordinate, output offset, decoded
-unit and on-chip address is compared with its bounds; a violation is
-recorded in the status word and the CTA winds down) and links them with the
-same backward objects.  Usage:
+``libattn_fwd_checked.so``, compiles every translation unit again with
+ATTN_CHECKED=1 (every computed copy coordinate, output offset, decoded unit
+and on-chip address of the forward and backward kernels is compared with
+its bounds; a violation is recorded in the status word and the CTA winds
+down).  Usage:
 ``python -m attention_forward_14_gb300.build [--force] [-v]``.
 """
 from __future__ import annotations
@@ -27,8 +27,8 @@ LIB_CHECKED = os.path.join(HERE, "libattn_fwd_checked.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["attn_fwd_api.cu", "inst_d64.cu", "inst_d128_noncausal.cu", "inst_d128_causal.cu", "inst_fp8.cu",
            "attn_bwd_inst.cu", "attn_bwd_inst_varlen.cu"]
-# the translation units that hold the forward kernel (compiled again, checked)
-FWD_SOURCES = ["attn_fwd_api.cu", "inst_d64.cu", "inst_d128_noncausal.cu", "inst_d128_causal.cu", "inst_fp8.cu"]
+# the translation units compiled again, checked (all of them: forward and backward)
+CHECKED_SOURCES = SOURCES
 
 
 def nvcc() -> str:
@@ -81,12 +81,12 @@ def build(force: bool = False, verbose: bool = False, checked: bool = True) -> s
             sys.stderr.write(r.stdout + r.stderr)
         return obj
 
-    jobs = [(src, False) for src in SOURCES]  # the checked library reuses the backward objects
-    jobs += [(src, True) for src in FWD_SOURCES if any(chk for _, chk in todo)]
+    jobs = [(src, False) for src in SOURCES]
+    jobs += [(src, True) for src in CHECKED_SOURCES if any(chk for _, chk in todo)]
     with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
         list(ex.map(compile_one, jobs))
     for lib, chk in todo:
-        objs = [obj_path(src, chk and src in FWD_SOURCES) for src in SOURCES]
+        objs = [obj_path(src, chk and src in CHECKED_SOURCES) for src in SOURCES]
         tmp = lib + f".tmp{os.getpid()}"
         r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
         if r.returncode != 0:

@@ -57,6 +57,14 @@
 
 #include "ptx.cuh"
 
+// Checked build: with ATTN_CHECKED=1 every computed copy coordinate, global
+// output offset, decoded unit, tensor-memory base and shared-memory window
+// of the backward is compared with its bounds (see in_bounds).  Off by
+// default.
+#ifndef ATTN_CHECKED
+#define ATTN_CHECKED 0
+#endif
+
 namespace attn {
 namespace bwd {
 
@@ -140,7 +148,21 @@ enum : uint32_t {
     SITE_BWD_LOAD_DO_EMPTY = 36,
     SITE_BWD_MMA_DO_FULL = 37,
     SITE_BWD_DRAIN_SYNC = 38,
+    // checked builds: the index that failed its bounds
+    SITE_BWD_CHK_SMEM = 40,     // dynamic shared memory window too small for the layout
+    SITE_BWD_CHK_TMEM = 41,     // tensor-memory allocation not the expected 512 columns at lane 0
+    SITE_BWD_CHK_UNIT = 42,     // claimed or decoded unit outside the problem
+    SITE_BWD_CHK_KV_LOAD = 43,  // K/V copy coordinates
+    SITE_BWD_CHK_Q_LOAD = 44,   // Q / dO copy coordinates, LSE / D vector rows
+    SITE_BWD_CHK_DQ_RED = 45,   // dQ reduce-add coordinates
+    SITE_BWD_CHK_DKV_ROW = 46,  // dK / dV row written by a thread
+    SITE_BWD_CHK_PREP = 47,     // prep kernel: O / dO / accumulator / LSE offsets
 };
+
+// Status codes (the forward's): a wait that ran out, and an index or layout
+// outside its bounds.
+constexpr uint32_t kStatusTimeout = 1u;
+constexpr uint32_t kStatusBounds = 3u;
 
 // Sizes for head dim D (64 or 128).  Tiles are always 128 rows (keys or
 // queries) of 128-byte swizzle panels of 64 elements.
@@ -326,7 +348,7 @@ __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl *ct
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > p.timeout_ns) {
             *abort_flag = 1u;
-            if (atomicCAS(&p.status[0], 0u, 1u) == 0u) {
+            if (atomicCAS(&p.status[0], 0u, kStatusTimeout) == 0u) {
                 p.status[1] = blockIdx.x;
                 p.status[2] = threadIdx.x >> 5;
                 p.status[3] = site;
@@ -349,6 +371,34 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Ctl *ct
     const bool w = bar_wait(bar, parity, ctl, p, site);
     return __all_sync(0xffffffffu, w);
 }
+
+__device__ __forceinline__ void record_bounds(const BwdParams &p, uint32_t site)
+{
+    if (atomicCAS(&p.status[0], 0u, kStatusBounds) == 0u) {
+        p.status[1] = blockIdx.x;
+        p.status[2] = threadIdx.x >> 5;
+        p.status[3] = site;
+        __threadfence();
+    }
+}
+
+// Checked builds: `ok` false records kStatusBounds at `site` and raises the
+// CTA's abort flag, so that the other warps wind down as after a wait that
+// ran out; the caller skips the access.  Normal builds: always true (the
+// condition is not evaluated).
+#if ATTN_CHECKED
+#define BWD_IN_BOUNDS(cond, site) in_bounds((cond), ctl, p, (site))
+__device__ __forceinline__ bool in_bounds(bool ok, Ctl *ctl, const BwdParams &p, uint32_t site)
+{
+    if (!ok) {
+        *reinterpret_cast<volatile uint32_t *>(&ctl->abort) = 1u;
+        record_bounds(p, site);
+    }
+    return ok;
+}
+#else
+#define BWD_IN_BOUNDS(cond, site) true
+#endif
 
 // Bounded wait that ignores the abort flag (lets this thread's own copies
 // and MMAs land before the CTA frees its resources).
@@ -420,6 +470,21 @@ __device__ __forceinline__ Unit decode_unit(int u, const BwdParams &p)
     un.n = n_tiles - un.t0;
     un.zero = has_keys && un.n == 0;
     return un;
+}
+
+// Checked builds: the decoded unit lies within the problem (its key block,
+// head plane, query tiles and, packed, its sequence's token ranges).
+template <bool VARLEN>
+__device__ __forceinline__ bool unit_ok(const Unit &un, const BwdParams &p)
+{
+    bool in = un.bh >= 0 && un.bh < p.bh && un.kb >= 0 && un.kb < p.num_kblk && un.t0 >= 0 && un.n >= 0 &&
+              (un.t0 + un.n) * 128 < un.sq + 128;
+    if constexpr (VARLEN)
+        in = in && un.head >= 0 && un.head < p.heads && un.q_tok0 >= 0 && un.q_tok0 + un.sq <= p.total_q &&
+             un.k_tok0 >= 0 && un.k_tok0 + un.sk <= p.total_k;
+    else
+        in = in && un.sq == p.sq && un.sk == p.sk;
+    return in;
 }
 
 // The k-th unit index of this CTA from the ring (-1: no more work), read by
@@ -503,7 +568,18 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p)
             elem = (bh * p.sq + i) * D;
             lse_at = bh * p.sq + i;
         }
-        const bool valid = i < sq;
+        bool valid = i < sq;
+#if ATTN_CHECKED
+        {
+            // the row of O / dO / the accumulator and its LSE entry are inside their tensors
+            const int64_t o_rows = VARLEN ? static_cast<int64_t>(p.total_q) * p.heads : static_cast<int64_t>(p.bh) * p.sq;
+            const int64_t lses = VARLEN ? static_cast<int64_t>(p.heads) * p.total_q : static_cast<int64_t>(p.bh) * p.sq;
+            if (valid && !(elem >= 0 && elem / D < o_rows && lse_at >= 0 && lse_at < lses)) {
+                record_bounds(p, SITE_BWD_CHK_PREP);
+                valid = false;
+            }
+        }
+#endif
         float acc = 0.f;
         if (valid) {
             const int64_t off = elem + sub * 8;
@@ -568,7 +644,7 @@ __global__ void __launch_bounds__(512, 1)
     // The whole budget is used, with no room to realign: the dynamic shared
     // window starts 1 KiB aligned.  Should it not, report and do nothing.
     if ((base_addr & 1023u) != 0u) {
-        if (threadIdx.x == 0 && atomicCAS(&p.status[0], 0u, 2u) == 0u) {
+        if (threadIdx.x == 0 && atomicCAS(&p.status[0], 0u, kStatusBounds) == 0u) {
             p.status[1] = blockIdx.x;
             p.status[2] = 0u;
             p.status[3] = SITE_BWD_SMEM_ALIGN;
@@ -630,6 +706,18 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
+#if ATTN_CHECKED
+    {
+        uint32_t dsmem;
+        asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dsmem));
+        const bool window = static_cast<uint32_t>(C::SMEM_BYTES) <= dsmem;
+        const bool tcols = (tmem >> 16) == 0u && (tmem & 0xFFFFu) + C::TMEM_COLS <= 512u;
+        const bool setup_ok = (threadIdx.x != 0) || (BWD_IN_BOUNDS(window, SITE_BWD_CHK_SMEM) &&
+                                                     BWD_IN_BOUNDS(tcols, SITE_BWD_CHK_TMEM));
+        // every thread takes the same decision: no role starts on a bad layout
+        if (!__syncthreads_and(setup_ok ? 1 : 0)) goto wind_down;
+    }
+#endif
 
     if (warp >= 12) {
         regs_dec<C::REGS_OTHER>();
@@ -652,7 +740,16 @@ __global__ void __launch_bounds__(512, 1)
                 }
                 u = __shfl_sync(0xffffffffu, u, 0);
                 if (u < 0) break;
+                if (!BWD_IN_BOUNDS(static_cast<int64_t>(u) < static_cast<int64_t>(p.bh) * p.num_kblk,
+                                   SITE_BWD_CHK_UNIT)) {  // before decode reads any offset
+                    ok = false;
+                    break;
+                }
                 const Unit un = decode_unit<CAUSAL, VARLEN>(u, p);
+                if (!BWD_IN_BOUNDS(unit_ok<VARLEN>(un, p), SITE_BWD_CHK_UNIT)) {
+                    ok = false;
+                    break;
+                }
                 if (un.n == 0) continue;
                 // TMA coordinates after the 64-column panel: dense maps are
                 // [bh][s][D] (row, plane = bh); packed maps are [token][head][D]
@@ -664,6 +761,12 @@ __global__ void __launch_bounds__(512, 1)
                 auto kplane = [&](int r) { return vl ? un.k_tok0 + r : un.bh; };
                 ok = warp_wait(B(ctl->kv_empty), (un_it & 1u) ^ 1u, ctl, p, SITE_BWD_LOAD_KV_EMPTY);
                 if (!ok) break;
+                if (!BWD_IN_BOUNDS(un.kb * C::BN < un.sk &&
+                                       (vl ? un.k_tok0 + un.kb * C::BN < p.total_k && un.head < p.heads : un.bh < p.bh),
+                                   SITE_BWD_CHK_KV_LOAD)) {
+                    ok = false;
+                    break;
+                }
                 if (elect_one()) {
                     mbar_arrive_expect_tx(B(ctl->kv_full), 2 * C::TILE_BYTES);
                     for (int pn = 0; pn < C::NPANEL; ++pn) {
@@ -683,6 +786,15 @@ __global__ void __launch_bounds__(512, 1)
                     if (!ok) break;
                     const int q0 = (un.t0 + t) * C::BM;
                     const uint32_t q_tile = sQ + st * 2 * C::TILE_BYTES;
+                    // the tile's Q / dO rows and its LSE / D vector rows (checked once: dO uses the same)
+                    if (!BWD_IN_BOUNDS(q0 >= 0 && q0 < un.sq &&
+                                           (vl ? un.q_tok0 + q0 < p.total_q && un.head < p.heads : un.bh < p.bh) &&
+                                           static_cast<int64_t>(un.bh) * p.sq_pad + q0 + C::BM <=
+                                               static_cast<int64_t>(p.bh) * p.sq_pad,
+                                       SITE_BWD_CHK_Q_LOAD)) {
+                        ok = false;
+                        break;
+                    }
                     if (elect_one()) {
                         const uint32_t bar = B(ctl->q_full[st]);
                         mbar_arrive_expect_tx(bar, C::TILE_BYTES + 2 * C::BM * 4);
@@ -756,7 +868,16 @@ __global__ void __launch_bounds__(512, 1)
                 int u;
                 if (!(ok = next_unit(kq, u, ctl, p))) break;
                 if (u < 0) break;
+                if (!BWD_IN_BOUNDS(static_cast<int64_t>(u) < static_cast<int64_t>(p.bh) * p.num_kblk,
+                                   SITE_BWD_CHK_UNIT)) {  // before decode reads any offset
+                    ok = false;
+                    break;
+                }
                 const Unit un = decode_unit<CAUSAL, VARLEN>(u, p);
+                if (!BWD_IN_BOUNDS(unit_ok<VARLEN>(un, p), SITE_BWD_CHK_UNIT)) {
+                    ok = false;
+                    break;
+                }
                 if (un.n == 0) continue;
                 if (!(ok = warp_wait(B(ctl->kv_full), un_it & 1u, ctl, p, SITE_BWD_MMA_KV_FULL))) break;
                 if constexpr (VARLEN) {  // keys past the sequence's end
@@ -912,15 +1033,35 @@ __global__ void __launch_bounds__(512, 1)
             int u;
             if (!(ok = next_unit(kq, u, ctl, p))) break;
             if (u < 0) break;
+            if (!BWD_IN_BOUNDS(static_cast<int64_t>(u) < static_cast<int64_t>(p.bh) * p.num_kblk,
+                               SITE_BWD_CHK_UNIT)) {  // before decode reads any offset
+                ok = false;
+                break;
+            }
             const Unit un = decode_unit<CAUSAL, VARLEN>(u, p);
+            if (!BWD_IN_BOUNDS(unit_ok<VARLEN>(un, p), SITE_BWD_CHK_UNIT)) {
+                ok = false;
+                break;
+            }
             constexpr bool vl = VARLEN;
             auto key_offset = [&](int key) {  // element offset of key row `key` of the unit's sequence in dK / dV
                 return vl ? (static_cast<size_t>(un.k_tok0 + key) * p.heads + un.head) * C::D
                           : (static_cast<size_t>(un.bh) * p.sk + key) * C::D;
             };
+            // checked builds: the row is one of dK's / dV's rows
+            auto dkv_row_ok = [&](int key) {
+                const size_t rows = vl ? static_cast<size_t>(p.total_k) * p.heads : static_cast<size_t>(p.bh) * p.sk;
+                return key >= 0 && key_offset(key) / C::D < rows;
+            };
             if (un.n == 0) {
                 if (un.zero) {  // a sequence with keys but no query: its dK and dV are 0
                     const int key = un.kb * C::BN + quad * 32 + lane;
+#if ATTN_CHECKED
+                    if (!__all_sync(0xffffffffu, BWD_IN_BOUNDS(key >= un.sk || dkv_row_ok(key), SITE_BWD_CHK_DKV_ROW))) {
+                        ok = false;
+                        break;
+                    }
+#endif
                     if (key < un.sk)
 #pragma unroll
                         for (int which = 0; which < 2; ++which) {
@@ -941,6 +1082,14 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_after();
                 const uint32_t st = q_it % C::NSTAGE;
                 const int q0 = (un.t0 + t) * C::BM;
+                // the reduce-adds start at a row of the tile's sequence (rows past the
+                // tensor are dropped by the copy engine)
+                if (!BWD_IN_BOUNDS(q0 >= 0 && q0 < un.sq &&
+                                       (vl ? un.q_tok0 + q0 < p.total_q && un.head < p.heads : un.bh < p.bh),
+                                   SITE_BWD_CHK_DQ_RED)) {
+                    ok = false;
+                    break;
+                }
                 if constexpr (C::DQ_T) {
                     uint32_t v[128];
                     tmem_ld128_wait(tmem + lane_off + C::TM_DP, v);
@@ -1006,6 +1155,12 @@ __global__ void __launch_bounds__(512, 1)
             tc_fence_after();
             const int key = un.kb * C::BN + quad * 32 + lane;
             const bool valid = key < un.sk;
+#if ATTN_CHECKED
+            if (!__all_sync(0xffffffffu, BWD_IN_BOUNDS(!valid || dkv_row_ok(key), SITE_BWD_CHK_DKV_ROW))) {
+                ok = false;
+                break;
+            }
+#endif
             const size_t roff = key_offset(valid ? key : 0);
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
@@ -1046,7 +1201,16 @@ __global__ void __launch_bounds__(512, 1)
             int u;
             if (!(ok = next_unit(kq, u, ctl, p))) break;
             if (u < 0) break;
+            if (!BWD_IN_BOUNDS(static_cast<int64_t>(u) < static_cast<int64_t>(p.bh) * p.num_kblk,
+                               SITE_BWD_CHK_UNIT)) {  // before decode reads any offset
+                ok = false;
+                break;
+            }
             const Unit un = decode_unit<CAUSAL, VARLEN>(u, p);
+            if (!BWD_IN_BOUNDS(unit_ok<VARLEN>(un, p), SITE_BWD_CHK_UNIT)) {
+                ok = false;
+                break;
+            }
             if (un.n == 0) continue;
             const int key = un.kb * C::BN + r;
             const int sk_ = VARLEN ? un.sk : p.sk, sq_ = VARLEN ? un.sq : p.sq;
@@ -1147,6 +1311,9 @@ __global__ void __launch_bounds__(512, 1)
         }
     }
 
+#if ATTN_CHECKED
+wind_down:
+#endif
     if (warp == 8 && lane == 0) bulk_wait_all();  // the dQ reduces have landed
     tc_fence_before();
     __syncthreads();

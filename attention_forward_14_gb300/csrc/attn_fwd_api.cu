@@ -485,9 +485,11 @@ cudaError_t launch_bwd_any(const bwd::BwdLaunchArgs &a, int64_t d, int dtype, in
     return causal ? bwd::launch_bwd<__half, true, 64, VARLEN>(a) : bwd::launch_bwd<__half, false, 64, VARLEN>(a);
 }
 
+// extra_units > 0 (the bounds self-test only) hands out that many units past
+// the end of the problem.
 int run_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse, void *dq,
             void *dk, void *dv, int64_t b, int64_t h, int64_t sq, int64_t sk, int64_t d, int causal, float scale,
-            int dtype, void *workspace, int64_t workspace_bytes, cudaStream_t stream)
+            int dtype, void *workspace, int64_t workspace_bytes, cudaStream_t stream, int extra_units = 0)
 {
     if (b < 0 || h < 0 || sq < 0 || sk < 0)
         return fail(ATTN_ERR_SHAPE, "negative size: b=%lld h=%lld sq=%lld sk=%lld", (long long)b, (long long)h,
@@ -552,7 +554,7 @@ int run_bwd(const void *q, const void *k, const void *v, const void *o, const vo
     p.sk = static_cast<int32_t>(sk);
     p.sq_pad = static_cast<int32_t>(sq_pad);
     p.num_kblk = static_cast<int32_t>((sk + 127) / 128);
-    p.num_units = static_cast<int32_t>(bh * p.num_kblk);
+    p.num_units = static_cast<int32_t>(bh * p.num_kblk) + extra_units;
     p.group = bwd_group(bh, sq, d);
 #ifdef ATTN_TRACE_ENABLE
     p.trace = g_trace_buf;
@@ -1219,6 +1221,30 @@ int attn_fwd_bounds_selftest(const void *q, const void *k, const void *v, void *
     (void)q, (void)k, (void)v, (void)o, (void)lse, (void)b, (void)h, (void)sq, (void)sk, (void)d, (void)scale;
     (void)dtype, (void)stream;
     return fail(ATTN_ERR_BUILD, "attn_fwd_bounds_selftest needs the checked build (libattn_fwd_checked.so)");
+#endif
+}
+
+int attn_bwd_bounds_selftest(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                             const float *lse, void *dq, void *dk, void *dv, int64_t b, int64_t h, int64_t sq,
+                             int64_t sk, int64_t d, float scale, int dtype, void *workspace, int64_t workspace_bytes,
+                             void *stream)
+{
+    g_err.clear();
+#if ATTN_CHECKED
+    if (b < 1 || h < 1 || sq < 1 || sk < 1 || b * h * sq > 4096 || sk > 1024)
+        return fail(ATTN_ERR_SHAPE, "self-test wants a tiny problem with rows and keys");
+    int rc = attn_fwd_status_clear();
+    if (rc != ATTN_OK) return rc;
+    // one unit past the end of a dense, unmasked problem: its index is out of
+    // range, which every warp role finds before decoding it
+    rc = run_bwd(q, k, v, o, dout, lse, dq, dk, dv, b, h, sq, sk, d, 0, scale, dtype, workspace, workspace_bytes,
+                 static_cast<cudaStream_t>(stream), 1);
+    if (rc != ATTN_OK) return rc;
+    return attn_fwd_status(nullptr);
+#else
+    (void)q, (void)k, (void)v, (void)o, (void)dout, (void)lse, (void)dq, (void)dk, (void)dv, (void)b, (void)h;
+    (void)sq, (void)sk, (void)d, (void)scale, (void)dtype, (void)workspace, (void)workspace_bytes, (void)stream;
+    return fail(ATTN_ERR_BUILD, "attn_bwd_bounds_selftest needs the checked build (libattn_fwd_checked.so)");
 #endif
 }
 

@@ -410,8 +410,8 @@ const char *attn_last_error(void);
  *   code ATTN_STATUS_TIMEOUT (1)         a wait ran out;
  *   code ATTN_STATUS_SCHED_COLLISION (2) a launch found its schedule slot
  *                                        held by another (attn_fwd_varlen);
- *   code ATTN_STATUS_BOUNDS (3)          checked build only: a computed index
- *                                        was outside its bounds (see below).
+ *   code ATTN_STATUS_BOUNDS (3)          checked build: a computed index was
+ *                                        outside its bounds (see below).
  * attn_fwd_status synchronises the current device, copies the status into
  * out[0..3] = {code, block, warp, site} (out may be NULL) and returns code
  * (0 = nothing recorded, <0 = CUDA error while reading).
@@ -452,14 +452,21 @@ int attn_fwd_watchdog_selftest(const void *q, const void *k, const void *v,
 
 /*
  * Checked build.  libattn_fwd_checked.so exports this same interface from
- * the same sources compiled with every computed index of the forward kernel
- * checked: copy coordinates of Q, K, V (page lookups included) and of the O
- * stores, thread-written O, LSE and split-partial offsets, the decoded work
- * units, the tensor-memory allocation and the shared-memory window.  An index
- * outside its bounds is not used: the kernel records {ATTN_STATUS_BOUNDS,
- * block, warp, site} in the status word and the CTA winds down as after a
- * wait that ran out.  It stands in for a memory checker, which is not
- * available on every machine, and is slower than the normal build.
+ * the same sources compiled with every computed index of the forward and
+ * backward kernels checked.  Forward: copy coordinates of Q, K, V (page
+ * lookups included) and of the O stores, thread-written O, LSE and
+ * split-partial offsets, the decoded work units, the tensor-memory
+ * allocation and the shared-memory window.  Backward: the claimed and
+ * decoded units, the copy coordinates of K, V, Q and dO and the rows of the
+ * LSE / D vectors, the dQ reduce-add coordinates, the thread-written dK / dV
+ * rows, the prep kernel's O / dO / accumulator / LSE offsets, the
+ * tensor-memory allocation and the shared-memory window.  An index outside
+ * its bounds is not used: the kernel records {ATTN_STATUS_BOUNDS, block,
+ * warp, site} in the status word and the CTA winds down as after a wait
+ * that ran out.  It stands in for a memory checker, which is not available
+ * on every machine, and is slower than the normal build.  (In every build,
+ * a backward launch whose shared-memory window is not 1 KiB aligned records
+ * ATTN_STATUS_BOUNDS and does nothing.)
  *
  * attn_fwd_bounds_selftest runs attn_fwd on tiny caller buffers (contract of
  * attn_fwd, no mask, b*h*sq <= 4096, 1 <= sk <= 1024) with one work unit past
@@ -471,6 +478,22 @@ int attn_fwd_bounds_selftest(const void *q, const void *k, const void *v,
                              void *o, float *lse, int64_t b, int64_t h,
                              int64_t sq, int64_t sk, int64_t d, float scale,
                              int dtype, void *stream);
+
+/*
+ * attn_bwd_bounds_selftest: the same for the backward -- attn_bwd on tiny
+ * caller buffers (contract of attn_bwd, no mask, b*h*sq <= 4096, 1 <= sk <=
+ * 1024) with one work unit past the end of the problem, whose index every
+ * warp role checks before decoding it; synchronises and returns the
+ * recorded status code (expected ATTN_STATUS_BOUNDS).  The normal build
+ * returns ATTN_ERR_BUILD.
+ */
+int attn_bwd_bounds_selftest(const void *q, const void *k, const void *v,
+                             const void *o, const void *dout,
+                             const float *lse, void *dq, void *dk, void *dv,
+                             int64_t b, int64_t h, int64_t sq, int64_t sk,
+                             int64_t d, float scale, int dtype,
+                             void *workspace, int64_t workspace_bytes,
+                             void *stream);
 
 /* Library version string. */
 const char *attn_version(void);

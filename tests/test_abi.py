@@ -206,11 +206,13 @@ def test_debug_status_and_slot_hook_without_device(lib):
 
 
 def test_checked_library_exports_the_same_interface(lib):
-    """The checked build (every computed index of the forward bounds-checked)
-    exports every declared symbol too; the bounds self-test needs it and the
-    normal build says so."""
+    """The checked build (every computed index of the forward and backward
+    bounds-checked) exports every declared symbol too; the bounds self-tests
+    need it and the normal build says so."""
     checked = binding.load(binding.CHECKED_LIB_PATH)
     for name in declared_functions():
         assert hasattr(checked, name), name
     rc = lib.attn_fwd_bounds_selftest(P, P, P, P, None, 1, 1, 4, 4, 64, 0.1, 1, None)
+    assert rc == -10 and "checked build" in lib.attn_last_error().decode()
+    rc = lib.attn_bwd_bounds_selftest(P, P, P, P, P, P, P, P, P, 1, 1, 4, 4, 64, 0.1, 1, P, 1 << 20, None)
     assert rc == -10 and "checked build" in lib.attn_last_error().decode()

@@ -1,13 +1,15 @@
 """The checked build (libattn_fwd_checked.so: the same sources with every
-computed index of the forward compared with its bounds -- copy coordinates,
-page lookups, thread-written O / LSE / split-partial offsets, decoded units,
-the tensor-memory allocation and the shared-memory window) runs the
-small-shape parity suite, the split-KV, packed, KV-cache, paged and e4m3
-cases, each against the fp64 oracle as in their own test files, with the
-status word read after every case: no check may fire on valid inputs.  Its
-self-test puts one unit past the end of a problem and checks that the
-bounds violation is reported instead of used.  Nothing here faults: an index
-that fails its check is not used."""
+computed index of the forward and backward compared with its bounds -- copy
+coordinates, page lookups, thread-written O / LSE / split-partial / dK / dV
+offsets, dQ reduce-add coordinates, decoded units, the tensor-memory
+allocation and the shared-memory window) runs the small-shape parity suite,
+the split-KV, packed, KV-cache, paged and e4m3 cases, the dense and packed
+backward cases and the >2^32-element problems, each against the fp64 oracle
+as in their own test files, with the status word read after every case: no
+check may fire on valid inputs.  Its self-tests put one unit past the end
+of a forward and of a backward problem and check that the bounds violation
+is reported instead of used.  Nothing here faults: an index that fails its
+check is not used."""
 import math
 
 import numpy as np
@@ -17,16 +19,18 @@ import torch
 from attention_forward_14_gb300 import binding
 from attention_forward_14_gb300 import workloads as W
 
+import test_bwd_gpu as BW
 import test_fp8_gpu as F8
 import test_kvcache_gpu as KV
 import test_max_size_gpu as MS
 import test_parity_gpu as P
 import test_splitkv_gpu as SK
+import test_varlen_bwd_gpu as VB
 import test_varlen_gpu as VL
 
 pytestmark = pytest.mark.gpu
 
-BOUNDS, SITE_CHK_UNIT = 3, 22
+BOUNDS, SITE_CHK_UNIT, SITE_BWD_CHK_UNIT = 3, 22, 42
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -91,12 +95,51 @@ def test_checked_fp8(causal, d):
 
 @pytest.mark.parametrize("which", ["dense", "varlen"])
 def test_checked_past_2_32_elements(which):
-    """The forwards of the >2^32-element problems: every computed offset of
-    the larger tensors within its bounds (and the boundary heads correct)."""
-    out = MS.dense_forward() if which == "dense" else MS.varlen_forward()
-    _clean(f"{which} forward past 2^32 elements")
-    del out
+    """The >2^32-element problems, forward and backward: every computed
+    offset of the larger tensors within its bounds (and the boundary heads
+    correct)."""
+    if which == "dense":
+        MS.test_dense_forward_and_backward_past_2_32_elements()
+    else:
+        MS.test_varlen_forward_and_backward_past_2_32_elements()
+    _clean(f"{which} forward and backward past 2^32 elements")
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("b,h,sq,sk,dtype,causal,d", BW.SHAPES)
+def test_checked_bwd(b, h, sq, sk, dtype, causal, d):
+    BW.test_bwd_matches_oracle(b, h, sq, sk, dtype, causal, d)
+    _clean(f"backward b{b} h{h} sq{sq} sk{sk} {dtype} c{int(causal)} d{d}")
+
+
+@pytest.mark.parametrize("lens_q,lens_k,h,d,dtype,causal", VB.CASES)
+def test_checked_bwd_varlen(lens_q, lens_k, h, d, dtype, causal):
+    VB.test_varlen_bwd_matches_oracle_and_dense(lens_q, lens_k, h, d, dtype, causal)
+    _clean(f"packed backward {lens_q} {lens_k} h{h} d{d} {dtype} c{int(causal)}")
+
+
+def test_checked_bwd_bounds_selftest_reports_instead_of_using():
+    """One backward unit past the end of a 1-head problem: every warp role
+    finds its index out of range before decoding it, the status says where,
+    and the next call on the same context is correct and clean."""
+    dev = torch.device("cuda", 0)
+    q, k, v, do = BW._draw(1, 1, 256, 256, "bf16", 5, d=64)
+    _, _, o, lse = BW._fwd_outputs(q, k, v, False, 0.125, "bf16")
+    qd, kd, vd, od, dod = (t.to(dev) for t in (q, k, v, o, do))
+    ld = lse.to(dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    nbytes = binding.bwd_workspace_bytes(1, 1, 256, 64)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    lib = binding.load()
+    rc = lib.attn_bwd_bounds_selftest(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(), dod.data_ptr(),
+                                      ld.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), 1, 1, 256, 256, 64,
+                                      0.125, 1, ws.data_ptr(), nbytes, None)
+    assert rc == BOUNDS, (rc, lib.attn_last_error())
+    st = binding.status()
+    assert st[0] == BOUNDS and st[3] == SITE_BWD_CHK_UNIT
+    binding.status_clear()
+    BW.test_bwd_matches_oracle(1, 2, 300, 300, "bf16", True, 64)
+    _clean("after the backward bounds self-test")
 
 
 def test_checked_bounds_selftest_reports_instead_of_using():

@@ -612,7 +612,7 @@ def bench_bwd_varlen(args, bw):
 
 
 def _finish_fp8(args, w, world, rank, dist, dev, q, k, v, qd, kd, vd, o, lse, stream, t_all0, t_all1, total_ms,
-                launch_ms, sampler, step):
+                launch_ms, sampler, step, l2_note):
     """e4m3 line: roofline against the 8-bit tensor peak (measured bf16 peak
     x the nominal fp8/bf16 ratio 2); e2e = H2D of q, k, v (pinned), the
     forward, D2H of O and LSE, each step."""
@@ -646,7 +646,7 @@ def _finish_fp8(args, w, world, rank, dist, dev, q, k, v, qd, kd, vd, o, lse, st
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
             "config": {"workload": w.name, "b": w.b, "h": w.h, "sq": w.sq, "sk": w.sk, "d": w.d, "causal": w.causal,
-                       "flops_per_step": w.flops(), "output": "bf16"},
+                       "flops_per_step": w.flops(), "output": "bf16", "l2": l2_note},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak8, "unit": "TFLOP/s",
                          "frac": achieved / peak8, "traffic": profiled_traffic(w.name),
                          "peak_kind": f"{peaks['source']} bf16 burst x 2 (nominal fp8/bf16 ratio)",
@@ -775,8 +775,11 @@ def main():
     # end to end through the host-buffer entry point: H2D of Q, K, V from
     # pinned memory, the forward, D2H of O and LSE, every step.
     if w.dtype == "e4m3":  # the host-buffer entry point takes 16-bit inputs; time the same calls with copies
+        l2_note = (f"inputs {in_bytes / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB, no flush" if flush is None else
+                   f"inputs {in_bytes / 1e6:.0f} MB fit in L2: 256 MB flush before each timed step, "
+                   "time from each step's own events")
         return _finish_fp8(args, w, world, rank, dist, dev, q, k, v, qd, kd, vd, o, lse, stream, t_all0, t_all1,
-                           total_ms, launch_ms, sampler, step)
+                           total_ms, launch_ms, sampler, step, l2_note)
     qh, kh, vh = (t.pin_memory() for t in (q, k, v))
     oh = torch.empty_like(qh).pin_memory()
     lh = torch.empty(q.shape[:3], dtype=torch.float32).pin_memory()

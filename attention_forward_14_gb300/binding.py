@@ -26,7 +26,7 @@ ERRORS = {
 EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_fwd_varlen", "attn_fwd_fp8", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
            "attn_fwd_splitkv_default_splits", "attn_fwd_splitkv_noalloc", "attn_last_error", "attn_fwd_status", "attn_fwd_status_clear",
            "attn_fwd_debug_status", "attn_fwd_sched_pin_slot", "attn_fwd_bounds_selftest", "attn_bwd_bounds_selftest",
-           "attn_fwd_watchdog_selftest", "attn_version", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_varlen",
+           "attn_fwd_watchdog_selftest", "attn_bwd_watchdog_selftest", "attn_version", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_varlen",
            "attn_bwd_varlen_workspace_bytes", "attn_fwd_kvcache", "attn_fwd_kvcache_paged"]
 
 
@@ -81,6 +81,9 @@ def _bind(lib):
     lib.attn_fwd_sched_pin_slot.argtypes = [c_int]
     lib.attn_fwd_bounds_selftest.restype = c_int
     lib.attn_fwd_bounds_selftest.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_float, c_int, vp]
+    lib.attn_bwd_watchdog_selftest.restype = c_int
+    lib.attn_bwd_watchdog_selftest.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int,
+                                               c_float, c_int, vp, i64, c_int, c_int, vp]
     lib.attn_bwd_bounds_selftest.restype = c_int
     lib.attn_bwd_bounds_selftest.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_float,
                                              c_int, vp, i64, vp]
@@ -459,6 +462,25 @@ def watchdog_selftest(q, k, v, o, lse, causal, scale, withheld_load: int, timeou
                                             lse.data_ptr() if lse is not None else None,
                                             b, h, sq, sk, d, int(bool(causal)), float(scale), _dtype_code(q),
                                             int(withheld_load), int(timeout_ms),
+                                            _stream_handle(None, q.device))
+    return _check(rc, lib)
+
+
+def bwd_watchdog_selftest(q, k, v, o, dout, lse, causal, scale, withheld_load: int, timeout_ms: int):
+    """Run the backward with one query-tile load withheld in every CTA;
+    returns the recorded code.  The gradients are not meaningful."""
+    import torch
+    lib = load()
+    b, h, sq, d = q.shape
+    sk = k.shape[2]
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = bwd_workspace_bytes(b, h, sq, d)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = lib.attn_bwd_watchdog_selftest(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                                            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                            b, h, sq, sk, d, int(bool(causal)), float(scale), _dtype_code(q),
+                                            ws.data_ptr(), nbytes, int(withheld_load), int(timeout_ms),
                                             _stream_handle(None, q.device))
     return _check(rc, lib)
 

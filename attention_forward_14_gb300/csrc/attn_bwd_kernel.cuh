@@ -96,6 +96,9 @@ struct BwdParams {
     float sl2e;            // scale * log2(e)
     float scale;           // folded into dS
     uint64_t timeout_ns;
+#if ATTN_CHECKED
+    int32_t withheld_load = -1;  // watchdog self-test: this CTA-local Q load is never issued
+#endif
 #ifdef ATTN_TRACE_ENABLE
     unsigned long long *trace;  // per-warp event records (timeline builds only)
 #endif
@@ -795,7 +798,12 @@ __global__ void __launch_bounds__(512, 1)
                         ok = false;
                         break;
                     }
-                    if (elect_one()) {
+#if ATTN_CHECKED
+                    const bool issue_q = static_cast<int32_t>(q_it) != p.withheld_load;
+#else
+                    constexpr bool issue_q = true;  // (a compare here costs the d = 64 kernel 1.5%)
+#endif
+                    if (issue_q && elect_one()) {
                         const uint32_t bar = B(ctl->q_full[st]);
                         mbar_arrive_expect_tx(bar, C::TILE_BYTES + 2 * C::BM * 4);
                         for (int pn = 0; pn < C::NPANEL; ++pn)
@@ -823,7 +831,10 @@ __global__ void __launch_bounds__(512, 1)
             // Wind-down: let the last copies land before the CTA exits.
             if (un_it > 0) drain_wait(B(ctl->kv_full), (un_it - 1) & 1u, p.timeout_ns);
             for (uint32_t k = (q_it > C::NSTAGE ? q_it - C::NSTAGE : 0u); k < q_it; ++k) {
-                drain_wait(B(ctl->q_full[k % C::NSTAGE]), (k / C::NSTAGE) & 1u, p.timeout_ns);
+#if ATTN_CHECKED
+                if (static_cast<int32_t>(k) != p.withheld_load)
+#endif
+                    drain_wait(B(ctl->q_full[k % C::NSTAGE]), (k / C::NSTAGE) & 1u, p.timeout_ns);
                 drain_wait(B(ctl->do_full[k % C::NSTAGE]), (k / C::NSTAGE) & 1u, p.timeout_ns);
             }
             __syncwarp();

@@ -485,11 +485,13 @@ cudaError_t launch_bwd_any(const bwd::BwdLaunchArgs &a, int64_t d, int dtype, in
     return causal ? bwd::launch_bwd<__half, true, 64, VARLEN>(a) : bwd::launch_bwd<__half, false, 64, VARLEN>(a);
 }
 
-// extra_units > 0 (the bounds self-test only) hands out that many units past
-// the end of the problem.
+// Self-test knobs: extra_units > 0 hands out that many units past the end
+// of the problem (bounds self-test); withheld_load >= 0 never issues that
+// CTA-local Q load, and timeout_ns bounds every wait (watchdog self-test).
 int run_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse, void *dq,
             void *dk, void *dv, int64_t b, int64_t h, int64_t sq, int64_t sk, int64_t d, int causal, float scale,
-            int dtype, void *workspace, int64_t workspace_bytes, cudaStream_t stream, int extra_units = 0)
+            int dtype, void *workspace, int64_t workspace_bytes, cudaStream_t stream, int extra_units = 0,
+            int withheld_load = -1, uint64_t timeout_ns = kDefaultTimeoutNs)
 {
     if (b < 0 || h < 0 || sq < 0 || sk < 0)
         return fail(ATTN_ERR_SHAPE, "negative size: b=%lld h=%lld sq=%lld sk=%lld", (long long)b, (long long)h,
@@ -561,7 +563,12 @@ int run_bwd(const void *q, const void *k, const void *v, const void *o, const vo
 #endif
     p.sl2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     p.scale = scale;
-    p.timeout_ns = kDefaultTimeoutNs;
+    p.timeout_ns = timeout_ns;
+#if ATTN_CHECKED
+    p.withheld_load = withheld_load;
+#else
+    (void)withheld_load;
+#endif
     p.cu_q = p.cu_k = nullptr;
     p.heads = static_cast<int32_t>(h);
     p.total_q = static_cast<int32_t>(sq);
@@ -1221,6 +1228,31 @@ int attn_fwd_bounds_selftest(const void *q, const void *k, const void *v, void *
     (void)q, (void)k, (void)v, (void)o, (void)lse, (void)b, (void)h, (void)sq, (void)sk, (void)d, (void)scale;
     (void)dtype, (void)stream;
     return fail(ATTN_ERR_BUILD, "attn_fwd_bounds_selftest needs the checked build (libattn_fwd_checked.so)");
+#endif
+}
+
+int attn_bwd_watchdog_selftest(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                               const float *lse, void *dq, void *dk, void *dv, int64_t b, int64_t h, int64_t sq,
+                               int64_t sk, int64_t d, int causal, float scale, int dtype, void *workspace,
+                               int64_t workspace_bytes, int withheld_load, int timeout_ms, void *stream)
+{
+    g_err.clear();
+#if ATTN_CHECKED
+    if (timeout_ms <= 0 || timeout_ms > 10000) return fail(ATTN_ERR_SHAPE, "timeout_ms must be in 1..10000");
+    if (withheld_load < 0) return fail(ATTN_ERR_SHAPE, "withheld_load must be >= 0");
+    if (b < 1 || h < 1 || sq < 1 || sk < 1 || b * h * sq > 4096 || sk > 1024)
+        return fail(ATTN_ERR_SHAPE, "self-test wants a tiny problem with rows and keys");
+    int rc = attn_fwd_status_clear();
+    if (rc != ATTN_OK) return rc;
+    rc = run_bwd(q, k, v, o, dout, lse, dq, dk, dv, b, h, sq, sk, d, causal, scale, dtype, workspace, workspace_bytes,
+                 static_cast<cudaStream_t>(stream), 0, withheld_load, static_cast<uint64_t>(timeout_ms) * 1000000ull);
+    if (rc != ATTN_OK) return rc;
+    return attn_fwd_status(nullptr);
+#else
+    (void)q, (void)k, (void)v, (void)o, (void)dout, (void)lse, (void)dq, (void)dk, (void)dv, (void)b, (void)h;
+    (void)sq, (void)sk, (void)d, (void)causal, (void)scale, (void)dtype, (void)workspace, (void)workspace_bytes;
+    (void)withheld_load, (void)timeout_ms, (void)stream;
+    return fail(ATTN_ERR_BUILD, "attn_bwd_watchdog_selftest needs the checked build (libattn_fwd_checked.so)");
 #endif
 }
 

@@ -451,6 +451,26 @@ int attn_fwd_watchdog_selftest(const void *q, const void *k, const void *v,
                                int timeout_ms, void *stream);
 
 /*
+ * attn_bwd_watchdog_selftest: the same for the backward -- attn_bwd on tiny
+ * caller buffers (contract of attn_bwd, b*h*sq <= 4096, 1 <= sk <= 1024)
+ * with the query-tile load number `withheld_load` of every CTA never issued
+ * and the wait limit set to `timeout_ms`; synchronises and returns the
+ * recorded status code (expected ATTN_STATUS_TIMEOUT), or a negative error.
+ * The gradients of that call are not meaningful.  The backward's waits are
+ * the same code in both builds; the knob that withholds the load exists in
+ * the checked build only (in the normal one it would cost the kernel time),
+ * so the normal build returns ATTN_ERR_BUILD.
+ */
+int attn_bwd_watchdog_selftest(const void *q, const void *k, const void *v,
+                               const void *o, const void *dout,
+                               const float *lse, void *dq, void *dk, void *dv,
+                               int64_t b, int64_t h, int64_t sq, int64_t sk,
+                               int64_t d, int causal, float scale, int dtype,
+                               void *workspace, int64_t workspace_bytes,
+                               int withheld_load, int timeout_ms,
+                               void *stream);
+
+/*
  * Checked build.  libattn_fwd_checked.so exports this same interface from
  * the same sources compiled with every computed index of the forward and
  * backward kernels checked.  Forward: copy coordinates of Q, K, V (page

@@ -216,3 +216,5 @@ def test_checked_library_exports_the_same_interface(lib):
     assert rc == -10 and "checked build" in lib.attn_last_error().decode()
     rc = lib.attn_bwd_bounds_selftest(P, P, P, P, P, P, P, P, P, 1, 1, 4, 4, 64, 0.1, 1, P, 1 << 20, None)
     assert rc == -10 and "checked build" in lib.attn_last_error().decode()
+    rc = lib.attn_bwd_watchdog_selftest(P, P, P, P, P, P, P, P, P, 1, 1, 4, 4, 64, 0, 0.1, 1, P, 1 << 20, 0, 50, None)
+    assert rc == -10 and "checked build" in lib.attn_last_error().decode()

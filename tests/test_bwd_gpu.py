@@ -166,3 +166,4 @@ def test_bwd_workload_sampled(name):
         print(name, (bi, hi), [(round(a, 3), f"{b:.2e}") for a, b in res])
     for t in (dq, dk, dv):
         assert torch.isfinite(t).all()
+

@@ -159,3 +159,22 @@ def test_checked_bounds_selftest_reports_instead_of_using():
     binding.status_clear()
     P.check_full(*W.draw(1, 2, 300, 300, 64, "bf16", seed=6), False, 0.125, "after the bounds self-test")
     _clean("after the bounds self-test")
+
+
+def test_checked_bwd_watchdog_reports_instead_of_hanging():
+    """The first query-tile load of every CTA is withheld: the waits run out
+    after 50 ms, the kernel records where, winds down and returns; the
+    context stays usable and the next backward is correct."""
+    dev = torch.device("cuda", 0)
+    q, k, v, do = BW._draw(1, 2, 256, 256, "bf16", 31900)
+    _, _, o, lse = BW._fwd_outputs(q, k, v, False, 0.1, "bf16")
+    code = binding.bwd_watchdog_selftest(q.to(dev), k.to(dev), v.to(dev), o.to(dev), do.to(dev), lse.to(dev),
+                                         False, 0.1, withheld_load=0, timeout_ms=50)
+    assert code == 1
+    st = binding.status()
+    # code 1 (a wait ran out) at one of the backward's wait sites
+    assert st[0] == 1 and 21 <= st[3] <= 38, st
+    binding.status_clear()
+    assert binding.status()[0] == 0
+    BW._check_all(q, k, v, do, False, 0.1, "bf16", "after the backward watchdog")
+    _clean("after the backward watchdog")

@@ -797,6 +797,14 @@ def main():
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, dist, dev)
     e2e_value = world * w.flops() / (e2e_ms * 1e-3) / 1e12
+    # this machine's host link, for reading the end-to-end figure: one pinned
+    # copy of the step's inputs to the device, alone
+    e0.record(stream)
+    for dst, src in ((qd, qh), (kd, kh), (vd, vh)):
+        dst.copy_(src, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    h2d_gbs = in_bytes / (e0.elapsed_time(e1) * 1e-3) / 1e9
 
     if rank == 0:
         peaks = load_peaks()
@@ -832,7 +840,8 @@ def main():
                           "algorithmic_bytes": w.bytes(), "num_splits": splits}),
             "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": in_bytes,
                     "d2h_bytes_per_step": q.numel() * q.element_size() + lse.numel() * 4,
-                    "ms_per_step": e2e_ms},
+                    "ms_per_step": e2e_ms, "host_to_device_gbs": h2d_gbs,
+                    "h2d_floor_ms": in_bytes / (h2d_gbs * 1e9) * 1e3},
             "gpu_launches": args.steps * (2 if splits > 1 else 1),
             "clocks": sampler.summary(),
         }

@@ -181,3 +181,43 @@ def test_varlen_forward_and_backward_past_2_32_elements():
                 check(f"varlen backward {name} sequence {si} head {hi}", _host(got[a:e, hi]), r[0, 0], bd)
     del q, k, v, o, lse, do, dq, dk, dv
     torch.cuda.empty_cache()
+
+
+def test_long_sequence_forward_and_backward_sampled_rows():
+    """Two heads of 2^17 tokens, causal: 1,024 key tiles for the last query
+    block, row and key indices up to 2^17.  Sampled rows (the first, the
+    last, the unit and tile boundaries and seeded others) of O, LSE and dQ
+    against the oracle; the backward gets the oracle's O and LSE on those
+    rows (the bound assumes them) and the forward's elsewhere."""
+    b, h, s, d, dtype = 1, 2, 1 << 17, 128, "bf16"
+    causal, scale = True, 1.0 / math.sqrt(d)
+    q, k, v = W.draw(b, h, s, s, d, dtype, seed=41020)
+    do = W.draw_grad(b, h, s, d, dtype, seed=41021)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    o, lse = af.attn_fwd(qd, kd, vd, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(41022)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, s // 2 - 1, s // 2, s - 257, s - 256, s - 1],
+                                     rng.integers(0, s, 16)]))
+    ref = {}
+    for hi in range(h):
+        qn, kn, vn = (t[0, hi].double().numpy() for t in (q, k, v))
+        o_r, lse_r = oracle.attn_head_rows(qn, kn, vn, rows, causal, scale)
+        compare(o[0, hi].float().cpu().double().numpy()[rows], lse[0, hi].cpu().double().numpy()[rows], o_r, lse_r,
+                dtype, f"forward rows of head {hi}")
+        ri = torch.from_numpy(rows).to(DEV)
+        o[0, hi, ri] = torch.from_numpy(o_r).to(o.dtype).to(DEV)
+        lse[0, hi, ri] = torch.from_numpy(lse_r).float().to(DEV)
+        ref[hi] = (qn, kn, vn)
+    dq, dk, dv = af.attn_bwd(qd, kd, vd, o, dod, lse, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t).all()
+    for hi, (qn, kn, vn) in ref.items():
+        don = do[0, hi].double().numpy()
+        dq_r = oracle.attn_bwd_dq_rows(qn, kn, vn, don, rows, causal, scale)
+        on = o[0, hi].float().cpu().double().numpy()
+        ln = lse[0, hi].cpu().double().numpy()
+        bq, _, _ = bounds(qn, kn, vn, don, on, ln, dq_r, np.zeros((0, d)), np.zeros((0, d)), causal, scale, dtype,
+                          rows=rows, cols=np.zeros(0, dtype=np.int64))
+        check(f"dq rows of head {hi}", dq[0, hi].float().cpu().double().numpy()[rows], dq_r, bq)

@@ -153,7 +153,7 @@ int encode_map(CUtensorMap *map, CUtensorMapDataType dt, const void *ptr, const 
             *map = e.map;
             return ATTN_OK;
         }
-    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     const int rc = get_encode(&enc);
     if (rc != ATTN_OK) return rc;
     const cuuint32_t estr[3] = {1, 1, 1};
